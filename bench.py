@@ -1,0 +1,348 @@
+"""Benchmark of the parallel Newton forward of the diagonal-mix GRU.
+
+python bench.py [--gpus N] [--steps K] [--warmup W] [--workload I] [--algo A]
+                [--impl ours|reference]
+
+A step is one Newton forward over one batch of the workload: K iterations of
+cell + Jacobian + residual + affine scan and the final residual gate
+(nrnn_newton_forward), preactivations resident in HBM.  The input projection
+is timed beside it (``with_projection``).  Prints one JSON line on rank 0.
+
+Under torchrun each rank runs its own replica of the workload on its own GPU
+(the batch rows are independent; there is no collective on the data path):
+weak scaling, value = tokens of all ranks / max over ranks of the time.
+
+``--impl reference`` times the float64 CPU oracle (the reference
+implementation of this method here) on a bounded sample of the same
+workload on the host cores, rank 0 only.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import synthetic as syn  # noqa: E402
+
+METRIC = "Newton forward tokens/s and achieved HBM GB/s vs GB300 peak (1 GPU)"
+L2_FLUSH_BYTES = 512 << 20
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as fh:
+            d = json.load(fh)
+        return {"hbm_gbs": d["hbm_gbs"], "src": "measured"}
+    return {"hbm_gbs": 6800.0, "src": "fallback"}
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+class ClockSampler:
+    """Samples nvidia-smi clocks and throttle reasons while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            if self.thread is not None:
+                self.thread.join(timeout=2)
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def workload_bytes(w, algo):
+    """Algorithmic HBM bytes of one Newton forward (per launch list)."""
+    s = 2 if w.dtype == "bf16" else 4
+    tok = w.B * w.T
+    if algo == "per_iter":
+        # iteration 1: read P, write H; later: read P and H, write H; the last
+        # launch evaluates the residual in-kernel (no extra pass)
+        per = [4 * w.d_h * s * tok] + [5 * w.d_h * s * tok] * (w.K - 1)
+        return per
+    return [4 * w.d_h * s * tok]
+
+
+def run_ours(args, w, rank, world, local):
+    import torch
+    import nonlinear_rnn_gb300 as nr
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    inp = syn.make_inputs(w)
+    tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+    x = torch.from_numpy(inp["x"]).to(dev).to(tdt)
+    W = torch.from_numpy(inp["W_x"]).to(dev).to(tdt)
+    prm = nr.params_tensor(inp["params"], w.d_h, dev)
+    cu = inp["cu_seqlens"]
+    P = nr.input_projection(x, W)
+    H = torch.empty((w.B, w.T, w.d_h), dtype=tdt, device=dev)
+    ws = torch.empty(nr.workspace_bytes(w.B, w.T, w.d_h, tdt, w.K, args.algo), dtype=torch.uint8,
+                     device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def newton():
+        return nr.newton_forward(P, prm, cu_seqlens=cu, K=w.K, algo=args.algo, check=False,
+                                 out=H, workspace=ws)
+
+    for _ in range(args.warmup):
+        flush.fill_(1.0)
+        newton()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    with ClockSampler(local) as clk:
+        t_wall = time.perf_counter()
+        for i in range(args.steps):
+            flush.fill_(1.0)          # L2 flush, outside the timed events
+            ev[i][0].record(stream)
+            _, rho = newton()
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        t_wall = time.perf_counter() - t_wall
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    ms = sum(step_ms) / len(step_ms)
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+        torch.distributed.barrier()
+
+    # projection beside it
+    pe = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+    proj_ms = []
+    for _ in range(max(3, min(args.steps, 10))):
+        flush.fill_(1.0)
+        pe[0].record(stream)
+        nr.input_projection(x, W, out=P)
+        pe[1].record(stream)
+        torch.cuda.synchronize()
+        proj_ms.append(pe[0].elapsed_time(pe[1]))
+    proj = statistics.median(proj_ms)
+
+    # end to end through the public call with host buffers
+    P_host = P.cpu().pin_memory()
+    H_host = torch.empty(H.shape, dtype=H.dtype).pin_memory()
+    rho_host = torch.empty((), dtype=torch.float32).pin_memory()
+    e2e = []
+    for i in range(max(3, min(args.steps, 10)) + 1):
+        flush.fill_(1.0)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        Pd = P_host.to(dev, non_blocking=True)
+        Hd, r = nr.newton_forward(Pd, prm, cu_seqlens=cu, K=w.K, algo=args.algo, check=False,
+                                  workspace=ws)
+        H_host.copy_(Hd, non_blocking=True)
+        rho_host.copy_(r, non_blocking=True)
+        b.record(stream)
+        torch.cuda.synchronize()
+        if i > 0:
+            e2e.append(a.elapsed_time(b))
+    e2e_ms = statistics.median(e2e)
+
+    tokens = w.B * w.T
+    pk = peaks()
+    byts = workload_bytes(w, args.algo)
+    per_launch_ms = ms / len(byts)
+    achieved = (sum(byts) / len(byts)) / (per_launch_ms * 1e-3) / 1e9
+    launches = len(byts) if w.K > 0 else 1
+    traffic = load_traffic(w, args.algo)
+    out = {
+        "metric": METRIC,
+        "value": tokens * world / (ms * 1e-3),
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": w.dtype,
+        "data": "synthetic (seeded SplitMix64: x~N(0,1), W_x~U(+-1/sqrt(d_in)), a~U(+-1), b=0)",
+        "config": {"workload": w.name, "B": w.B, "T": w.T, "d_in": w.d_in, "d_h": w.d_h,
+                   "K": w.K, "segments": w.segments, "algo": args.algo,
+                   "parallelism": f"replica x{world}",
+                   "l2": f"flushed between steps ({L2_FLUSH_BYTES >> 20} MiB write, untimed)"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                     "frac": achieved / pk["hbm_gbs"], "traffic": traffic,
+                     "kernel": "k_newton<%s,%s>" % ("bf16" if w.dtype == "bf16" else "float",
+                                                     "fused" if args.algo != "per_iter" else "per_iter"),
+                     "algorithmic_bytes_per_launch": sum(byts) / len(byts),
+                     "peak_src": pk["src"] + " (MEASURED_PEAKS.json hbm_gbs)"},
+        "e2e": {"value": tokens * world / (e2e_ms * 1e-3), "unit": "tokens/s",
+                "h2d_bytes_per_step": P.numel() * P.element_size(),
+                "d2h_bytes_per_step": H.numel() * H.element_size() + 4},
+        "gpu_launches": launches * args.steps,
+        "with_projection": {"projection_ms": proj, "tokens_per_s": tokens * world / ((ms + proj) * 1e-3)},
+        "residual": float(rho.item()),
+        "wall_s": t_wall,
+        "clocks": clk.summary(),
+    }
+    return out
+
+
+def load_traffic(w, algo):
+    """DRAM bytes per launch of the dominant kernel from a committed ncu summary, if any."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as fh:
+        d = json.load(fh)
+    return d.get(f"{w.name}|{algo}")
+
+
+def cpu_baseline(w, budget_s=12.0, steps=1):
+    """Times the float64 oracle on a bounded sample (whole rows of T steps for a
+    few hidden units) with all host cores; returns tokens/s scaled to full tokens."""
+    import oracle
+
+    cores = os.cpu_count() or 1
+    inp = syn.make_inputs(w, with_x=False)
+    prm = inp["params"]
+    cu = inp["cu_seqlens"]
+    rows = [0]
+    # pilot: one unit, one row
+    units = np.array([0])
+    Pc = syn.preact_uniform_columns(w, units, rows=rows)
+    t = time.perf_counter()
+    oracle.newton(Pc, oracle.pack_params(prm)[:, units], w.K, cu_seqlens=cu, threads=1)
+    per_unit = max(time.perf_counter() - t, 1e-4)
+    n_units = int(max(1, min(w.d_h, budget_s / per_unit * cores / max(steps, 1))))
+    n_rows = 1
+    while n_units == w.d_h and n_rows < w.B and per_unit * n_units * (n_rows + 1) / cores * steps < budget_s:
+        n_rows += 1
+    units = np.arange(n_units)
+    rows = list(range(n_rows))
+    Pc = syn.preact_uniform_columns(w, units, rows=rows)
+    pp = oracle.pack_params(prm)[:, units]
+    times = []
+    for _ in range(steps):
+        t = time.perf_counter()
+        oracle.newton(Pc, pp, w.K, cu_seqlens=cu, threads=cores)
+        times.append(time.perf_counter() - t)
+    sec = statistics.mean(times)
+    unit_tokens = n_units * n_rows * w.T
+    return {"value": unit_tokens / w.d_h / sec, "unit": "tokens/s", "cores": min(cores, n_units),
+            "kind": "oracle",
+            "sample": f"oracle.newton float64, K={w.K}, {n_units} of {w.d_h} units x {n_rows} of "
+                      f"{w.B} rows x T={w.T} (uniform preact), {sec:.2f} s per pass",
+            "seconds": sec}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", type=int, default=1)
+    ap.add_argument("--algo", default="auto", choices=["auto", "fused", "per_iter"])
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    w = syn.WORKLOADS[args.workload]
+    rank, world, local = dist_env()
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        cb = cpu_baseline(w, budget_s=max(2.0, 60.0 / max(args.steps + args.warmup, 1)),
+                          steps=args.steps)
+        out = {"impl": "reference", "metric": METRIC, "value": cb["value"], "unit": "tokens/s",
+               "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+               "ms_per_step": 1e3 * w.B * w.T / cb["value"], "higher_is_better": True,
+               "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+               "data": "synthetic (seeded SplitMix64)",
+               "config": {"workload": w.name, "B": w.B, "T": w.T, "d_in": w.d_in, "d_h": w.d_h,
+                          "K": w.K, "segments": w.segments},
+               "cpu_baseline": {k: cb[k] for k in ("value", "unit", "cores", "kind", "sample")},
+               "e2e": {"value": cb["value"], "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                       "d2h_bytes_per_step": 0}}
+        print(json.dumps(out))
+        return
+
+    import torch
+    if world > 1:
+        torch.distributed.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    out = run_ours(args, w, rank, world, local)
+    if rank == 0 and not args.no_cpu_baseline:
+        cb = cpu_baseline(w)
+        out["cpu_baseline"] = {k: cb[k] for k in ("value", "unit", "cores", "kind", "sample")}
+    if world > 1:
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(out))
+
+
+if __name__ == "__main__":
+    main()

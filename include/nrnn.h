@@ -1,0 +1,183 @@
+/*
+ * nrnn.h -- C ABI of the GB300 parallel-Newton forward for a diagonal-mix GRU.
+ *
+ * The method (pararnn-torch pages: FAQs "Does parallel Newton match sequential
+ * unroll?" and "What is critical Newton depth (K*)?", numerics contract
+ * "Invariant", "Two thresholds" and "Four echelons / 1. Runtime",
+ * shapes_layout "cu_seqlens"):
+ *
+ *   cell    z = sig(P_z + a_z h + b_z),  r = sig(P_r + a_r h + b_r),
+ *           c = tanh(P_c + a_c (r h) + b_c),  f(h, P) = (1 - z) h + z c
+ *           with P = W_x x the input projection, gate blocks [z | r | c];
+ *   Newton  H^(0) = 0; for k = 1..K: at the shifted trajectory evaluate
+ *           F_t = H_t - f(H_{t-1}, P_t) and J_t = df/dh(H_{t-1}, P_t), solve
+ *           delta_t = J_t delta_{t-1} - F_t by a parallel scan over t, and set
+ *           H <- H + delta.  At t = 0 and at every segment head of a ragged
+ *           pack J = 0 and the shifted state is 0 (each segment starts from h=0);
+ *   gate    rho = max |F(H^(K))| (NaN counts as +inf); rho > residual_fail is
+ *           the divergence signal (NewtonDivergenceError on the pages).
+ *
+ * Conventions shared by every entry point
+ *   - Every buffer is caller-owned.  The library allocates no memory.
+ *   - Device buffers are contiguous, row-major, 16-byte aligned.
+ *   - dtype selects the storage type of preact, x, W_x and H: NRNN_F32 or
+ *     NRNN_BF16 (bfloat16 storage; all arithmetic inside the kernels is fp32).
+ *     Parameters are always fp32.
+ *   - params: device, fp32, shape (6, d_h): rows a_z, a_r, a_c, b_z, b_r, b_c.
+ *   - stream: a cudaStream_t (NULL = legacy default stream).  Calls are
+ *     asynchronous on that stream unless stated otherwise.
+ *   - cu_seqlens (nullable): device int32 array of num_segments + 1 offsets
+ *     for a ragged pack; then B must be 1 and T is the packed length N.  The
+ *     offsets must satisfy cu[0] = 0, cu[i] <= cu[i+1], cu[S] = N; check
+ *     them with nrnn_validate_cu_seqlens on a host copy before the call (the
+ *     kernels only read them and stay in bounds for any values, but give
+ *     meaningless results for invalid ones).  Empty segments are allowed.
+ *   - Alignment: d_h must be a multiple of 8 (TMA tile rows are 16-byte
+ *     aligned); other d_h return NRNN_ERR_UNSUPPORTED.
+ *   - Return value: an nrnn_status (0 = success, negative = error).  Errors
+ *     detected before any launch leave every output untouched.
+ */
+#ifndef NRNN_H
+#define NRNN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    NRNN_OK = 0,
+    NRNN_ERR_INVALID_ARG = -1,  /* null pointer, negative size, bad dtype, misaligned */
+    NRNN_ERR_CU_SEQLENS = -2,   /* cu_seqlens violates the rules above */
+    NRNN_ERR_UNSUPPORTED = -3,  /* valid request this build does not handle (d_h % 8) */
+    NRNN_ERR_CUDA = -4,         /* a CUDA runtime/driver call or a launch failed */
+    NRNN_ERR_DIVERGED = -5,     /* rho > residual_fail, or rho is NaN/inf */
+    NRNN_ERR_TIMEOUT = -6,      /* a bounded device wait gave up (result invalid) */
+    NRNN_ERR_WORKSPACE = -7     /* workspace null or smaller than required */
+} nrnn_status;
+
+typedef enum { NRNN_F32 = 0, NRNN_BF16 = 1 } nrnn_dtype;
+
+/* Newton implementation.  Both compute the same iteration in the same order
+ * of operations per element; they differ in HBM traffic.
+ *   NRNN_ALGO_PER_ITER: one fused cell+Jacobian+scan kernel per iteration;
+ *                       H goes through HBM between iterations.
+ *   NRNN_ALGO_FUSED:    one kernel runs all K iterations per T-chunk in
+ *                       on-chip memory; P is read once and H written once.
+ *   NRNN_ALGO_AUTO:     the library picks (currently NRNN_ALGO_FUSED).     */
+typedef enum { NRNN_ALGO_AUTO = 0, NRNN_ALGO_PER_ITER = 1, NRNN_ALGO_FUSED = 2 } nrnn_algo;
+
+/* Human-readable name of a status code (static storage, never NULL). */
+const char *nrnn_status_string(int status);
+
+/* ABI version: major * 10000 + minor * 100 + patch. */
+int nrnn_version(void);
+
+/*
+ * Rules of cu_seqlens (shapes_layout page, "cu_seqlens": batch 1, length N,
+ * S+1 offsets; validate_cu_seqlens): cu_host has num_segments + 1 >= 2
+ * entries, cu[0] = 0, non-decreasing, cu[num_segments] = N.  Host pointer;
+ * no CUDA call.  Returns NRNN_OK or NRNN_ERR_CU_SEQLENS (NRNN_ERR_INVALID_ARG
+ * for a null pointer or negative sizes).
+ */
+int nrnn_validate_cu_seqlens(const int32_t *cu_host, int64_t num_segments, int64_t N);
+
+/*
+ * Workspace bytes nrnn_newton_forward needs for this shape, K and algo
+ * (NRNN_ALGO_PER_ITER also holds one H buffer of B*T*d_h elements).
+ * Returns 0 for invalid arguments.
+ */
+size_t nrnn_newton_workspace_bytes(int64_t B, int64_t T, int64_t d_h, int dtype, int K,
+                                   int algo);
+
+/*
+ * Parallel Newton forward (numerics contract, "Invariant"; FAQs "How many
+ * Newton iterations should I use?": a fixed K).
+ *
+ *   preact        device, (B, T, 3 d_h) of dtype, gate blocks [z | r | c]
+ *   params        device, fp32 (6, d_h)
+ *   B, T, d_h     sizes; B, T >= 0, d_h > 0 and a multiple of 8
+ *   cu_seqlens    device int32 (num_segments + 1) or NULL (rectangular batch)
+ *   K             Newton iterations, 0 <= K <= 64 (K = 0: H = 0)
+ *   residual_fail divergence threshold (the pages' default is 1.0)
+ *   algo          nrnn_algo
+ *   H_out         device, (B, T, d_h) of dtype: H^(K)
+ *   residual_dev  device, 1 float: rho = max|F(H^(K))|, +inf if any F is NaN
+ *   residual_host NULL: fully asynchronous, no gate, no timeout report.
+ *                 Non-NULL: the call synchronises the stream, stores rho
+ *                 there, and returns NRNN_ERR_TIMEOUT if a bounded device
+ *                 wait gave up, else NRNN_ERR_DIVERGED if rho > residual_fail
+ *                 or rho is not finite (H_out is written either way).
+ *   workspace     device, ws_bytes >= nrnn_newton_workspace_bytes(...);
+ *                 256-byte aligned; its contents need no initialisation and
+ *                 are scratch after the call.  Calls that share a
+ *                 workspace must not overlap on the GPU.
+ *   stream        cudaStream_t
+ */
+int nrnn_newton_forward(const void *preact, int dtype, const float *params, int64_t B,
+                        int64_t T, int64_t d_h, const int32_t *cu_seqlens,
+                        int64_t num_segments, int K, float residual_fail, int algo,
+                        void *H_out, float *residual_dev, float *residual_host,
+                        void *workspace, size_t ws_bytes, void *stream);
+
+/*
+ * Sequential forward on the GPU (sequential_apply on the pages: "eval()"
+ * runs the sequential step): h_t = f(h_{t-1}, P_t) from h = 0 for each row,
+ * or for each segment of a pack; one thread per (row or segment, unit).
+ *   preact (B, T, 3 d_h) dtype -> H_out (B, T, d_h) dtype.  No workspace.
+ */
+int nrnn_sequential_forward(const void *preact, int dtype, const float *params, int64_t B,
+                            int64_t T, int64_t d_h, const int32_t *cu_seqlens,
+                            int64_t num_segments, void *H_out, void *stream);
+
+/*
+ * Residual of a given trajectory: rho = max |G_t - f(G_{t-1}, P_t)| over all
+ * (b, t, j), with G_{-1} = 0 at t = 0 and at segment heads (the residual gate
+ * of the numerics contract, "Two thresholds").  G (B, T, d_h) dtype.
+ * residual_dev: device, 1 float (overwritten).
+ */
+int nrnn_residual(const void *preact, int dtype, const float *params, int64_t B, int64_t T,
+                  int64_t d_h, const int32_t *cu_seqlens, int64_t num_segments,
+                  const void *G, float *residual_dev, void *stream);
+
+/*
+ * Input projection P = x W_x^T (shapes_layout page: "W_x" reads x of layout
+ * (B, T, d_in)); x (rows, d_in), W_x (3 d_h, d_in), preact (rows, 3 d_h), all
+ * of dtype, fp32 accumulation.  NRNN_F32 keeps fp32 accuracy (no TF32
+ * rounding of the operands); NRNN_BF16 uses the bf16 tensor-core path and
+ * rounds the fp32 accumulator to bf16.  d_in must be a multiple of 8.
+ */
+int nrnn_input_projection(const void *x, const void *W_x, int dtype, int64_t rows,
+                          int64_t d_in, int64_t d_h, void *preact, void *stream);
+
+/*
+ * Debug export of the segment-head mask the Newton kernels use
+ * (shapes_layout page: "Segment heads use J=0 on the scan"): mask_dev[t] = 1
+ * if t = 0 or t = cu[i] < cu[i+1] for some i, else 0, for t in [0, N).
+ * Uses the same device routine as the Newton kernels.  mask_dev: device, N bytes.
+ */
+int nrnn_debug_head_mask(const int32_t *cu_seqlens, int64_t num_segments, int64_t N,
+                         uint8_t *mask_dev, void *stream);
+
+/*
+ * Debug check of the bounded device wait used by the scan's look-back: one
+ * thread waits for *flag_dev to become nonzero for at most wait_ns
+ * nanoseconds.  *result_dev (device, 1 uint32) receives 1 if the flag was
+ * seen, 2 if the wait gave up.  Never hangs: a flag nobody sets returns 2.
+ */
+int nrnn_debug_bounded_wait(const uint32_t *flag_dev, uint64_t wait_ns, uint32_t *result_dev,
+                            void *stream);
+
+/*
+ * Upper limit, in nanoseconds, of every bounded device wait that later calls
+ * launch (default 2e9 = 2 s).  Process-wide; returns the previous value.
+ */
+uint64_t nrnn_set_wait_limit_ns(uint64_t ns);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* NRNN_H */

@@ -1,0 +1,30 @@
+"""GB300-native parallel Newton forward of a diagonal-mix GRU.
+
+The computation runs in ``libnrnn.so`` (hand-written CUDA for sm_103a, C ABI in
+``include/nrnn.h``); this package is its Python binding.  Importing it loads
+the library and fails if it cannot."""
+from ._binding import (  # noqa: F401
+    ALGOS,
+    EXPORTED,
+    GATE_ORDER,
+    AgreementError,
+    AgreementReport,
+    NewtonDivergenceError,
+    NrnnError,
+    bounded_wait,
+    default_agreement_atol,
+    head_mask,
+    input_projection,
+    lib_path,
+    load,
+    newton_forward,
+    params_tensor,
+    residual,
+    sequential_forward,
+    set_wait_limit_ns,
+    validate_cu_seqlens,
+    verify_agreement,
+    workspace_bytes,
+)
+
+load()

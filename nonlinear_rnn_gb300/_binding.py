@@ -1,0 +1,309 @@
+"""ctypes binding of libnrnn.so (C ABI in include/nrnn.h).
+
+Argument marshalling only: every step of the computation runs in the CUDA
+library.  torch supplies device memory (outputs and the workspace) and the
+current stream.  There is no fallback: if the library cannot be loaded the
+import of this module fails."""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from dataclasses import dataclass, field
+
+import numpy as np
+import torch
+
+from . import build as _build
+
+# status codes (include/nrnn.h)
+OK, ERR_INVALID_ARG, ERR_CU_SEQLENS, ERR_UNSUPPORTED = 0, -1, -2, -3
+ERR_CUDA, ERR_DIVERGED, ERR_TIMEOUT, ERR_WORKSPACE = -4, -5, -6, -7
+F32, BF16 = 0, 1
+ALGOS = {"auto": 0, "per_iter": 1, "fused": 2}
+GATE_ORDER = ("a_z", "a_r", "a_c", "b_z", "b_r", "b_c")
+
+_lock = threading.Lock()
+_lib = None
+
+_c = ctypes
+_vp, _i64, _int, _f, _sz, _u64 = _c.c_void_p, _c.c_int64, _c.c_int, _c.c_float, _c.c_size_t, _c.c_uint64
+_SIGNATURES = {
+    "nrnn_status_string": ([_int], _c.c_char_p),
+    "nrnn_version": ([], _int),
+    "nrnn_validate_cu_seqlens": ([_vp, _i64, _i64], _int),
+    "nrnn_newton_workspace_bytes": ([_i64, _i64, _i64, _int, _int, _int], _sz),
+    "nrnn_newton_forward": ([_vp, _int, _vp, _i64, _i64, _i64, _vp, _i64, _int, _f, _int, _vp,
+                             _vp, _vp, _vp, _sz, _vp], _int),
+    "nrnn_sequential_forward": ([_vp, _int, _vp, _i64, _i64, _i64, _vp, _i64, _vp, _vp], _int),
+    "nrnn_residual": ([_vp, _int, _vp, _i64, _i64, _i64, _vp, _i64, _vp, _vp, _vp], _int),
+    "nrnn_input_projection": ([_vp, _vp, _int, _i64, _i64, _i64, _vp, _vp], _int),
+    "nrnn_debug_head_mask": ([_vp, _i64, _i64, _vp, _vp], _int),
+    "nrnn_debug_bounded_wait": ([_vp, _u64, _vp, _vp], _int),
+    "nrnn_set_wait_limit_ns": ([_u64], _u64),
+}
+EXPORTED = tuple(_SIGNATURES)
+
+
+def lib_path() -> str:
+    return _build.LIB
+
+
+def load():
+    """Loads libnrnn.so (building it first if it is missing or stale)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = _build.build()
+            lib = ctypes.CDLL(path)
+            for name, (args, res) in _SIGNATURES.items():
+                fn = getattr(lib, name)
+                fn.argtypes = args
+                fn.restype = res
+            _lib = lib
+    return _lib
+
+
+class NrnnError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {load().nrnn_status_string(status).decode()} ({status})")
+
+
+class NewtonDivergenceError(NrnnError):
+    """max|F(H^(K))| above residual_fail (or not finite); H and rho are attached."""
+
+    def __init__(self, status, what, H=None, residual=None):
+        super().__init__(status, what)
+        self.H = H
+        self.residual = residual
+
+
+class AgreementError(AssertionError):
+    pass
+
+
+def _raise(status: int, what: str, **kw):
+    if status == OK:
+        return
+    if status == ERR_DIVERGED:
+        raise NewtonDivergenceError(status, what, **kw)
+    if status == ERR_UNSUPPORTED:
+        raise TypeError(f"{what}: {load().nrnn_status_string(status).decode()}")
+    if status in (ERR_INVALID_ARG, ERR_CU_SEQLENS):
+        raise ValueError(f"{what}: {load().nrnn_status_string(status).decode()}")
+    raise NrnnError(status, what)
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return F32
+    if t.dtype == torch.bfloat16:
+        return BF16
+    raise TypeError(f"unsupported dtype {t.dtype}; use float32 or bfloat16")
+
+
+def _stream(device) -> int:
+    return torch.cuda.current_stream(device).cuda_stream
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _device_tensor(t: torch.Tensor, what: str) -> torch.Tensor:
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError(f"{what} must be a CUDA tensor")
+    return t.contiguous()   # strided views are copied (shapes_layout: one extra copy)
+
+
+def params_tensor(params, d_h: int, device) -> torch.Tensor:
+    """(6, d_h) fp32 device tensor from a dict (a_z, a_r, a_c, b_z, b_r, b_c) or array."""
+    if isinstance(params, dict):
+        rows = [torch.as_tensor(np.asarray(params[k]) if not isinstance(params[k], torch.Tensor)
+                                else params[k]) for k in GATE_ORDER]
+        p = torch.stack([r.to(torch.float32).reshape(-1).cpu() for r in rows])
+    else:
+        p = torch.as_tensor(params).to(torch.float32)
+    if tuple(p.shape) != (6, d_h):
+        raise ValueError(f"params must have shape (6, {d_h}), got {tuple(p.shape)}")
+    return p.to(device).contiguous()
+
+
+def validate_cu_seqlens(cu_seqlens, N: int) -> np.ndarray:
+    """Host check of a cu_seqlens array (S+1 offsets, 0 .. N, non-decreasing)."""
+    cu = cu_seqlens.detach().cpu().numpy() if isinstance(cu_seqlens, torch.Tensor) else np.asarray(cu_seqlens)
+    if cu.ndim != 1 or cu.size < 2:
+        raise ValueError("cu_seqlens must be 1-D with at least 2 entries")
+    if cu.min() < np.iinfo(np.int32).min or cu.max() > np.iinfo(np.int32).max:
+        raise ValueError("cu_seqlens does not fit in int32")
+    cu32 = np.ascontiguousarray(cu, dtype=np.int32)
+    st = load().nrnn_validate_cu_seqlens(cu32.ctypes.data_as(ctypes.c_void_p), cu32.size - 1, int(N))
+    _raise(st, "validate_cu_seqlens")
+    return cu32
+
+
+def _cu_device(cu_seqlens, B, T, device):
+    if cu_seqlens is None:
+        return None, 0
+    if B != 1:
+        raise ValueError("cu_seqlens requires batch 1 (x of shape (1, N, d))")
+    cu32 = validate_cu_seqlens(cu_seqlens, T)
+    return torch.from_numpy(cu32).to(device), cu32.size - 1
+
+
+def workspace_bytes(B, T, d_h, dtype=torch.float32, K=3, algo="auto") -> int:
+    code = F32 if dtype == torch.float32 else BF16
+    return int(load().nrnn_newton_workspace_bytes(B, T, d_h, code, K, ALGOS[algo]))
+
+
+def newton_forward(preact: torch.Tensor, params, cu_seqlens=None, K: int = 3,
+                   residual_fail: float = 1.0, algo: str = "auto", check: bool = True,
+                   out: torch.Tensor | None = None, workspace: torch.Tensor | None = None):
+    """Parallel Newton forward.  preact (B, T, 3 d_h) float32/bfloat16 CUDA tensor.
+
+    Returns (H, residual): H (B, T, d_h) in preact's dtype and residual, a
+    0-dim float32 CUDA tensor holding max|F(H^(K))|.  With check=True the call
+    synchronises and raises NewtonDivergenceError if the residual exceeds
+    residual_fail (the pages' runtime gate); with check=False nothing syncs."""
+    lib = load()
+    preact = _device_tensor(preact, "preact")
+    if preact.dim() != 3 or preact.shape[2] % 3:
+        raise ValueError("preact must have shape (B, T, 3 d_h)")
+    B, T, d_h = preact.shape[0], preact.shape[1], preact.shape[2] // 3
+    code = _dtype_code(preact)
+    dev = preact.device
+    prm = params_tensor(params, d_h, dev)
+    cu, S = _cu_device(cu_seqlens, B, T, dev)
+    H = out if out is not None else torch.empty((B, T, d_h), dtype=preact.dtype, device=dev)
+    if tuple(H.shape) != (B, T, d_h) or H.dtype != preact.dtype or not H.is_contiguous():
+        raise ValueError("out has the wrong shape, dtype or layout")
+    rho = torch.empty((), dtype=torch.float32, device=dev)
+    nbytes = lib.nrnn_newton_workspace_bytes(B, T, d_h, code, int(K), ALGOS[algo])
+    if nbytes == 0:
+        raise ValueError("invalid shape, K or algo")
+    if workspace is None or workspace.numel() < nbytes:
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    host = ctypes.c_float(0.0) if check else None
+    with torch.cuda.device(dev):
+        st = lib.nrnn_newton_forward(_ptr(preact), code, _ptr(prm), B, T, d_h, _ptr(cu), S, int(K),
+                                     float(residual_fail), ALGOS[algo], _ptr(H), _ptr(rho),
+                                     ctypes.byref(host) if host is not None else None,
+                                     _ptr(workspace), workspace.numel(), _stream(dev))
+    _raise(st, "newton_forward", H=H, residual=(host.value if host is not None else None))
+    return H, rho
+
+
+def sequential_forward(preact: torch.Tensor, params, cu_seqlens=None,
+                       out: torch.Tensor | None = None) -> torch.Tensor:
+    """Sequential unroll on the GPU (one thread per row/segment and unit)."""
+    lib = load()
+    preact = _device_tensor(preact, "preact")
+    if preact.dim() != 3 or preact.shape[2] % 3:
+        raise ValueError("preact must have shape (B, T, 3 d_h)")
+    B, T, d_h = preact.shape[0], preact.shape[1], preact.shape[2] // 3
+    dev = preact.device
+    prm = params_tensor(params, d_h, dev)
+    cu, S = _cu_device(cu_seqlens, B, T, dev)
+    H = out if out is not None else torch.empty((B, T, d_h), dtype=preact.dtype, device=dev)
+    with torch.cuda.device(dev):
+        st = lib.nrnn_sequential_forward(_ptr(preact), _dtype_code(preact), _ptr(prm), B, T, d_h,
+                                         _ptr(cu), S, _ptr(H), _stream(dev))
+    _raise(st, "sequential_forward")
+    return H
+
+
+def residual(preact: torch.Tensor, params, G: torch.Tensor, cu_seqlens=None) -> torch.Tensor:
+    """max|F(G)| of a trajectory G (B, T, d_h) as a 0-dim CUDA tensor."""
+    lib = load()
+    preact = _device_tensor(preact, "preact")
+    G = _device_tensor(G, "G")
+    B, T, d_h = preact.shape[0], preact.shape[1], preact.shape[2] // 3
+    if tuple(G.shape) != (B, T, d_h) or G.dtype != preact.dtype:
+        raise ValueError("G must match preact's (B, T, d_h) and dtype")
+    dev = preact.device
+    prm = params_tensor(params, d_h, dev)
+    cu, S = _cu_device(cu_seqlens, B, T, dev)
+    rho = torch.empty((), dtype=torch.float32, device=dev)
+    with torch.cuda.device(dev):
+        st = lib.nrnn_residual(_ptr(preact), _dtype_code(preact), _ptr(prm), B, T, d_h, _ptr(cu),
+                               S, _ptr(G), _ptr(rho), _stream(dev))
+    _raise(st, "residual")
+    return rho
+
+
+def input_projection(x: torch.Tensor, W_x: torch.Tensor, out: torch.Tensor | None = None):
+    """P = x W_x^T: x (..., d_in), W_x (3 d_h, d_in) -> (..., 3 d_h), same dtype."""
+    lib = load()
+    x = _device_tensor(x, "x")
+    W_x = _device_tensor(W_x, "W_x")
+    if x.dtype != W_x.dtype:
+        raise TypeError("x and W_x must share a dtype")
+    d_in = x.shape[-1]
+    n_out = W_x.shape[0]
+    if W_x.shape[1] != d_in or n_out % 3:
+        raise ValueError("W_x must have shape (3 d_h, d_in)")
+    rows = x.numel() // d_in
+    P = out if out is not None else torch.empty((*x.shape[:-1], n_out), dtype=x.dtype, device=x.device)
+    with torch.cuda.device(x.device):
+        st = lib.nrnn_input_projection(_ptr(x), _ptr(W_x), _dtype_code(x), rows, d_in, n_out // 3,
+                                       _ptr(P), _stream(x.device))
+    _raise(st, "input_projection")
+    return P
+
+
+def head_mask(cu_seqlens, N: int, device="cuda") -> torch.Tensor:
+    """Segment-head mask as computed on the device by the Newton kernels' routine."""
+    lib = load()
+    cu32 = validate_cu_seqlens(cu_seqlens, N)
+    cu = torch.from_numpy(cu32).to(device)
+    mask = torch.empty(N, dtype=torch.uint8, device=device)
+    st = lib.nrnn_debug_head_mask(_ptr(cu), cu32.size - 1, N, _ptr(mask), _stream(torch.device(device)))
+    _raise(st, "head_mask")
+    return mask
+
+
+def bounded_wait(flag: torch.Tensor, wait_ns: int) -> int:
+    """Runs the device bounded wait on flag (uint32/int32 CUDA tensor); 1 = seen, 2 = gave up."""
+    lib = load()
+    res = torch.zeros(1, dtype=torch.int32, device=flag.device)
+    st = lib.nrnn_debug_bounded_wait(_ptr(flag), int(wait_ns), _ptr(res), _stream(flag.device))
+    _raise(st, "bounded_wait")
+    return int(res.item())
+
+
+def set_wait_limit_ns(ns: int) -> int:
+    return int(load().nrnn_set_wait_limit_ns(int(ns)))
+
+
+@dataclass
+class AgreementReport:
+    ok: bool
+    max_abs: float
+    atol: float
+    K: int
+    residual: float
+    dtype: str
+    extra: dict = field(default_factory=dict)
+
+    def to_dict(self):
+        return {"ok": self.ok, "max_abs": self.max_abs, "atol": self.atol, "K": self.K,
+                "residual": self.residual, "dtype": self.dtype, **self.extra}
+
+
+def default_agreement_atol(dtype) -> float:
+    return 1e-4 if dtype == torch.float32 else 5e-2
+
+
+def verify_agreement(preact, params, K: int = 3, cu_seqlens=None, atol: float | None = None,
+                     raise_on_fail: bool = False, algo: str = "auto") -> AgreementReport:
+    """Runs Newton and the sequential unroll on the same batch and compares them
+    by max-abs (numerics contract, "Four echelons / 3. Opt-in oracle")."""
+    Hn, rho = newton_forward(preact, params, cu_seqlens=cu_seqlens, K=K, algo=algo, check=False)
+    Hs = sequential_forward(preact, params, cu_seqlens=cu_seqlens)
+    tol = default_agreement_atol(preact.dtype) if atol is None else float(atol)
+    err = float((Hn.float() - Hs.float()).abs().max().item()) if Hn.numel() else 0.0
+    rep = AgreementReport(err <= tol, err, tol, int(K), float(rho.item()), str(preact.dtype))
+    if raise_on_fail and not rep.ok:
+        raise AgreementError(f"Newton vs sequential max_abs {err:.3e} > atol {tol:.1e}")
+    return rep

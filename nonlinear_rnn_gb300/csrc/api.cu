@@ -1,0 +1,284 @@
+// C ABI entry points (declared in include/nrnn.h): argument checks, workspace
+// layout, TMA descriptors and the launch sequence of each call.
+#include <atomic>
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include <cudaTypedefs.h>
+
+#include "../../include/nrnn.h"
+#include "nrnn_internal.h"
+
+using namespace nrnn;
+
+namespace {
+
+std::atomic<uint64_t> g_wait_ns{2000000000ull};
+constexpr int MAX_K = 64;
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+size_t elem_size(int dtype) { return dtype == NRNN_BF16 ? 2 : 4; }
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Workspace: [flags K x n_tiles u32 | counters (K+1) u32 | error u32] zeroed per
+// call, then [slots K x n_tiles x 32 u64], then (per-iteration) one H buffer.
+SyncLayout layout(int64_t B, int64_t T, int64_t d_h, int dtype, int K, bool fused) {
+    SyncLayout s{};
+    const int64_t n_ut = (d_h + TILE_U - 1) / TILE_U;
+    const int64_t n_chunks = (T + NEWTON_L - 1) / NEWTON_L;
+    const int64_t kk = K > 0 ? K : 1;
+    s.n_tiles = B * n_ut * n_chunks;
+    s.flags_off = 0;
+    s.counters_off = align_up(s.flags_off + sizeof(uint32_t) * kk * s.n_tiles, 16);
+    s.error_off = s.counters_off + sizeof(uint32_t) * (kk + 1);
+    s.zero_bytes = align_up(s.error_off + sizeof(uint32_t), 16);
+    s.slots_off = align_up(s.zero_bytes, 256);
+    size_t end = s.slots_off + sizeof(unsigned long long) * 32 * kk * s.n_tiles;
+    s.hbuf_off = align_up(end, 256);
+    if (!fused && K > 1) end = s.hbuf_off + elem_size(dtype) * B * T * d_h;
+    s.total = align_up(end, 256);
+    return s;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// 3-D map over a (B, T, width) row-major array with a (TILE_U x NEWTON_L x 1) box.
+bool make_map(CUtensorMap *m, const void *base, int dtype, int64_t width, int64_t T, int64_t B) {
+    auto fn = encode_fn();
+    if (fn == nullptr) return false;
+    const size_t es = elem_size(dtype);
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(width), static_cast<cuuint64_t>(T),
+                          static_cast<cuuint64_t>(B)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(width * es),
+                             static_cast<cuuint64_t>(width * es * T)};
+    cuuint32_t box[3] = {TILE_U, NEWTON_L, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    const CUresult r = fn(m, dtype == NRNN_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+                          3, const_cast<void *>(base), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+int check_common(const void *preact, int dtype, const float *params, int64_t B, int64_t T,
+                 int64_t d_h, const int32_t *cu, int64_t S) {
+    if (dtype != NRNN_F32 && dtype != NRNN_BF16) return NRNN_ERR_INVALID_ARG;
+    if (B < 0 || T < 0 || d_h <= 0 || S < 0) return NRNN_ERR_INVALID_ARG;
+    if (B * T > 0 && (preact == nullptr || params == nullptr)) return NRNN_ERR_INVALID_ARG;
+    if (B > INT32_MAX || T > INT32_MAX || d_h > (1 << 24) || S > INT32_MAX - 1)
+        return NRNN_ERR_UNSUPPORTED;
+    if (d_h % 8 != 0) return NRNN_ERR_UNSUPPORTED;
+    if (cu != nullptr && (B != 1 || S < 1)) return NRNN_ERR_CU_SEQLENS;
+    if (preact != nullptr && !aligned16(preact)) return NRNN_ERR_INVALID_ARG;
+    return NRNN_OK;
+}
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? NRNN_OK : NRNN_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+const char *nrnn_status_string(int status) {
+    switch (status) {
+        case NRNN_OK: return "ok";
+        case NRNN_ERR_INVALID_ARG: return "invalid argument";
+        case NRNN_ERR_CU_SEQLENS: return "invalid cu_seqlens";
+        case NRNN_ERR_UNSUPPORTED: return "unsupported configuration";
+        case NRNN_ERR_CUDA: return "CUDA error";
+        case NRNN_ERR_DIVERGED: return "Newton residual above residual_fail (diverged)";
+        case NRNN_ERR_TIMEOUT: return "bounded device wait timed out";
+        case NRNN_ERR_WORKSPACE: return "workspace missing or too small";
+        default: return "unknown status";
+    }
+}
+
+int nrnn_version(void) { return 100; }
+
+uint64_t nrnn_set_wait_limit_ns(uint64_t ns) { return g_wait_ns.exchange(ns); }
+
+int nrnn_validate_cu_seqlens(const int32_t *cu_host, int64_t num_segments, int64_t N) {
+    if (cu_host == nullptr || num_segments < 0 || N < 0) return NRNN_ERR_INVALID_ARG;
+    if (num_segments < 1) return NRNN_ERR_CU_SEQLENS;
+    if (cu_host[0] != 0) return NRNN_ERR_CU_SEQLENS;
+    for (int64_t i = 0; i < num_segments; ++i)
+        if (cu_host[i + 1] < cu_host[i]) return NRNN_ERR_CU_SEQLENS;
+    if (static_cast<int64_t>(cu_host[num_segments]) != N) return NRNN_ERR_CU_SEQLENS;
+    return NRNN_OK;
+}
+
+size_t nrnn_newton_workspace_bytes(int64_t B, int64_t T, int64_t d_h, int dtype, int K,
+                                   int algo) {
+    if (B < 0 || T < 0 || d_h <= 0 || K < 0 || K > MAX_K) return 0;
+    if (dtype != NRNN_F32 && dtype != NRNN_BF16) return 0;
+    if (algo < NRNN_ALGO_AUTO || algo > NRNN_ALGO_FUSED) return 0;
+    return layout(B, T, d_h, dtype, K, algo != NRNN_ALGO_PER_ITER).total;
+}
+
+int nrnn_newton_forward(const void *preact, int dtype, const float *params, int64_t B,
+                        int64_t T, int64_t d_h, const int32_t *cu_seqlens,
+                        int64_t num_segments, int K, float residual_fail, int algo,
+                        void *H_out, float *residual_dev, float *residual_host,
+                        void *workspace, size_t ws_bytes, void *stream_) {
+    int st = check_common(preact, dtype, params, B, T, d_h, cu_seqlens, num_segments);
+    if (st != NRNN_OK) return st;
+    if (K < 0 || K > MAX_K || residual_dev == nullptr) return NRNN_ERR_INVALID_ARG;
+    if (algo < NRNN_ALGO_AUTO || algo > NRNN_ALGO_FUSED) return NRNN_ERR_INVALID_ARG;
+    if (B * T > 0 && (H_out == nullptr || !aligned16(H_out))) return NRNN_ERR_INVALID_ARG;
+    const bool fused = algo != NRNN_ALGO_PER_ITER;
+    const SyncLayout ly = layout(B, T, d_h, dtype, K, fused);
+    if (workspace == nullptr || ws_bytes < ly.total ||
+        (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+        return NRNN_ERR_WORKSPACE;
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+    unsigned char *ws = static_cast<unsigned char *>(workspace);
+    uint32_t *res_bits = reinterpret_cast<uint32_t *>(residual_dev);
+    uint32_t *err = reinterpret_cast<uint32_t *>(ws + ly.error_off);
+    const int S = static_cast<int>(cu_seqlens ? num_segments : 0);
+
+    cudaError_t e = cudaMemsetAsync(ws, 0, ly.zero_bytes, stream);
+    if (e == cudaSuccess) e = cudaMemsetAsync(residual_dev, 0, sizeof(float), stream);
+    if (e != cudaSuccess) return NRNN_ERR_CUDA;
+
+    if (B * T > 0) {
+        if (K == 0) {
+            e = cudaMemsetAsync(H_out, 0, elem_size(dtype) * B * T * d_h, stream);
+            if (e == cudaSuccess)
+                e = launch_residual(dtype, preact, params, nullptr, static_cast<int>(B),
+                                    static_cast<int>(T), static_cast<int>(d_h), cu_seqlens, S,
+                                    res_bits, stream);
+            if (e != cudaSuccess) return NRNN_ERR_CUDA;
+        } else {
+            CUtensorMap tmP;
+            if (!make_map(&tmP, preact, dtype, 3 * d_h, T, B)) return NRNN_ERR_CUDA;
+            NewtonArgs a{};
+            a.params = params;
+            a.cu = cu_seqlens;
+            a.S = S;
+            a.B = static_cast<int>(B);
+            a.T = static_cast<int>(T);
+            a.d_h = static_cast<int>(d_h);
+            a.n_ut = static_cast<int>((d_h + TILE_U - 1) / TILE_U);
+            a.n_chunks = static_cast<int>((T + NEWTON_L - 1) / NEWTON_L);
+            a.flags = reinterpret_cast<uint32_t *>(ws + ly.flags_off);
+            a.slots = reinterpret_cast<unsigned long long *>(ws + ly.slots_off);
+            a.residual_bits = res_bits;
+            a.error = err;
+            a.wait_ns = g_wait_ns.load();
+            uint32_t *counters = reinterpret_cast<uint32_t *>(ws + ly.counters_off);
+            if (fused) {
+                a.H_prev = nullptr;
+                a.H_next = H_out;
+                a.k_first = 1;
+                a.k_last = K;
+                a.last = 1;
+                a.ticket = counters;
+                e = launch_newton(dtype, true, tmP, tmP, a, ly.n_tiles, stream);
+                if (e != cudaSuccess) return NRNN_ERR_CUDA;
+            } else {
+                void *hbuf = ws + ly.hbuf_off;
+                const void *prev = nullptr;
+                for (int k = 1; k <= K; ++k) {
+                    // iteration K lands in H_out; earlier ones alternate with hbuf
+                    void *dst = ((K - k) % 2 == 0) ? H_out : hbuf;
+                    CUtensorMap tmH = tmP;
+                    if (prev != nullptr && !make_map(&tmH, prev, dtype, d_h, T, B))
+                        return NRNN_ERR_CUDA;
+                    a.H_prev = prev;
+                    a.H_next = dst;
+                    a.k_first = a.k_last = k;
+                    a.last = (k == K) ? 1 : 0;
+                    a.ticket = counters + k;
+                    e = launch_newton(dtype, false, tmP, tmH, a, ly.n_tiles, stream);
+                    if (e != cudaSuccess) return NRNN_ERR_CUDA;
+                    prev = dst;
+                }
+            }
+        }
+    }
+    if (residual_host == nullptr) return NRNN_OK;
+    uint32_t err_host = 0;
+    e = cudaMemcpyAsync(residual_host, residual_dev, sizeof(float), cudaMemcpyDeviceToHost, stream);
+    if (e == cudaSuccess)
+        e = cudaMemcpyAsync(&err_host, err, sizeof(uint32_t), cudaMemcpyDeviceToHost, stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) return NRNN_ERR_CUDA;
+    if (err_host != 0) return NRNN_ERR_TIMEOUT;
+    const float rho = *residual_host;
+    if (!std::isfinite(rho) || rho > residual_fail) return NRNN_ERR_DIVERGED;
+    return NRNN_OK;
+}
+
+int nrnn_sequential_forward(const void *preact, int dtype, const float *params, int64_t B,
+                            int64_t T, int64_t d_h, const int32_t *cu_seqlens,
+                            int64_t num_segments, void *H_out, void *stream) {
+    int st = check_common(preact, dtype, params, B, T, d_h, cu_seqlens, num_segments);
+    if (st != NRNN_OK) return st;
+    if (B * T > 0 && H_out == nullptr) return NRNN_ERR_INVALID_ARG;
+    if (B * T == 0) return NRNN_OK;
+    return cuda_status(launch_sequential(dtype, preact, params, static_cast<int>(B),
+                                         static_cast<int>(T), static_cast<int>(d_h), cu_seqlens,
+                                         static_cast<int>(cu_seqlens ? num_segments : 0), H_out,
+                                         static_cast<cudaStream_t>(stream)));
+}
+
+int nrnn_residual(const void *preact, int dtype, const float *params, int64_t B, int64_t T,
+                  int64_t d_h, const int32_t *cu_seqlens, int64_t num_segments, const void *G,
+                  float *residual_dev, void *stream_) {
+    int st = check_common(preact, dtype, params, B, T, d_h, cu_seqlens, num_segments);
+    if (st != NRNN_OK) return st;
+    if (residual_dev == nullptr || (B * T > 0 && G == nullptr)) return NRNN_ERR_INVALID_ARG;
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+    if (cudaMemsetAsync(residual_dev, 0, sizeof(float), stream) != cudaSuccess) return NRNN_ERR_CUDA;
+    if (B * T == 0) return NRNN_OK;
+    return cuda_status(launch_residual(dtype, preact, params, G, static_cast<int>(B),
+                                       static_cast<int>(T), static_cast<int>(d_h), cu_seqlens,
+                                       static_cast<int>(cu_seqlens ? num_segments : 0),
+                                       reinterpret_cast<uint32_t *>(residual_dev), stream));
+}
+
+int nrnn_input_projection(const void *x, const void *W_x, int dtype, int64_t rows, int64_t d_in,
+                          int64_t d_h, void *preact, void *stream) {
+    if (dtype != NRNN_F32 && dtype != NRNN_BF16) return NRNN_ERR_INVALID_ARG;
+    if (rows < 0 || d_in <= 0 || d_h <= 0) return NRNN_ERR_INVALID_ARG;
+    if (rows > 0 && (x == nullptr || W_x == nullptr || preact == nullptr)) return NRNN_ERR_INVALID_ARG;
+    if (d_in % 8 != 0 || d_h % 8 != 0 || d_in > INT32_MAX || 3 * d_h > INT32_MAX)
+        return NRNN_ERR_UNSUPPORTED;
+    return cuda_status(launch_projection(dtype, x, W_x, rows, static_cast<int>(d_in),
+                                         static_cast<int>(3 * d_h), preact,
+                                         static_cast<cudaStream_t>(stream)));
+}
+
+int nrnn_debug_head_mask(const int32_t *cu_seqlens, int64_t num_segments, int64_t N,
+                         uint8_t *mask_dev, void *stream) {
+    if (N < 0 || num_segments < 0 || (N > 0 && mask_dev == nullptr)) return NRNN_ERR_INVALID_ARG;
+    if (N == 0) return NRNN_OK;
+    if (num_segments > INT32_MAX - 1) return NRNN_ERR_UNSUPPORTED;
+    return cuda_status(launch_head_mask(cu_seqlens, static_cast<int>(num_segments), N, mask_dev,
+                                        static_cast<cudaStream_t>(stream)));
+}
+
+int nrnn_debug_bounded_wait(const uint32_t *flag_dev, uint64_t wait_ns, uint32_t *result_dev,
+                            void *stream) {
+    if (flag_dev == nullptr || result_dev == nullptr) return NRNN_ERR_INVALID_ARG;
+    return cuda_status(
+        launch_bounded_wait(flag_dev, wait_ns, result_dev, static_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

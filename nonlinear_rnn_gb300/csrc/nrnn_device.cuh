@@ -1,0 +1,220 @@
+// Device helpers for the diagonal-GRU Newton kernels (sm_103a).
+//
+// Cell of ParaGRU(mix='diag') (pararnn-torch; equations as stated for its
+// diag-GRU benches): z = sig(P_z + a_z h + b_z), r = sig(P_r + a_r h + b_r),
+// c = tanh(P_c + a_c (r h) + b_c), f = (1 - z) h + z c.  Its derivative with
+// respect to h (chain rule) is
+//   J = (1 - z) + z (1 - z) a_z (c - h) + z (1 - c^2) a_c (r + h r (1 - r) a_r).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace nrnn {
+
+constexpr unsigned FULL_MASK = 0xffffffffu;
+
+// ---------------------------------------------------------------- storage types
+__device__ __forceinline__ float to_f32(float v) { return v; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 v) { return __bfloat162float(v); }
+
+template <typename TS> __device__ __forceinline__ TS from_f32(float v);
+template <> __device__ __forceinline__ float from_f32<float>(float v) { return v; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float v) {
+    return __float2bfloat16_rn(v);
+}
+// value of v after a round trip through the storage type
+template <typename TS> __device__ __forceinline__ float round_to(float v) {
+    return to_f32(from_f32<TS>(v));
+}
+
+// ------------------------------------------------------------- PTX primitives
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+__device__ __forceinline__ float rcp_approx(float x) {
+    float y;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t *p) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_release_u32(uint32_t *p, uint32_t v) {
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long long *p) {
+    unsigned long long v;
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_relaxed_u64(unsigned long long *p, unsigned long long v) {
+    asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+// mbarrier + TMA (cp.async.bulk.tensor) for one CTA
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+                 : "memory");
+}
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+__device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, uint64_t *bar,
+                                            int x, int y, int z) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes "
+        "[%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z)
+        : "memory");
+}
+__device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+// Bounded wait on an mbarrier phase; sets *error bit 2 and returns false on timeout.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity,
+                                                  uint64_t limit_ns, uint32_t *error) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (globaltimer_ns() - t0 > limit_ns) {
+            atomicOr(error, 2u);
+            return false;
+        }
+    }
+    return true;
+}
+
+// ------------------------------------------------------------------ the cell
+struct UnitParams {
+    float a_z, a_r, a_c, b_z, b_r, b_c;
+};
+
+__device__ __forceinline__ UnitParams load_unit_params(const float *params, int d_h, int u,
+                                                       bool valid) {
+    UnitParams p{0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    if (valid) {
+        p.a_z = __ldg(params + 0 * d_h + u);
+        p.a_r = __ldg(params + 1 * d_h + u);
+        p.a_c = __ldg(params + 2 * d_h + u);
+        p.b_z = __ldg(params + 3 * d_h + u);
+        p.b_r = __ldg(params + 4 * d_h + u);
+        p.b_c = __ldg(params + 5 * d_h + u);
+    }
+    return p;
+}
+
+constexpr float LOG2E = 1.4426950408889634f;
+
+// logistic sigmoid: 1 / (1 + 2^(-x log2 e)); saturates to exactly 0 / 1
+__device__ __forceinline__ float sigmoid_f(float x) {
+    return rcp_approx(1.0f + ex2_approx(-LOG2E * x));
+}
+// tanh(x) = 1 - 2 / (1 + e^(2x)); saturates to exactly -1 / +1
+__device__ __forceinline__ float tanh_f(float x) {
+    return fmaf(-2.0f, rcp_approx(1.0f + ex2_approx((2.0f * LOG2E) * x)), 1.0f);
+}
+
+// f(h, P) and df/dh
+__device__ __forceinline__ void cell_fj(float h, float pz, float pr, float pc,
+                                        const UnitParams &p, float &f, float &J) {
+    const float z = sigmoid_f(fmaf(p.a_z, h, pz + p.b_z));
+    const float r = sigmoid_f(fmaf(p.a_r, h, pr + p.b_r));
+    const float c = tanh_f(fmaf(p.a_c, r * h, pc + p.b_c));
+    const float cmh = c - h;
+    f = fmaf(z, cmh, h);
+    const float omz = 1.0f - z;
+    const float dz = z * omz * p.a_z;               // dz/dh
+    const float dq = fmaf(h, fmaf(-r, r, r) * p.a_r, r);  // d(r h)/dh
+    const float dc = fmaf(-c, c, 1.0f) * p.a_c * dq;      // dc/dh
+    J = fmaf(dz, cmh, fmaf(z, dc, omz));
+}
+
+// f(h, P) only
+__device__ __forceinline__ float cell_f(float h, float pz, float pr, float pc,
+                                        const UnitParams &p) {
+    const float z = sigmoid_f(fmaf(p.a_z, h, pz + p.b_z));
+    const float r = sigmoid_f(fmaf(p.a_r, h, pr + p.b_r));
+    const float c = tanh_f(fmaf(p.a_c, r * h, pc + p.b_c));
+    return fmaf(z, c - h, h);
+}
+
+// |F| for the residual gate; NaN counts as +inf
+__device__ __forceinline__ float abs_residual(float F) {
+    const float a = fabsf(F);
+    return (a <= 3.402823466e38f) ? a : __int_as_float(0x7f800000);
+}
+
+// ----------------------------------------------------------- segment heads
+// Sets bit (t - t0) of bits[] for every head t in [t0, t0 + len): t = 0, or
+// t = cu[i] with cu[i] < cu[i + 1] (shapes_layout page: segment heads of a
+// cu_seqlens pack use J = 0).  bits[] must be zeroed by the caller.  Stays
+// inside cu[0 .. S] and inside bits[] for any contents of cu.
+__device__ __forceinline__ void mark_heads(const int32_t *cu, int S, int64_t t0, int len,
+                                           uint32_t *bits) {
+    if (t0 == 0 && len > 0) bits[0] |= 1u;
+    if (cu == nullptr || S <= 0) return;
+    int lo = 0, hi = S + 1;  // first i in [0, S] with cu[i] >= t0
+    while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (static_cast<int64_t>(__ldg(cu + mid)) < t0) lo = mid + 1;
+        else hi = mid;
+    }
+    for (int i = lo; i < S; ++i) {
+        const int64_t s = __ldg(cu + i);
+        if (s >= t0 + len) break;
+        if (s >= t0 && s < static_cast<int64_t>(__ldg(cu + i + 1))) {
+            const int o = static_cast<int>(s - t0);
+            bits[o >> 5] |= 1u << (o & 31);
+        }
+    }
+}
+
+__device__ __forceinline__ bool head_bit(const uint32_t *bits, int r) {
+    return (bits[r >> 5] >> (r & 31)) & 1u;
+}
+
+// pack / unpack an affine pair (A, b) into one 64-bit word (single-copy atomic)
+__device__ __forceinline__ unsigned long long pack_pair(float A, float b) {
+    return (static_cast<unsigned long long>(__float_as_uint(b)) << 32) | __float_as_uint(A);
+}
+__device__ __forceinline__ float pair_A(unsigned long long v) {
+    return __uint_as_float(static_cast<uint32_t>(v));
+}
+__device__ __forceinline__ float pair_b(unsigned long long v) {
+    return __uint_as_float(static_cast<uint32_t>(v >> 32));
+}
+
+}  // namespace nrnn

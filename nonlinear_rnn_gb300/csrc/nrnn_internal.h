@@ -1,0 +1,64 @@
+// Internal launch interface between the C ABI (api.cu) and the kernels.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace nrnn {
+
+// Tile of one Newton CTA: 32 hidden units (one per lane) x L time steps,
+// L = NW warps x SEG steps per warp.
+constexpr int TILE_U = 32;
+constexpr int NEWTON_NW = 8;
+constexpr int NEWTON_SEG = 16;
+constexpr int NEWTON_L = NEWTON_NW * NEWTON_SEG;
+
+struct NewtonArgs {
+    const void *H_prev;           // (B, T, d_h) storage type; null when H^(k-1) = 0
+    void *H_next;                 // (B, T, d_h) storage type
+    const float *params;          // (6, d_h)
+    const int32_t *cu;            // null or (S + 1)
+    int S;
+    int B, T, d_h;
+    int n_ut, n_chunks;           // unit tiles, time chunks
+    int k_first, k_last;          // iterations this launch runs (1-based, inclusive)
+    int last;                     // this launch ends with H^(K): compute the residual
+    uint32_t *flags;              // [K][n_tiles] look-back status (0 = empty)
+    unsigned long long *slots;    // [K][n_tiles][32] packed (A, b)
+    uint32_t *ticket;             // this launch's CTA ticket counter
+    uint32_t *residual_bits;      // float bits of rho (atomicMax), or null
+    uint32_t *error;              // error word (bit 0: look-back timeout, bit 1: TMA timeout)
+    unsigned long long wait_ns;   // limit of every bounded wait
+};
+
+// Look-back status region of the workspace for one call.
+struct SyncLayout {
+    size_t flags_off, counters_off, error_off, zero_bytes;  // [0, zero_bytes) is memset to 0
+    size_t slots_off, hbuf_off, total;
+    int64_t n_tiles;
+};
+
+size_t newton_smem_bytes(int dtype, bool fused);
+
+cudaError_t launch_newton(int dtype, bool fused, const CUtensorMap &tmP, const CUtensorMap &tmH,
+                          const NewtonArgs &a, int64_t n_ctas, cudaStream_t stream);
+
+cudaError_t launch_residual(int dtype, const void *P, const float *params, const void *G,
+                            int B, int T, int d_h, const int32_t *cu, int S,
+                            uint32_t *residual_bits, cudaStream_t stream);
+
+cudaError_t launch_sequential(int dtype, const void *P, const float *params, int B, int T,
+                              int d_h, const int32_t *cu, int S, void *H, cudaStream_t stream);
+
+cudaError_t launch_head_mask(const int32_t *cu, int S, int64_t N, uint8_t *mask,
+                             cudaStream_t stream);
+
+cudaError_t launch_bounded_wait(const uint32_t *flag, uint64_t wait_ns, uint32_t *result,
+                                cudaStream_t stream);
+
+cudaError_t launch_projection(int dtype, const void *x, const void *W, int64_t rows, int d_in,
+                              int n_out, void *P, cudaStream_t stream);
+
+}  // namespace nrnn

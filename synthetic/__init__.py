@@ -220,3 +220,71 @@ def direct_preact(w: Workload, scale: float = 1.0 / math.sqrt(3.0)) -> np.ndarra
     if w.dtype == "bf16":
         p = round_bf16(p)
     return p
+
+
+# ------------------------------------------------------------------------
+# Preactivations drawn directly, reproducible bit for bit on any device.
+#
+# For kernel-level runs at full size the preactivation buffer itself is the
+# input.  P ~ U(-1, 1) has the variance (1/3) of x W_x^T with x ~ N(0, 1) and
+# W_x ~ U(+-1/sqrt(d_in)).  The value at flat index i of the (B, T, 3 d_h)
+# buffer is 2 u_i - 1 with u_i the i-th uniform of stream STREAM_PREACT; the
+# computation is integer mixing, an exact scaling and one rounding to float32,
+# so torch on the GPU and numpy on the host produce identical values.  The
+# host side can therefore regenerate any sampled columns without the rest.
+# ------------------------------------------------------------------------
+def _as_i64(v: int) -> int:
+    v &= 0xFFFFFFFFFFFFFFFF
+    return v - (1 << 64) if v >= (1 << 63) else v
+
+
+def _torch_mix(z):
+    import torch
+    m30 = (1 << 34) - 1
+    m27 = (1 << 37) - 1
+    m31 = (1 << 33) - 1
+    z = (z ^ ((z >> 30) & m30)) * _as_i64(0xBF58476D1CE4E5B9)
+    z = (z ^ ((z >> 27) & m27)) * _as_i64(0x94D049BB133111EB)
+    return z ^ ((z >> 31) & m31)
+
+
+def preact_uniform_torch(w: Workload, device="cuda", dtype=None):
+    """Full (B, T, 3 d_h) preactivation buffer of U(-1, 1) draws as a torch tensor."""
+    import torch
+    n = w.B * w.T * 3 * w.d_h
+    key = _as_i64(int(_key(w.seed, STREAM_PREACT)))
+    out = torch.empty(n, dtype=torch.float32, device=device)
+    blk = 1 << 26
+    for o in range(0, n, blk):
+        m = min(blk, n - o)
+        ctr = torch.arange(o + 1, o + m + 1, dtype=torch.int64, device=device)
+        z = _torch_mix(ctr * _as_i64(int(GAMMA)) + key)
+        u = ((z >> 11) & ((1 << 53) - 1)).to(torch.float64) * (1.0 / 9007199254740992.0)
+        out[o:o + m] = (2.0 * u - 1.0).to(torch.float32)
+    out = out.reshape(w.B, w.T, 3 * w.d_h)
+    if dtype is None:
+        dtype = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+    return out.to(dtype)
+
+
+def preact_uniform_at(w: Workload, flat_index: np.ndarray) -> np.ndarray:
+    """Values of the same buffer at the given flat indices (numpy float32; for a
+    bf16 workload, rounded to bfloat16 values)."""
+    idx = np.asarray(flat_index, dtype=np.uint64)
+    key = _key(w.seed, STREAM_PREACT)
+    with np.errstate(over="ignore"):
+        z = _mix(key + (idx + np.uint64(1)) * GAMMA)
+    u = (z >> np.uint64(11)).astype(np.float64) * (1.0 / 9007199254740992.0)
+    p = (2.0 * u - 1.0).astype(np.float32)
+    return round_bf16(p) if w.dtype == "bf16" else p
+
+
+def preact_uniform_columns(w: Workload, units, rows=None) -> np.ndarray:
+    """(len(rows), T, 3 len(units)) slice of the buffer: all three gates of the
+    given hidden units, gate-major like the full buffer."""
+    units = np.asarray(units, dtype=np.int64)
+    rows = np.arange(w.B) if rows is None else np.asarray(rows, dtype=np.int64)
+    cols = np.concatenate([units, w.d_h + units, 2 * w.d_h + units])
+    t = np.arange(w.T, dtype=np.int64)
+    flat = ((rows[:, None, None] * w.T + t[None, :, None]) * (3 * w.d_h) + cols[None, None, :])
+    return preact_uniform_at(w, flat.reshape(-1)).reshape(len(rows), w.T, len(cols))

@@ -15,8 +15,8 @@ import synthetic as syn  # noqa: E402
 
 
 def tiny_case():
-    """B=2, T=12, d_h=3 rectangular batch and a 3-segment pack (N=12)."""
-    w = syn.small_workload(B=2, T=12, d_in=4, d_h=3, seed=101)
+    """B=2, T=12, d_h=8 rectangular batch and a 4-segment pack (N=12)."""
+    w = syn.small_workload(B=2, T=12, d_in=4, d_h=8, seed=101)
     P = syn.direct_preact(w)
     prm = syn.make_params(w)
     out = {

@@ -1,0 +1,92 @@
+"""Host-side checks of the C ABI: the library loads, exports every entry point
+the header declares, and its host logic (cu_seqlens rules, workspace sizes,
+status strings, argument checks) behaves as documented.  No GPU needed."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import nonlinear_rnn_gb300 as nr
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "nrnn.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(nrnn_\w+)\s*\(", src)))
+
+
+def test_header_symbols_are_exported_and_bound():
+    lib = nr.load()
+    names = _declared()
+    assert len(names) >= 10
+    for name in names:
+        assert hasattr(lib, name), name
+    assert sorted(nr.EXPORTED) == names
+
+
+def test_status_strings_and_version():
+    lib = nr.load()
+    assert lib.nrnn_version() >= 100
+    for code in range(0, -8, -1):
+        s = lib.nrnn_status_string(code).decode()
+        assert s and s != "unknown status"
+    assert lib.nrnn_status_string(-99).decode() == "unknown status"
+
+
+def _validate(cu, N):
+    cu = np.ascontiguousarray(cu, dtype=np.int32)
+    return nr.load().nrnn_validate_cu_seqlens(cu.ctypes.data_as(ctypes.c_void_p), cu.size - 1, N)
+
+
+def test_validate_cu_seqlens_rules():
+    assert _validate([0, 3, 3, 10], 10) == 0          # empty segment allowed
+    assert _validate([0, 10], 10) == 0
+    assert _validate([1, 3, 10], 10) == -2            # must start at 0
+    assert _validate([0, 5, 4, 10], 10) == -2         # decreasing
+    assert _validate([0, 3, 9], 10) == -2             # must end at N
+    assert _validate([0], 0) == -2                    # at least one segment
+    assert nr.load().nrnn_validate_cu_seqlens(None, 1, 1) == -1
+    with pytest.raises(ValueError):
+        nr.validate_cu_seqlens([0, 4, 2], 2)
+
+
+def test_workspace_bytes():
+    lib = nr.load()
+    f = lib.nrnn_newton_workspace_bytes
+    fused = f(8, 4096, 256, 0, 3, 2)
+    per = f(8, 4096, 256, 0, 3, 1)
+    # per-iteration keeps one extra H buffer (B*T*d_h*4 bytes)
+    assert per - fused >= 8 * 4096 * 256 * 4
+    assert f(8, 4096, 256, 0, 1, 1) < per               # K = 1 needs no H buffer
+    assert f(8, 4096, 256, 0, 3, 0) == fused            # auto = fused
+    assert f(8, 4096, 256, 0, 65, 2) == 0               # K above the limit
+    assert f(8, 4096, 256, 5, 3, 2) == 0                # bad dtype
+    assert fused % 256 == 0
+
+
+def test_forward_rejects_bad_arguments_before_any_launch():
+    lib = nr.load()
+    fake = ctypes.c_void_p(256)   # never dereferenced: checks fail first
+    res = ctypes.c_void_p(512)
+    args = dict(pre=fake, dtype=0, prm=fake, B=1, T=8, d=16, cu=None, S=0, K=3, fail=1.0, algo=0,
+                H=fake, rd=res, rh=None, ws=fake, wsb=1 << 20, st=None)
+
+    def call(**kw):
+        a = dict(args, **kw)
+        return lib.nrnn_newton_forward(a["pre"], a["dtype"], a["prm"], a["B"], a["T"], a["d"],
+                                       a["cu"], a["S"], a["K"], a["fail"], a["algo"], a["H"],
+                                       a["rd"], a["rh"], a["ws"], a["wsb"], a["st"])
+    assert call(dtype=7) == -1
+    assert call(d=12) == -3                       # d_h % 8 != 0
+    assert call(K=-1) == -1
+    assert call(K=65) == -1
+    assert call(algo=9) == -1
+    assert call(B=2, cu=fake, S=2) == -2          # packs need B == 1
+    assert call(wsb=16) == -7                     # workspace too small
+    assert call(ws=ctypes.c_void_p(256 + 16)) == -7   # workspace misaligned
+    assert call(pre=ctypes.c_void_p(260)) == -1   # preact misaligned
+    assert call(rd=None) == -1

@@ -1,0 +1,246 @@
+"""GPU parity of the CUDA path (called through the C ABI via the binding)
+against the float64 oracle, element by element on the same seeded inputs.
+
+Bars: fp32 storage max-abs <= 1e-4 (the pages' agreement tau); bf16 storage
+(fp32 math) <= 5e-2; head masks bit-exact.  The oracle runs the same
+algorithm (K Newton iterations) in float64, so these bars bound the
+implementation error; the method error (Newton at K vs the unroll) is
+measured separately in test_gpu_workloads.py."""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synthetic as syn
+
+pytestmark = pytest.mark.gpu
+HERE = os.path.dirname(os.path.abspath(__file__))
+TOL = {"f32": 1e-4, "bf16": 5e-2}
+TDT = {"f32": torch.float32, "bf16": torch.bfloat16}
+
+
+@pytest.fixture(scope="module")
+def nr():
+    import nonlinear_rnn_gb300 as m
+    return m
+
+
+def dev(a, dtype=torch.float32):
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).cuda().to(dtype)
+
+
+def host(t):
+    return t.float().cpu().numpy().astype(np.float64)
+
+
+def nan_out(B, T, d_h, dtype):
+    return torch.full((B, T, d_h), float("nan"), dtype=dtype, device="cuda")
+
+
+@pytest.mark.parametrize("algo", ["fused", "per_iter"])
+def test_golden_tiny(nr, algo):
+    with open(os.path.join(HERE, "golden", "tiny_newton.json")) as fh:
+        g = json.load(fh)
+    P = np.array(g["P"], dtype=np.float32)
+    prm = {k: np.array(v, dtype=np.float32) for k, v in g["params"].items()}
+    for K, v in g["newton"].items():
+        H, rho = nr.newton_forward(dev(P), prm, K=int(K), algo=algo, check=False)
+        np.testing.assert_allclose(host(H), np.array(v["H"]), atol=2e-6)
+        assert abs(rho.item() - v["rho"]) < 2e-6
+    cu = np.array(g["pack"]["cu_seqlens"], dtype=np.int32)
+    H, _ = nr.newton_forward(dev(P[:1]), prm, cu_seqlens=cu, K=3, algo=algo, check=False)
+    np.testing.assert_allclose(host(H), np.array(g["pack"]["newton3"]), atol=2e-6)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("algo", ["fused", "per_iter"])
+@pytest.mark.parametrize("K", [1, 2, 3, 6])
+def test_newton_matches_oracle_small(nr, dtype, algo, K):
+    # 3 rows x 300 steps (2 full 128-step tiles + a ragged tail) x 40 units
+    # (one full 32-unit tile + a ragged 8)
+    w = syn.small_workload(B=3, T=300, d_h=40, dtype=dtype, seed=20 + K)
+    P = syn.direct_preact(w)
+    prm = syn.make_params(w)
+    Href, rho_ref = oracle.newton(P, prm, K)
+    out = nan_out(w.B, w.T, w.d_h, TDT[dtype])
+    H, rho = nr.newton_forward(dev(P, TDT[dtype]), prm, K=K, algo=algo, check=False, out=out)
+    err = np.max(np.abs(host(H) - Href))
+    assert not torch.isnan(H).any()
+    assert err <= TOL[dtype], err
+    if dtype == "f32":
+        assert err <= 2e-5, err          # implementation error well inside tau
+        assert abs(rho.item() - rho_ref) <= 2e-5
+    else:
+        assert abs(rho.item() - rho_ref) <= 5e-2
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_fused_and_per_iteration_agree(nr, dtype):
+    w = syn.small_workload(B=2, T=1000, d_h=64, dtype=dtype, seed=5)
+    P = dev(syn.direct_preact(w), TDT[dtype])
+    prm = syn.make_params(w)
+    Ha, ra = nr.newton_forward(P, prm, K=3, algo="fused", check=False)
+    Hb, rb = nr.newton_forward(P, prm, K=3, algo="per_iter", check=False)
+    tol = 1e-5 if dtype == "f32" else 2e-2
+    assert (Ha.float() - Hb.float()).abs().max().item() <= tol
+
+
+def test_newton_K0_is_zero_state_residual(nr):
+    w = syn.small_workload(B=2, T=200, d_h=16, seed=7)
+    P = syn.direct_preact(w)
+    prm = syn.make_params(w)
+    _, rho_ref = oracle.newton(P, prm, 0)
+    H, rho = nr.newton_forward(dev(P), prm, K=0, check=False, out=nan_out(2, 200, 16, torch.float32))
+    assert torch.count_nonzero(H).item() == 0
+    assert abs(rho.item() - rho_ref) < 1e-6
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_sequential_matches_oracle(nr, dtype):
+    w = syn.small_workload(B=3, T=700, d_h=48, dtype=dtype, seed=9)
+    P = syn.direct_preact(w)
+    prm = syn.make_params(w)
+    Href = oracle.sequential(P, prm)
+    H = nr.sequential_forward(dev(P, TDT[dtype]), prm, out=nan_out(3, 700, 48, TDT[dtype]))
+    err = np.max(np.abs(host(H) - Href))
+    assert err <= (1e-5 if dtype == "f32" else 4e-3), err
+
+
+RAGGED = [
+    [1, 5, 127, 128, 129, 300, 2, 40],
+    [0, 128, 0, 0, 128, 1, 1, 1, 256, 0],
+    [500],
+    [3] * 90,
+]
+
+
+@pytest.mark.parametrize("lens", RAGGED)
+@pytest.mark.parametrize("algo", ["fused", "per_iter"])
+def test_ragged_pack_matches_oracle(nr, lens, algo):
+    cu = syn.cu_from_lengths(lens)
+    N = int(cu[-1])
+    w = syn.small_workload(B=1, T=N, d_h=24, seed=len(lens))
+    P = syn.direct_preact(w)
+    prm = syn.make_params(w)
+    for K in (1, 3):
+        Href, rho_ref = oracle.newton(P, prm, K, cu_seqlens=cu)
+        H, rho = nr.newton_forward(dev(P), prm, cu_seqlens=cu, K=K, algo=algo, check=False)
+        assert np.max(np.abs(host(H) - Href)) <= 2e-5
+        assert abs(rho.item() - rho_ref) <= 2e-5
+    Hs = nr.sequential_forward(dev(P), prm, cu_seqlens=cu)
+    assert np.max(np.abs(host(Hs) - oracle.sequential(P, prm, cu_seqlens=cu))) <= 1e-5
+
+
+def test_segment_head_value_is_first_step_of_cell(nr):
+    """After any K >= 1 the first token of each segment is f(0, P) of that token."""
+    lens = [7, 200, 1, 64]
+    cu = syn.cu_from_lengths(lens)
+    w = syn.small_workload(B=1, T=int(cu[-1]), d_h=8, seed=3)
+    P = syn.direct_preact(w)
+    prm = syn.make_params(w)
+    Hs = oracle.sequential(P, prm, cu_seqlens=cu)
+    for K in (1, 2):
+        H, _ = nr.newton_forward(dev(P), prm, cu_seqlens=cu, K=K, check=False)
+        heads = cu[:-1][np.diff(cu) > 0]
+        np.testing.assert_allclose(host(H)[0, heads], Hs[0, heads], atol=1e-6)
+
+
+def _heads_np(cu, N):
+    m = np.zeros(N, np.uint8)
+    if N:
+        m[0] = 1
+    for i in range(len(cu) - 1):
+        if cu[i] < cu[i + 1]:
+            m[cu[i]] = 1
+    return m
+
+
+def test_head_mask_bit_exact(nr):
+    rng = np.random.default_rng(0)
+    cases = [[0, 128, 128, 256, 1000], [0, 1, 2, 3, 4, 5, 6], [0, 0, 0, 5000]]
+    for _ in range(5):
+        lens = rng.integers(0, 700, size=rng.integers(1, 60))
+        cases.append(list(syn.cu_from_lengths(lens)))
+    cases.append(list(syn.cu_from_lengths(syn.segment_lengths(4, 64, 262144, 256, 8192))))
+    for cu in cases:
+        cu = np.asarray(cu, np.int32)
+        N = int(cu[-1])
+        if N == 0:
+            continue
+        m = nr.head_mask(cu, N).cpu().numpy()
+        np.testing.assert_array_equal(m, _heads_np(cu, N))
+
+
+def test_residual_entry_point(nr):
+    w = syn.small_workload(B=2, T=300, d_h=16, seed=12)
+    P = syn.direct_preact(w)
+    prm = syn.make_params(w)
+    Hs = oracle.sequential(P, prm)
+    assert nr.residual(dev(P), prm, dev(Hs)).item() < 2e-6
+    G = np.zeros_like(Hs)
+    G[1, 17, 3] = 0.5
+    ref = oracle.residual(P, prm, G)
+    assert abs(nr.residual(dev(P), prm, dev(G)).item() - ref) < 1e-6
+
+
+def test_divergence_gate(nr):
+    w = syn.small_workload(B=1, T=64, d_h=8, seed=1)
+    P = syn.direct_preact(w)
+    prm = syn.make_params(w)
+    with pytest.raises(nr.NewtonDivergenceError) as ei:
+        nr.newton_forward(dev(P), prm, K=0, residual_fail=1e-3)
+    assert ei.value.residual > 1e-3 and ei.value.H is not None
+    P2 = P.copy()
+    P2[0, 10, 3] = np.nan
+    with pytest.raises(nr.NewtonDivergenceError) as ei:
+        nr.newton_forward(dev(P2), prm, K=3)
+    assert math.isinf(ei.value.residual)
+    H, rho = nr.newton_forward(dev(P), prm, K=12)        # converged: passes the gate
+    assert rho.item() < 1e-5
+
+
+def test_noncontiguous_preact_is_copied(nr):
+    w = syn.small_workload(B=2, T=400, d_h=16, seed=2)
+    P = dev(syn.direct_preact(w))
+    prm = syn.make_params(w)
+    view = P[:, ::2]
+    assert not view.is_contiguous()
+    Ha, _ = nr.newton_forward(view, prm, K=3, check=False)
+    Hb, _ = nr.newton_forward(view.contiguous(), prm, K=3, check=False)
+    assert torch.equal(Ha, Hb)
+
+
+def test_empty_inputs(nr):
+    prm = syn.make_params(syn.small_workload(d_h=8))
+    for shape in [(0, 10, 24), (2, 0, 24)]:
+        P = torch.zeros(shape, device="cuda")
+        H, rho = nr.newton_forward(P, prm, K=3)
+        assert H.shape == (shape[0], shape[1], 8) and rho.item() == 0.0
+        assert nr.sequential_forward(P, prm).shape == (shape[0], shape[1], 8)
+
+
+def test_bounded_wait_gives_up_and_context_survives(nr):
+    flag = torch.zeros(1, dtype=torch.int32, device="cuda")
+    assert nr.bounded_wait(flag, 50_000_000) == 2          # nobody sets it: gives up
+    flag.fill_(1)
+    assert nr.bounded_wait(flag, 50_000_000) == 1
+    assert torch.ones(4, device="cuda").sum().item() == 4.0  # context still usable
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_input_projection_matches_oracle(nr, dtype):
+    rows, d_in, d_h = 1000, 136, 72
+    rng = np.random.default_rng(3)
+    x = rng.normal(size=(rows, d_in)).astype(np.float32)
+    W = rng.uniform(-1, 1, size=(3 * d_h, d_in)).astype(np.float32) / math.sqrt(d_in)
+    if dtype == "bf16":
+        x, W = syn.round_bf16(x), syn.round_bf16(W)
+    ref = oracle.input_projection(x, W)
+    P = nr.input_projection(dev(x, TDT[dtype]), dev(W, TDT[dtype]))
+    scale = np.abs(x) @ np.abs(W).T
+    rel = np.max(np.abs(host(P) - ref) / (scale + 1e-30))
+    assert rel <= (1e-6 if dtype == "f32" else 8e-3), rel
