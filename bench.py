@@ -154,13 +154,21 @@ def run_ours(args, w, rank, world, local):
         flush.fill_(1.0)
         newton()
     torch.cuda.synchronize()
-    if world > 1:
-        torch.distributed.barrier()
-    torch.cuda.synchronize()
 
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(args.steps)]
     with ClockSampler(local) as clk:
+        # keep the GPU busy while the sampler starts, so that its samples cover
+        # the load the timed steps run under (untimed)
+        t_pre = time.perf_counter()
+        while time.perf_counter() - t_pre < args.preroll_s:
+            for _ in range(20):
+                flush.fill_(1.0)
+                newton()
+            torch.cuda.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
         t_wall = time.perf_counter()
         for i in range(args.steps):
             flush.fill_(1.0)          # L2 flush, outside the timed events
@@ -261,41 +269,47 @@ def load_traffic(w, algo):
     return d.get(f"{w.name}|{algo}")
 
 
-def cpu_baseline(w, budget_s=12.0, steps=1):
-    """Times the float64 oracle on a bounded sample (whole rows of T steps for a
-    few hidden units) with all host cores; returns tokens/s scaled to full tokens."""
+def cpu_baseline(w, budget_s=10.0, steps=1):
+    """Times the float64 oracle (as it stands) on a bounded sample of the workload
+    on all host cores: whole rows of T steps for a subset of hidden units (units
+    are independent), as many rows and units as fit in about budget_s per pass.
+    Returns tokens/s scaled to full tokens (d_h units per token)."""
     import oracle
 
     cores = os.cpu_count() or 1
     inp = syn.make_inputs(w, with_x=False)
-    prm = inp["params"]
+    prm = oracle.pack_params(inp["params"])
     cu = inp["cu_seqlens"]
-    rows = [0]
-    # pilot: one unit, one row
-    units = np.array([0])
-    Pc = syn.preact_uniform_columns(w, units, rows=rows)
+    n0 = min(w.d_h, cores)
+    units = np.arange(n0)
+    Pc = syn.preact_uniform_columns(w, units, rows=[0])
     t = time.perf_counter()
-    oracle.newton(Pc, oracle.pack_params(prm)[:, units], w.K, cu_seqlens=cu, threads=1)
-    per_unit = max(time.perf_counter() - t, 1e-4)
-    n_units = int(max(1, min(w.d_h, budget_s / per_unit * cores / max(steps, 1))))
-    n_rows = 1
-    while n_units == w.d_h and n_rows < w.B and per_unit * n_units * (n_rows + 1) / cores * steps < budget_s:
-        n_rows += 1
+    oracle.newton(Pc, prm[:, units], w.K, cu_seqlens=cu, threads=cores)
+    t_unit_row = max(time.perf_counter() - t, 1e-4)     # one unit per core, one row
+    waves = lambda n: -(-n // cores)                      # noqa: E731
+    n_units, n_rows = w.d_h, w.B
+    while n_rows > 1 and t_unit_row * waves(n_units) * n_rows > budget_s:
+        n_rows -= 1
+    while n_units > 1 and t_unit_row * waves(n_units) * n_rows > budget_s:
+        n_units = max(1, n_units // 2)
     units = np.arange(n_units)
     rows = list(range(n_rows))
     Pc = syn.preact_uniform_columns(w, units, rows=rows)
-    pp = oracle.pack_params(prm)[:, units]
+    pp = prm[:, units]
+    reps = max(1, int(budget_s / max(t_unit_row * waves(n_units) * n_rows, 1e-3)))
     times = []
     for _ in range(steps):
         t = time.perf_counter()
-        oracle.newton(Pc, pp, w.K, cu_seqlens=cu, threads=cores)
-        times.append(time.perf_counter() - t)
+        for _ in range(reps):
+            oracle.newton(Pc, pp, w.K, cu_seqlens=cu, threads=cores)
+        times.append((time.perf_counter() - t) / reps)
     sec = statistics.mean(times)
     unit_tokens = n_units * n_rows * w.T
     return {"value": unit_tokens / w.d_h / sec, "unit": "tokens/s", "cores": min(cores, n_units),
             "kind": "oracle",
-            "sample": f"oracle.newton float64, K={w.K}, {n_units} of {w.d_h} units x {n_rows} of "
-                      f"{w.B} rows x T={w.T} (uniform preact), {sec:.2f} s per pass",
+            "sample": f"oracle.newton float64 K={w.K} on {n_units} of {w.d_h} units x {n_rows} of "
+                      f"{w.B} rows x T={w.T} (uniform preact), {sec:.3f} s per pass, "
+                      f"{reps} passes per step",
             "seconds": sec}
 
 
@@ -308,6 +322,7 @@ def main():
     ap.add_argument("--algo", default="auto", choices=["auto", "fused", "per_iter"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--preroll-s", type=float, default=1.0)
     args = ap.parse_args()
     w = syn.WORKLOADS[args.workload]
     rank, world, local = dist_env()
@@ -315,8 +330,7 @@ def main():
     if args.impl == "reference":
         if rank != 0:
             return
-        cb = cpu_baseline(w, budget_s=max(2.0, 60.0 / max(args.steps + args.warmup, 1)),
-                          steps=args.steps)
+        cb = cpu_baseline(w, budget_s=max(1.0, 90.0 / max(args.steps, 1)), steps=args.steps)
         out = {"impl": "reference", "metric": METRIC, "value": cb["value"], "unit": "tokens/s",
                "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
                "ms_per_step": 1e3 * w.B * w.T / cb["value"], "higher_is_better": True,

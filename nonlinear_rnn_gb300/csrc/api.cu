@@ -23,20 +23,21 @@ size_t elem_size(int dtype) { return dtype == NRNN_BF16 ? 2 : 4; }
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// Workspace: [flags K x n_tiles u32 | counters (K+1) u32 | error u32] zeroed per
-// call, then [slots K x n_tiles x 32 u64], then (per-iteration) one H buffer.
+// Workspace: [counters (K+1) u32 | error u32] zeroed per call, then
+// [slots K x n_tiles x 32 u64] set to all-ones bytes per call, then
+// (per-iteration, K > 1) one H buffer.
 SyncLayout layout(int64_t B, int64_t T, int64_t d_h, int dtype, int K, bool fused) {
     SyncLayout s{};
     const int64_t n_ut = (d_h + TILE_U - 1) / TILE_U;
     const int64_t n_chunks = (T + NEWTON_L - 1) / NEWTON_L;
     const int64_t kk = K > 0 ? K : 1;
     s.n_tiles = B * n_ut * n_chunks;
-    s.flags_off = 0;
-    s.counters_off = align_up(s.flags_off + sizeof(uint32_t) * kk * s.n_tiles, 16);
-    s.error_off = s.counters_off + sizeof(uint32_t) * (kk + 1);
+    s.counters_off = 0;
+    s.error_off = sizeof(uint32_t) * (kk + 1);
     s.zero_bytes = align_up(s.error_off + sizeof(uint32_t), 16);
     s.slots_off = align_up(s.zero_bytes, 256);
-    size_t end = s.slots_off + sizeof(unsigned long long) * 32 * kk * s.n_tiles;
+    s.slots_bytes = sizeof(unsigned long long) * 32 * kk * s.n_tiles;
+    size_t end = s.slots_off + s.slots_bytes;
     s.hbuf_off = align_up(end, 256);
     if (!fused && K > 1) end = s.hbuf_off + elem_size(dtype) * B * T * d_h;
     s.total = align_up(end, 256);
@@ -153,6 +154,8 @@ int nrnn_newton_forward(const void *preact, int dtype, const float *params, int6
     const int S = static_cast<int>(cu_seqlens ? num_segments : 0);
 
     cudaError_t e = cudaMemsetAsync(ws, 0, ly.zero_bytes, stream);
+    if (e == cudaSuccess && K > 0 && ly.slots_bytes > 0)
+        e = cudaMemsetAsync(ws + ly.slots_off, 0xff, ly.slots_bytes, stream);
     if (e == cudaSuccess) e = cudaMemsetAsync(residual_dev, 0, sizeof(float), stream);
     if (e != cudaSuccess) return NRNN_ERR_CUDA;
 
@@ -176,7 +179,6 @@ int nrnn_newton_forward(const void *preact, int dtype, const float *params, int6
             a.d_h = static_cast<int>(d_h);
             a.n_ut = static_cast<int>((d_h + TILE_U - 1) / TILE_U);
             a.n_chunks = static_cast<int>((T + NEWTON_L - 1) / NEWTON_L);
-            a.flags = reinterpret_cast<uint32_t *>(ws + ly.flags_off);
             a.slots = reinterpret_cast<unsigned long long *>(ws + ly.slots_off);
             a.residual_bits = res_bits;
             a.error = err;

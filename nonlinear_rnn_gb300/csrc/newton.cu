@@ -1,23 +1,24 @@
 // Parallel Newton forward of the diagonal-mix GRU (sm_103a).
 //
 // One CTA owns a tile of 32 hidden units (one per lane) x L = 128 time steps
-// of one batch row.  Per Newton iteration it
-//   1. evaluates the cell at the shifted trajectory H_{t-1} for every step of
-//      the tile: F_t = H_t - f(H_{t-1}, P_t), J_t = df/dh (J = 0 and shifted
-//      state 0 at segment heads; pararnn-torch shapes_layout, "cu_seqlens");
-//   2. composes the affine maps delta -> J_t delta - F_t serially inside each
-//      warp's 16 steps, then across the 8 warps in shared memory;
-//   3. obtains the carry delta_{t0-1} from earlier chunks by a decoupled
-//      look-back over per-chunk published (A, b) pairs, each warp of the CTA
-//      inspecting one predecessor of an 8-chunk window per round;
-//   4. applies the carry and updates H <- H + delta.
-// The fused variant repeats 1-4 for all K iterations on the tile held in
-// shared memory/registers (the shifted state at the tile's first step is
-// tracked as H^(k)_{t0-1} = H^(k-1)_{t0-1} + carry_k), so P is read once and
-// H written once.  The per-iteration variant runs one iteration per launch
-// and streams H^(k-1) in and H^(k) out.  The launch that produces H^(K)
-// evaluates F(H^(K)) once more for the residual gate max|F| (numerics
-// contract, "Two thresholds").
+// of one batch row; warp w owns rows [16 w, 16 w + 16).  Per Newton iteration
+//   1. each thread evaluates the cell at the shifted trajectory for its 16
+//      steps, F_t = H_t - f(H_{t-1}, P_t) and J_t = df/dh (J = 0 and shifted
+//      state 0 at segment heads; pararnn-torch shapes_layout, "cu_seqlens"),
+//      and composes the affine maps delta -> J_t delta - F_t serially;
+//   2. the 8 warp aggregates meet in shared memory (one barrier): each warp
+//      takes its exclusive prefix, warp 0 the chunk aggregate, which it
+//      publishes and then completes by a decoupled look-back over earlier
+//      chunks (one lane per unit, 8 predecessors read per round);
+//   3. after a second barrier every thread applies the carry:
+//      delta_t = J_t delta_{t-1} - F_t, H <- H + delta.
+// Each warp advances the shifted state at its first row itself
+// (H^(k)_{r0-1} = H^(k-1)_{r0-1} + carry into the warp), so iterations need no
+// other exchange.  The fused variant runs all K iterations on the tile kept
+// in shared memory (P) and registers (H): P is read once and H written once.
+// The per-iteration variant runs one iteration per launch, streaming H^(k-1)
+// in and H^(k) out.  The launch that produces H^(K) evaluates F(H^(K)) once
+// more for the residual gate max|F| (numerics contract, "Two thresholds").
 //
 // Tiles of P (three gate blocks) and of H^(k-1) are staged in shared memory
 // by TMA (cp.async.bulk.tensor, completion on an mbarrier).  CTAs take tiles
@@ -36,96 +37,102 @@ constexpr int NW = NEWTON_NW;
 constexpr int SEG = NEWTON_SEG;
 constexpr int L = NEWTON_L;
 constexpr int U = TILE_U;
+constexpr int WIN = 8;   // predecessors read in parallel per look-back round
 
-constexpr uint32_t FLAG_AGGREGATE = 1u;
-constexpr uint32_t FLAG_INCLUSIVE = 2u;
+// A slot holding SLOT_EMPTY has not been published yet.  Published pairs never
+// take this value (arithmetic NaNs are 0x7fffffff; see publish()).
+constexpr unsigned long long SLOT_EMPTY = 0xffffffffffffffffull;
 
-// Publishes one (A, b) pair per lane for a chunk, then its status flag.
-__device__ __forceinline__ void publish(uint32_t *flag, unsigned long long *slot, float A,
-                                        float b, uint32_t kind, int lane) {
-    st_relaxed_u64(slot, pack_pair(A, b));
-    __threadfence();
-    __syncwarp();
-    if (lane == 0) st_release_u32(flag, kind);
+// Publishes this lane's (A, b) for a chunk.  The 64-bit word is both the data
+// and its ready flag (single-copy atomic), so no fence is needed: a reader
+// sees either SLOT_EMPTY, the aggregate or the inclusive prefix, and the
+// aggregate and the inclusive prefix (A = 0) both compose correctly.
+__device__ __forceinline__ void publish(unsigned long long *slot, float A, float b) {
+    unsigned long long v = pack_pair(A, b);
+    if (v == SLOT_EMPTY) v = pack_pair(__int_as_float(0x7fffffff), b);
+    st_relaxed_u64(slot, v);
 }
 
-struct LookbackSmem {
-    float winA[NW][32];
-    float winB[NW][32];
-    float cA[32];
-    float cB[32];
-    int done;
-};
-
-// Decoupled look-back for the chunk at `tile` (chunk index c > 0): returns the
-// carry delta_{t0-1} for this lane's unit.  All warps of the CTA take part;
-// warp w reads predecessor base - w of the current window.  Must be called by
-// the whole CTA (it contains barriers); s.cA/s.cB must hold (1, 0).
-__device__ __forceinline__ float lookback(const uint32_t *flags, const unsigned long long *slots,
-                                          int tile, int c, LookbackSmem &s, uint64_t wait_ns,
-                                          uint32_t *error) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    for (int base = c - 1;; base -= NW) {
-        const int p = base - warp;
-        float pa = 0.f, pb = 0.f;   // p < 0: the sequence start, delta = 0
-        if (p >= 0) {
-            const int pt = tile - (c - p);
-            uint32_t f = ld_acquire_u32(flags + pt);
-            if (!__all_sync(FULL_MASK, f != 0u)) {
-                const uint64_t ts = globaltimer_ns();
-                for (;;) {
-                    __nanosleep(32);
-                    f = ld_acquire_u32(flags + pt);
-                    if (__all_sync(FULL_MASK, f != 0u)) break;
-                    const bool late = (globaltimer_ns() - ts) > wait_ns;
-                    if (__any_sync(FULL_MASK, late)) {
-                        if (lane == 0) atomicOr(error, 1u);
-                        break;
-                    }
-                }
-            }
-            if (__all_sync(FULL_MASK, f != 0u)) {
-                const unsigned long long v = ld_relaxed_u64(slots + static_cast<size_t>(pt) * 32 + lane);
-                pa = pair_A(v);
-                pb = pair_b(v);
-            }
-        }
-        s.winA[warp][lane] = pa;
-        s.winB[warp][lane] = pb;
-        __syncthreads();
-        if (warp == 0) {
-            float cA = s.cA[lane], cB = s.cB[lane];
+// Decoupled look-back for one unit (one lane): composes the pairs of chunks
+// c-1, c-2, ... until a closed prefix (A = 0) or the start of the sequence,
+// and returns the carry delta_{t0-1}.  `slot` is this lane's slot of chunk c;
+// chunk q's slot is slot - (c - q) * 32.  Up to WIN predecessors are read per
+// round with independent loads.  Bounded: gives up after wait_ns without
+// progress, sets bit 0 of *error and returns the partial prefix.
+__device__ __forceinline__ float lookback_lane(const unsigned long long *slot, int c,
+                                               uint64_t wait_ns, uint32_t *error) {
+    float cA = 1.f, cB = 0.f;
+    int p = c - 1;
+    uint64_t t_wait = 0;
+    bool waiting = false;
+    while (p >= 0) {
+        unsigned long long v[WIN];
 #pragma unroll
-            for (int w = 0; w < NW; ++w) {
-                if (cA != 0.f) {
-                    cB = fmaf(cA, s.winB[w][lane], cB);
-                    cA *= s.winA[w][lane];
-                }
-            }
-            s.cA[lane] = cA;
-            s.cB[lane] = cB;
-            // done when every lane's prefix is closed (A = 0) or the window has
-            // reached chunk 0 (a NaN input keeps A = NaN, never 0)
-            const bool all_done = __all_sync(FULL_MASK, cA == 0.f) || base - (NW - 1) <= 0;
-            if (lane == 0) s.done = all_done ? 1 : 0;
+        for (int i = 0; i < WIN; ++i)
+            v[i] = (p - i >= 0) ? ld_relaxed_u64(slot - static_cast<size_t>(c - p + i) * 32)
+                                : pack_pair(0.f, 0.f);
+        int folded = 0;
+#pragma unroll
+        for (int i = 0; i < WIN; ++i) {
+            if (folded < i || v[i] == SLOT_EMPTY) break;
+            cB = fmaf(cA, pair_b(v[i]), cB);
+            cA *= pair_A(v[i]);
+            ++folded;
         }
-        __syncthreads();
-        if (s.done) break;
+        if (cA == 0.f) break;          // closed prefix (an inclusive or a head)
+        p -= folded;
+        if (folded == 0) {
+            const uint64_t now = globaltimer_ns();
+            if (!waiting) { t_wait = now; waiting = true; }
+            else if (now - t_wait > wait_ns) { atomicOr(error, 1u); break; }
+            __nanosleep(32);
+        } else {
+            waiting = false;
+        }
     }
-    return s.cB[lane];
+    return cB;
+}
+
+// Pairs (J_t, -F_t) of this warp's SEG rows at the shifted iterate, composed
+// into the warp aggregate (A, B).  GENERAL handles segment heads (J = 0,
+// shifted state 0) and rows past T (identity map).
+template <typename TS, bool GENERAL>
+__device__ __forceinline__ void warp_pairs(const TS *Ps, int r0, int lane, const float (&Hreg)[SEG],
+                                           float hprev, uint32_t hm, int nvalid,
+                                           const UnitParams &prm, float (&Jr)[SEG],
+                                           float (&Fr)[SEG], float &A, float &Bv) {
+    A = 1.f;
+    Bv = 0.f;
+#pragma unroll
+    for (int i = 0; i < SEG; ++i) {
+        const int r = r0 + i;
+        const bool head = GENERAL && ((hm >> i) & 1u);
+        float f, J;
+        cell_fj(head ? 0.f : hprev, to_f32(Ps[(0 * L + r) * U + lane]),
+                to_f32(Ps[(1 * L + r) * U + lane]), to_f32(Ps[(2 * L + r) * U + lane]), prm, f, J);
+        float F = Hreg[i] - f;
+        if (GENERAL) {
+            if (head) J = 0.f;
+            if (i >= nvalid) { J = 1.f; F = 0.f; }
+        }
+        Jr[i] = J;
+        Fr[i] = F;
+        Bv = fmaf(J, Bv, -F);
+        A *= J;
+        hprev = Hreg[i];
+    }
 }
 
 template <typename TS, bool FUSED>
-__global__ void __launch_bounds__(NW * 32)
+__global__ void __launch_bounds__(NW * 32, 3)
     k_newton(const __grid_constant__ CUtensorMap tmP, const __grid_constant__ CUtensorMap tmH,
              const NewtonArgs a) {
     extern __shared__ __align__(128) unsigned char dsmem[];
     TS *Ps = reinterpret_cast<TS *>(dsmem);   // [3][L][U]
     TS *Hs = Ps + 3 * L * U;                  // [L][U] (per-iteration variant only)
-    __shared__ float s_exA[NW][32], s_exB[NW][32];   // per-warp aggregate, then exclusive prefix
-    __shared__ float s_last[NW][32];                 // last H of each warp's rows
-    __shared__ float s_chunkA[32], s_chunkB[32];
-    __shared__ LookbackSmem s_lb;
+    __shared__ float s_aggA[NW][32], s_aggB[NW][32];
+    __shared__ float s_C[32];
+    __shared__ float s_hlast[NW][32];
     __shared__ uint32_t s_heads[L / 32];
     __shared__ __align__(8) uint64_t s_bar;
     __shared__ uint32_t s_ticket;
@@ -157,107 +164,86 @@ __global__ void __launch_bounds__(NW * 32)
     const int u = u0 + lane;
     const bool uok = u < a.d_h;
     const UnitParams prm = load_unit_params(a.params, a.d_h, u, uok);
-    float hb = 0.f;   // H^(k-1) at t0 - 1, this lane's unit
-    if (load_h && t0 > 0 && uok)
+    const int r0 = warp * SEG;
+    // shifted state at this warp's first row: H^(k-1) at row r0 - 1
+    float hb = 0.f;
+    if (load_h && warp == 0 && t0 > 0 && uok)
         hb = to_f32(reinterpret_cast<const TS *>(a.H_prev)[(static_cast<size_t>(b) * a.T + t0 - 1) *
                                                                a.d_h + u]);
     __syncthreads();   // barrier initialised, head bits visible
     mbar_wait_bounded(&s_bar, 0, a.wait_ns, a.error);
 
-    const int r0 = warp * SEG;
     float Hreg[SEG];
 #pragma unroll
     for (int i = 0; i < SEG; ++i) Hreg[i] = load_h ? to_f32(Hs[(r0 + i) * U + lane]) : 0.f;
-    s_last[warp][lane] = Hreg[SEG - 1];
-    __syncthreads();
+    if (load_h && warp > 0) hb = to_f32(Hs[(r0 - 1) * U + lane]);
+    const uint32_t hm = (s_heads[r0 >> 5] >> (r0 & 31)) & ((1u << SEG) - 1u);
+    const int nvalid = min(SEG, a.T - (t0 + r0));
+    const bool general = (hm != 0u) || (nvalid < SEG);
 
     const int n_tiles = a.B * a.n_ut * a.n_chunks;
     const int tile = (b * a.n_ut + ut) * a.n_chunks + c;
 
     for (int k = a.k_first; k <= a.k_last; ++k) {
-        // 1. pairs (J_t, -F_t) at the shifted iterate, composed over this warp's steps
-        float Jr[SEG], Fr[SEG];
-        float A = 1.f, Bv = 0.f;
-        float hprev = (warp == 0) ? hb : s_last[warp - 1][lane];
-#pragma unroll
-        for (int i = 0; i < SEG; ++i) {
-            const int r = r0 + i;
-            const bool head = head_bit(s_heads, r);
-            const float hs = head ? 0.f : hprev;
-            float f, J;
-            cell_fj(hs, to_f32(Ps[(0 * L + r) * U + lane]), to_f32(Ps[(1 * L + r) * U + lane]),
-                    to_f32(Ps[(2 * L + r) * U + lane]), prm, f, J);
-            float F = Hreg[i] - f;
-            if (head) J = 0.f;
-            if (t0 + r >= a.T) { J = 1.f; F = 0.f; }   // past the end: identity map
-            Jr[i] = J;
-            Fr[i] = F;
-            Bv = fmaf(J, Bv, -F);
-            A *= J;
-            hprev = Hreg[i];
-        }
-        s_exA[warp][lane] = A;
-        s_exB[warp][lane] = Bv;
+        float Jr[SEG], Fr[SEG], A, Bv;
+        if (general) warp_pairs<TS, true>(Ps, r0, lane, Hreg, hb, hm, nvalid, prm, Jr, Fr, A, Bv);
+        else warp_pairs<TS, false>(Ps, r0, lane, Hreg, hb, hm, nvalid, prm, Jr, Fr, A, Bv);
+        s_aggA[warp][lane] = A;
+        s_aggB[warp][lane] = Bv;
         __syncthreads();
 
-        // 2. chunk aggregate and per-warp exclusive prefixes; publish
-        uint32_t *flags = a.flags + static_cast<size_t>(k - 1) * n_tiles;
-        unsigned long long *slots = a.slots + static_cast<size_t>(k - 1) * n_tiles * 32;
+        // exclusive prefix of this warp within the chunk
+        float eA = 1.f, eB = 0.f;
+        for (int w = 0; w < warp; ++w) {
+            eB = fmaf(s_aggA[w][lane], eB, s_aggB[w][lane]);
+            eA *= s_aggA[w][lane];
+        }
         if (warp == 0) {
-            float eA = 1.f, eB = 0.f;
+            float tA = 1.f, tB = 0.f;
 #pragma unroll
             for (int w = 0; w < NW; ++w) {
-                const float wa = s_exA[w][lane], wb = s_exB[w][lane];
-                s_exA[w][lane] = eA;
-                s_exB[w][lane] = eB;
-                eB = fmaf(wa, eB, wb);
-                eA *= wa;
+                tB = fmaf(s_aggA[w][lane], tB, s_aggB[w][lane]);
+                tA *= s_aggA[w][lane];
             }
-            s_chunkA[lane] = eA;
-            s_chunkB[lane] = eB;
-            s_lb.cA[lane] = 1.f;
-            s_lb.cB[lane] = 0.f;
-            if (c == 0) publish(flags + tile, slots + static_cast<size_t>(tile) * 32 + lane, 0.f, eB,
-                                FLAG_INCLUSIVE, lane);
-            else publish(flags + tile, slots + static_cast<size_t>(tile) * 32 + lane, eA, eB,
-                         FLAG_AGGREGATE, lane);
+            unsigned long long *slot =
+                a.slots + (static_cast<size_t>(k - 1) * n_tiles + tile) * 32 + lane;
+            float C = 0.f;
+            if (c == 0) {
+                publish(slot, 0.f, tB);
+            } else {
+                publish(slot, tA, tB);
+                C = lookback_lane(slot, c, a.wait_ns, a.error);
+                publish(slot, 0.f, fmaf(tA, C, tB));
+            }
+            s_C[lane] = C;
         }
         __syncthreads();
 
-        // 3. carry from earlier chunks
-        float C = 0.f;
-        if (c > 0) {
-            C = lookback(flags, slots, tile, c, s_lb, a.wait_ns, a.error);
-            if (warp == 0)
-                publish(flags + tile, slots + static_cast<size_t>(tile) * 32 + lane, 0.f,
-                        fmaf(s_chunkA[lane], C, s_chunkB[lane]), FLAG_INCLUSIVE, lane);
-        }
-
-        // 4. delta_t = J_t delta_{t-1} - F_t from the carry; H <- H + delta
-        float d = fmaf(s_exA[warp][lane], C, s_exB[warp][lane]);
+        // delta_t = J_t delta_{t-1} - F_t from the carry; H <- H + delta
+        float d = fmaf(eA, s_C[lane], eB);
+        hb = FUSED ? (hb + d) : round_to<TS>(hb + d);   // H^(k) at row r0 - 1
 #pragma unroll
         for (int i = 0; i < SEG; ++i) {
             d = fmaf(Jr[i], d, -Fr[i]);
             Hreg[i] = FUSED ? (Hreg[i] + d) : round_to<TS>(Hreg[i] + d);
         }
-        hb = FUSED ? (hb + C) : round_to<TS>(hb + C);
-        s_last[warp][lane] = Hreg[SEG - 1];
-        __syncthreads();
     }
 
     // residual max|F(H^(K))| at the values as stored
     if (a.last && a.residual_bits != nullptr) {
+        s_hlast[warp][lane] = round_to<TS>(Hreg[SEG - 1]);
+        __syncthreads();
         float m = 0.f;
-        float hprev = round_to<TS>((warp == 0) ? hb : s_last[warp - 1][lane]);
+        float hprev = (warp == 0) ? round_to<TS>(hb) : s_hlast[warp - 1][lane];
 #pragma unroll
         for (int i = 0; i < SEG; ++i) {
             const int r = r0 + i;
-            const bool head = head_bit(s_heads, r);
+            const bool head = (hm >> i) & 1u;
             const float hq = round_to<TS>(Hreg[i]);
             const float f = cell_f(head ? 0.f : hprev, to_f32(Ps[(0 * L + r) * U + lane]),
                                    to_f32(Ps[(1 * L + r) * U + lane]),
                                    to_f32(Ps[(2 * L + r) * U + lane]), prm);
-            if (uok && t0 + r < a.T) m = fmaxf(m, abs_residual(hq - f));
+            if (uok && i < nvalid) m = fmaxf(m, abs_residual(hq - f));
             hprev = hq;
         }
         const uint32_t v = __reduce_max_sync(FULL_MASK, __float_as_uint(m));
@@ -276,7 +262,7 @@ __global__ void __launch_bounds__(NW * 32)
 #pragma unroll
         for (int i = 0; i < SEG; ++i) {
             const int t = t0 + r0 + i;
-            if (t < a.T) Hn[(static_cast<size_t>(b) * a.T + t) * a.d_h + u] = from_f32<TS>(Hreg[i]);
+            if (i < nvalid) Hn[(static_cast<size_t>(b) * a.T + t) * a.d_h + u] = from_f32<TS>(Hreg[i]);
         }
     }
 }

@@ -25,18 +25,18 @@ struct NewtonArgs {
     int n_ut, n_chunks;           // unit tiles, time chunks
     int k_first, k_last;          // iterations this launch runs (1-based, inclusive)
     int last;                     // this launch ends with H^(K): compute the residual
-    uint32_t *flags;              // [K][n_tiles] look-back status (0 = empty)
-    unsigned long long *slots;    // [K][n_tiles][32] packed (A, b)
+    unsigned long long *slots;    // [K][n_tiles][32] packed (A, b); all-ones = not published
     uint32_t *ticket;             // this launch's CTA ticket counter
     uint32_t *residual_bits;      // float bits of rho (atomicMax), or null
     uint32_t *error;              // error word (bit 0: look-back timeout, bit 1: TMA timeout)
     unsigned long long wait_ns;   // limit of every bounded wait
 };
 
-// Look-back status region of the workspace for one call.
+// Workspace of one call: [counters | error] zeroed, [slots] set to all-ones
+// bytes, then (per-iteration variant, K > 1) one H buffer.
 struct SyncLayout {
-    size_t flags_off, counters_off, error_off, zero_bytes;  // [0, zero_bytes) is memset to 0
-    size_t slots_off, hbuf_off, total;
+    size_t counters_off, error_off, zero_bytes;
+    size_t slots_off, slots_bytes, hbuf_off, total;
     int64_t n_tiles;
 };
 
