@@ -9,7 +9,7 @@
 //   2. the 8 warp aggregates meet in shared memory (one barrier): each warp
 //      takes its exclusive prefix, warp 0 the chunk aggregate, which it
 //      publishes and then completes by a decoupled look-back over earlier
-//      chunks (one lane per unit, 8 predecessors read per round);
+//      chunks (one lane per unit, 4 predecessors read per round);
 //   3. after a second barrier every thread applies the carry:
 //      delta_t = J_t delta_{t-1} - F_t, H <- H + delta.
 // Each warp advances the shifted state at its first row itself
@@ -37,7 +37,7 @@ constexpr int NW = NEWTON_NW;
 constexpr int SEG = NEWTON_SEG;
 constexpr int L = NEWTON_L;
 constexpr int U = TILE_U;
-constexpr int WIN = 8;   // predecessors read in parallel per look-back round
+constexpr int WIN = 4;   // predecessors read in parallel per look-back round
 
 // A slot holding SLOT_EMPTY has not been published yet.  Published pairs never
 // take this value (arithmetic NaNs are 0x7fffffff; see publish()).
@@ -63,8 +63,6 @@ __device__ __forceinline__ float lookback_lane(const unsigned long long *slot, i
                                                uint64_t wait_ns, uint32_t *error) {
     float cA = 1.f, cB = 0.f;
     int p = c - 1;
-    uint64_t t_wait = 0;
-    bool waiting = false;
     while (p >= 0) {
         unsigned long long v[WIN];
 #pragma unroll
@@ -82,57 +80,79 @@ __device__ __forceinline__ float lookback_lane(const unsigned long long *slot, i
         if (cA == 0.f) break;          // closed prefix (an inclusive or a head)
         p -= folded;
         if (folded == 0) {
-            const uint64_t now = globaltimer_ns();
-            if (!waiting) { t_wait = now; waiting = true; }
-            else if (now - t_wait > wait_ns) { atomicOr(error, 1u); break; }
-            __nanosleep(32);
-        } else {
-            waiting = false;
+            // nothing ready: poll the nearest predecessor alone (bounded)
+            const unsigned long long *q = slot - static_cast<size_t>(c - p) * 32;
+            const uint64_t t_wait = globaltimer_ns();
+            while (ld_relaxed_u64(q) == SLOT_EMPTY) {
+                __nanosleep(64);
+                if (globaltimer_ns() - t_wait > wait_ns) {
+                    atomicOr(error, 1u);
+                    return cB;
+                }
+            }
         }
     }
     return cB;
 }
 
-// Pairs (J_t, -F_t) of this warp's SEG rows at the shifted iterate, composed
-// into the warp aggregate (A, B).  GENERAL handles segment heads (J = 0,
-// shifted state 0) and rows past T (identity map).
-template <typename TS, bool GENERAL>
-__device__ __forceinline__ void warp_pairs(const TS *Ps, int r0, int lane, const float (&Hreg)[SEG],
+// Affine pairs (J_t, g_t) of this warp's SEG rows at the shifted iterate,
+// with g_t = f(h~_t) - J_t h~_t, so that the new iterate solves
+// H^(k)_t = J_t H^(k)_{t-1} + g_t: the Newton step delta_t = J_t delta_{t-1} - F_t
+// written for delta_t = H^(k)_t - H^(k-1)_t.  Composed into the warp
+// aggregate (A, Bv).  On return G[i] holds g_t.  SCALED: Ps holds fp32
+// pre-scaled arguments; otherwise raw preactivations of type TS.  GENERAL
+// handles segment heads (J = 0, shifted state 0) and rows past T (identity).
+template <typename TS, bool SCALED, bool GENERAL>
+__device__ __forceinline__ void warp_pairs(const void *Pv, int r0, int lane, float (&G)[SEG],
                                            float hprev, uint32_t hm, int nvalid,
-                                           const UnitParams &prm, float (&Jr)[SEG],
-                                           float (&Fr)[SEG], float &A, float &Bv) {
+                                           const ScaledParams &prm, float (&Jr)[SEG], float &A,
+                                           float &Bv) {
     A = 1.f;
     Bv = 0.f;
 #pragma unroll
     for (int i = 0; i < SEG; ++i) {
         const int r = r0 + i;
-        const bool head = GENERAL && ((hm >> i) & 1u);
-        float f, J;
-        cell_fj(head ? 0.f : hprev, to_f32(Ps[(0 * L + r) * U + lane]),
-                to_f32(Ps[(1 * L + r) * U + lane]), to_f32(Ps[(2 * L + r) * U + lane]), prm, f, J);
-        float F = Hreg[i] - f;
-        if (GENERAL) {
-            if (head) J = 0.f;
-            if (i >= nvalid) { J = 1.f; F = 0.f; }
+        float sz, sr, sc;
+        if (SCALED) {
+            const float *P = static_cast<const float *>(Pv);
+            sz = P[(0 * L + r) * U + lane];
+            sr = P[(1 * L + r) * U + lane];
+            sc = P[(2 * L + r) * U + lane];
+        } else {
+            const TS *P = static_cast<const TS *>(Pv);
+            scale_preact(to_f32(P[(0 * L + r) * U + lane]), to_f32(P[(1 * L + r) * U + lane]),
+                         to_f32(P[(2 * L + r) * U + lane]), prm, sz, sr, sc);
         }
+        const float hs = (GENERAL && ((hm >> i) & 1u)) ? 0.f : hprev;
+        float f, J;
+        cell_fj_scaled(hs, sz, sr, sc, prm, f, J);
+        float g = fmaf(-J, hs, f);
+        if (GENERAL) {
+            if ((hm >> i) & 1u) J = 0.f;
+            if (i >= nvalid) { J = 1.f; g = 0.f; }
+        }
+        hprev = G[i];
         Jr[i] = J;
-        Fr[i] = F;
-        Bv = fmaf(J, Bv, -F);
+        G[i] = g;
+        Bv = fmaf(J, Bv, g);
         A *= J;
-        hprev = Hreg[i];
     }
 }
 
 template <typename TS, bool FUSED>
-__global__ void __launch_bounds__(NW * 32, 3)
+__global__ void __launch_bounds__(NW * 32, 4)
     k_newton(const __grid_constant__ CUtensorMap tmP, const __grid_constant__ CUtensorMap tmH,
              const NewtonArgs a) {
     extern __shared__ __align__(128) unsigned char dsmem[];
-    TS *Ps = reinterpret_cast<TS *>(dsmem);   // [3][L][U]
-    TS *Hs = Ps + 3 * L * U;                  // [L][U] (per-iteration variant only)
+    // FUSED: [3][L][U] fp32 pre-scaled arguments; a bf16 tile lands by TMA in
+    // the upper half and is widened in place.  Per-iteration: [3][L][U] raw
+    // preactivations followed by the [L][U] tile of H^(k-1), both of type TS.
+    float *Pf = reinterpret_cast<float *>(dsmem);
+    TS *Pt = FUSED ? reinterpret_cast<TS *>(dsmem + (sizeof(TS) == 2 ? 3 * L * U * 2 : 0))
+                   : reinterpret_cast<TS *>(dsmem);
+    TS *Hs = reinterpret_cast<TS *>(dsmem) + 3 * L * U;
     __shared__ float s_aggA[NW][32], s_aggB[NW][32];
     __shared__ float s_C[32];
-    __shared__ float s_hlast[NW][32];
     __shared__ uint32_t s_heads[L / 32];
     __shared__ __align__(8) uint64_t s_bar;
     __shared__ uint32_t s_ticket;
@@ -157,13 +177,13 @@ __global__ void __launch_bounds__(NW * 32, 3)
         mbar_arrive_expect_tx(&s_bar, bytes);
 #pragma unroll
         for (int g = 0; g < 3; ++g)
-            tma_load_3d(Ps + g * L * U, &tmP, &s_bar, g * a.d_h + u0, t0, b);
+            tma_load_3d(Pt + g * L * U, &tmP, &s_bar, g * a.d_h + u0, t0, b);
         if (load_h) tma_load_3d(Hs, &tmH, &s_bar, u0, t0, b);
         mark_heads(a.cu, a.S, t0, L, s_heads);
     }
     const int u = u0 + lane;
     const bool uok = u < a.d_h;
-    const UnitParams prm = load_unit_params(a.params, a.d_h, u, uok);
+    const ScaledParams prm = scale_params(load_unit_params(a.params, a.d_h, u, uok));
     const int r0 = warp * SEG;
     // shifted state at this warp's first row: H^(k-1) at row r0 - 1
     float hb = 0.f;
@@ -173,21 +193,43 @@ __global__ void __launch_bounds__(NW * 32, 3)
     __syncthreads();   // barrier initialised, head bits visible
     mbar_wait_bounded(&s_bar, 0, a.wait_ns, a.error);
 
-    float Hreg[SEG];
+    if (FUSED) {
+        // pre-scale the tile once: P' = scale (P + b) per gate, fp32
+        constexpr int PER = L * U / (NW * 32);
+        float v[3][PER];
 #pragma unroll
-    for (int i = 0; i < SEG; ++i) Hreg[i] = load_h ? to_f32(Hs[(r0 + i) * U + lane]) : 0.f;
+        for (int g = 0; g < 3; ++g)
+#pragma unroll
+            for (int j = 0; j < PER; ++j) v[g][j] = to_f32(Pt[g * L * U + tid + j * NW * 32]);
+        if (sizeof(TS) == 2) __syncthreads();   // bf16 tile overlaps the fp32 destination
+        // element tid + 256 j belongs to unit (tid mod 32) = this lane's unit
+#pragma unroll
+        for (int j = 0; j < PER; ++j) {
+            float sz, sr, sc;
+            scale_preact(v[0][j], v[1][j], v[2][j], prm, sz, sr, sc);
+            Pf[0 * L * U + tid + j * NW * 32] = sz;
+            Pf[1 * L * U + tid + j * NW * 32] = sr;
+            Pf[2 * L * U + tid + j * NW * 32] = sc;
+        }
+        __syncthreads();
+    }
+
+    float G[SEG];   // H of this warp's rows (between iterations) / g_t (inside)
+#pragma unroll
+    for (int i = 0; i < SEG; ++i) G[i] = load_h ? to_f32(Hs[(r0 + i) * U + lane]) : 0.f;
     if (load_h && warp > 0) hb = to_f32(Hs[(r0 - 1) * U + lane]);
     const uint32_t hm = (s_heads[r0 >> 5] >> (r0 & 31)) & ((1u << SEG) - 1u);
     const int nvalid = min(SEG, a.T - (t0 + r0));
     const bool general = (hm != 0u) || (nvalid < SEG);
+    const void *Pv = FUSED ? static_cast<const void *>(Pf) : static_cast<const void *>(Pt);
 
     const int n_tiles = a.B * a.n_ut * a.n_chunks;
     const int tile = (b * a.n_ut + ut) * a.n_chunks + c;
 
     for (int k = a.k_first; k <= a.k_last; ++k) {
-        float Jr[SEG], Fr[SEG], A, Bv;
-        if (general) warp_pairs<TS, true>(Ps, r0, lane, Hreg, hb, hm, nvalid, prm, Jr, Fr, A, Bv);
-        else warp_pairs<TS, false>(Ps, r0, lane, Hreg, hb, hm, nvalid, prm, Jr, Fr, A, Bv);
+        float Jr[SEG], A, Bv;
+        if (general) warp_pairs<TS, FUSED, true>(Pv, r0, lane, G, hb, hm, nvalid, prm, Jr, A, Bv);
+        else warp_pairs<TS, FUSED, false>(Pv, r0, lane, G, hb, hm, nvalid, prm, Jr, A, Bv);
         s_aggA[warp][lane] = A;
         s_aggB[warp][lane] = Bv;
         __syncthreads();
@@ -207,7 +249,7 @@ __global__ void __launch_bounds__(NW * 32, 3)
             }
             unsigned long long *slot =
                 a.slots + (static_cast<size_t>(k - 1) * n_tiles + tile) * 32 + lane;
-            float C = 0.f;
+            float C = 0.f;   // H^(k) at t0 - 1 (0 before the first step)
             if (c == 0) {
                 publish(slot, 0.f, tB);
             } else {
@@ -219,30 +261,39 @@ __global__ void __launch_bounds__(NW * 32, 3)
         }
         __syncthreads();
 
-        // delta_t = J_t delta_{t-1} - F_t from the carry; H <- H + delta
-        float d = fmaf(eA, s_C[lane], eB);
-        hb = FUSED ? (hb + d) : round_to<TS>(hb + d);   // H^(k) at row r0 - 1
+        // H^(k) of this warp's rows from H^(k) at row r0 - 1
+        float h = fmaf(eA, s_C[lane], eB);
+        hb = FUSED ? h : round_to<TS>(h);
 #pragma unroll
         for (int i = 0; i < SEG; ++i) {
-            d = fmaf(Jr[i], d, -Fr[i]);
-            Hreg[i] = FUSED ? (Hreg[i] + d) : round_to<TS>(Hreg[i] + d);
+            h = fmaf(Jr[i], h, G[i]);
+            G[i] = FUSED ? h : round_to<TS>(h);
         }
     }
 
     // residual max|F(H^(K))| at the values as stored
     if (a.last && a.residual_bits != nullptr) {
-        s_hlast[warp][lane] = round_to<TS>(Hreg[SEG - 1]);
+        // s_aggA was last read before the previous barrier: reuse it for the
+        // last row of each warp
+        s_aggA[warp][lane] = round_to<TS>(G[SEG - 1]);
         __syncthreads();
         float m = 0.f;
-        float hprev = (warp == 0) ? round_to<TS>(hb) : s_hlast[warp - 1][lane];
+        float hprev = (warp == 0) ? round_to<TS>(hb) : s_aggA[warp - 1][lane];
 #pragma unroll
         for (int i = 0; i < SEG; ++i) {
             const int r = r0 + i;
+            float sz, sr, sc;
+            if (FUSED) {
+                sz = Pf[(0 * L + r) * U + lane];
+                sr = Pf[(1 * L + r) * U + lane];
+                sc = Pf[(2 * L + r) * U + lane];
+            } else {
+                scale_preact(to_f32(Pt[(0 * L + r) * U + lane]), to_f32(Pt[(1 * L + r) * U + lane]),
+                             to_f32(Pt[(2 * L + r) * U + lane]), prm, sz, sr, sc);
+            }
             const bool head = (hm >> i) & 1u;
-            const float hq = round_to<TS>(Hreg[i]);
-            const float f = cell_f(head ? 0.f : hprev, to_f32(Ps[(0 * L + r) * U + lane]),
-                                   to_f32(Ps[(1 * L + r) * U + lane]),
-                                   to_f32(Ps[(2 * L + r) * U + lane]), prm);
+            const float hq = round_to<TS>(G[i]);
+            const float f = cell_f_scaled(head ? 0.f : hprev, sz, sr, sc, prm);
             if (uok && i < nvalid) m = fmaxf(m, abs_residual(hq - f));
             hprev = hq;
         }
@@ -262,7 +313,7 @@ __global__ void __launch_bounds__(NW * 32, 3)
 #pragma unroll
         for (int i = 0; i < SEG; ++i) {
             const int t = t0 + r0 + i;
-            if (i < nvalid) Hn[(static_cast<size_t>(b) * a.T + t) * a.d_h + u] = from_f32<TS>(Hreg[i]);
+            if (i < nvalid) Hn[(static_cast<size_t>(b) * a.T + t) * a.d_h + u] = from_f32<TS>(G[i]);
         }
     }
 }
@@ -335,7 +386,8 @@ __global__ void k_bounded_wait(const uint32_t *flag, uint64_t wait_ns, uint32_t 
 
 template <typename TS, bool FUSED>
 size_t smem_bytes_for() {
-    return static_cast<size_t>(FUSED ? 3 : 4) * L * U * sizeof(TS);
+    return FUSED ? static_cast<size_t>(3) * L * U * sizeof(float)
+                 : static_cast<size_t>(4) * L * U * sizeof(TS);
 }
 
 template <typename TS, bool FUSED>

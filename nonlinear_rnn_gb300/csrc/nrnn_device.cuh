@@ -41,6 +41,12 @@ __device__ __forceinline__ float rcp_approx(float x) {
     asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
 }
+// min that propagates NaN (a NaN input must reach the residual gate)
+__device__ __forceinline__ float min_nan(float a, float b) {
+    float y;
+    asm("min.NaN.f32 %0, %1, %2;" : "=f"(y) : "f"(a), "f"(b));
+    return y;
+}
 __device__ __forceinline__ uint64_t globaltimer_ns() {
     uint64_t t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
@@ -168,6 +174,76 @@ __device__ __forceinline__ float cell_f(float h, float pz, float pr, float pc,
     const float z = sigmoid_f(fmaf(p.a_z, h, pz + p.b_z));
     const float r = sigmoid_f(fmaf(p.a_r, h, pr + p.b_r));
     const float c = tanh_f(fmaf(p.a_c, r * h, pc + p.b_c));
+    return fmaf(z, c - h, h);
+}
+
+// ---------------------------------------------- cell on pre-scaled arguments
+// The gate arguments are carried in exponent-2 units:
+//   sz = -log2(e) (P_z + b_z),  sr = -log2(e) (P_r + b_r),  sc = 2 log2(e) (P_c + b_c)
+// so that z = 1 / (1 + 2^(sz - log2(e) a_z h)) and tanh(x) = 1 - 2 / (1 + 2^(2 log2(e) x))
+// each start from one FFMA.  z and the tanh share one reciprocal:
+// 1/(dz dc) times dc gives 1/dz and times dz gives 1/dc; the arguments are
+// clamped at 63 so that dz dc stays finite (below 2^126); the clamp moves
+// sigmoid by less than 1e-19 and leaves tanh at exactly 1 in fp32.
+struct ScaledParams {
+    float na_z, na_r, a_c2;   // -log2(e) a_z, -log2(e) a_r, 2 log2(e) a_c
+    float a_z, a_r, a_c;      // for the Jacobian
+    float nb_z, nb_r, b_c2;   // -log2(e) b_z, -log2(e) b_r, 2 log2(e) b_c
+};
+
+__device__ __forceinline__ ScaledParams scale_params(const UnitParams &p) {
+    ScaledParams s;
+    s.na_z = -LOG2E * p.a_z;
+    s.na_r = -LOG2E * p.a_r;
+    s.a_c2 = 2.0f * LOG2E * p.a_c;
+    s.a_z = p.a_z;
+    s.a_r = p.a_r;
+    s.a_c = p.a_c;
+    s.nb_z = -LOG2E * p.b_z;
+    s.nb_r = -LOG2E * p.b_r;
+    s.b_c2 = 2.0f * LOG2E * p.b_c;
+    return s;
+}
+
+// pre-scaled arguments of one step from raw preactivations
+__device__ __forceinline__ void scale_preact(float pz, float pr, float pc, const ScaledParams &p,
+                                             float &sz, float &sr, float &sc) {
+    sz = fmaf(pz, -LOG2E, p.nb_z);
+    sr = fmaf(pr, -LOG2E, p.nb_r);
+    sc = fmaf(pc, 2.0f * LOG2E, p.b_c2);
+}
+
+constexpr float EXP2_CLAMP = 63.0f;
+
+// gates z, r, c at state h
+__device__ __forceinline__ void gates_scaled(float h, float sz, float sr, float sc,
+                                             const ScaledParams &p, float &z, float &r,
+                                             float &c) {
+    const float dz = 1.0f + ex2_approx(min_nan(fmaf(p.na_z, h, sz), EXP2_CLAMP));
+    r = rcp_approx(1.0f + ex2_approx(fmaf(p.na_r, h, sr)));
+    const float dc = 1.0f + ex2_approx(min_nan(fmaf(p.a_c2, r * h, sc), EXP2_CLAMP));
+    const float inv = rcp_approx(dz * dc);
+    z = dc * inv;
+    c = fmaf(-2.0f, dz * inv, 1.0f);
+}
+
+// f(h) and J = df/dh from pre-scaled arguments
+__device__ __forceinline__ void cell_fj_scaled(float h, float sz, float sr, float sc,
+                                               const ScaledParams &p, float &f, float &J) {
+    float z, r, c;
+    gates_scaled(h, sz, sr, sc, p, z, r, c);
+    const float omz = 1.0f - z;
+    const float cmh = c - h;
+    f = fmaf(z, cmh, h);
+    const float dq = fmaf(h * p.a_r, fmaf(-r, r, r), r);          // d(r h)/dh
+    const float t2 = fmaf(-c, c, 1.0f) * p.a_c * dq;               // (1 - c^2) a_c d(rh)/dh
+    J = fmaf(z, fmaf(omz * p.a_z, cmh, t2), omz);
+}
+
+__device__ __forceinline__ float cell_f_scaled(float h, float sz, float sr, float sc,
+                                               const ScaledParams &p) {
+    float z, r, c;
+    gates_scaled(h, sz, sr, sc, p, z, r, c);
     return fmaf(z, c - h, h);
 }
 
