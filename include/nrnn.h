@@ -171,6 +171,39 @@ int nrnn_debug_bounded_wait(const uint32_t *flag_dev, uint64_t wait_ns, uint32_t
                             void *stream);
 
 /*
+ * Size of the device scratch array that nrnn_newton_forward_noalloc uses
+ * (64 MiB on every GPU where the library is used, held until process exit).
+ */
+#define NRNN_NOALLOC_SCRATCH_BYTES (64u * 1024u * 1024u)
+
+/*
+ * Newton forward that allocates nothing and takes no workspace.  The pages
+ * describe no counterpart of this entry point; it exists for callers that
+ * cannot allocate device memory -- e.g. a plugin inside a host framework that
+ * owns all device allocations and offers it no pool, or a latency-bounded
+ * loop that must not call cudaMalloc/cudaFree (they can synchronise the
+ * device) -- and so cannot pass the workspace nrnn_newton_forward needs.
+ *
+ * Same arguments and results as nrnn_newton_forward with algo =
+ * NRNN_ALGO_FUSED, minus the workspace: the look-back scratch lives in one
+ * library-owned device array of NRNN_NOALLOC_SCRATCH_BYTES per GPU.
+ *   - Requests whose workspace (nrnn_newton_workspace_bytes with
+ *     NRNN_ALGO_FUSED) exceeds NRNN_NOALLOC_SCRATCH_BYTES return
+ *     NRNN_ERR_WORKSPACE before any CUDA call.
+ *   - The first call on a device looks up the array's device address with
+ *     that device current (cudaGetSymbolAddress) and caches it; make that
+ *     first call before any stream capture on the device.
+ *   - Every call on a device shares the one array; each call re-initialises
+ *     the parts that must start cleared.  Calls that overlap on the GPU
+ *     (different streams, no ordering between them) race on it: serialise them.
+ * Calls no cudaMalloc, cudaFree or allocating library routine.
+ */
+int nrnn_newton_forward_noalloc(const void *preact, int dtype, const float *params, int64_t B,
+                                int64_t T, int64_t d_h, const int32_t *cu_seqlens,
+                                int64_t num_segments, int K, float residual_fail, void *H_out,
+                                float *residual_dev, float *residual_host, void *stream);
+
+/*
  * Upper limit, in nanoseconds, of every bounded device wait that later calls
  * launch (default 2e9 = 2 s).  Process-wide; returns the previous value.
  */

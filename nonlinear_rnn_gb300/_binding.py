@@ -41,6 +41,8 @@ _SIGNATURES = {
     "nrnn_debug_head_mask": ([_vp, _i64, _i64, _vp, _vp], _int),
     "nrnn_debug_bounded_wait": ([_vp, _u64, _vp, _vp], _int),
     "nrnn_set_wait_limit_ns": ([_u64], _u64),
+    "nrnn_newton_forward_noalloc": ([_vp, _int, _vp, _i64, _i64, _i64, _vp, _i64, _int, _f, _vp,
+                                     _vp, _vp, _vp], _int),
 }
 EXPORTED = tuple(_SIGNATURES)
 
