@@ -116,15 +116,39 @@ class ClockSampler:
 
 
 def workload_bytes(w, algo):
-    """Algorithmic HBM bytes of one Newton forward (per launch list)."""
+    """Algorithmic HBM bytes per launch of one Newton forward."""
     s = 2 if w.dtype == "bf16" else 4
     tok = w.B * w.T
     if algo == "per_iter":
-        # iteration 1: read P, write H; later: read P and H, write H; the last
-        # launch evaluates the residual in-kernel (no extra pass)
-        per = [4 * w.d_h * s * tok] + [5 * w.d_h * s * tok] * (w.K - 1)
-        return per
-    return [4 * w.d_h * s * tok]
+        # iteration 1: read P, write H; later ones: read P and H^(k-1), write H^(k);
+        # the last launch evaluates the residual in-kernel (no extra pass)
+        return [4 * w.d_h * s * tok] + [5 * w.d_h * s * tok] * (w.K - 1)
+    return [4 * w.d_h * s * tok]          # fused: read P once, write H once
+
+
+# XU (MUFU) operations per cell evaluation in the Newton kernels (three
+# exp2, one reciprocal for r, one shared reciprocal for z and tanh), and the
+# XU issue rate of an SM (16 results per clock).
+XU_PER_EVAL = 5
+XU_PER_CLK_PER_SM = 16
+
+
+def time_steps(torch, fn, steps, flush, stream, nvtx=True):
+    """Per-step device time (ms) with CUDA events; L2 flushed between steps, untimed."""
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    out = None
+    for i in range(steps):
+        flush.fill_(1.0)
+        if nvtx:
+            torch.cuda.nvtx.range_push("nrnn_step")
+        ev[i][0].record(stream)
+        out = fn()
+        ev[i][1].record(stream)
+        if nvtx:
+            torch.cuda.nvtx.range_pop()
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in ev], out
 
 
 def run_ours(args, w, rank, world, local):
@@ -133,6 +157,7 @@ def run_ours(args, w, rank, world, local):
 
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
+    props = torch.cuda.get_device_properties(dev)
     inp = syn.make_inputs(w)
     tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
     x = torch.from_numpy(inp["x"]).to(dev).to(tdt)
@@ -141,13 +166,14 @@ def run_ours(args, w, rank, world, local):
     cu = inp["cu_seqlens"]
     P = nr.input_projection(x, W)
     H = torch.empty((w.B, w.T, w.d_h), dtype=tdt, device=dev)
-    ws = torch.empty(nr.workspace_bytes(w.B, w.T, w.d_h, tdt, w.K, args.algo), dtype=torch.uint8,
-                     device=dev)
+    algo = args.algo
+    ws = torch.empty(max(nr.workspace_bytes(w.B, w.T, w.d_h, tdt, w.K, a) for a in ("fused", "per_iter")),
+                     dtype=torch.uint8, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
 
-    def newton():
-        return nr.newton_forward(P, prm, cu_seqlens=cu, K=w.K, algo=args.algo, check=False,
+    def newton(a=algo):
+        return nr.newton_forward(P, prm, cu_seqlens=cu, K=w.K, algo=a, check=False,
                                  out=H, workspace=ws)
 
     for _ in range(args.warmup):
@@ -155,8 +181,6 @@ def run_ours(args, w, rank, world, local):
         newton()
     torch.cuda.synchronize()
 
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(args.steps)]
     with ClockSampler(local) as clk:
         # keep the GPU busy while the sampler starts, so that its samples cover
         # the load the timed steps run under (untimed)
@@ -170,14 +194,8 @@ def run_ours(args, w, rank, world, local):
             torch.distributed.barrier()
         torch.cuda.synchronize()
         t_wall = time.perf_counter()
-        for i in range(args.steps):
-            flush.fill_(1.0)          # L2 flush, outside the timed events
-            ev[i][0].record(stream)
-            _, rho = newton()
-            ev[i][1].record(stream)
-        torch.cuda.synchronize()
+        step_ms, (_, rho) = time_steps(torch, newton, args.steps, flush, stream)
         t_wall = time.perf_counter() - t_wall
-    step_ms = [a.elapsed_time(b) for a, b in ev]
     ms = sum(step_ms) / len(step_ms)
     if world > 1:
         t = torch.tensor([ms], device=dev)
@@ -185,45 +203,70 @@ def run_ours(args, w, rank, world, local):
         ms = float(t.item())
         torch.distributed.barrier()
 
-    # projection beside it
-    pe = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-    proj_ms = []
-    for _ in range(max(3, min(args.steps, 10))):
-        flush.fill_(1.0)
-        pe[0].record(stream)
-        nr.input_projection(x, W, out=P)
-        pe[1].record(stream)
-        torch.cuda.synchronize()
-        proj_ms.append(pe[0].elapsed_time(pe[1]))
-    proj = statistics.median(proj_ms)
+    tokens = w.B * w.T
+    pk = peaks()
+    clocks = clk.summary()
+    fused = algo != "per_iter"
+    byts = workload_bytes(w, algo)
+    launches = len(byts) if w.K > 0 else 1
+    per_launch_ms = ms / launches
+    hbm_achieved = (sum(byts) / len(byts)) / (per_launch_ms * 1e-3) / 1e9
+    kname = "k_newton<%s,%s>" % ("bf16" if w.dtype == "bf16" else "float",
+                                 "fused" if fused else "per_iter")
+    hbm = {"bound": "hbm", "achieved": hbm_achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
+           "frac": hbm_achieved / pk["hbm_gbs"], "traffic": load_traffic(w, algo),
+           "kernel": kname, "algorithmic_bytes_per_launch": sum(byts) / len(byts),
+           "peak_src": pk["src"] + " (MEASURED_PEAKS.json hbm_gbs)"}
+    if fused:
+        # one launch runs K iterations plus the residual evaluation
+        xu_ops = XU_PER_EVAL * (w.K + 1) * tokens * w.d_h
+        xu_achieved = xu_ops / (ms * 1e-3) / 1e9
+        xu_peak = XU_PER_CLK_PER_SM * props.multi_processor_count * 2070e6 / 1e9
+        roof = {"bound": "alu", "achieved": xu_achieved, "peak": xu_peak, "unit": "Gop/s (XU)",
+                "frac": xu_achieved / xu_peak, "traffic": load_traffic(w, algo), "kernel": kname,
+                "algorithmic_ops_per_launch": xu_ops,
+                "peak_src": f"{XU_PER_CLK_PER_SM} XU results/clk/SM x {props.multi_processor_count} SMs "
+                            "x 2070 MHz (maximum SM clock)",
+                "hbm": {k: hbm[k] for k in ("achieved", "peak", "unit", "frac",
+                                            "algorithmic_bytes_per_launch")}}
+    else:
+        roof = hbm
+
+    # the per-iteration kernel's HBM roofline, timed the same way
+    per_iter = None
+    if fused and w.K > 0 and not args.skip_per_iter:
+        pms, _ = time_steps(torch, lambda: newton("per_iter"), args.steps, flush, stream, nvtx=False)
+        pb = workload_bytes(w, "per_iter")
+        pl = (sum(pms) / len(pms)) / len(pb)
+        pa = (sum(pb) / len(pb)) / (pl * 1e-3) / 1e9
+        per_iter = {"bound": "hbm", "achieved": pa, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                    "frac": pa / pk["hbm_gbs"], "ms_per_step": sum(pms) / len(pms),
+                    "launches_per_step": len(pb), "traffic": load_traffic(w, "per_iter"),
+                    "kernel": kname.replace("fused", "per_iter"),
+                    "algorithmic_bytes_per_launch": sum(pb) / len(pb)}
+
+    # projection and the GPU sequential unroll beside it
+    proj_ms, _ = time_steps(torch, lambda: nr.input_projection(x, W, out=P), max(3, min(args.steps, 10)),
+                            flush, stream, nvtx=False)
+    seq_ms, _ = time_steps(torch, lambda: nr.sequential_forward(P, prm, cu_seqlens=cu, out=H), 3,
+                           flush, stream, nvtx=False)
 
     # end to end through the public call with host buffers
     P_host = P.cpu().pin_memory()
     H_host = torch.empty(H.shape, dtype=H.dtype).pin_memory()
     rho_host = torch.empty((), dtype=torch.float32).pin_memory()
-    e2e = []
-    for i in range(max(3, min(args.steps, 10)) + 1):
-        flush.fill_(1.0)
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
+
+    def e2e_step():
         Pd = P_host.to(dev, non_blocking=True)
-        Hd, r = nr.newton_forward(Pd, prm, cu_seqlens=cu, K=w.K, algo=args.algo, check=False,
+        Hd, r = nr.newton_forward(Pd, prm, cu_seqlens=cu, K=w.K, algo=algo, check=False,
                                   workspace=ws)
         H_host.copy_(Hd, non_blocking=True)
         rho_host.copy_(r, non_blocking=True)
-        b.record(stream)
-        torch.cuda.synchronize()
-        if i > 0:
-            e2e.append(a.elapsed_time(b))
+    e2e_step()
+    e2e, _ = time_steps(torch, e2e_step, max(3, min(args.steps, 10)), flush, stream, nvtx=False)
     e2e_ms = statistics.median(e2e)
 
-    tokens = w.B * w.T
-    pk = peaks()
-    byts = workload_bytes(w, args.algo)
-    per_launch_ms = ms / len(byts)
-    achieved = (sum(byts) / len(byts)) / (per_launch_ms * 1e-3) / 1e9
-    launches = len(byts) if w.K > 0 else 1
-    traffic = load_traffic(w, args.algo)
+    proj = statistics.median(proj_ms)
     out = {
         "metric": METRIC,
         "value": tokens * world / (ms * 1e-3),
@@ -238,23 +281,22 @@ def run_ours(args, w, rank, world, local):
         "dtype": w.dtype,
         "data": "synthetic (seeded SplitMix64: x~N(0,1), W_x~U(+-1/sqrt(d_in)), a~U(+-1), b=0)",
         "config": {"workload": w.name, "B": w.B, "T": w.T, "d_in": w.d_in, "d_h": w.d_h,
-                   "K": w.K, "segments": w.segments, "algo": args.algo,
+                   "K": w.K, "segments": w.segments, "algo": algo,
                    "parallelism": f"replica x{world}",
                    "l2": f"flushed between steps ({L2_FLUSH_BYTES >> 20} MiB write, untimed)"},
-        "roofline": {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
-                     "frac": achieved / pk["hbm_gbs"], "traffic": traffic,
-                     "kernel": "k_newton<%s,%s>" % ("bf16" if w.dtype == "bf16" else "float",
-                                                     "fused" if args.algo != "per_iter" else "per_iter"),
-                     "algorithmic_bytes_per_launch": sum(byts) / len(byts),
-                     "peak_src": pk["src"] + " (MEASURED_PEAKS.json hbm_gbs)"},
+        "roofline": roof,
+        "per_iter_roofline": per_iter,
         "e2e": {"value": tokens * world / (e2e_ms * 1e-3), "unit": "tokens/s",
                 "h2d_bytes_per_step": P.numel() * P.element_size(),
                 "d2h_bytes_per_step": H.numel() * H.element_size() + 4},
         "gpu_launches": launches * args.steps,
-        "with_projection": {"projection_ms": proj, "tokens_per_s": tokens * world / ((ms + proj) * 1e-3)},
+        "with_projection": {"projection_ms": proj,
+                            "tokens_per_s": tokens * world / ((ms + proj) * 1e-3)},
+        "sequential_gpu": {"ms": statistics.median(seq_ms),
+                           "tokens_per_s": tokens / (statistics.median(seq_ms) * 1e-3)},
         "residual": float(rho.item()),
         "wall_s": t_wall,
-        "clocks": clk.summary(),
+        "clocks": clocks,
     }
     return out
 
@@ -323,6 +365,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--preroll-s", type=float, default=1.0)
+    ap.add_argument("--skip-per-iter", action="store_true")
     args = ap.parse_args()
     w = syn.WORKLOADS[args.workload]
     rank, world, local = dist_env()
