@@ -77,6 +77,23 @@ bool make_map(CUtensorMap *m, const void *base, int dtype, int64_t width, int64_
     return r == CUDA_SUCCESS;
 }
 
+// 2-D bf16 map over a (outer, inner) row-major array, box (box_inner x box_outer),
+// 128-byte swizzle (box_inner * 2 must be 128 bytes).
+bool make_map_2d_sw128(CUtensorMap *m, const void *base, int64_t inner, int64_t outer,
+                       uint32_t box_inner, uint32_t box_outer) {
+    auto fn = encode_fn();
+    if (fn == nullptr) return false;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(outer)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(inner * 2)};
+    cuuint32_t box[2] = {box_inner, box_outer};
+    cuuint32_t estr[2] = {1, 1};
+    const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims,
+                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 int check_common(const void *preact, int dtype, const float *params, int64_t B, int64_t T,
                  int64_t d_h, const int32_t *cu, int64_t S) {
     if (dtype != NRNN_F32 && dtype != NRNN_BF16) return NRNN_ERR_INVALID_ARG;
@@ -262,6 +279,17 @@ int nrnn_input_projection(const void *x, const void *W_x, int dtype, int64_t row
     if (rows > 0 && (x == nullptr || W_x == nullptr || preact == nullptr)) return NRNN_ERR_INVALID_ARG;
     if (d_in % 8 != 0 || d_h % 8 != 0 || d_in > INT32_MAX || 3 * d_h > INT32_MAX)
         return NRNN_ERR_UNSUPPORTED;
+    if (rows == 0) return NRNN_OK;
+    if (dtype == NRNN_BF16) {
+        if (!aligned16(x) || !aligned16(W_x) || !aligned16(preact)) return NRNN_ERR_INVALID_ARG;
+        CUtensorMap tmA, tmB;
+        if (!make_map_2d_sw128(&tmA, x, d_in, rows, PROJ_TC_BOX_K, PROJ_TC_BOX_M) ||
+            !make_map_2d_sw128(&tmB, W_x, d_in, 3 * d_h, PROJ_TC_BOX_K, PROJ_TC_BOX_N))
+            return NRNN_ERR_CUDA;
+        return cuda_status(launch_projection_tc(tmA, tmB, rows, static_cast<int>(d_in),
+                                                static_cast<int>(3 * d_h), preact,
+                                                static_cast<cudaStream_t>(stream)));
+    }
     return cuda_status(launch_projection(dtype, x, W_x, rows, static_cast<int>(d_in),
                                          static_cast<int>(3 * d_h), preact,
                                          static_cast<cudaStream_t>(stream)));

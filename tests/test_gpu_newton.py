@@ -231,16 +231,24 @@ def test_bounded_wait_gives_up_and_context_survives(nr):
     assert torch.ones(4, device="cuda").sum().item() == 4.0  # context still usable
 
 
+PROJ_SHAPES = [(1000, 136, 72), (128, 8, 16), (4097, 512, 256), (300, 1024, 344)]
+
+
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
-def test_input_projection_matches_oracle(nr, dtype):
-    rows, d_in, d_h = 1000, 136, 72
-    rng = np.random.default_rng(3)
+@pytest.mark.parametrize("shape", PROJ_SHAPES)
+def test_input_projection_matches_oracle(nr, dtype, shape):
+    # ragged rows (M), gate columns (N = 3 d_h) and d_in (K) against the tiles
+    rows, d_in, d_h = shape
+    rng = np.random.default_rng(rows + d_in)
     x = rng.normal(size=(rows, d_in)).astype(np.float32)
     W = rng.uniform(-1, 1, size=(3 * d_h, d_in)).astype(np.float32) / math.sqrt(d_in)
     if dtype == "bf16":
         x, W = syn.round_bf16(x), syn.round_bf16(W)
     ref = oracle.input_projection(x, W)
-    P = nr.input_projection(dev(x, TDT[dtype]), dev(W, TDT[dtype]))
+    out = torch.full((rows, 3 * d_h), float("nan"), dtype=TDT[dtype], device="cuda")
+    P = nr.input_projection(dev(x, TDT[dtype]), dev(W, TDT[dtype]), out=out)
+    assert not torch.isnan(P).any()
     scale = np.abs(x) @ np.abs(W).T
     rel = np.max(np.abs(host(P) - ref) / (scale + 1e-30))
+    # f32: fp32 products and sums; bf16: exact products, fp32 sums, one bf16 rounding
     assert rel <= (1e-6 if dtype == "f32" else 8e-3), rel
