@@ -48,6 +48,21 @@ def peaks():
     return {"hbm_gbs": 6800.0, "src": "fallback"}
 
 
+def max_over_ranks(ms, world, device):
+    """Slowest rank's time (all ranks call this)."""
+    import torch
+    if world <= 1:
+        return ms
+    t = torch.tensor([float(ms)], device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def tokens_all_ranks(tokens_per_rank, world):
+    """Weak scaling: every rank runs a full replica of the workload."""
+    return tokens_per_rank * world
+
+
 def dist_env():
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -196,11 +211,8 @@ def run_ours(args, w, rank, world, local):
         t_wall = time.perf_counter()
         step_ms, (_, rho) = time_steps(torch, newton, args.steps, flush, stream)
         t_wall = time.perf_counter() - t_wall
-    ms = sum(step_ms) / len(step_ms)
+    ms = max_over_ranks(sum(step_ms) / len(step_ms), world, dev)
     if world > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
         torch.distributed.barrier()
 
     tokens = w.B * w.T
@@ -269,7 +281,7 @@ def run_ours(args, w, rank, world, local):
     proj = statistics.median(proj_ms)
     out = {
         "metric": METRIC,
-        "value": tokens * world / (ms * 1e-3),
+        "value": tokens_all_ranks(tokens, world) / (ms * 1e-3),
         "unit": "tokens/s",
         "n_gpus": world,
         "steps": args.steps,
