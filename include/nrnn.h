@@ -123,6 +123,38 @@ int nrnn_newton_forward(const void *preact, int dtype, const float *params, int6
                         void *workspace, size_t ws_bytes, void *stream);
 
 /*
+ * Parallel Newton forward started from a given iterate H^(0) = H_init instead
+ * of 0 (a warm start, e.g. from nrnn_picard; FAQs "How many Newton
+ * iterations should I use?": "try Picard warm-start").  Arguments as
+ * nrnn_newton_forward; H_init: device, (B, T, d_h) of dtype, 16-byte aligned,
+ * must not overlap H_out (NRNN_ERR_INVALID_ARG), or NULL for H^(0) = 0.
+ * With K = 0 the call returns H_out = H_init and rho = max|F(H_init)|.
+ * The fused algorithm needs L*32*elem bytes more shared memory per CTA for
+ * the initial tile; the workspace size does not change.
+ */
+int nrnn_newton_forward_init(const void *preact, int dtype, const float *params, int64_t B,
+                             int64_t T, int64_t d_h, const int32_t *cu_seqlens,
+                             int64_t num_segments, const void *H_init, int K,
+                             float residual_fail, int algo, void *H_out, float *residual_dev,
+                             float *residual_host, void *workspace, size_t ws_bytes,
+                             void *stream);
+
+/*
+ * Picard warm start (FAQs "How many Newton iterations should I use?":
+ * "try Picard warm-start (picard_iters)"; read as fixed-point sweeps):
+ * from G = 0, each sweep sets G_t = f(G_{t-1}, P_t) for all t at once from
+ * the previous sweep (shifted state 0 at t = 0 and at segment heads).  Sweep
+ * s makes steps 1..s exact.  One elementwise launch per sweep, no scan.
+ *   sweeps  >= 0 (0: H_out = 0)
+ *   H_out   device, (B, T, d_h) of dtype: the last sweep
+ *   H_tmp   device scratch of the same size, needed when sweeps >= 2; must
+ *           not overlap H_out
+ */
+int nrnn_picard(const void *preact, int dtype, const float *params, int64_t B, int64_t T,
+                int64_t d_h, const int32_t *cu_seqlens, int64_t num_segments, int sweeps,
+                void *H_out, void *H_tmp, void *stream);
+
+/*
  * Sequential forward on the GPU (sequential_apply on the pages: "eval()"
  * runs the sequential step): h_t = f(h_{t-1}, P_t) from h = 0 for each row,
  * or for each segment of a pack; one thread per (row or segment, unit).

@@ -19,6 +19,7 @@ from ._binding import (  # noqa: F401
     load,
     newton_forward,
     params_tensor,
+    picard,
     residual,
     sequential_forward,
     set_wait_limit_ns,

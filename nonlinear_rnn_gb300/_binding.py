@@ -35,6 +35,9 @@ _SIGNATURES = {
     "nrnn_newton_workspace_bytes": ([_i64, _i64, _i64, _int, _int, _int], _sz),
     "nrnn_newton_forward": ([_vp, _int, _vp, _i64, _i64, _i64, _vp, _i64, _int, _f, _int, _vp,
                              _vp, _vp, _vp, _sz, _vp], _int),
+    "nrnn_newton_forward_init": ([_vp, _int, _vp, _i64, _i64, _i64, _vp, _i64, _vp, _int, _f,
+                                  _int, _vp, _vp, _vp, _vp, _sz, _vp], _int),
+    "nrnn_picard": ([_vp, _int, _vp, _i64, _i64, _i64, _vp, _i64, _int, _vp, _vp, _vp], _int),
     "nrnn_sequential_forward": ([_vp, _int, _vp, _i64, _i64, _i64, _vp, _i64, _vp, _vp], _int),
     "nrnn_residual": ([_vp, _int, _vp, _i64, _i64, _i64, _vp, _i64, _vp, _vp, _vp], _int),
     "nrnn_input_projection": ([_vp, _vp, _int, _i64, _i64, _i64, _vp, _vp], _int),
@@ -161,14 +164,21 @@ def workspace_bytes(B, T, d_h, dtype=torch.float32, K=3, algo="auto") -> int:
 
 def newton_forward(preact: torch.Tensor, params, cu_seqlens=None, K: int = 3,
                    residual_fail: float = 1.0, algo: str = "auto", check: bool = True,
-                   out: torch.Tensor | None = None, workspace: torch.Tensor | None = None):
+                   out: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
+                   H_init: torch.Tensor | None = None, picard_iters: int = 0):
     """Parallel Newton forward.  preact (B, T, 3 d_h) float32/bfloat16 CUDA tensor.
 
     Returns (H, residual): H (B, T, d_h) in preact's dtype and residual, a
     0-dim float32 CUDA tensor holding max|F(H^(K))|.  With check=True the call
     synchronises and raises NewtonDivergenceError if the residual exceeds
-    residual_fail (the pages' runtime gate); with check=False nothing syncs."""
+    residual_fail (the pages' runtime gate); with check=False nothing syncs.
+    H_init starts Newton from a given iterate; picard_iters > 0 first runs that
+    many Picard sweeps from zero and starts Newton from their result."""
     lib = load()
+    if picard_iters > 0:
+        if H_init is not None:
+            raise ValueError("give either H_init or picard_iters")
+        H_init = picard(preact, params, picard_iters, cu_seqlens=cu_seqlens)
     preact = _device_tensor(preact, "preact")
     if preact.dim() != 3 or preact.shape[2] % 3:
         raise ValueError("preact must have shape (B, T, 3 d_h)")
@@ -187,13 +197,36 @@ def newton_forward(preact: torch.Tensor, params, cu_seqlens=None, K: int = 3,
     if workspace is None or workspace.numel() < nbytes:
         workspace = torch.empty(nbytes, dtype=torch.uint8, device=dev)
     host = ctypes.c_float(0.0) if check else None
+    if H_init is not None:
+        H_init = _device_tensor(H_init, "H_init")
+        if tuple(H_init.shape) != (B, T, d_h) or H_init.dtype != preact.dtype:
+            raise ValueError("H_init must match (B, T, d_h) and preact's dtype")
     with torch.cuda.device(dev):
-        st = lib.nrnn_newton_forward(_ptr(preact), code, _ptr(prm), B, T, d_h, _ptr(cu), S, int(K),
-                                     float(residual_fail), ALGOS[algo], _ptr(H), _ptr(rho),
-                                     ctypes.byref(host) if host is not None else None,
-                                     _ptr(workspace), workspace.numel(), _stream(dev))
+        st = lib.nrnn_newton_forward_init(_ptr(preact), code, _ptr(prm), B, T, d_h, _ptr(cu), S,
+                                          _ptr(H_init), int(K), float(residual_fail),
+                                          ALGOS[algo], _ptr(H), _ptr(rho),
+                                          ctypes.byref(host) if host is not None else None,
+                                          _ptr(workspace), workspace.numel(), _stream(dev))
     _raise(st, "newton_forward", H=H, residual=(host.value if host is not None else None))
     return H, rho
+
+
+def picard(preact: torch.Tensor, params, sweeps: int, cu_seqlens=None,
+           out: torch.Tensor | None = None) -> torch.Tensor:
+    """Picard sweeps G_t <- f(G_{t-1}, P_t) from G = 0 on the GPU."""
+    lib = load()
+    preact = _device_tensor(preact, "preact")
+    B, T, d_h = preact.shape[0], preact.shape[1], preact.shape[2] // 3
+    dev = preact.device
+    prm = params_tensor(params, d_h, dev)
+    cu, S = _cu_device(cu_seqlens, B, T, dev)
+    G = out if out is not None else torch.empty((B, T, d_h), dtype=preact.dtype, device=dev)
+    tmp = torch.empty_like(G) if sweeps >= 2 else None
+    with torch.cuda.device(dev):
+        st = lib.nrnn_picard(_ptr(preact), _dtype_code(preact), _ptr(prm), B, T, d_h, _ptr(cu), S,
+                             int(sweeps), _ptr(G), _ptr(tmp), _stream(dev))
+    _raise(st, "picard")
+    return G
 
 
 def sequential_forward(preact: torch.Tensor, params, cu_seqlens=None,

@@ -23,6 +23,12 @@ size_t elem_size(int dtype) { return dtype == NRNN_BF16 ? 2 : 4; }
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+bool overlaps(const void *a, const void *b, size_t bytes) {
+    if (a == nullptr || b == nullptr || bytes == 0) return false;
+    const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+    return x < y + bytes && y < x + bytes;
+}
+
 // Workspace: [counters (K+1) u32 | error u32] zeroed per call, then
 // [slots K x n_tiles x 32 u64] set to all-ones bytes per call, then
 // (per-iteration, K > 1) one H buffer.
@@ -153,9 +159,24 @@ int nrnn_newton_forward(const void *preact, int dtype, const float *params, int6
                         int64_t T, int64_t d_h, const int32_t *cu_seqlens,
                         int64_t num_segments, int K, float residual_fail, int algo,
                         void *H_out, float *residual_dev, float *residual_host,
-                        void *workspace, size_t ws_bytes, void *stream_) {
+                        void *workspace, size_t ws_bytes, void *stream) {
+    return nrnn_newton_forward_init(preact, dtype, params, B, T, d_h, cu_seqlens, num_segments,
+                                    nullptr, K, residual_fail, algo, H_out, residual_dev,
+                                    residual_host, workspace, ws_bytes, stream);
+}
+
+int nrnn_newton_forward_init(const void *preact, int dtype, const float *params, int64_t B,
+                             int64_t T, int64_t d_h, const int32_t *cu_seqlens,
+                             int64_t num_segments, const void *H_init, int K,
+                             float residual_fail, int algo, void *H_out, float *residual_dev,
+                             float *residual_host, void *workspace, size_t ws_bytes,
+                             void *stream_) {
     int st = check_common(preact, dtype, params, B, T, d_h, cu_seqlens, num_segments);
     if (st != NRNN_OK) return st;
+    if (H_init != nullptr &&
+        (!aligned16(H_init) ||
+         overlaps(H_init, H_out, elem_size(dtype) * static_cast<size_t>(B * T * d_h))))
+        return NRNN_ERR_INVALID_ARG;
     if (K < 0 || K > MAX_K || residual_dev == nullptr) return NRNN_ERR_INVALID_ARG;
     if (algo < NRNN_ALGO_AUTO || algo > NRNN_ALGO_FUSED) return NRNN_ERR_INVALID_ARG;
     if (B * T > 0 && (H_out == nullptr || !aligned16(H_out))) return NRNN_ERR_INVALID_ARG;
@@ -178,11 +199,13 @@ int nrnn_newton_forward(const void *preact, int dtype, const float *params, int6
 
     if (B * T > 0) {
         if (K == 0) {
-            e = cudaMemsetAsync(H_out, 0, elem_size(dtype) * B * T * d_h, stream);
+            const size_t hbytes = elem_size(dtype) * B * T * d_h;
+            e = H_init ? cudaMemcpyAsync(H_out, H_init, hbytes, cudaMemcpyDeviceToDevice, stream)
+                       : cudaMemsetAsync(H_out, 0, hbytes, stream);
             if (e == cudaSuccess)
-                e = launch_residual(dtype, preact, params, nullptr, static_cast<int>(B),
-                                    static_cast<int>(T), static_cast<int>(d_h), cu_seqlens, S,
-                                    res_bits, stream);
+                e = launch_residual(dtype, preact, params, H_init ? H_out : nullptr,
+                                    static_cast<int>(B), static_cast<int>(T),
+                                    static_cast<int>(d_h), cu_seqlens, S, res_bits, stream);
             if (e != cudaSuccess) return NRNN_ERR_CUDA;
         } else {
             CUtensorMap tmP;
@@ -202,17 +225,20 @@ int nrnn_newton_forward(const void *preact, int dtype, const float *params, int6
             a.wait_ns = g_wait_ns.load();
             uint32_t *counters = reinterpret_cast<uint32_t *>(ws + ly.counters_off);
             if (fused) {
-                a.H_prev = nullptr;
+                CUtensorMap tmH = tmP;
+                if (H_init != nullptr && !make_map(&tmH, H_init, dtype, d_h, T, B))
+                    return NRNN_ERR_CUDA;
+                a.H_prev = H_init;
                 a.H_next = H_out;
                 a.k_first = 1;
                 a.k_last = K;
                 a.last = 1;
                 a.ticket = counters;
-                e = launch_newton(dtype, true, tmP, tmP, a, ly.n_tiles, stream);
+                e = launch_newton(dtype, true, tmP, tmH, a, ly.n_tiles, stream);
                 if (e != cudaSuccess) return NRNN_ERR_CUDA;
             } else {
                 void *hbuf = ws + ly.hbuf_off;
-                const void *prev = nullptr;
+                const void *prev = H_init;
                 for (int k = 1; k <= K; ++k) {
                     // iteration K lands in H_out; earlier ones alternate with hbuf
                     void *dst = ((K - k) % 2 == 0) ? H_out : hbuf;
@@ -241,6 +267,30 @@ int nrnn_newton_forward(const void *preact, int dtype, const float *params, int6
     if (err_host != 0) return NRNN_ERR_TIMEOUT;
     const float rho = *residual_host;
     if (!std::isfinite(rho) || rho > residual_fail) return NRNN_ERR_DIVERGED;
+    return NRNN_OK;
+}
+
+int nrnn_picard(const void *preact, int dtype, const float *params, int64_t B, int64_t T,
+                int64_t d_h, const int32_t *cu_seqlens, int64_t num_segments, int sweeps,
+                void *H_out, void *H_tmp, void *stream_) {
+    int st = check_common(preact, dtype, params, B, T, d_h, cu_seqlens, num_segments);
+    if (st != NRNN_OK) return st;
+    const size_t hbytes = elem_size(dtype) * static_cast<size_t>(B * T * d_h);
+    if (sweeps < 0 || (B * T > 0 && H_out == nullptr)) return NRNN_ERR_INVALID_ARG;
+    if (sweeps >= 2 && B * T > 0 && (H_tmp == nullptr || overlaps(H_tmp, H_out, hbytes)))
+        return NRNN_ERR_INVALID_ARG;
+    if (B * T == 0) return NRNN_OK;
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+    if (sweeps == 0) return cuda_status(cudaMemsetAsync(H_out, 0, hbytes, stream));
+    const void *src = nullptr;
+    for (int k = 1; k <= sweeps; ++k) {
+        void *dst = ((sweeps - k) % 2 == 0) ? H_out : H_tmp;   // the last sweep lands in H_out
+        cudaError_t e = launch_picard(dtype, preact, params, src, dst, static_cast<int>(B),
+                                      static_cast<int>(T), static_cast<int>(d_h), cu_seqlens,
+                                      static_cast<int>(cu_seqlens ? num_segments : 0), stream);
+        if (e != cudaSuccess) return NRNN_ERR_CUDA;
+        src = dst;
+    }
     return NRNN_OK;
 }
 

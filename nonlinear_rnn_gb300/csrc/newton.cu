@@ -144,13 +144,15 @@ __global__ void __launch_bounds__(NW * 32, 4)
     k_newton(const __grid_constant__ CUtensorMap tmP, const __grid_constant__ CUtensorMap tmH,
              const NewtonArgs a) {
     extern __shared__ __align__(128) unsigned char dsmem[];
-    // FUSED: [3][L][U] fp32 pre-scaled arguments; a bf16 tile lands by TMA in
-    // the upper half and is widened in place.  Per-iteration: [3][L][U] raw
-    // preactivations followed by the [L][U] tile of H^(k-1), both of type TS.
+    // FUSED: [3][L][U] fp32 pre-scaled arguments (a bf16 tile lands by TMA in
+    // the upper half and is widened in place), then, with an initial iterate,
+    // its [L][U] tile.  Per-iteration: [3][L][U] raw preactivations followed by
+    // the [L][U] tile of H^(k-1), both of type TS.
     float *Pf = reinterpret_cast<float *>(dsmem);
     TS *Pt = FUSED ? reinterpret_cast<TS *>(dsmem + (sizeof(TS) == 2 ? 3 * L * U * 2 : 0))
                    : reinterpret_cast<TS *>(dsmem);
-    TS *Hs = reinterpret_cast<TS *>(dsmem) + 3 * L * U;
+    TS *Hs = FUSED ? reinterpret_cast<TS *>(dsmem + 3 * L * U * sizeof(float))
+                   : reinterpret_cast<TS *>(dsmem) + 3 * L * U;
     __shared__ float s_aggA[NW][32], s_aggB[NW][32];
     __shared__ float s_C[32];
     __shared__ uint32_t s_heads[L / 32];
@@ -168,7 +170,7 @@ __global__ void __launch_bounds__(NW * 32, 4)
     const int rem = static_cast<int>(s_ticket - static_cast<uint32_t>(c) * per_chunk);
     const int b = rem / a.n_ut, ut = rem - (rem / a.n_ut) * a.n_ut;
     const int t0 = c * L, u0 = ut * U;
-    const bool load_h = !FUSED && a.H_prev != nullptr;
+    const bool load_h = a.H_prev != nullptr;   // H^(k-1) (per-iteration) or H^(0) (fused)
 
     if (tid == 0) {
         mbar_init(&s_bar, 1);
@@ -360,6 +362,37 @@ __global__ void __launch_bounds__(256)
     }
 }
 
+// One Picard sweep G_out_t = f(G_in_{t-1}, P_t) for every t (G_in == null: the
+// zero trajectory; shifted state 0 at t = 0 and at segment heads).
+template <typename TS>
+__global__ void __launch_bounds__(256)
+    k_picard(const TS *__restrict__ P, const float *__restrict__ params,
+             const TS *__restrict__ G_in, TS *__restrict__ G_out, int T, int d_h,
+             const int32_t *cu, int S) {
+    __shared__ uint32_t s_heads[L / 32];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int u = blockIdx.x * U + lane, t0 = blockIdx.y * L, b = blockIdx.z;
+    if (tid < L / 32) s_heads[tid] = 0u;
+    __syncthreads();
+    if (tid == 0) mark_heads(cu, S, t0, L, s_heads);
+    __syncthreads();
+    if (u >= d_h) return;
+    const UnitParams prm = load_unit_params(params, d_h, u, true);
+    const int r0 = warp * SEG;
+    const size_t row0 = static_cast<size_t>(b) * T;
+    float hprev = (G_in != nullptr && t0 + r0 > 0) ? to_f32(G_in[(row0 + t0 + r0 - 1) * d_h + u]) : 0.f;
+    for (int i = 0; i < SEG; ++i) {
+        const int r = r0 + i, t = t0 + r;
+        if (t >= T) break;
+        const TS *p = P + (row0 + t) * 3 * d_h + u;
+        const float g = (G_in != nullptr) ? to_f32(G_in[(row0 + t) * d_h + u]) : 0.f;
+        const float hs = head_bit(s_heads, r) ? 0.f : hprev;
+        G_out[(row0 + t) * d_h + u] =
+            from_f32<TS>(cell_f(hs, to_f32(p[0]), to_f32(p[d_h]), to_f32(p[2 * d_h]), prm));
+        hprev = g;
+    }
+}
+
 __global__ void k_head_mask(const int32_t *cu, int S, int64_t N, uint8_t *mask) {
     constexpr int SPAN = 1024;
     __shared__ uint32_t bits[SPAN / 32];
@@ -385,8 +418,8 @@ __global__ void k_bounded_wait(const uint32_t *flag, uint64_t wait_ns, uint32_t 
 }
 
 template <typename TS, bool FUSED>
-size_t smem_bytes_for() {
-    return FUSED ? static_cast<size_t>(3) * L * U * sizeof(float)
+size_t smem_bytes_for(bool with_h) {
+    return FUSED ? static_cast<size_t>(3) * L * U * sizeof(float) + (with_h ? L * U * sizeof(TS) : 0)
                  : static_cast<size_t>(4) * L * U * sizeof(TS);
 }
 
@@ -394,11 +427,11 @@ template <typename TS, bool FUSED>
 cudaError_t launch_one(const CUtensorMap &tmP, const CUtensorMap &tmH, const NewtonArgs &a,
                        int64_t n_ctas, cudaStream_t stream) {
     static bool configured = false;
-    const size_t smem = smem_bytes_for<TS, FUSED>();
+    const size_t smem = smem_bytes_for<TS, FUSED>(a.H_prev != nullptr);
     if (!configured) {
         cudaError_t e = cudaFuncSetAttribute(k_newton<TS, FUSED>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(smem));
+                                             static_cast<int>(smem_bytes_for<TS, FUSED>(true)));
         if (e != cudaSuccess) return e;
         configured = true;
     }
@@ -409,8 +442,9 @@ cudaError_t launch_one(const CUtensorMap &tmP, const CUtensorMap &tmH, const New
 }  // namespace
 
 size_t newton_smem_bytes(int dtype, bool fused) {
-    if (dtype == 1) return fused ? smem_bytes_for<__nv_bfloat16, true>() : smem_bytes_for<__nv_bfloat16, false>();
-    return fused ? smem_bytes_for<float, true>() : smem_bytes_for<float, false>();
+    if (dtype == 1)
+        return fused ? smem_bytes_for<__nv_bfloat16, true>(true) : smem_bytes_for<__nv_bfloat16, false>(true);
+    return fused ? smem_bytes_for<float, true>(true) : smem_bytes_for<float, false>(true);
 }
 
 cudaError_t launch_newton(int dtype, bool fused, const CUtensorMap &tmP, const CUtensorMap &tmH,
@@ -434,6 +468,21 @@ cudaError_t launch_residual(int dtype, const void *P, const float *params, const
         k_residual<float><<<grid, 256, 0, stream>>>(static_cast<const float *>(P), params,
                                                     static_cast<const float *>(G), T, d_h, cu, S,
                                                     residual_bits);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_picard(int dtype, const void *P, const float *params, const void *G_in,
+                          void *G_out, int B, int T, int d_h, const int32_t *cu, int S,
+                          cudaStream_t stream) {
+    const dim3 grid((d_h + U - 1) / U, (T + L - 1) / L, B);
+    if (dtype == 1)
+        k_picard<__nv_bfloat16><<<grid, 256, 0, stream>>>(
+            static_cast<const __nv_bfloat16 *>(P), params, static_cast<const __nv_bfloat16 *>(G_in),
+            static_cast<__nv_bfloat16 *>(G_out), T, d_h, cu, S);
+    else
+        k_picard<float><<<grid, 256, 0, stream>>>(static_cast<const float *>(P), params,
+                                                  static_cast<const float *>(G_in),
+                                                  static_cast<float *>(G_out), T, d_h, cu, S);
     return cudaGetLastError();
 }
 

@@ -16,7 +16,8 @@ constexpr int NEWTON_SEG = 16;
 constexpr int NEWTON_L = NEWTON_NW * NEWTON_SEG;
 
 struct NewtonArgs {
-    const void *H_prev;           // (B, T, d_h) storage type; null when H^(k-1) = 0
+    const void *H_prev;           // (B, T, d_h) storage type: H^(k-1) (per-iteration) or the
+                                  // initial iterate H^(0) (fused); null = zero
     void *H_next;                 // (B, T, d_h) storage type
     const float *params;          // (6, d_h)
     const int32_t *cu;            // null or (S + 1)
@@ -48,6 +49,10 @@ cudaError_t launch_newton(int dtype, bool fused, const CUtensorMap &tmP, const C
 cudaError_t launch_residual(int dtype, const void *P, const float *params, const void *G,
                             int B, int T, int d_h, const int32_t *cu, int S,
                             uint32_t *residual_bits, cudaStream_t stream);
+
+cudaError_t launch_picard(int dtype, const void *P, const float *params, const void *G_in,
+                          void *G_out, int B, int T, int d_h, const int32_t *cu, int S,
+                          cudaStream_t stream);
 
 cudaError_t launch_sequential(int dtype, const void *P, const float *params, int B, int T,
                               int d_h, const int32_t *cu, int S, void *H, cudaStream_t stream);

@@ -16,6 +16,8 @@ shapes_layout "cu_seqlens"):
                         solved by a sequential loop, H <- H + delta; returns H and
                         rho = max|F(H^(K))| (J = 0 and shifted state 0 at segment heads);
 * ``residual``       -- max|F(G)| for a given trajectory G;
+* ``picard``         -- Picard sweeps G_t <- f(G_{t-1}, P_t) from G = 0 (warm start);
+* ``newton_init``    -- the Newton algorithm started from a given iterate;
 * ``cell``           -- one step f(h, P) and df/dh;
 * ``input_projection`` -- P = x W_x^T in float64 (a library matmul).
 
@@ -73,6 +75,11 @@ def _load():
             lib.oracle_newton.restype = ctypes.c_double
             lib.oracle_residual.argtypes = [dp, dp, i64, i64, i64, lp, i64, i64, i64, dp]
             lib.oracle_residual.restype = ctypes.c_double
+            lib.oracle_picard.argtypes = [dp, dp, i64, i64, i64, lp, i64, i64, i64, i64, dp]
+            lib.oracle_picard.restype = None
+            lib.oracle_newton_init.argtypes = [dp, dp, i64, i64, i64, lp, i64, i64, dp, i64, i64,
+                                               dp]
+            lib.oracle_newton_init.restype = ctypes.c_double
             _lib = lib
     return _lib
 
@@ -162,6 +169,31 @@ def residual(P, params, G, cu_seqlens=None, threads: int = 1) -> float:
     rhos = _run(lambda j0, j1: lib.oracle_residual(_dptr(P), _dptr(prm), B, T, d_h, cup, S,
                                                    j0, j1, _dptr(G)), d_h, threads)
     return _max_rho(rhos)
+
+
+def picard(P, params, sweeps: int, cu_seqlens=None, threads: int = 1) -> np.ndarray:
+    """Picard sweeps G_t <- f(G_{t-1}, P_t) from G = 0; returns G (B, T, d_h) float64."""
+    lib = _load()
+    P, prm, B, T, d_h, cu, S = _prep(P, params, cu_seqlens)
+    G = np.zeros((B, T, d_h), dtype=np.float64)
+    cup = cu.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)) if cu is not None else None
+    _run(lambda j0, j1: lib.oracle_picard(_dptr(P), _dptr(prm), B, T, d_h, cup, S, int(sweeps),
+                                          j0, j1, _dptr(G)), d_h, threads)
+    return G
+
+
+def newton_init(P, params, K: int, H0, cu_seqlens=None, threads: int = 1):
+    """K Newton iterations from the iterate H0; returns (H, rho)."""
+    lib = _load()
+    P, prm, B, T, d_h, cu, S = _prep(P, params, cu_seqlens)
+    H0 = np.ascontiguousarray(np.asarray(H0, dtype=np.float64))
+    assert H0.shape == (B, T, d_h)
+    H = np.zeros((B, T, d_h), dtype=np.float64)
+    cup = cu.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)) if cu is not None else None
+    rhos = _run(lambda j0, j1: lib.oracle_newton_init(_dptr(P), _dptr(prm), B, T, d_h, cup, S,
+                                                      int(K), _dptr(H0), j0, j1, _dptr(H)),
+                d_h, threads)
+    return H, _max_rho(rhos)
 
 
 def _max_rho(rhos):

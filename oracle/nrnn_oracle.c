@@ -191,3 +191,75 @@ double oracle_residual(const double *P, const double *params, int64_t B, int64_t
     free(head); free(G);
     return rho;
 }
+
+/*
+ * Picard (fixed-point) sweeps, the plainest reading of the FAQ's Picard warm
+ * start ("How many Newton iterations should I use?": "try Picard warm-start
+ * (picard_iters)"): starting from G = 0, each sweep sets G_t = f(G_{t-1}, P_t)
+ * for every t at once from the previous sweep (shifted state 0 at heads).
+ * Writes G[b, t, j] for j in [j0, j1).
+ */
+void oracle_picard(const double *P, const double *params, int64_t B, int64_t T, int64_t d_h,
+                   const int64_t *cu, int64_t S, int64_t sweeps, int64_t j0, int64_t j1,
+                   double *Gout)
+{
+    unsigned char *head = (unsigned char *)malloc((size_t)(T > 0 ? T : 1));
+    double *G = (double *)malloc(sizeof(double) * (size_t)(T > 0 ? T : 1));
+    double *Gn = (double *)malloc(sizeof(double) * (size_t)(T > 0 ? T : 1));
+    head_mask(cu, S, T, head);
+    for (int64_t b = 0; b < B; ++b) {
+        const double *Pb = P + b * T * 3 * d_h;
+        for (int64_t j = j0; j < j1; ++j) {
+            double prm[6];
+            unit_params(params, d_h, j, prm);
+            for (int64_t t = 0; t < T; ++t) G[t] = 0.0;
+            for (int64_t s = 0; s < sweeps; ++s) {
+                for (int64_t t = 0; t < T; ++t) {
+                    const double *p = Pb + t * 3 * d_h;
+                    const double hs = head[t] ? 0.0 : G[t - 1];
+                    oracle_cell(hs, p[j], p[d_h + j], p[2 * d_h + j], prm, &Gn[t], NULL);
+                }
+                for (int64_t t = 0; t < T; ++t) G[t] = Gn[t];
+            }
+            for (int64_t t = 0; t < T; ++t) Gout[(b * T + t) * d_h + j] = G[t];
+        }
+    }
+    free(head); free(G); free(Gn);
+}
+
+/*
+ * The parallel-Newton algorithm of oracle_newton started from a given iterate
+ * H^(0) = H0 (B, T, d_h) instead of 0 (a warm start).  H and H0 may alias.
+ */
+double oracle_newton_init(const double *P, const double *params, int64_t B, int64_t T,
+                          int64_t d_h, const int64_t *cu, int64_t S, int64_t K,
+                          const double *H0, int64_t j0, int64_t j1, double *H)
+{
+    unsigned char *head = (unsigned char *)malloc((size_t)(T > 0 ? T : 1));
+    double *G = (double *)malloc(sizeof(double) * (size_t)(T > 0 ? T : 1));
+    double *F = (double *)malloc(sizeof(double) * (size_t)(T > 0 ? T : 1));
+    double *J = (double *)malloc(sizeof(double) * (size_t)(T > 0 ? T : 1));
+    head_mask(cu, S, T, head);
+    double rho = 0.0;
+    for (int64_t b = 0; b < B; ++b) {
+        const double *Pb = P + b * T * 3 * d_h;
+        for (int64_t j = j0; j < j1; ++j) {
+            double prm[6];
+            unit_params(params, d_h, j, prm);
+            for (int64_t t = 0; t < T; ++t) G[t] = H0[(b * T + t) * d_h + j];
+            for (int64_t k = 0; k < K; ++k) {
+                residual_row(Pb, prm, T, d_h, j, head, G, F, J);
+                double delta = 0.0;
+                for (int64_t t = 0; t < T; ++t) {
+                    delta = J[t] * delta - F[t];
+                    G[t] += delta;
+                }
+            }
+            const double r = residual_row(Pb, prm, T, d_h, j, head, G, NULL, NULL);
+            if (!(r <= rho)) rho = r;
+            for (int64_t t = 0; t < T; ++t) H[(b * T + t) * d_h + j] = G[t];
+        }
+    }
+    free(head); free(G); free(F); free(J);
+    return rho;
+}

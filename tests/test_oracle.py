@@ -241,3 +241,48 @@ def test_input_projection_is_matmul():
     P = oracle.input_projection(x, W)
     assert P.shape == (2, 5, 6)
     assert P[1, 3, 4] == pytest.approx(sum(x[1, 3, i] * W[4, i] for i in range(4)), abs=1e-14)
+
+
+# ------------------------------------------------- Picard and warm-started Newton
+@pytest.mark.parametrize("n", [1, 2, 5])
+def test_picard_first_n_steps_exact_and_T_sweeps_is_unroll(n):
+    """Sweep n makes step n exact (the shifted state of step n is exact after
+    n - 1 sweeps); T sweeps reproduce the unroll."""
+    T, d_h = 30, 4
+    P = RNG.normal(0, 1, (2, T, 3 * d_h))
+    prm = _params(d_h, RNG)
+    Hs = oracle.sequential(P, prm)
+    G = oracle.picard(P, prm, n)
+    np.testing.assert_allclose(G[:, :n], Hs[:, :n], atol=1e-15)
+    assert np.max(np.abs(G[:, n:] - Hs[:, n:])) > 1e-12
+    np.testing.assert_allclose(oracle.picard(P, prm, T), Hs, atol=1e-15)
+
+
+def test_picard_fixed_point_is_the_unroll():
+    w = syn.small_workload(B=2, T=200, d_h=8, seed=8)
+    P = syn.direct_preact(w).astype(np.float64)
+    prm = syn.make_params(w)
+    Hs = oracle.sequential(P, prm)
+    # one more sweep applied to the unroll changes nothing: f(h_{t-1}) = h_t
+    G = oracle.picard(P, prm, 1)  # from zero: first step only
+    assert np.allclose(G[:, 0], Hs[:, 0], atol=1e-15)
+    Hn, rho = oracle.newton_init(P, prm, 3, Hs)   # Newton at the fixed point stays there
+    np.testing.assert_allclose(Hn, Hs, atol=1e-15)
+    assert rho < 1e-15
+
+
+def test_newton_init_from_zero_equals_newton_and_warm_start_exactness():
+    T, d_h = 40, 3
+    P = RNG.normal(0, 1, (1, T, 3 * d_h))
+    prm = _params(d_h, RNG)
+    a, ra = oracle.newton(P, prm, 3)
+    b, rb = oracle.newton_init(P, prm, 3, np.zeros((1, T, d_h)))
+    np.testing.assert_array_equal(a, b)
+    assert ra == rb
+    Hs = oracle.sequential(P, prm)
+    G = oracle.picard(P, prm, 2)            # steps 1..2 exact
+    H, _ = oracle.newton_init(P, prm, 3, G)  # each Newton iteration adds one exact step
+    np.testing.assert_allclose(H[:, :5], Hs[:, :5], atol=1e-15)
+    cu = syn.cu_from_lengths([9, 0, 20, 11])
+    Gp = oracle.picard(P, prm, 40, cu_seqlens=cu)
+    np.testing.assert_allclose(Gp, oracle.sequential(P, prm, cu_seqlens=cu), atol=1e-15)
