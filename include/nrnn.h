@@ -140,6 +140,27 @@ int nrnn_newton_forward_init(const void *preact, int dtype, const float *params,
                              void *stream);
 
 /*
+ * Backward (adjoint) pass for training (shapes_layout page: "train
+ * forward+backward surface"; no equations on the pages, plainest reading):
+ * with gH = dL/dH at the trajectory H (e.g. the Newton result),
+ *   lambda_t = gH_t + J_{t+1} lambda_{t+1} (0 after the end; J = 0 at segment
+ *   heads), dL/dP_{t,g} = lambda_t df/dP_g,
+ *   dL/d(a_g, b_g) = sum over (b, t) of lambda_t df/d(a_g, b_g),
+ * derivatives taken at (H_{t-1}, P_t) (H_{-1} = 0 at heads).  Solved by the
+ * same chunked decoupled look-back scan as the forward, in reverse time.
+ *   H, gH     device, (B, T, d_h) of dtype, 16-byte aligned
+ *   gP        device, (B, T, 3 d_h) of dtype (out)
+ *   gparams   device, fp32 (6, d_h) (out; overwritten)
+ *   workspace >= nrnn_newton_workspace_bytes(B, T, d_h, dtype, 1, NRNN_ALGO_FUSED)
+ * Results are accumulated with atomics: within float rounding, not bitwise
+ * reproducible.
+ */
+int nrnn_newton_backward(const void *preact, int dtype, const float *params, int64_t B,
+                         int64_t T, int64_t d_h, const int32_t *cu_seqlens, int64_t num_segments,
+                         const void *H, const void *gH, void *gP, float *gparams,
+                         void *workspace, size_t ws_bytes, void *stream);
+
+/*
  * Picard warm start (FAQs "How many Newton iterations should I use?":
  * "try Picard warm-start (picard_iters)"; read as fixed-point sweeps):
  * from G = 0, each sweep sets G_t = f(G_{t-1}, P_t) for all t at once from
@@ -173,6 +194,31 @@ int nrnn_sequential_forward(const void *preact, int dtype, const float *params, 
 int nrnn_residual(const void *preact, int dtype, const float *params, int64_t B, int64_t T,
                   int64_t d_h, const int32_t *cu_seqlens, int64_t num_segments,
                   const void *G, float *residual_dev, void *stream);
+
+/*
+ * Decode step (FAQs "How do I pass recurrent state between decode steps?":
+ * a fixed-size carry (slots, d_h); decode_step(..., out=)): one T = 1 step
+ * h_out = f(h_in, P) per slot.
+ *   preact  device, (slots, 3 d_h) of dtype, gate blocks [z | r | c]
+ *   h_in    device, (slots, d_h) of dtype, or NULL for the zero state
+ *   h_out   device, (slots, d_h) of dtype; may be h_in (in place), must not
+ *           overlap preact
+ * No alignment or d_h restriction.
+ */
+int nrnn_decode_step(const void *preact, int dtype, const float *params, int64_t slots,
+                     int64_t d_h, const void *h_in, void *h_out, void *stream);
+
+/*
+ * Decode step with the input projection fused in (FAQs: "decode_wx +
+ * decode_step"): P_s = W_x x_s (fp32 accumulation, rounded to dtype as the
+ * stored preactivation would be), then h_out = f(h_in, P).
+ *   x       device, (slots, d_in) of dtype;  W_x device, (3 d_h, d_in) of dtype
+ *   h_in    device (slots, d_h) or NULL;  h_out device (slots, d_h), may be h_in
+ *   slots <= 262140.
+ */
+int nrnn_decode_step_x(const void *x, const void *W_x, int dtype, const float *params,
+                       int64_t slots, int64_t d_in, int64_t d_h, const void *h_in, void *h_out,
+                       void *stream);
 
 /*
  * Input projection P = x W_x^T (shapes_layout page: "W_x" reads x of layout

@@ -12,11 +12,13 @@ from ._binding import (  # noqa: F401
     NewtonDivergenceError,
     NrnnError,
     bounded_wait,
+    decode_step,
     default_agreement_atol,
     head_mask,
     input_projection,
     lib_path,
     load,
+    newton_backward,
     newton_forward,
     params_tensor,
     picard,

@@ -37,7 +37,11 @@ _SIGNATURES = {
                              _vp, _vp, _vp, _sz, _vp], _int),
     "nrnn_newton_forward_init": ([_vp, _int, _vp, _i64, _i64, _i64, _vp, _i64, _vp, _int, _f,
                                   _int, _vp, _vp, _vp, _vp, _sz, _vp], _int),
+    "nrnn_newton_backward": ([_vp, _int, _vp, _i64, _i64, _i64, _vp, _i64, _vp, _vp, _vp, _vp,
+                              _vp, _sz, _vp], _int),
     "nrnn_picard": ([_vp, _int, _vp, _i64, _i64, _i64, _vp, _i64, _int, _vp, _vp, _vp], _int),
+    "nrnn_decode_step": ([_vp, _int, _vp, _i64, _i64, _vp, _vp, _vp], _int),
+    "nrnn_decode_step_x": ([_vp, _vp, _int, _vp, _i64, _i64, _i64, _vp, _vp, _vp], _int),
     "nrnn_sequential_forward": ([_vp, _int, _vp, _i64, _i64, _i64, _vp, _i64, _vp, _vp], _int),
     "nrnn_residual": ([_vp, _int, _vp, _i64, _i64, _i64, _vp, _i64, _vp, _vp, _vp], _int),
     "nrnn_input_projection": ([_vp, _vp, _int, _i64, _i64, _i64, _vp, _vp], _int),
@@ -211,6 +215,35 @@ def newton_forward(preact: torch.Tensor, params, cu_seqlens=None, K: int = 3,
     return H, rho
 
 
+def newton_backward(preact: torch.Tensor, params, H: torch.Tensor, gH: torch.Tensor,
+                    cu_seqlens=None):
+    """Adjoint of the recurrence at trajectory H for upstream gradient gH = dL/dH.
+    Returns (gP (B, T, 3 d_h) in preact's dtype, gparams (6, d_h) fp32)."""
+    lib = load()
+    preact = _device_tensor(preact, "preact")
+    H = _device_tensor(H, "H")
+    gH = _device_tensor(gH, "gH")
+    B, T, d_h = preact.shape[0], preact.shape[1], preact.shape[2] // 3
+    if tuple(H.shape) != (B, T, d_h) or tuple(gH.shape) != (B, T, d_h):
+        raise ValueError("H and gH must be (B, T, d_h)")
+    if H.dtype != preact.dtype or gH.dtype != preact.dtype:
+        raise TypeError("H and gH must share preact's dtype")
+    dev = preact.device
+    prm = params_tensor(params, d_h, dev)
+    cu, S = _cu_device(cu_seqlens, B, T, dev)
+    code = _dtype_code(preact)
+    gP = torch.empty_like(preact)
+    gprm = torch.empty((6, d_h), dtype=torch.float32, device=dev)
+    nbytes = lib.nrnn_newton_workspace_bytes(B, T, d_h, code, 1, ALGOS["fused"])
+    ws = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=dev)
+    with torch.cuda.device(dev):
+        st = lib.nrnn_newton_backward(_ptr(preact), code, _ptr(prm), B, T, d_h, _ptr(cu), S,
+                                      _ptr(H), _ptr(gH), _ptr(gP), _ptr(gprm), _ptr(ws),
+                                      ws.numel(), _stream(dev))
+    _raise(st, "newton_backward")
+    return gP, gprm
+
+
 def picard(preact: torch.Tensor, params, sweeps: int, cu_seqlens=None,
            out: torch.Tensor | None = None) -> torch.Tensor:
     """Picard sweeps G_t <- f(G_{t-1}, P_t) from G = 0 on the GPU."""
@@ -245,6 +278,38 @@ def sequential_forward(preact: torch.Tensor, params, cu_seqlens=None,
         st = lib.nrnn_sequential_forward(_ptr(preact), _dtype_code(preact), _ptr(prm), B, T, d_h,
                                          _ptr(cu), S, _ptr(H), _stream(dev))
     _raise(st, "sequential_forward")
+    return H
+
+
+def decode_step(params, h: torch.Tensor | None = None, preact: torch.Tensor | None = None,
+                x: torch.Tensor | None = None, W_x: torch.Tensor | None = None,
+                out: torch.Tensor | None = None) -> torch.Tensor:
+    """One T = 1 step per slot: h_out = f(h, P) from preact (slots, 3 d_h), or
+    from x (slots, d_in) and W_x (3 d_h, d_in) with the projection fused in.
+    h (slots, d_h) is the carried state (None = zeros); out may be h."""
+    lib = load()
+    if (preact is None) == (x is None):
+        raise ValueError("give preact, or x and W_x")
+    src = preact if preact is not None else x
+    src = _device_tensor(src, "preact" if preact is not None else "x")
+    dev = src.device
+    slots = src.shape[0]
+    d_h = (src.shape[1] // 3) if preact is not None else W_x.shape[0] // 3
+    prm = params_tensor(params, d_h, dev)
+    if h is not None:
+        h = _device_tensor(h, "h")
+        if tuple(h.shape) != (slots, d_h) or h.dtype != src.dtype:
+            raise ValueError("h must be (slots, d_h) in the input dtype")
+    H = out if out is not None else torch.empty((slots, d_h), dtype=src.dtype, device=dev)
+    with torch.cuda.device(dev):
+        if preact is not None:
+            st = lib.nrnn_decode_step(_ptr(src), _dtype_code(src), _ptr(prm), slots, d_h, _ptr(h),
+                                      _ptr(H), _stream(dev))
+        else:
+            W_x = _device_tensor(W_x, "W_x")
+            st = lib.nrnn_decode_step_x(_ptr(src), _ptr(W_x), _dtype_code(src), _ptr(prm), slots,
+                                        src.shape[1], d_h, _ptr(h), _ptr(H), _stream(dev))
+    _raise(st, "decode_step")
     return H
 
 

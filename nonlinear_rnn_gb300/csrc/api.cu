@@ -270,6 +270,52 @@ int nrnn_newton_forward_init(const void *preact, int dtype, const float *params,
     return NRNN_OK;
 }
 
+int nrnn_newton_backward(const void *preact, int dtype, const float *params, int64_t B,
+                         int64_t T, int64_t d_h, const int32_t *cu_seqlens, int64_t num_segments,
+                         const void *H, const void *gH, void *gP, float *gparams,
+                         void *workspace, size_t ws_bytes, void *stream_) {
+    int st = check_common(preact, dtype, params, B, T, d_h, cu_seqlens, num_segments);
+    if (st != NRNN_OK) return st;
+    if (gparams == nullptr) return NRNN_ERR_INVALID_ARG;
+    if (B * T > 0 && (H == nullptr || gH == nullptr || gP == nullptr || !aligned16(H) ||
+                      !aligned16(gH) || !aligned16(gP)))
+        return NRNN_ERR_INVALID_ARG;
+    const SyncLayout ly = layout(B, T, d_h, dtype, 1, true);
+    if (workspace == nullptr || ws_bytes < ly.total ||
+        (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+        return NRNN_ERR_WORKSPACE;
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+    unsigned char *ws = static_cast<unsigned char *>(workspace);
+    cudaError_t e = cudaMemsetAsync(gparams, 0, sizeof(float) * 6 * d_h, stream);
+    if (e != cudaSuccess) return NRNN_ERR_CUDA;
+    if (B * T == 0) return NRNN_OK;
+    e = cudaMemsetAsync(ws, 0, ly.zero_bytes, stream);
+    if (e == cudaSuccess) e = cudaMemsetAsync(ws + ly.slots_off, 0xff, ly.slots_bytes, stream);
+    if (e != cudaSuccess) return NRNN_ERR_CUDA;
+    CUtensorMap tmP, tmH, tmG;
+    if (!make_map(&tmP, preact, dtype, 3 * d_h, T, B) || !make_map(&tmH, H, dtype, d_h, T, B) ||
+        !make_map(&tmG, gH, dtype, d_h, T, B))
+        return NRNN_ERR_CUDA;
+    BackwardArgs a{};
+    a.H = H;
+    a.gH = gH;
+    a.gP = gP;
+    a.gparams = gparams;
+    a.params = params;
+    a.cu = cu_seqlens;
+    a.S = static_cast<int>(cu_seqlens ? num_segments : 0);
+    a.B = static_cast<int>(B);
+    a.T = static_cast<int>(T);
+    a.d_h = static_cast<int>(d_h);
+    a.n_ut = static_cast<int>((d_h + TILE_U - 1) / TILE_U);
+    a.n_chunks = static_cast<int>((T + NEWTON_L - 1) / NEWTON_L);
+    a.slots = reinterpret_cast<unsigned long long *>(ws + ly.slots_off);
+    a.ticket = reinterpret_cast<uint32_t *>(ws + ly.counters_off);
+    a.error = reinterpret_cast<uint32_t *>(ws + ly.error_off);
+    a.wait_ns = g_wait_ns.load();
+    return cuda_status(launch_backward(dtype, tmP, tmH, tmG, a, ly.n_tiles, stream));
+}
+
 int nrnn_picard(const void *preact, int dtype, const float *params, int64_t B, int64_t T,
                 int64_t d_h, const int32_t *cu_seqlens, int64_t num_segments, int sweeps,
                 void *H_out, void *H_tmp, void *stream_) {
@@ -305,6 +351,35 @@ int nrnn_sequential_forward(const void *preact, int dtype, const float *params, 
                                          static_cast<int>(T), static_cast<int>(d_h), cu_seqlens,
                                          static_cast<int>(cu_seqlens ? num_segments : 0), H_out,
                                          static_cast<cudaStream_t>(stream)));
+}
+
+int nrnn_decode_step(const void *preact, int dtype, const float *params, int64_t slots,
+                     int64_t d_h, const void *h_in, void *h_out, void *stream) {
+    if (dtype != NRNN_F32 && dtype != NRNN_BF16) return NRNN_ERR_INVALID_ARG;
+    if (slots < 0 || d_h <= 0) return NRNN_ERR_INVALID_ARG;
+    if (slots == 0) return NRNN_OK;
+    if (preact == nullptr || params == nullptr || h_out == nullptr) return NRNN_ERR_INVALID_ARG;
+    if (slots * d_h > INT32_MAX || d_h > INT32_MAX / 3) return NRNN_ERR_UNSUPPORTED;
+    if (overlaps(h_out, preact, elem_size(dtype) * static_cast<size_t>(slots * 3 * d_h)))
+        return NRNN_ERR_INVALID_ARG;
+    return cuda_status(launch_decode_step(dtype, preact, params, h_in, h_out,
+                                          static_cast<int>(slots), static_cast<int>(d_h),
+                                          static_cast<cudaStream_t>(stream)));
+}
+
+int nrnn_decode_step_x(const void *x, const void *W_x, int dtype, const float *params,
+                       int64_t slots, int64_t d_in, int64_t d_h, const void *h_in, void *h_out,
+                       void *stream) {
+    if (dtype != NRNN_F32 && dtype != NRNN_BF16) return NRNN_ERR_INVALID_ARG;
+    if (slots < 0 || d_in <= 0 || d_h <= 0) return NRNN_ERR_INVALID_ARG;
+    if (slots == 0) return NRNN_OK;
+    if (x == nullptr || W_x == nullptr || params == nullptr || h_out == nullptr)
+        return NRNN_ERR_INVALID_ARG;
+    if (slots > 4 * 65535 || d_h > INT32_MAX / 3 || d_in > INT32_MAX) return NRNN_ERR_UNSUPPORTED;
+    return cuda_status(launch_decode_step_x(dtype, x, W_x, params, h_in, h_out,
+                                            static_cast<int>(slots), static_cast<int>(d_in),
+                                            static_cast<int>(d_h),
+                                            static_cast<cudaStream_t>(stream)));
 }
 
 int nrnn_residual(const void *preact, int dtype, const float *params, int64_t B, int64_t T,

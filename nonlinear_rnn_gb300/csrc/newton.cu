@@ -37,64 +37,6 @@ constexpr int NW = NEWTON_NW;
 constexpr int SEG = NEWTON_SEG;
 constexpr int L = NEWTON_L;
 constexpr int U = TILE_U;
-constexpr int WIN = 4;   // predecessors read in parallel per look-back round
-
-// A slot holding SLOT_EMPTY has not been published yet.  Published pairs never
-// take this value (arithmetic NaNs are 0x7fffffff; see publish()).
-constexpr unsigned long long SLOT_EMPTY = 0xffffffffffffffffull;
-
-// Publishes this lane's (A, b) for a chunk.  The 64-bit word is both the data
-// and its ready flag (single-copy atomic), so no fence is needed: a reader
-// sees either SLOT_EMPTY, the aggregate or the inclusive prefix, and the
-// aggregate and the inclusive prefix (A = 0) both compose correctly.
-__device__ __forceinline__ void publish(unsigned long long *slot, float A, float b) {
-    unsigned long long v = pack_pair(A, b);
-    if (v == SLOT_EMPTY) v = pack_pair(__int_as_float(0x7fffffff), b);
-    st_relaxed_u64(slot, v);
-}
-
-// Decoupled look-back for one unit (one lane): composes the pairs of chunks
-// c-1, c-2, ... until a closed prefix (A = 0) or the start of the sequence,
-// and returns the carry delta_{t0-1}.  `slot` is this lane's slot of chunk c;
-// chunk q's slot is slot - (c - q) * 32.  Up to WIN predecessors are read per
-// round with independent loads.  Bounded: gives up after wait_ns without
-// progress, sets bit 0 of *error and returns the partial prefix.
-__device__ __forceinline__ float lookback_lane(const unsigned long long *slot, int c,
-                                               uint64_t wait_ns, uint32_t *error) {
-    float cA = 1.f, cB = 0.f;
-    int p = c - 1;
-    while (p >= 0) {
-        unsigned long long v[WIN];
-#pragma unroll
-        for (int i = 0; i < WIN; ++i)
-            v[i] = (p - i >= 0) ? ld_relaxed_u64(slot - static_cast<size_t>(c - p + i) * 32)
-                                : pack_pair(0.f, 0.f);
-        int folded = 0;
-#pragma unroll
-        for (int i = 0; i < WIN; ++i) {
-            if (folded < i || v[i] == SLOT_EMPTY) break;
-            cB = fmaf(cA, pair_b(v[i]), cB);
-            cA *= pair_A(v[i]);
-            ++folded;
-        }
-        if (cA == 0.f) break;          // closed prefix (an inclusive or a head)
-        p -= folded;
-        if (folded == 0) {
-            // nothing ready: poll the nearest predecessor alone (bounded)
-            const unsigned long long *q = slot - static_cast<size_t>(c - p) * 32;
-            const uint64_t t_wait = globaltimer_ns();
-            while (ld_relaxed_u64(q) == SLOT_EMPTY) {
-                __nanosleep(64);
-                if (globaltimer_ns() - t_wait > wait_ns) {
-                    atomicOr(error, 1u);
-                    return cB;
-                }
-            }
-        }
-    }
-    return cB;
-}
-
 // Affine pairs (J_t, g_t) of this warp's SEG rows at the shifted iterate,
 // with g_t = f(h~_t) - J_t h~_t, so that the new iterate solves
 // H^(k)_t = J_t H^(k)_{t-1} + g_t: the Newton step delta_t = J_t delta_{t-1} - F_t
@@ -256,7 +198,7 @@ __global__ void __launch_bounds__(NW * 32, 4)
                 publish(slot, 0.f, tB);
             } else {
                 publish(slot, tA, tB);
-                C = lookback_lane(slot, c, a.wait_ns, a.error);
+                C = lookback_lane(slot, c, -1, a.n_chunks, a.wait_ns, a.error);
                 publish(slot, 0.f, fmaf(tA, C, tB));
             }
             s_C[lane] = C;

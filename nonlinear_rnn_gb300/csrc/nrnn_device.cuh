@@ -293,4 +293,70 @@ __device__ __forceinline__ float pair_b(unsigned long long v) {
     return __uint_as_float(static_cast<uint32_t>(v >> 32));
 }
 
+// ------------------------------------------------- decoupled look-back slots
+// One 64-bit word per (chunk, unit) holds the chunk's affine pair (A, b) and is
+// its own ready flag: SLOT_EMPTY (all ones, written by a per-call memset)
+// means not yet published.  Published pairs never take that value (arithmetic
+// NaNs are 0x7fffffff; publish() remaps the one colliding pattern).  Because
+// a 64-bit aligned access is single-copy atomic, a reader sees either
+// SLOT_EMPTY, the chunk aggregate, or the inclusive prefix (A = 0), and the
+// latter two both compose correctly: no fence is needed on either side.
+constexpr unsigned long long SLOT_EMPTY = 0xffffffffffffffffull;
+constexpr int LOOKBACK_WIN = 4;   // neighbours read in parallel per round
+
+__device__ __forceinline__ void publish(unsigned long long *slot, float A, float b) {
+    unsigned long long v = pack_pair(A, b);
+    if (v == SLOT_EMPTY) v = pack_pair(__int_as_float(0x7fffffff), b);
+    st_relaxed_u64(slot, v);
+}
+
+// Decoupled look-back for one unit (one lane) of chunk c: composes the pairs
+// of chunks c + dir, c + 2 dir, ... (dir = -1: earlier chunks, forward scan;
+// dir = +1: later chunks, reverse scan) until a closed prefix (A = 0) or the
+// end of the sequence, and returns the carry into chunk c.  `slot` is this
+// lane's slot of chunk c; chunk c + dir d has slot + dir d 32.  Up to
+// LOOKBACK_WIN neighbours are read per round with independent loads; while
+// nothing is ready only the nearest is polled.  Bounded: gives up after
+// wait_ns without progress, sets bit 0 of *error and returns the partial
+// prefix.
+__device__ __forceinline__ float lookback_lane(const unsigned long long *slot, int c, int dir,
+                                               int n_chunks, uint64_t wait_ns, uint32_t *error) {
+    float cA = 1.f, cB = 0.f;
+    int d = 1;   // distance of the next neighbour to fold
+    for (;;) {
+        const int q = c + dir * d;
+        if (q < 0 || q >= n_chunks) break;
+        unsigned long long v[LOOKBACK_WIN];
+#pragma unroll
+        for (int i = 0; i < LOOKBACK_WIN; ++i) {
+            const int qi = c + dir * (d + i);
+            v[i] = (qi >= 0 && qi < n_chunks)
+                       ? ld_relaxed_u64(slot + static_cast<ptrdiff_t>(dir) * (d + i) * 32)
+                       : pack_pair(0.f, 0.f);
+        }
+        int folded = 0;
+#pragma unroll
+        for (int i = 0; i < LOOKBACK_WIN; ++i) {
+            if (folded < i || v[i] == SLOT_EMPTY) break;
+            cB = fmaf(cA, pair_b(v[i]), cB);
+            cA *= pair_A(v[i]);
+            ++folded;
+        }
+        if (cA == 0.f) break;          // closed prefix (an inclusive or a head)
+        d += folded;
+        if (folded == 0) {
+            const unsigned long long *nq = slot + static_cast<ptrdiff_t>(dir) * d * 32;
+            const uint64_t t_wait = globaltimer_ns();
+            while (ld_relaxed_u64(nq) == SLOT_EMPTY) {
+                __nanosleep(64);
+                if (globaltimer_ns() - t_wait > wait_ns) {
+                    atomicOr(error, 1u);
+                    return cB;
+                }
+            }
+        }
+    }
+    return cB;
+}
+
 }  // namespace nrnn

@@ -33,6 +33,26 @@ struct NewtonArgs {
     unsigned long long wait_ns;   // limit of every bounded wait
 };
 
+struct BackwardArgs {
+    const void *H;                // (B, T, d_h) trajectory the derivatives are taken at
+    const void *gH;               // (B, T, d_h) dL/dH
+    void *gP;                     // (B, T, 3 d_h) dL/dP (out)
+    float *gparams;               // (6, d_h) dL/d(params), accumulated (zeroed by the caller)
+    const float *params;
+    const int32_t *cu;
+    int S;
+    int B, T, d_h;
+    int n_ut, n_chunks;
+    unsigned long long *slots;    // [n_tiles][32]
+    uint32_t *ticket;
+    uint32_t *error;
+    unsigned long long wait_ns;
+};
+
+cudaError_t launch_backward(int dtype, const CUtensorMap &tmP, const CUtensorMap &tmH,
+                            const CUtensorMap &tmG, const BackwardArgs &a, int64_t n_ctas,
+                            cudaStream_t stream);
+
 // Workspace of one call: [counters | error] zeroed, [slots] set to all-ones
 // bytes, then (per-iteration variant, K > 1) one H buffer.
 struct SyncLayout {
@@ -53,6 +73,12 @@ cudaError_t launch_residual(int dtype, const void *P, const float *params, const
 cudaError_t launch_picard(int dtype, const void *P, const float *params, const void *G_in,
                           void *G_out, int B, int T, int d_h, const int32_t *cu, int S,
                           cudaStream_t stream);
+
+cudaError_t launch_decode_step(int dtype, const void *P, const float *params, const void *h_in,
+                               void *h_out, int slots, int d_h, cudaStream_t stream);
+cudaError_t launch_decode_step_x(int dtype, const void *x, const void *W, const float *params,
+                                 const void *h_in, void *h_out, int slots, int d_in, int d_h,
+                                 cudaStream_t stream);
 
 cudaError_t launch_sequential(int dtype, const void *P, const float *params, int B, int T,
                               int d_h, const int32_t *cu, int S, void *H, cudaStream_t stream);

@@ -19,6 +19,8 @@ shapes_layout "cu_seqlens"):
 * ``picard``         -- Picard sweeps G_t <- f(G_{t-1}, P_t) from G = 0 (warm start);
 * ``newton_init``    -- the Newton algorithm started from a given iterate;
 * ``cell``           -- one step f(h, P) and df/dh;
+* ``decode_step``    -- one T = 1 step per slot with a carried state;
+* ``backward``       -- adjoint of the unroll: dL/dP and dL/d(params) from dL/dH;
 * ``input_projection`` -- P = x W_x^T in float64 (a library matmul).
 
 The arithmetic lives in ``nrnn_oracle.c`` (plain C, float64, no fused
@@ -80,6 +82,9 @@ def _load():
             lib.oracle_newton_init.argtypes = [dp, dp, i64, i64, i64, lp, i64, i64, dp, i64, i64,
                                                dp]
             lib.oracle_newton_init.restype = ctypes.c_double
+            lib.oracle_backward.argtypes = [dp, dp, i64, i64, i64, lp, i64, dp, dp, i64, i64,
+                                            dp, dp]
+            lib.oracle_backward.restype = None
             _lib = lib
     return _lib
 
@@ -201,6 +206,37 @@ def _max_rho(rhos):
     for r in rhos:
         if not (r <= out):
             out = float(r)
+    return out
+
+
+def backward(P, params, H, gH, cu_seqlens=None, threads: int = 1):
+    """Adjoint pass through h_t = f(h_{t-1}, P_t) at trajectory H for upstream
+    gradient gH (both (B, T, d_h)); returns (gP (B, T, 3 d_h), gparams (6, d_h))."""
+    lib = _load()
+    P, prm, B, T, d_h, cu, S = _prep(P, params, cu_seqlens)
+    H = np.ascontiguousarray(np.asarray(H, dtype=np.float64))
+    gH = np.ascontiguousarray(np.asarray(gH, dtype=np.float64))
+    assert H.shape == gH.shape == (B, T, d_h)
+    gP = np.zeros((B, T, 3 * d_h))
+    gprm = np.zeros((6, d_h))
+    cup = cu.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)) if cu is not None else None
+    _run(lambda j0, j1: lib.oracle_backward(_dptr(P), _dptr(prm), B, T, d_h, cup, S, _dptr(H),
+                                            _dptr(gH), j0, j1, _dptr(gP), _dptr(gprm)),
+         d_h, threads)
+    return gP, gprm
+
+
+def decode_step(P, params, h=None) -> np.ndarray:
+    """One T = 1 step per slot: h_out[s, j] = f(h[s, j], P[s]) (h None = zeros);
+    P (slots, 3 d_h).  The sequential unroll taken one step at a time."""
+    P = np.asarray(P, dtype=np.float64)
+    slots, d_h = P.shape[0], P.shape[1] // 3
+    h = np.zeros((slots, d_h)) if h is None else np.asarray(h, dtype=np.float64)
+    prm = pack_params(params)
+    out = np.empty((slots, d_h))
+    for s in range(slots):
+        for j in range(d_h):
+            out[s, j] = cell(h[s, j], P[s, j], P[s, d_h + j], P[s, 2 * d_h + j], prm[:, j])[0]
     return out
 
 

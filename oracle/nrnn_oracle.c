@@ -263,3 +263,56 @@ double oracle_newton_init(const double *P, const double *params, int64_t B, int6
     free(head); free(G); free(F); free(J);
     return rho;
 }
+
+/*
+ * Backward (adjoint) pass through the recurrence h_t = f(h_{t-1}, P_t), the
+ * plainest reading of the pages' "train forward+backward surface" (shapes_layout
+ * page): given the trajectory H and dL/dH, the total derivative
+ *   lambda_t = dL/dh_t = dL/dH_t + J_{t+1} lambda_{t+1}   (lambda after the end = 0,
+ *   J = 0 at segment heads, so nothing flows across a segment boundary)
+ * gives dL/dP_{t,g} = lambda_t df/dP_g and dL/da_g, dL/db_g summed over (b, t).
+ * Derivatives at (h~ = H_{t-1}, P_t):
+ *   df/dP_z = z (1 - z) (c - h~),  df/dP_c = z (1 - c^2),
+ *   df/dP_r = z (1 - c^2) a_c h~ r (1 - r);  df/db_g = df/dP_g;
+ *   df/da_z = df/dP_z h~,  df/da_r = df/dP_r h~,  df/da_c = df/dP_c r h~.
+ * Writes gP (B, T, 3 d_h) and adds into gprm (6, d_h) for units [j0, j1).
+ */
+void oracle_backward(const double *P, const double *params, int64_t B, int64_t T, int64_t d_h,
+                     const int64_t *cu, int64_t S, const double *H, const double *gH,
+                     int64_t j0, int64_t j1, double *gP, double *gprm)
+{
+    unsigned char *head = (unsigned char *)malloc((size_t)(T > 0 ? T : 1));
+    head_mask(cu, S, T, head);
+    for (int64_t b = 0; b < B; ++b) {
+        for (int64_t j = j0; j < j1; ++j) {
+            double prm[6];
+            unit_params(params, d_h, j, prm);
+            double carry = 0.0;   /* J_{t+1} lambda_{t+1} */
+            for (int64_t t = T - 1; t >= 0; --t) {
+                const double *p = P + (b * T + t) * 3 * d_h;
+                const double hs = head[t] ? 0.0 : H[(b * T + t - 1) * d_h + j];
+                const double z = sigmoid(p[j] + prm[0] * hs + prm[3]);
+                const double r = sigmoid(p[d_h + j] + prm[1] * hs + prm[4]);
+                const double c = tanh(p[2 * d_h + j] + prm[2] * r * hs + prm[5]);
+                const double lambda = gH[(b * T + t) * d_h + j] + carry;
+                const double dPz = z * (1.0 - z) * (c - hs);
+                const double dPc = z * (1.0 - c * c);
+                const double dPr = dPc * prm[2] * hs * r * (1.0 - r);
+                double *g = gP + (b * T + t) * 3 * d_h;
+                g[j] = lambda * dPz;
+                g[d_h + j] = lambda * dPr;
+                g[2 * d_h + j] = lambda * dPc;
+                gprm[0 * d_h + j] += lambda * dPz * hs;
+                gprm[1 * d_h + j] += lambda * dPr * hs;
+                gprm[2 * d_h + j] += lambda * dPc * r * hs;
+                gprm[3 * d_h + j] += lambda * dPz;
+                gprm[4 * d_h + j] += lambda * dPr;
+                gprm[5 * d_h + j] += lambda * dPc;
+                double J = 0.0;
+                if (!head[t]) oracle_cell(hs, p[j], p[d_h + j], p[2 * d_h + j], prm, NULL, &J);
+                carry = J * lambda;
+            }
+        }
+    }
+    free(head);
+}

@@ -1,0 +1,57 @@
+"""Decode steps on the GPU against the oracle: one step, carried state over
+many steps (equals the unroll), and the projection-fused variant."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synthetic as syn
+
+pytestmark = pytest.mark.gpu
+
+
+def dev(a, dtype=torch.float32):
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).cuda().to(dtype)
+
+
+def host(t):
+    return t.float().cpu().numpy().astype(np.float64)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_decode_step_matches_oracle_and_carries_state(dtype):
+    import nonlinear_rnn_gb300 as nr
+    tdt = torch.float32 if dtype == "f32" else torch.bfloat16
+    w = syn.small_workload(B=37, T=50, d_h=20, dtype=dtype, seed=61)   # 37 slots
+    P = syn.direct_preact(w)
+    prm = syn.make_params(w)
+    Pd = dev(P, tdt)
+    h = nr.decode_step(prm, preact=Pd[:, 0])
+    np.testing.assert_allclose(host(h), oracle.decode_step(P[:, 0], prm), atol=1e-6 if dtype == "f32" else 4e-3)
+    Hs = oracle.sequential(P, prm)
+    for t in range(1, w.T):
+        h = nr.decode_step(prm, h=h, preact=Pd[:, t], out=h)          # in place
+    tol = 1e-5 if dtype == "f32" else 3e-2                            # bf16 carry rounds every step
+    assert np.max(np.abs(host(h) - Hs[:, -1])) <= tol
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_decode_step_with_fused_projection(dtype):
+    import nonlinear_rnn_gb300 as nr
+    tdt = torch.float32 if dtype == "f32" else torch.bfloat16
+    slots, d_in, d_h = 13, 72, 24
+    rng = np.random.default_rng(62)
+    x = rng.normal(size=(slots, d_in)).astype(np.float32)
+    W = (rng.uniform(-1, 1, size=(3 * d_h, d_in)) / math.sqrt(d_in)).astype(np.float32)
+    h0 = rng.uniform(-0.5, 0.5, size=(slots, d_h)).astype(np.float32)
+    if dtype == "bf16":
+        x, W, h0 = syn.round_bf16(x), syn.round_bf16(W), syn.round_bf16(h0)
+    prm = syn.make_params(syn.small_workload(d_h=d_h, seed=63))
+    P = oracle.input_projection(x, W)
+    if dtype == "bf16":
+        P = syn.round_bf16(P.astype(np.float32))
+    ref = oracle.decode_step(P, prm, h0)
+    h = nr.decode_step(prm, h=dev(h0, tdt), x=dev(x, tdt), W_x=dev(W, tdt))
+    assert np.max(np.abs(host(h) - ref)) <= (2e-6 if dtype == "f32" else 1.6e-2)

@@ -286,3 +286,54 @@ def test_newton_init_from_zero_equals_newton_and_warm_start_exactness():
     cu = syn.cu_from_lengths([9, 0, 20, 11])
     Gp = oracle.picard(P, prm, 40, cu_seqlens=cu)
     np.testing.assert_allclose(Gp, oracle.sequential(P, prm, cu_seqlens=cu), atol=1e-15)
+
+
+def test_decode_steps_repeated_are_the_unroll():
+    """T decode steps with the state carried reproduce the unroll of the same
+    preactivations (each slot a row)."""
+    w = syn.small_workload(B=3, T=20, d_h=5, seed=60)
+    P = syn.direct_preact(w).astype(np.float64)
+    prm = syn.make_params(w)
+    Hs = oracle.sequential(P, prm)
+    h = None
+    for t in range(w.T):
+        h = oracle.decode_step(P[:, t], prm, h)
+        np.testing.assert_allclose(h, Hs[:, t], atol=1e-15)
+
+
+# --------------------------------------------------------------- the adjoint
+def _loss(P, prm, wts, cu=None):
+    return float(np.sum(wts * oracle.sequential(P, prm, cu_seqlens=cu)))
+
+
+@pytest.mark.parametrize("ragged", [False, True])
+def test_backward_matches_finite_differences(ragged):
+    """dL/dP and dL/d(params) of L = sum(w * H_unroll) against central
+    differences of the unroll (a path that never calls the adjoint)."""
+    rng = np.random.default_rng(70)
+    if ragged:
+        cu = syn.cu_from_lengths([6, 0, 9, 1, 4])
+        B, T = 1, int(cu[-1])
+    else:
+        cu, B, T = None, 2, 14
+    d_h = 3
+    P = rng.normal(0, 1, (B, T, 3 * d_h))
+    prm = oracle.pack_params(_params(d_h, rng, scale=1.2, bias=0.4))
+    wts = rng.normal(size=(B, T, d_h))
+    H = oracle.sequential(P, prm, cu_seqlens=cu)
+    gP, gprm = oracle.backward(P, prm, H, wts, cu_seqlens=cu)
+    eps = 1e-6
+    for idx in [(0, 0, 0), (0, T - 1, 3 * d_h - 1), (B - 1, T // 2, d_h + 1), (0, 3, 2 * d_h),
+                (B - 1, 1, 4)]:
+        Pp, Pm = P.copy(), P.copy()
+        Pp[idx] += eps
+        Pm[idx] -= eps
+        fd = (_loss(Pp, prm, wts, cu) - _loss(Pm, prm, wts, cu)) / (2 * eps)
+        assert gP[idx] == pytest.approx(fd, abs=1e-7)
+    for g in range(6):
+        for j in range(d_h):
+            pp, pm = prm.copy(), prm.copy()
+            pp[g, j] += eps
+            pm[g, j] -= eps
+            fd = (_loss(P, pp, wts, cu) - _loss(P, pm, wts, cu)) / (2 * eps)
+            assert gprm[g, j] == pytest.approx(fd, abs=1e-7)
