@@ -378,8 +378,13 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--preroll-s", type=float, default=1.0)
     ap.add_argument("--skip-per-iter", action="store_true")
+    ap.add_argument("--batch", type=int, default=0,
+                    help="override the workload's batch rows (smaller profiling captures)")
     args = ap.parse_args()
     w = syn.WORKLOADS[args.workload]
+    if args.batch > 0:
+        import dataclasses
+        w = dataclasses.replace(w, B=args.batch, name=w.name.replace(f"B{w.B} ", f"B{args.batch} "))
     rank, world, local = dist_env()
 
     if args.impl == "reference":

@@ -83,17 +83,20 @@ bool make_map(CUtensorMap *m, const void *base, int dtype, int64_t width, int64_
     return r == CUDA_SUCCESS;
 }
 
-// 2-D bf16 map over a (outer, inner) row-major array, box (box_inner x box_outer),
-// 128-byte swizzle (box_inner * 2 must be 128 bytes).
+// 2-D map over a (outer, inner) row-major bf16 or fp32 array, box
+// (box_inner x box_outer), 128-byte swizzle (box_inner * elem must be 128 bytes).
 bool make_map_2d_sw128(CUtensorMap *m, const void *base, int64_t inner, int64_t outer,
-                       uint32_t box_inner, uint32_t box_outer) {
+                       uint32_t box_inner, uint32_t box_outer, int dtype = NRNN_BF16) {
     auto fn = encode_fn();
     if (fn == nullptr) return false;
+    const size_t es = elem_size(dtype);
     cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(outer)};
-    cuuint64_t strides[1] = {static_cast<cuuint64_t>(inner * 2)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(inner * es)};
     cuuint32_t box[2] = {box_inner, box_outer};
     cuuint32_t estr[2] = {1, 1};
-    const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims,
+    const CUresult r = fn(m, dtype == NRNN_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+                          2, const_cast<void *>(base), dims,
                           strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -415,9 +418,15 @@ int nrnn_input_projection(const void *x, const void *W_x, int dtype, int64_t row
                                                 static_cast<int>(3 * d_h), preact,
                                                 static_cast<cudaStream_t>(stream)));
     }
-    return cuda_status(launch_projection(dtype, x, W_x, rows, static_cast<int>(d_in),
-                                         static_cast<int>(3 * d_h), preact,
-                                         static_cast<cudaStream_t>(stream)));
+    if (!aligned16(x) || !aligned16(W_x) || !aligned16(preact)) return NRNN_ERR_INVALID_ARG;
+    CUtensorMap tmA, tmB;
+    if (!make_map_2d_sw128(&tmA, x, d_in, rows, PROJ_T3_BOX_K, PROJ_T3_BOX_MN, NRNN_F32) ||
+        !make_map_2d_sw128(&tmB, W_x, d_in, 3 * d_h, PROJ_T3_BOX_K, PROJ_T3_BOX_MN, NRNN_F32))
+        return NRNN_ERR_CUDA;
+    return cuda_status(launch_projection_tf32x3(tmA, tmB, rows, static_cast<int>(d_in),
+                                                static_cast<int>(3 * d_h),
+                                                static_cast<float *>(preact),
+                                                static_cast<cudaStream_t>(stream)));
 }
 
 int nrnn_debug_head_mask(const int32_t *cu_seqlens, int64_t num_segments, int64_t N,

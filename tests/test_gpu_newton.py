@@ -250,5 +250,7 @@ def test_input_projection_matches_oracle(nr, dtype, shape):
     assert not torch.isnan(P).any()
     scale = np.abs(x) @ np.abs(W).T
     rel = np.max(np.abs(host(P) - ref) / (scale + 1e-30))
-    # f32: fp32 products and sums; bf16: exact products, fp32 sums, one bf16 rounding
-    assert rel <= (1e-6 if dtype == "f32" else 8e-3), rel
+    # f32: split-TF32 tensor-core products (three TF32 terms, error of order
+    # 2^-21 of sum |x||W|) with fp32 sums, checked against the 1e-5 relative
+    # band of the projection; bf16: exact products, fp32 sums, one bf16 rounding
+    assert rel <= (1e-5 if dtype == "f32" else 8e-3), rel
