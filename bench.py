@@ -178,7 +178,7 @@ def run_ours(args, w, rank, world, local):
     x = torch.from_numpy(inp["x"]).to(dev).to(tdt)
     W = torch.from_numpy(inp["W_x"]).to(dev).to(tdt)
     prm = nr.params_tensor(inp["params"], w.d_h, dev)
-    cu = inp["cu_seqlens"]
+    cu = None if inp["cu_seqlens"] is None else nr.DeviceCuSeqlens(inp["cu_seqlens"], w.T, dev)
     P = nr.input_projection(x, W)
     H = torch.empty((w.B, w.T, w.d_h), dtype=tdt, device=dev)
     algo = args.algo
@@ -187,9 +187,20 @@ def run_ours(args, w, rank, world, local):
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
 
-    def newton(a=algo):
+    def newton_call(a=algo):
         return nr.newton_forward(P, prm, cu_seqlens=cu, K=w.K, algo=a, check=False,
                                  out=H, workspace=ws)
+
+    def graphed(a):
+        """The forward (per-call memsets + kernels) captured once as a CUDA graph."""
+        newton_call(a)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            res = newton_call(a)
+        return lambda: (g.replay(), res)[1]
+
+    newton = graphed(algo) if args.graph else newton_call
 
     for _ in range(args.warmup):
         flush.fill_(1.0)
@@ -247,7 +258,10 @@ def run_ours(args, w, rank, world, local):
     # the per-iteration kernel's HBM roofline, timed the same way
     per_iter = None
     if fused and w.K > 0 and not args.skip_per_iter:
-        pms, _ = time_steps(torch, lambda: newton("per_iter"), args.steps, flush, stream, nvtx=False)
+        per_iter_step = graphed("per_iter") if args.graph else (lambda: newton_call("per_iter"))
+        for _ in range(args.warmup):
+            per_iter_step()
+        pms, _ = time_steps(torch, per_iter_step, args.steps, flush, stream, nvtx=False)
         pb = workload_bytes(w, "per_iter")
         pl = (sum(pms) / len(pms)) / len(pb)
         pa = (sum(pb) / len(pb)) / (pl * 1e-3) / 1e9
@@ -295,6 +309,7 @@ def run_ours(args, w, rank, world, local):
         "config": {"workload": w.name, "B": w.B, "T": w.T, "d_in": w.d_in, "d_h": w.d_h,
                    "K": w.K, "segments": w.segments, "algo": algo,
                    "parallelism": f"replica x{world}",
+                   "launch": "CUDA graph replay of one forward" if args.graph else "eager launches",
                    "l2": f"flushed between steps ({L2_FLUSH_BYTES >> 20} MiB write, untimed)"},
         "roofline": roof,
         "per_iter_roofline": per_iter,
@@ -378,6 +393,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--preroll-s", type=float, default=1.0)
     ap.add_argument("--skip-per-iter", action="store_true")
+    ap.add_argument("--no-graph", dest="graph", action="store_false",
+                    help="launch each forward eagerly instead of replaying a CUDA graph")
     ap.add_argument("--batch", type=int, default=0,
                     help="override the workload's batch rows (smaller profiling captures)")
     args = ap.parse_args()

@@ -9,6 +9,7 @@ from ._binding import (  # noqa: F401
     GATE_ORDER,
     AgreementError,
     AgreementReport,
+    DeviceCuSeqlens,
     NewtonDivergenceError,
     NrnnError,
     bounded_wait,

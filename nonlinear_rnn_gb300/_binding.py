@@ -152,11 +152,26 @@ def validate_cu_seqlens(cu_seqlens, N: int) -> np.ndarray:
     return cu32
 
 
+class DeviceCuSeqlens:
+    """cu_seqlens validated once on the host and kept on the device, so that
+    calls (and CUDA-graph captures of them) need no host-to-device copy."""
+
+    def __init__(self, cu_seqlens, N: int, device="cuda"):
+        cu32 = validate_cu_seqlens(cu_seqlens, N)
+        self.N = int(N)
+        self.num_segments = cu32.size - 1
+        self.tensor = torch.from_numpy(cu32).to(device)
+
+
 def _cu_device(cu_seqlens, B, T, device):
     if cu_seqlens is None:
         return None, 0
     if B != 1:
         raise ValueError("cu_seqlens requires batch 1 (x of shape (1, N, d))")
+    if isinstance(cu_seqlens, DeviceCuSeqlens):
+        if cu_seqlens.N != T or cu_seqlens.tensor.device != torch.device(device):
+            raise ValueError("cu_seqlens was validated for another length or device")
+        return cu_seqlens.tensor, cu_seqlens.num_segments
     cu32 = validate_cu_seqlens(cu_seqlens, T)
     return torch.from_numpy(cu32).to(device), cu32.size - 1
 

@@ -252,13 +252,12 @@ __global__ void __launch_bounds__(NW * 32, 4)
         }
     }
 
-    TS *Hn = reinterpret_cast<TS *>(a.H_next);
     if (uok) {
+        TS *o = reinterpret_cast<TS *>(a.H_next) +
+                (static_cast<size_t>(b) * a.T + t0 + r0) * a.d_h + u;
 #pragma unroll
-        for (int i = 0; i < SEG; ++i) {
-            const int t = t0 + r0 + i;
-            if (i < nvalid) Hn[(static_cast<size_t>(b) * a.T + t) * a.d_h + u] = from_f32<TS>(G[i]);
-        }
+        for (int i = 0; i < SEG; ++i, o += a.d_h)
+            if (i < nvalid) *o = from_f32<TS>(G[i]);
     }
 }
 
