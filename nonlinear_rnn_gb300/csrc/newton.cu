@@ -44,7 +44,9 @@ constexpr int U = TILE_U;
 // aggregate (A, Bv).  On return G[i] holds g_t.  SCALED: Ps holds fp32
 // pre-scaled arguments; otherwise raw preactivations of type TS.  GENERAL
 // handles segment heads (J = 0, shifted state 0) and rows past T (identity).
-template <typename TS, bool SCALED, bool GENERAL>
+// ZERO: the first iteration from H^(0) = 0, where every shifted state is 0 and
+// g = f(0); the gate arguments lose their state terms.
+template <typename TS, bool SCALED, bool GENERAL, bool ZERO = false>
 __device__ __forceinline__ void warp_pairs(const void *Pv, int r0, int lane, float (&G)[SEG],
                                            float hprev, uint32_t hm, int nvalid,
                                            const ScaledParams &prm, float (&Jr)[SEG], float &A,
@@ -65,10 +67,15 @@ __device__ __forceinline__ void warp_pairs(const void *Pv, int r0, int lane, flo
             scale_preact(to_f32(P[(0 * L + r) * U + lane]), to_f32(P[(1 * L + r) * U + lane]),
                          to_f32(P[(2 * L + r) * U + lane]), prm, sz, sr, sc);
         }
-        const float hs = (GENERAL && ((hm >> i) & 1u)) ? 0.f : hprev;
-        float f, J;
-        cell_fj_scaled(hs, sz, sr, sc, prm, f, J);
-        float g = fmaf(-J, hs, f);
+        const float hs = (ZERO || (GENERAL && ((hm >> i) & 1u))) ? 0.f : hprev;
+        float f, J, g;
+        if (ZERO) {
+            cell_fj_scaled_at_zero(sz, sr, sc, prm, f, J);
+            g = f;
+        } else {
+            cell_fj_scaled(hs, sz, sr, sc, prm, f, J);
+            g = fmaf(-J, hs, f);
+        }
         if (GENERAL) {
             if ((hm >> i) & 1u) J = 0.f;
             if (i >= nvalid) { J = 1.f; g = 0.f; }
@@ -172,24 +179,28 @@ __global__ void __launch_bounds__(NW * 32, 4)
 
     for (int k = a.k_first; k <= a.k_last; ++k) {
         float Jr[SEG], A, Bv;
-        if (general) warp_pairs<TS, FUSED, true>(Pv, r0, lane, G, hb, hm, nvalid, prm, Jr, A, Bv);
-        else warp_pairs<TS, FUSED, false>(Pv, r0, lane, G, hb, hm, nvalid, prm, Jr, A, Bv);
+        if (FUSED && k == 1 && !load_h) {
+            if (general) warp_pairs<TS, true, true, true>(Pv, r0, lane, G, hb, hm, nvalid, prm, Jr, A, Bv);
+            else warp_pairs<TS, true, false, true>(Pv, r0, lane, G, hb, hm, nvalid, prm, Jr, A, Bv);
+        } else if (general) {
+            warp_pairs<TS, FUSED, true>(Pv, r0, lane, G, hb, hm, nvalid, prm, Jr, A, Bv);
+        } else {
+            warp_pairs<TS, FUSED, false>(Pv, r0, lane, G, hb, hm, nvalid, prm, Jr, A, Bv);
+        }
         s_aggA[warp][lane] = A;
         s_aggB[warp][lane] = Bv;
         __syncthreads();
 
-        // exclusive prefix of this warp within the chunk
-        float eA = 1.f, eB = 0.f;
-        for (int w = 0; w < warp; ++w) {
-            eB = fmaf(s_aggA[w][lane], eB, s_aggB[w][lane]);
-            eA *= s_aggA[w][lane];
-        }
         if (warp == 0) {
+            // chunk aggregate; every warp's exclusive prefix replaces its aggregate
             float tA = 1.f, tB = 0.f;
 #pragma unroll
             for (int w = 0; w < NW; ++w) {
-                tB = fmaf(s_aggA[w][lane], tB, s_aggB[w][lane]);
-                tA *= s_aggA[w][lane];
+                const float wa = s_aggA[w][lane], wb = s_aggB[w][lane];
+                s_aggA[w][lane] = tA;
+                s_aggB[w][lane] = tB;
+                tB = fmaf(wa, tB, wb);
+                tA *= wa;
             }
             unsigned long long *slot =
                 a.slots + (static_cast<size_t>(k - 1) * n_tiles + tile) * 32 + lane;
@@ -206,7 +217,7 @@ __global__ void __launch_bounds__(NW * 32, 4)
         __syncthreads();
 
         // H^(k) of this warp's rows from H^(k) at row r0 - 1
-        float h = fmaf(eA, s_C[lane], eB);
+        float h = fmaf(s_aggA[warp][lane], s_C[lane], s_aggB[warp][lane]);
         hb = FUSED ? h : round_to<TS>(h);
 #pragma unroll
         for (int i = 0; i < SEG; ++i) {
@@ -217,8 +228,8 @@ __global__ void __launch_bounds__(NW * 32, 4)
 
     // residual max|F(H^(K))| at the values as stored
     if (a.last && a.residual_bits != nullptr) {
-        // s_aggA was last read before the previous barrier: reuse it for the
-        // last row of each warp
+        // each warp read only its own prefix slot in the apply step: reuse the
+        // slots for the last row of each warp
         s_aggA[warp][lane] = round_to<TS>(G[SEG - 1]);
         __syncthreads();
         float m = 0.f;

@@ -243,6 +243,21 @@ __device__ __forceinline__ void cell_fj_scaled(float h, float sz, float sr, floa
     J = fmaf(z, fmaf(omz * p.a_z, cmh, t2), omz);
 }
 
+// f(0) and J at the zero state: z = sig(P_z + b_z), r = sig(P_r + b_r),
+// c = tanh(P_c + b_c), f = z c, J = (1 - z) + z ((1 - z) a_z c + (1 - c^2) a_c r)
+__device__ __forceinline__ void cell_fj_scaled_at_zero(float sz, float sr, float sc,
+                                                       const ScaledParams &p, float &f, float &J) {
+    const float dz = 1.0f + ex2_approx(min_nan(sz, EXP2_CLAMP));
+    const float r = rcp_approx(1.0f + ex2_approx(sr));
+    const float dc = 1.0f + ex2_approx(min_nan(sc, EXP2_CLAMP));
+    const float inv = rcp_approx(dz * dc);
+    const float z = dc * inv;
+    const float c = fmaf(-2.0f, dz * inv, 1.0f);
+    const float omz = 1.0f - z;
+    f = z * c;
+    J = fmaf(z, fmaf(omz * p.a_z, c, fmaf(-c, c, 1.0f) * p.a_c * r), omz);
+}
+
 __device__ __forceinline__ float cell_f_scaled(float h, float sz, float sr, float sc,
                                                const ScaledParams &p) {
     float z, r, c;
