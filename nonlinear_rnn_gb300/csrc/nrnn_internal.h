@@ -89,9 +89,6 @@ cudaError_t launch_head_mask(const int32_t *cu, int S, int64_t N, uint8_t *mask,
 cudaError_t launch_bounded_wait(const uint32_t *flag, uint64_t wait_ns, uint32_t *result,
                                 cudaStream_t stream);
 
-cudaError_t launch_projection(int dtype, const void *x, const void *W, int64_t rows, int d_in,
-                              int n_out, void *P, cudaStream_t stream);
-
 // bf16 tensor-core projection: tmA over x (d_in, rows), tmB over W_x (d_in, n_out),
 // both bf16 with a 64 x 128 / 64 x 256 box and the 128-byte swizzle.
 constexpr int PROJ_TC_BOX_K = 64, PROJ_TC_BOX_M = 128, PROJ_TC_BOX_N = 256;
