@@ -282,6 +282,17 @@ int nrnn_newton_forward_noalloc(const void *preact, int dtype, const float *para
                                 float *residual_dev, float *residual_host, void *stream);
 
 /*
+ * Debug: from the next call on, the Newton tile with index `tile` (tile =
+ * (b * ceil(d_h / 32) + unit_tile) * ceil(T / 128) + chunk) never publishes
+ * its look-back slot, so that the later chunks of its column wait for it
+ * until their bounded wait gives up.  The call then still terminates and,
+ * with residual_host non-NULL, returns NRNN_ERR_TIMEOUT (H_out is invalid).
+ * tile < 0 switches it off (the default).  Process-wide; returns the
+ * previous value.  For testing the failure path only.
+ */
+int64_t nrnn_debug_withhold_publish(int64_t tile);
+
+/*
  * Upper limit, in nanoseconds, of every bounded device wait that later calls
  * launch (default 2e9 = 2 s).  Process-wide; returns the previous value.
  */

@@ -13,6 +13,7 @@ from ._binding import (  # noqa: F401
     NewtonDivergenceError,
     NrnnError,
     bounded_wait,
+    debug_withhold_publish,
     decode_step,
     default_agreement_atol,
     head_mask,

@@ -48,6 +48,7 @@ _SIGNATURES = {
     "nrnn_debug_head_mask": ([_vp, _i64, _i64, _vp, _vp], _int),
     "nrnn_debug_bounded_wait": ([_vp, _u64, _vp, _vp], _int),
     "nrnn_set_wait_limit_ns": ([_u64], _u64),
+    "nrnn_debug_withhold_publish": ([_i64], _i64),
     "nrnn_newton_forward_noalloc": ([_vp, _int, _vp, _i64, _i64, _i64, _vp, _i64, _int, _f, _vp,
                                      _vp, _vp, _vp], _int),
 }
@@ -389,6 +390,11 @@ def bounded_wait(flag: torch.Tensor, wait_ns: int) -> int:
 
 def set_wait_limit_ns(ns: int) -> int:
     return int(load().nrnn_set_wait_limit_ns(int(ns)))
+
+
+def debug_withhold_publish(tile: int) -> int:
+    """Debug: the given Newton tile stops publishing its look-back slot (-1: off)."""
+    return int(load().nrnn_debug_withhold_publish(int(tile)))
 
 
 @dataclass

@@ -15,6 +15,7 @@ using namespace nrnn;
 namespace {
 
 std::atomic<uint64_t> g_wait_ns{2000000000ull};
+std::atomic<int64_t> g_withhold_tile{-1};
 constexpr int MAX_K = 64;
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
@@ -140,6 +141,10 @@ int nrnn_version(void) { return 100; }
 
 uint64_t nrnn_set_wait_limit_ns(uint64_t ns) { return g_wait_ns.exchange(ns); }
 
+int64_t nrnn_debug_withhold_publish(int64_t tile) {
+    return g_withhold_tile.exchange(tile < 0 || tile > INT32_MAX ? -1 : tile);
+}
+
 int nrnn_validate_cu_seqlens(const int32_t *cu_host, int64_t num_segments, int64_t N) {
     if (cu_host == nullptr || num_segments < 0 || N < 0) return NRNN_ERR_INVALID_ARG;
     if (num_segments < 1) return NRNN_ERR_CU_SEQLENS;
@@ -226,6 +231,7 @@ int nrnn_newton_forward_init(const void *preact, int dtype, const float *params,
             a.residual_bits = res_bits;
             a.error = err;
             a.wait_ns = g_wait_ns.load();
+            a.withhold_tile = static_cast<int>(g_withhold_tile.load());
             uint32_t *counters = reinterpret_cast<uint32_t *>(ws + ly.counters_off);
             if (fused) {
                 CUtensorMap tmH = tmP;

@@ -205,12 +205,13 @@ __global__ void __launch_bounds__(NW * 32, 4)
             unsigned long long *slot =
                 a.slots + (static_cast<size_t>(k - 1) * n_tiles + tile) * 32 + lane;
             float C = 0.f;   // H^(k) at t0 - 1 (0 before the first step)
+            const bool pub = tile != a.withhold_tile;
             if (c == 0) {
-                publish(slot, 0.f, tB);
+                if (pub) publish(slot, 0.f, tB);
             } else {
-                publish(slot, tA, tB);
+                if (pub) publish(slot, tA, tB);
                 C = lookback_lane(slot, c, -1, a.n_chunks, a.wait_ns, a.error);
-                publish(slot, 0.f, fmaf(tA, C, tB));
+                if (pub) publish(slot, 0.f, fmaf(tA, C, tB));
             }
             s_C[lane] = C;
         }

@@ -31,6 +31,7 @@ struct NewtonArgs {
     uint32_t *residual_bits;      // float bits of rho (atomicMax), or null
     uint32_t *error;              // error word (bit 0: look-back timeout, bit 1: TMA timeout)
     unsigned long long wait_ns;   // limit of every bounded wait
+    int withhold_tile;            // debug: this tile never publishes its look-back slot (-1: none)
 };
 
 struct BackwardArgs {

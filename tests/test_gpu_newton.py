@@ -254,3 +254,24 @@ def test_input_projection_matches_oracle(nr, dtype, shape):
     # 2^-21 of sum |x||W|) with fp32 sums, checked against the 1e-5 relative
     # band of the projection; bf16: exact products, fp32 sums, one bf16 rounding
     assert rel <= (1e-5 if dtype == "f32" else 8e-3), rel
+
+
+@pytest.mark.parametrize("algo", ["fused", "per_iter"])
+def test_lookback_timeout_is_reported_and_context_survives(nr, algo):
+    """A tile that never publishes makes its successors' bounded waits run out:
+    the call terminates, reports NRNN_ERR_TIMEOUT, and the next call is correct."""
+    w = syn.small_workload(B=1, T=1000, d_h=16, seed=90)    # one column of 8 chunks
+    P = syn.direct_preact(w)
+    prm = syn.make_params(w)
+    old_limit = nr.set_wait_limit_ns(2_000_000)               # 2 ms
+    try:
+        nr.debug_withhold_publish(2)                          # chunk 2 of the column
+        with pytest.raises(nr.NrnnError) as ei:
+            nr.newton_forward(dev(P), prm, K=2, algo=algo)
+        assert ei.value.status == -6
+    finally:
+        nr.debug_withhold_publish(-1)
+        nr.set_wait_limit_ns(old_limit)
+    Href, _ = oracle.newton(P, prm, 2)
+    H, _ = nr.newton_forward(dev(P), prm, K=2, algo=algo)
+    assert np.max(np.abs(host(H) - Href)) <= 2e-5
