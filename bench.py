@@ -293,6 +293,27 @@ def run_ours(args, w, rank, world, local):
     e2e_ms = statistics.median(e2e)
 
     proj = statistics.median(proj_ms)
+
+    # bf16: the projection fused into the Newton kernel (P never written)
+    fused_x = None
+    if w.dtype == "bf16" and w.K > 0:
+        def fx():
+            return nr.newton_forward_x(x, W, prm, cu_seqlens=cu, K=w.K, check=False, out=H,
+                                       workspace=ws)
+        fx()
+        torch.cuda.synchronize()
+        if args.graph:
+            gx = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gx):
+                fx()
+            fx_step = gx.replay
+        else:
+            fx_step = fx
+        for _ in range(args.warmup):
+            fx_step()
+        fx_ms, _ = time_steps(torch, fx_step, max(3, min(args.steps, 10)), flush, stream, nvtx=False)
+        fused_x = {"ms": statistics.median(fx_ms),
+                   "tokens_per_s": tokens * world / (statistics.median(fx_ms) * 1e-3)}
     out = {
         "metric": METRIC,
         "value": tokens_all_ranks(tokens, world) / (ms * 1e-3),
@@ -318,7 +339,8 @@ def run_ours(args, w, rank, world, local):
                 "d2h_bytes_per_step": H.numel() * H.element_size() + 4},
         "gpu_launches": launches * args.steps,
         "with_projection": {"projection_ms": proj,
-                            "tokens_per_s": tokens * world / ((ms + proj) * 1e-3)},
+                            "tokens_per_s": tokens * world / ((ms + proj) * 1e-3),
+                            "fused_in_kernel": fused_x},
         "sequential_gpu": {"ms": statistics.median(seq_ms),
                            "tokens_per_s": tokens / (statistics.median(seq_ms) * 1e-3)},
         "residual": float(rho.item()),

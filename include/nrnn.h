@@ -140,6 +140,24 @@ int nrnn_newton_forward_init(const void *preact, int dtype, const float *params,
                              void *stream);
 
 /*
+ * Newton forward with the input projection fused in (bf16 only): each CTA
+ * computes its tile of P = x W_x^T on the tensor cores in on-chip memory and
+ * runs the fused Newton iterations on it, so P never goes through HBM.  The
+ * tile's fp32 accumulator is rounded to bf16 first, so the result equals
+ * nrnn_input_projection followed by nrnn_newton_forward (NRNN_ALGO_FUSED)
+ * up to the accumulation order of the projection.
+ *   x      device, (B, T, d_in) bf16;  W_x device, (3 d_h, d_in) bf16
+ *   d_in   multiple of 8;  K >= 1
+ *   other arguments as nrnn_newton_forward; workspace size as for
+ *   NRNN_ALGO_FUSED.  NRNN_F32 returns NRNN_ERR_UNSUPPORTED.
+ */
+int nrnn_newton_forward_x(const void *x, const void *W_x, int dtype, const float *params,
+                          int64_t B, int64_t T, int64_t d_in, int64_t d_h,
+                          const int32_t *cu_seqlens, int64_t num_segments, int K,
+                          float residual_fail, void *H_out, float *residual_dev,
+                          float *residual_host, void *workspace, size_t ws_bytes, void *stream);
+
+/*
  * Backward (adjoint) pass for training (shapes_layout page: "train
  * forward+backward surface"; no equations on the pages, plainest reading):
  * with gH = dL/dH at the trajectory H (e.g. the Newton result),

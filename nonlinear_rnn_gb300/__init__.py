@@ -22,6 +22,7 @@ from ._binding import (  # noqa: F401
     load,
     newton_backward,
     newton_forward,
+    newton_forward_x,
     params_tensor,
     picard,
     residual,

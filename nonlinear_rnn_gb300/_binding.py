@@ -37,6 +37,8 @@ _SIGNATURES = {
                              _vp, _vp, _vp, _sz, _vp], _int),
     "nrnn_newton_forward_init": ([_vp, _int, _vp, _i64, _i64, _i64, _vp, _i64, _vp, _int, _f,
                                   _int, _vp, _vp, _vp, _vp, _sz, _vp], _int),
+    "nrnn_newton_forward_x": ([_vp, _vp, _int, _vp, _i64, _i64, _i64, _i64, _vp, _i64, _int, _f,
+                               _vp, _vp, _vp, _vp, _sz, _vp], _int),
     "nrnn_newton_backward": ([_vp, _int, _vp, _i64, _i64, _i64, _vp, _i64, _vp, _vp, _vp, _vp,
                               _vp, _sz, _vp], _int),
     "nrnn_picard": ([_vp, _int, _vp, _i64, _i64, _i64, _vp, _i64, _int, _vp, _vp, _vp], _int),
@@ -228,6 +230,39 @@ def newton_forward(preact: torch.Tensor, params, cu_seqlens=None, K: int = 3,
                                           ctypes.byref(host) if host is not None else None,
                                           _ptr(workspace), workspace.numel(), _stream(dev))
     _raise(st, "newton_forward", H=H, residual=(host.value if host is not None else None))
+    return H, rho
+
+
+def newton_forward_x(x: torch.Tensor, W_x: torch.Tensor, params, cu_seqlens=None, K: int = 3,
+                     residual_fail: float = 1.0, check: bool = True,
+                     out: torch.Tensor | None = None, workspace: torch.Tensor | None = None):
+    """Newton forward from x (B, T, d_in) and W_x (3 d_h, d_in), bf16, with the
+    input projection computed inside the Newton kernel (P never written)."""
+    lib = load()
+    x = _device_tensor(x, "x")
+    W_x = _device_tensor(W_x, "W_x")
+    if x.dim() != 3 or W_x.dim() != 2 or W_x.shape[1] != x.shape[2] or W_x.shape[0] % 3:
+        raise ValueError("x must be (B, T, d_in) and W_x (3 d_h, d_in)")
+    if x.dtype != W_x.dtype:
+        raise TypeError("x and W_x must share a dtype")
+    B, T, d_in = x.shape
+    d_h = W_x.shape[0] // 3
+    code = _dtype_code(x)
+    dev = x.device
+    prm = params_tensor(params, d_h, dev)
+    cu, S = _cu_device(cu_seqlens, B, T, dev)
+    H = out if out is not None else torch.empty((B, T, d_h), dtype=x.dtype, device=dev)
+    rho = torch.empty((), dtype=torch.float32, device=dev)
+    nbytes = lib.nrnn_newton_workspace_bytes(B, T, d_h, code, int(K), ALGOS["fused"])
+    if workspace is None or workspace.numel() < nbytes:
+        workspace = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=dev)
+    host = ctypes.c_float(0.0) if check else None
+    with torch.cuda.device(dev):
+        st = lib.nrnn_newton_forward_x(_ptr(x), _ptr(W_x), code, _ptr(prm), B, T, d_in, d_h,
+                                       _ptr(cu), S, int(K), float(residual_fail), _ptr(H),
+                                       _ptr(rho), ctypes.byref(host) if host is not None else None,
+                                       _ptr(workspace), workspace.numel(), _stream(dev))
+    _raise(st, "newton_forward_x", H=H, residual=(host.value if host is not None else None))
     return H, rho
 
 

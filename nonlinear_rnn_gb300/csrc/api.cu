@@ -104,6 +104,25 @@ bool make_map_2d_sw128(CUtensorMap *m, const void *base, int64_t inner, int64_t 
     return r == CUDA_SUCCESS;
 }
 
+// 3-D bf16 map over x (B, T, d_in) row-major: dims (d_in, T, B), box (64, rows, 1),
+// 128-byte swizzle.
+bool make_map_x_sw128(CUtensorMap *m, const void *x, int64_t d_in, int64_t T, int64_t B,
+                      uint32_t box_rows) {
+    auto fn = encode_fn();
+    if (fn == nullptr) return false;
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(d_in), static_cast<cuuint64_t>(T),
+                          static_cast<cuuint64_t>(B)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(d_in * 2),
+                             static_cast<cuuint64_t>(d_in * 2 * T)};
+    cuuint32_t box[3] = {64, box_rows, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(x), dims,
+                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 int check_common(const void *preact, int dtype, const float *params, int64_t B, int64_t T,
                  int64_t d_h, const int32_t *cu, int64_t S) {
     if (dtype != NRNN_F32 && dtype != NRNN_BF16) return NRNN_ERR_INVALID_ARG;
@@ -276,6 +295,69 @@ int nrnn_newton_forward_init(const void *preact, int dtype, const float *params,
     if (err_host != 0) return NRNN_ERR_TIMEOUT;
     const float rho = *residual_host;
     if (!std::isfinite(rho) || rho > residual_fail) return NRNN_ERR_DIVERGED;
+    return NRNN_OK;
+}
+
+int nrnn_newton_forward_x(const void *x, const void *W_x, int dtype, const float *params,
+                          int64_t B, int64_t T, int64_t d_in, int64_t d_h,
+                          const int32_t *cu_seqlens, int64_t num_segments, int K,
+                          float residual_fail, void *H_out, float *residual_dev,
+                          float *residual_host, void *workspace, size_t ws_bytes, void *stream_) {
+    if (dtype == NRNN_F32) return NRNN_ERR_UNSUPPORTED;
+    int st = check_common(x, dtype, params, B, T, d_h, cu_seqlens, num_segments);
+    if (st != NRNN_OK) return st;
+    if (K < 1 || K > MAX_K || residual_dev == nullptr || d_in <= 0) return NRNN_ERR_INVALID_ARG;
+    if (d_in % 8 != 0 || d_in > INT32_MAX) return NRNN_ERR_UNSUPPORTED;
+    if (B * T > 0 && (W_x == nullptr || H_out == nullptr || !aligned16(W_x) || !aligned16(H_out)))
+        return NRNN_ERR_INVALID_ARG;
+    const SyncLayout ly = layout(B, T, d_h, dtype, K, true);
+    if (workspace == nullptr || ws_bytes < ly.total ||
+        (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+        return NRNN_ERR_WORKSPACE;
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+    unsigned char *ws = static_cast<unsigned char *>(workspace);
+    uint32_t *err = reinterpret_cast<uint32_t *>(ws + ly.error_off);
+    cudaError_t e = cudaMemsetAsync(ws, 0, ly.zero_bytes, stream);
+    if (e == cudaSuccess) e = cudaMemsetAsync(ws + ly.slots_off, 0xff, ly.slots_bytes, stream);
+    if (e == cudaSuccess) e = cudaMemsetAsync(residual_dev, 0, sizeof(float), stream);
+    if (e != cudaSuccess) return NRNN_ERR_CUDA;
+    if (B * T > 0) {
+        CUtensorMap tmX, tmW;
+        if (!make_map_x_sw128(&tmX, x, d_in, T, B, NEWTON_L) ||
+            !make_map_2d_sw128(&tmW, W_x, d_in, 3 * d_h, 64, TILE_U))
+            return NRNN_ERR_CUDA;
+        NewtonArgs a{};
+        a.params = params;
+        a.cu = cu_seqlens;
+        a.S = static_cast<int>(cu_seqlens ? num_segments : 0);
+        a.B = static_cast<int>(B);
+        a.T = static_cast<int>(T);
+        a.d_h = static_cast<int>(d_h);
+        a.d_in = static_cast<int>(d_in);
+        a.n_ut = static_cast<int>((d_h + TILE_U - 1) / TILE_U);
+        a.n_chunks = static_cast<int>((T + NEWTON_L - 1) / NEWTON_L);
+        a.slots = reinterpret_cast<unsigned long long *>(ws + ly.slots_off);
+        a.residual_bits = reinterpret_cast<uint32_t *>(residual_dev);
+        a.error = err;
+        a.wait_ns = g_wait_ns.load();
+        a.withhold_tile = static_cast<int>(g_withhold_tile.load());
+        a.H_prev = nullptr;
+        a.H_next = H_out;
+        a.k_first = 1;
+        a.k_last = K;
+        a.last = 1;
+        a.ticket = reinterpret_cast<uint32_t *>(ws + ly.counters_off);
+        if (launch_newton_x(tmX, tmW, a, ly.n_tiles, stream) != cudaSuccess) return NRNN_ERR_CUDA;
+    }
+    if (residual_host == nullptr) return NRNN_OK;
+    uint32_t err_host = 0;
+    e = cudaMemcpyAsync(residual_host, residual_dev, sizeof(float), cudaMemcpyDeviceToHost, stream);
+    if (e == cudaSuccess)
+        e = cudaMemcpyAsync(&err_host, err, sizeof(uint32_t), cudaMemcpyDeviceToHost, stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) return NRNN_ERR_CUDA;
+    if (err_host != 0) return NRNN_ERR_TIMEOUT;
+    if (!std::isfinite(*residual_host) || *residual_host > residual_fail) return NRNN_ERR_DIVERGED;
     return NRNN_OK;
 }
 

@@ -28,6 +28,7 @@
 // word instead of hanging.
 #include "nrnn_device.cuh"
 #include "nrnn_internal.h"
+#include "tcgen05.cuh"
 
 namespace nrnn {
 
@@ -37,6 +38,15 @@ constexpr int NW = NEWTON_NW;
 constexpr int SEG = NEWTON_SEG;
 constexpr int L = NEWTON_L;
 constexpr int U = TILE_U;
+
+// fused-projection prologue (XPROJ): bf16 operands, 64-wide K slices
+constexpr int XP_BK = 64;
+constexpr int XP_W_BOX_BYTES = 32 * XP_BK * 2;               // 32 W_x rows of one gate
+constexpr int XP_A_BYTES = 128 * XP_BK * 2;                  // 128 M rows (96 used)
+constexpr int XP_X_BYTES = L * XP_BK * 2;                    // 128 x rows (time steps)
+constexpr int XP_STAGE_BYTES = XP_A_BYTES + XP_X_BYTES;      // 32 KiB
+constexpr uint32_t XP_TMEM_COLS = L;                         // one fp32 column per time step
+constexpr uint32_t XP_IDESC = idesc_kmajor<false>(128, L);
 // Affine pairs (J_t, g_t) of this warp's SEG rows at the shifted iterate,
 // with g_t = f(h~_t) - J_t h~_t, so that the new iterate solves
 // H^(k)_t = J_t H^(k)_{t-1} + g_t: the Newton step delta_t = J_t delta_{t-1} - F_t
@@ -88,11 +98,24 @@ __device__ __forceinline__ void warp_pairs(const void *Pv, int r0, int lane, flo
     }
 }
 
-template <typename TS, bool FUSED>
+// XPROJ (bf16, fused only): the tile's preactivations are not read from HBM
+// but computed in the prologue from x and W_x on the tensor cores:
+// D = W_tile x_tile^T with M = 128 TMEM lanes = (gate, unit) rows (3 x 32 used),
+// N = 128 columns = time steps, K = d_in in 64-wide slices through a 2-stage
+// TMA ring that aliases the P' tile; warps 0..2 then read their gate's lanes
+// (tcgen05.ld: lane = unit, registers = time), round to bf16 as a stored
+// preactivation would be, and write the pre-scaled arguments.
+template <typename TS, bool FUSED, bool XPROJ = false>
 __global__ void __launch_bounds__(NW * 32, 4)
     k_newton(const __grid_constant__ CUtensorMap tmP, const __grid_constant__ CUtensorMap tmH,
+             const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
              const NewtonArgs a) {
-    extern __shared__ __align__(128) unsigned char dsmem[];
+    extern __shared__ __align__(128) unsigned char dsmem_raw[];
+    // the 128-byte swizzle of the XPROJ stages needs a 1024-byte aligned base
+    unsigned char *dsmem = XPROJ ? reinterpret_cast<unsigned char *>(
+                                       (reinterpret_cast<uintptr_t>(dsmem_raw) + 1023) &
+                                       ~static_cast<uintptr_t>(1023))
+                                 : dsmem_raw;
     // FUSED: [3][L][U] fp32 pre-scaled arguments (a bf16 tile lands by TMA in
     // the upper half and is widened in place), then, with an initial iterate,
     // its [L][U] tile.  Per-iteration: [3][L][U] raw preactivations followed by
@@ -106,6 +129,8 @@ __global__ void __launch_bounds__(NW * 32, 4)
     __shared__ float s_C[32];
     __shared__ uint32_t s_heads[L / 32];
     __shared__ __align__(8) uint64_t s_bar;
+    __shared__ __align__(8) uint64_t s_xfull[2], s_xempty[2], s_xacc;   // XPROJ only
+    __shared__ uint32_t s_tmem;                                         // XPROJ only
     __shared__ uint32_t s_ticket;
     __shared__ uint32_t s_red[NW];
 
@@ -122,15 +147,34 @@ __global__ void __launch_bounds__(NW * 32, 4)
     const bool load_h = a.H_prev != nullptr;   // H^(k-1) (per-iteration) or H^(0) (fused)
 
     if (tid == 0) {
-        mbar_init(&s_bar, 1);
-        fence_mbar_init();
-        const uint32_t bytes = (3u + (load_h ? 1u : 0u)) * L * U * sizeof(TS);
-        mbar_arrive_expect_tx(&s_bar, bytes);
+        if constexpr (XPROJ) {
+            for (int i = 0; i < 2; ++i) {
+                mbar_init(&s_xfull[i], 1);
+                mbar_init(&s_xempty[i], 1);
+            }
+            mbar_init(&s_xacc, 1);
+            fence_mbar_init();
+        } else {
+            mbar_init(&s_bar, 1);
+            fence_mbar_init();
+            const uint32_t bytes = (3u + (load_h ? 1u : 0u)) * L * U * sizeof(TS);
+            mbar_arrive_expect_tx(&s_bar, bytes);
 #pragma unroll
-        for (int g = 0; g < 3; ++g)
-            tma_load_3d(Pt + g * L * U, &tmP, &s_bar, g * a.d_h + u0, t0, b);
-        if (load_h) tma_load_3d(Hs, &tmH, &s_bar, u0, t0, b);
+            for (int g = 0; g < 3; ++g)
+                tma_load_3d(Pt + g * L * U, &tmP, &s_bar, g * a.d_h + u0, t0, b);
+            if (load_h) tma_load_3d(Hs, &tmH, &s_bar, u0, t0, b);
+        }
         mark_heads(a.cu, a.S, t0, L, s_heads);
+    }
+    if constexpr (XPROJ) {
+        if (warp == 2) {
+            asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                             smem_u32(&s_tmem)),
+                         "r"(XP_TMEM_COLS)
+                         : "memory");
+            asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+        }
+        asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
     }
     const int u = u0 + lane;
     const bool uok = u < a.d_h;
@@ -141,10 +185,73 @@ __global__ void __launch_bounds__(NW * 32, 4)
     if (load_h && warp == 0 && t0 > 0 && uok)
         hb = to_f32(reinterpret_cast<const TS *>(a.H_prev)[(static_cast<size_t>(b) * a.T + t0 - 1) *
                                                                a.d_h + u]);
-    __syncthreads();   // barrier initialised, head bits visible
-    mbar_wait_bounded(&s_bar, 0, a.wait_ns, a.error);
+    __syncthreads();   // barriers initialised, head bits visible
+    if constexpr (XPROJ) {
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        const uint32_t tmem = s_tmem;
+        const int kt_count = (a.d_in + XP_BK - 1) / XP_BK;
+        if (warp == 0 && lane == 0) {
+            // TMA producer: W_x rows of the three gates of this unit tile, x rows of this chunk
+            for (int kt = 0; kt < kt_count; ++kt) {
+                const int st = kt & 1;
+                if (kt >= 2) mbar_wait_bounded(&s_xempty[st], ((kt >> 1) - 1) & 1, a.wait_ns, a.error);
+                unsigned char *A = dsmem + st * XP_STAGE_BYTES;
+                mbar_arrive_expect_tx(&s_xfull[st], 3 * XP_W_BOX_BYTES + XP_X_BYTES);
+#pragma unroll
+                for (int g = 0; g < 3; ++g)
+                    tma_load_2d(A + g * XP_W_BOX_BYTES, &tmW, &s_xfull[st], kt * XP_BK, g * a.d_h + u0);
+                tma_load_3d(A + XP_A_BYTES, &tmX, &s_xfull[st], kt * XP_BK, t0, b);
+            }
+        } else if (warp == 1 && lane == 0) {
+            // MMA issuer
+            for (int kt = 0; kt < kt_count; ++kt) {
+                const int st = kt & 1;
+                mbar_wait_bounded(&s_xfull[st], (kt >> 1) & 1, a.wait_ns, a.error);
+                asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+                const uint32_t A = smem_u32(dsmem + st * XP_STAGE_BYTES);
+#pragma unroll
+                for (int kk = 0; kk < XP_BK / 16; ++kk)
+                    mma<false, XP_IDESC>(tmem, sw128_desc(A + kk * 32),
+                                         sw128_desc(A + XP_A_BYTES + kk * 32),
+                                         (kt > 0 || kk > 0) ? 1u : 0u);
+                mma_commit(&s_xempty[st]);
+            }
+            mma_commit(&s_xacc);
+        }
+        __syncwarp();
+        const bool ok = mbar_wait_bounded(&s_xacc, 0, a.wait_ns, a.error);
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // P' overwrites the stages
+        if (warp < 3) {
+            // lane = unit of gate `warp`, registers = 32 time steps per load
+#pragma unroll 1
+            for (int cc = 0; cc < L / 32; ++cc) {
+                uint32_t v[32];
+                tmem_ld_32cols(tmem + (static_cast<uint32_t>(warp * 32) << 16) + cc * 32, v);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    const float p = round_to<__nv_bfloat16>(__uint_as_float(v[i]));
+                    float sc;
+                    if (warp == 0) sc = fmaf(p, -LOG2E, prm.nb_z);
+                    else if (warp == 1) sc = fmaf(p, -LOG2E, prm.nb_r);
+                    else sc = fmaf(p, 2.0f * LOG2E, prm.b_c2);
+                    Pf[(warp * L + cc * 32 + i) * U + lane] = ok ? sc : __int_as_float(0x7fffffff);
+                }
+            }
+        }
+        asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+        __syncthreads();
+        if (warp == 2) {
+            asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+            asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                         "r"(XP_TMEM_COLS)
+                         : "memory");
+        }
+    } else {
+        mbar_wait_bounded(&s_bar, 0, a.wait_ns, a.error);
+    }
 
-    if (FUSED) {
+    if (FUSED && !XPROJ) {
         // pre-scale the tile once: P' = scale (P + b) per gate, fp32
         constexpr int PER = L * U / (NW * 32);
         float v[3][PER];
@@ -388,7 +495,25 @@ cudaError_t launch_one(const CUtensorMap &tmP, const CUtensorMap &tmH, const New
         if (e != cudaSuccess) return e;
         configured = true;
     }
-    k_newton<TS, FUSED><<<static_cast<unsigned>(n_ctas), NW * 32, smem, stream>>>(tmP, tmH, a);
+    k_newton<TS, FUSED><<<static_cast<unsigned>(n_ctas), NW * 32, smem, stream>>>(tmP, tmH, tmP,
+                                                                                tmP, a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_x(const CUtensorMap &tmX, const CUtensorMap &tmW, const NewtonArgs &a,
+                     int64_t n_ctas, cudaStream_t stream) {
+    static bool configured = false;
+    const size_t smem = 2 * XP_STAGE_BYTES + 1024;   // stages alias the P' tile; + alignment
+    static_assert(2 * XP_STAGE_BYTES >= 3 * L * U * 4, "P' tile must fit in the stage ring");
+    if (!configured) {
+        cudaError_t e = cudaFuncSetAttribute(k_newton<__nv_bfloat16, true, true>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(smem));
+        if (e != cudaSuccess) return e;
+        configured = true;
+    }
+    k_newton<__nv_bfloat16, true, true><<<static_cast<unsigned>(n_ctas), NW * 32, smem, stream>>>(
+        tmX, tmX, tmX, tmW, a);
     return cudaGetLastError();
 }
 
@@ -407,6 +532,11 @@ cudaError_t launch_newton(int dtype, bool fused, const CUtensorMap &tmP, const C
                      : launch_one<__nv_bfloat16, false>(tmP, tmH, a, n_ctas, stream);
     return fused ? launch_one<float, true>(tmP, tmH, a, n_ctas, stream)
                  : launch_one<float, false>(tmP, tmH, a, n_ctas, stream);
+}
+
+cudaError_t launch_newton_x(const CUtensorMap &tmX, const CUtensorMap &tmW, const NewtonArgs &a,
+                            int64_t n_ctas, cudaStream_t stream) {
+    return launch_x(tmX, tmW, a, n_ctas, stream);
 }
 
 cudaError_t launch_residual(int dtype, const void *P, const float *params, const void *G, int B,

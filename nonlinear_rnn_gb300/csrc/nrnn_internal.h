@@ -32,6 +32,7 @@ struct NewtonArgs {
     uint32_t *error;              // error word (bit 0: look-back timeout, bit 1: TMA timeout)
     unsigned long long wait_ns;   // limit of every bounded wait
     int withhold_tile;            // debug: this tile never publishes its look-back slot (-1: none)
+    int d_in;                     // fused projection only: input width
 };
 
 struct BackwardArgs {
@@ -66,6 +67,12 @@ size_t newton_smem_bytes(int dtype, bool fused);
 
 cudaError_t launch_newton(int dtype, bool fused, const CUtensorMap &tmP, const CUtensorMap &tmH,
                           const NewtonArgs &a, int64_t n_ctas, cudaStream_t stream);
+
+// fused algorithm with the input projection computed in-kernel (bf16): tmX over
+// x (d_in, T, B) with a 64 x 128 x 1 box, tmW over W_x (d_in, 3 d_h) with a
+// 64 x 32 box, both with the 128-byte swizzle
+cudaError_t launch_newton_x(const CUtensorMap &tmX, const CUtensorMap &tmW, const NewtonArgs &a,
+                            int64_t n_ctas, cudaStream_t stream);
 
 cudaError_t launch_residual(int dtype, const void *P, const float *params, const void *G,
                             int B, int T, int d_h, const int32_t *cu, int S,
