@@ -140,6 +140,25 @@ int cuda_status(cudaError_t e) { return e == cudaSuccess ? NRNN_OK : NRNN_ERR_CU
 
 }  // namespace
 
+// Synchronous tail of the forward entry points: copies rho and the error word
+// to the host, then applies the timeout and residual gates.  With no host
+// pointer the call stays asynchronous and returns NRNN_OK.
+static int gate_residual(const float *residual_dev, float *residual_host, const uint32_t *err,
+                         float residual_fail, cudaStream_t stream) {
+    if (residual_host == nullptr) return NRNN_OK;
+    uint32_t err_host = 0;
+    cudaError_t e =
+        cudaMemcpyAsync(residual_host, residual_dev, sizeof(float), cudaMemcpyDeviceToHost, stream);
+    if (e == cudaSuccess)
+        e = cudaMemcpyAsync(&err_host, err, sizeof(uint32_t), cudaMemcpyDeviceToHost, stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) return NRNN_ERR_CUDA;
+    if (err_host != 0) return NRNN_ERR_TIMEOUT;
+    const float rho = *residual_host;
+    if (!std::isfinite(rho) || rho > residual_fail) return NRNN_ERR_DIVERGED;
+    return NRNN_OK;
+}
+
 extern "C" {
 
 const char *nrnn_status_string(int status) {
@@ -285,17 +304,7 @@ int nrnn_newton_forward_init(const void *preact, int dtype, const float *params,
             }
         }
     }
-    if (residual_host == nullptr) return NRNN_OK;
-    uint32_t err_host = 0;
-    e = cudaMemcpyAsync(residual_host, residual_dev, sizeof(float), cudaMemcpyDeviceToHost, stream);
-    if (e == cudaSuccess)
-        e = cudaMemcpyAsync(&err_host, err, sizeof(uint32_t), cudaMemcpyDeviceToHost, stream);
-    if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
-    if (e != cudaSuccess) return NRNN_ERR_CUDA;
-    if (err_host != 0) return NRNN_ERR_TIMEOUT;
-    const float rho = *residual_host;
-    if (!std::isfinite(rho) || rho > residual_fail) return NRNN_ERR_DIVERGED;
-    return NRNN_OK;
+    return gate_residual(residual_dev, residual_host, err, residual_fail, stream);
 }
 
 int nrnn_newton_forward_x(const void *x, const void *W_x, int dtype, const float *params,
@@ -349,16 +358,7 @@ int nrnn_newton_forward_x(const void *x, const void *W_x, int dtype, const float
         a.ticket = reinterpret_cast<uint32_t *>(ws + ly.counters_off);
         if (launch_newton_x(tmX, tmW, a, ly.n_tiles, stream) != cudaSuccess) return NRNN_ERR_CUDA;
     }
-    if (residual_host == nullptr) return NRNN_OK;
-    uint32_t err_host = 0;
-    e = cudaMemcpyAsync(residual_host, residual_dev, sizeof(float), cudaMemcpyDeviceToHost, stream);
-    if (e == cudaSuccess)
-        e = cudaMemcpyAsync(&err_host, err, sizeof(uint32_t), cudaMemcpyDeviceToHost, stream);
-    if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
-    if (e != cudaSuccess) return NRNN_ERR_CUDA;
-    if (err_host != 0) return NRNN_ERR_TIMEOUT;
-    if (!std::isfinite(*residual_host) || *residual_host > residual_fail) return NRNN_ERR_DIVERGED;
-    return NRNN_OK;
+    return gate_residual(residual_dev, residual_host, err, residual_fail, stream);
 }
 
 int nrnn_newton_backward(const void *preact, int dtype, const float *params, int64_t B,

@@ -194,14 +194,13 @@ __global__ void __launch_bounds__(NW * 32, 2)
 template <typename TS>
 cudaError_t launch_bw(const CUtensorMap &tmP, const CUtensorMap &tmH, const CUtensorMap &tmG,
                       const BackwardArgs &a, int64_t n_ctas, cudaStream_t stream) {
-    static bool configured = false;
-    const size_t smem = static_cast<size_t>(5) * L * U * sizeof(TS);
-    if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(k_backward<TS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(smem));
-        if (e != cudaSuccess) return e;
-        configured = true;
-    }
+    static std::atomic<unsigned long long> configured{0};
+    constexpr size_t smem = static_cast<size_t>(5) * L * U * sizeof(TS);
+    cudaError_t e = once_per_device(configured, [](int) {
+        return cudaFuncSetAttribute(k_backward<TS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    static_cast<int>(smem));
+    });
+    if (e != cudaSuccess) return e;
     k_backward<TS><<<static_cast<unsigned>(n_ctas), NW * 32, smem, stream>>>(tmP, tmH, tmG, a);
     return cudaGetLastError();
 }

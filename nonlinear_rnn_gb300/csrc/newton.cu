@@ -47,55 +47,124 @@ constexpr int XP_X_BYTES = L * XP_BK * 2;                    // 128 x rows (time
 constexpr int XP_STAGE_BYTES = XP_A_BYTES + XP_X_BYTES;      // 32 KiB
 constexpr uint32_t XP_TMEM_COLS = L;                         // one fp32 column per time step
 constexpr uint32_t XP_IDESC = idesc_kmajor<false>(128, L);
+// Each thread's SEG rows are split into two halves of HALF rows that run side
+// by side as the two lanes of f32x2 values: element j of a pair array holds
+// rows (r0 + j, r0 + HALF + j).  The fused kernel keeps its pre-scaled tile in
+// shared memory in the same order, [3][NW][HALF][U] float2, so that one 64-bit
+// load per gate fetches both rows.
+constexpr int HALF = SEG / 2;
+
+// float2 index of rows (r0 + j, r0 + HALF + j) of gate g, lane `lane`, in the
+// pair-ordered tile
+__device__ __forceinline__ int pf2_index(int g, int warp, int j, int lane) {
+    return (g * NW * HALF + warp * HALF + j) * U + lane;
+}
+
 // Affine pairs (J_t, g_t) of this warp's SEG rows at the shifted iterate,
 // with g_t = f(h~_t) - J_t h~_t, so that the new iterate solves
 // H^(k)_t = J_t H^(k)_{t-1} + g_t: the Newton step delta_t = J_t delta_{t-1} - F_t
-// written for delta_t = H^(k)_t - H^(k-1)_t.  Composed into the warp
-// aggregate (A, Bv).  On return G[i] holds g_t.  SCALED: Ps holds fp32
-// pre-scaled arguments; otherwise raw preactivations of type TS.  GENERAL
-// handles segment heads (J = 0, shifted state 0) and rows past T (identity).
-// ZERO: the first iteration from H^(0) = 0, where every shifted state is 0 and
-// g = f(0); the gate arguments lose their state terms.
+// written for delta_t = H^(k)_t - H^(k-1)_t.  Composed per half into
+// (A2, B2); the warp aggregate (A, Bv) composes the second half after the
+// first; (A_lo, B_lo) is the first half's map, from which the second half's
+// starting state follows.  On entry G holds H^(k-1), on return g_t.
+// SCALED: Pv is the pair-ordered fp32 tile of pre-scaled arguments; otherwise
+// raw [3][L][U] preactivations of type TS.  GENERAL handles segment heads
+// (J = 0, shifted state 0) and rows past T (identity).  ZERO: the first
+// iteration from H^(0) = 0, where every shifted state is 0 and g = f(0).
 template <typename TS, bool SCALED, bool GENERAL, bool ZERO = false>
-__device__ __forceinline__ void warp_pairs(const void *Pv, int r0, int lane, float (&G)[SEG],
-                                           float hprev, uint32_t hm, int nvalid,
-                                           const ScaledParams &prm, float (&Jr)[SEG], float &A,
-                                           float &Bv) {
-    A = 1.f;
-    Bv = 0.f;
+__device__ __forceinline__ void warp_pairs(const void *Pv, int warp, int lane,
+                                           float2 (&G)[HALF], float hb, uint32_t hm, int nvalid,
+                                           const ScaledParams2 &prm, float2 (&J2)[HALF],
+                                           float &A_lo, float &B_lo, float &A, float &Bv) {
+    const int r0 = warp * SEG;
+    float2 A2 = splat2(1.f), B2 = splat2(0.f);
+    float2 prev = make_float2(hb, G[HALF - 1].x);   // H^(k-1) at rows r0 - 1, r0 + HALF - 1
 #pragma unroll
-    for (int i = 0; i < SEG; ++i) {
-        const int r = r0 + i;
-        float sz, sr, sc;
+    for (int j = 0; j < HALF; ++j) {
+        float2 sz, sr, sc;
         if (SCALED) {
-            const float *P = static_cast<const float *>(Pv);
-            sz = P[(0 * L + r) * U + lane];
-            sr = P[(1 * L + r) * U + lane];
-            sc = P[(2 * L + r) * U + lane];
+            const float2 *P = static_cast<const float2 *>(Pv);
+            sz = P[pf2_index(0, warp, j, lane)];
+            sr = P[pf2_index(1, warp, j, lane)];
+            sc = P[pf2_index(2, warp, j, lane)];
         } else {
             const TS *P = static_cast<const TS *>(Pv);
-            scale_preact(to_f32(P[(0 * L + r) * U + lane]), to_f32(P[(1 * L + r) * U + lane]),
-                         to_f32(P[(2 * L + r) * U + lane]), prm, sz, sr, sc);
+            const int lo = (r0 + j) * U + lane, hi = lo + HALF * U;
+            scale_preact2(make_float2(to_f32(P[lo]), to_f32(P[hi])),
+                          make_float2(to_f32(P[L * U + lo]), to_f32(P[L * U + hi])),
+                          make_float2(to_f32(P[2 * L * U + lo]), to_f32(P[2 * L * U + hi])), prm,
+                          sz, sr, sc);
         }
-        const float hs = (ZERO || (GENERAL && ((hm >> i) & 1u))) ? 0.f : hprev;
-        float f, J, g;
+        const bool head_lo = GENERAL && ((hm >> j) & 1u);
+        const bool head_hi = GENERAL && ((hm >> (j + HALF)) & 1u);
+        const float2 cur = G[j];
+        float2 J, g;
         if (ZERO) {
-            cell_fj_scaled_at_zero(sz, sr, sc, prm, f, J);
-            g = f;
+            cell_jg2_at_zero(sz, sr, sc, prm, J, g);
         } else {
-            cell_fj_scaled(hs, sz, sr, sc, prm, f, J);
-            g = fmaf(-J, hs, f);
+            float2 hs = prev;
+            if (head_lo) hs.x = 0.f;
+            if (head_hi) hs.y = 0.f;
+            cell_jg2(hs, sz, sr, sc, prm, J, g);
         }
         if (GENERAL) {
-            if ((hm >> i) & 1u) J = 0.f;
-            if (i >= nvalid) { J = 1.f; g = 0.f; }
+            if (head_lo) J.x = 0.f;
+            if (head_hi) J.y = 0.f;
+            if (j >= nvalid) { J.x = 1.f; g.x = 0.f; }
+            if (j + HALF >= nvalid) { J.y = 1.f; g.y = 0.f; }
         }
-        hprev = G[i];
-        Jr[i] = J;
-        G[i] = g;
-        Bv = fmaf(J, Bv, g);
-        A *= J;
+        prev = cur;
+        J2[j] = J;
+        G[j] = g;
+        B2 = fma2(J, B2, g);
+        A2 = mul2(A2, J);
     }
+    A_lo = A2.x;
+    B_lo = B2.x;
+    A = A2.y * A2.x;
+    Bv = fmaf(A2.y, B2.x, B2.y);
+}
+
+// max |F_t| = max |H_t - f(H_{t-1}, P_t)| over this thread's rows of the
+// final iterate (values as stored).  prev holds the stored H at rows r0 - 1
+// and r0 + HALF - 1.  NaN propagates.
+template <typename TS, bool FUSED, bool GENERAL>
+__device__ __forceinline__ float residual_rows(const float *Pf, const TS *Pt, int warp, int lane,
+                                               const float2 (&G)[HALF], float2 prev, uint32_t hm,
+                                               int nvalid, const ScaledParams2 &prm) {
+    const int r0 = warp * SEG;
+    float m = 0.f;
+#pragma unroll
+    for (int j = 0; j < HALF; ++j) {
+        float2 sz, sr, sc;
+        if (FUSED) {
+            const float2 *P2 = reinterpret_cast<const float2 *>(Pf);
+            sz = P2[pf2_index(0, warp, j, lane)];
+            sr = P2[pf2_index(1, warp, j, lane)];
+            sc = P2[pf2_index(2, warp, j, lane)];
+        } else {
+            const int lo = (r0 + j) * U + lane, hi = lo + HALF * U;
+            scale_preact2(make_float2(to_f32(Pt[lo]), to_f32(Pt[hi])),
+                          make_float2(to_f32(Pt[L * U + lo]), to_f32(Pt[L * U + hi])),
+                          make_float2(to_f32(Pt[2 * L * U + lo]), to_f32(Pt[2 * L * U + hi])),
+                          prm, sz, sr, sc);
+        }
+        const float2 hq = make_float2(round_to<TS>(G[j].x), round_to<TS>(G[j].y));
+        float2 hs = prev;
+        if (GENERAL) {
+            if ((hm >> j) & 1u) hs.x = 0.f;
+            if ((hm >> (j + HALF)) & 1u) hs.y = 0.f;
+        }
+        const float2 F = fma2(cell_f2(hs, sz, sr, sc, prm), splat2(-1.0f), hq);
+        float fx = fabsf(F.x), fy = fabsf(F.y);
+        if (GENERAL) {
+            if (j >= nvalid) fx = 0.f;
+            if (j + HALF >= nvalid) fy = 0.f;
+        }
+        m = max_nan(m, max_nan(fx, fy));
+        prev = hq;
+    }
+    return m;
 }
 
 // XPROJ (bf16, fused only): the tile's preactivations are not read from HBM
@@ -179,6 +248,7 @@ __global__ void __launch_bounds__(NW * 32, 4)
     const int u = u0 + lane;
     const bool uok = u < a.d_h;
     const ScaledParams prm = scale_params(load_unit_params(a.params, a.d_h, u, uok));
+    const ScaledParams2 prm2 = pair_params(prm);
     const int r0 = warp * SEG;
     // shifted state at this warp's first row: H^(k-1) at row r0 - 1
     float hb = 0.f;
@@ -224,18 +294,23 @@ __global__ void __launch_bounds__(NW * 32, 4)
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // P' overwrites the stages
         if (warp < 3) {
             // lane = unit of gate `warp`, registers = 32 time steps per load
+            // (two warps' rows), written in pair order
+            const float mul = warp == 2 ? 2.0f * LOG2E : -LOG2E;
+            const float add = warp == 0 ? prm.nb_z : (warp == 1 ? prm.nb_r : prm.b_c2);
+            float2 *P2 = reinterpret_cast<float2 *>(Pf);
 #pragma unroll 1
             for (int cc = 0; cc < L / 32; ++cc) {
                 uint32_t v[32];
                 tmem_ld_32cols(tmem + (static_cast<uint32_t>(warp * 32) << 16) + cc * 32, v);
 #pragma unroll
                 for (int i = 0; i < 32; ++i) {
-                    const float p = round_to<__nv_bfloat16>(__uint_as_float(v[i]));
-                    float sc;
-                    if (warp == 0) sc = fmaf(p, -LOG2E, prm.nb_z);
-                    else if (warp == 1) sc = fmaf(p, -LOG2E, prm.nb_r);
-                    else sc = fmaf(p, 2.0f * LOG2E, prm.b_c2);
-                    Pf[(warp * L + cc * 32 + i) * U + lane] = ok ? sc : __int_as_float(0x7fffffff);
+                    if ((i % SEG) >= HALF) continue;
+                    const float lo = fmaf(round_to<__nv_bfloat16>(__uint_as_float(v[i])), mul, add);
+                    const float hi =
+                        fmaf(round_to<__nv_bfloat16>(__uint_as_float(v[i + HALF])), mul, add);
+                    const float nan = __int_as_float(0x7fffffff);
+                    P2[pf2_index(warp, cc * 2 + i / SEG, i % SEG, lane)] =
+                        ok ? make_float2(lo, hi) : make_float2(nan, nan);
                 }
             }
         }
@@ -252,29 +327,38 @@ __global__ void __launch_bounds__(NW * 32, 4)
     }
 
     if (FUSED && !XPROJ) {
-        // pre-scale the tile once: P' = scale (P + b) per gate, fp32
-        constexpr int PER = L * U / (NW * 32);
-        float v[3][PER];
+        // pre-scale the tile once, P' = scale (P + b) per gate, into pair order:
+        // this thread takes row pairs p = warp + NW m (owner warp p / HALF,
+        // j = p mod HALF) of its lane's unit
+        constexpr int PER = HALF;   // NW * HALF row pairs over NW warps
+        float2 v[3][PER];
 #pragma unroll
-        for (int g = 0; g < 3; ++g)
+        for (int m = 0; m < PER; ++m) {
+            const int pr = warp + NW * m;
+            const int lo = ((pr / HALF) * SEG + pr % HALF) * U + lane, hi = lo + HALF * U;
 #pragma unroll
-            for (int j = 0; j < PER; ++j) v[g][j] = to_f32(Pt[g * L * U + tid + j * NW * 32]);
-        if (sizeof(TS) == 2) __syncthreads();   // bf16 tile overlaps the fp32 destination
-        // element tid + 256 j belongs to unit (tid mod 32) = this lane's unit
+            for (int g = 0; g < 3; ++g)
+                v[g][m] = make_float2(to_f32(Pt[g * L * U + lo]), to_f32(Pt[g * L * U + hi]));
+        }
+        __syncthreads();   // the pair-ordered destination overlaps the tile as loaded
+        float2 *P2 = reinterpret_cast<float2 *>(Pf);
 #pragma unroll
-        for (int j = 0; j < PER; ++j) {
-            float sz, sr, sc;
-            scale_preact(v[0][j], v[1][j], v[2][j], prm, sz, sr, sc);
-            Pf[0 * L * U + tid + j * NW * 32] = sz;
-            Pf[1 * L * U + tid + j * NW * 32] = sr;
-            Pf[2 * L * U + tid + j * NW * 32] = sc;
+        for (int m = 0; m < PER; ++m) {
+            const int pr = warp + NW * m;
+            float2 sz, sr, sc;
+            scale_preact2(v[0][m], v[1][m], v[2][m], prm2, sz, sr, sc);
+            P2[pf2_index(0, pr / HALF, pr % HALF, lane)] = sz;
+            P2[pf2_index(1, pr / HALF, pr % HALF, lane)] = sr;
+            P2[pf2_index(2, pr / HALF, pr % HALF, lane)] = sc;
         }
         __syncthreads();
     }
 
-    float G[SEG];   // H of this warp's rows (between iterations) / g_t (inside)
+    float2 G[HALF];   // H of this warp's rows (between iterations) / g_t (inside), in pairs
 #pragma unroll
-    for (int i = 0; i < SEG; ++i) G[i] = load_h ? to_f32(Hs[(r0 + i) * U + lane]) : 0.f;
+    for (int j = 0; j < HALF; ++j)
+        G[j] = load_h ? make_float2(to_f32(Hs[(r0 + j) * U + lane]), to_f32(Hs[(r0 + HALF + j) * U + lane]))
+                      : splat2(0.f);
     if (load_h && warp > 0) hb = to_f32(Hs[(r0 - 1) * U + lane]);
     const uint32_t hm = (s_heads[r0 >> 5] >> (r0 & 31)) & ((1u << SEG) - 1u);
     const int nvalid = min(SEG, a.T - (t0 + r0));
@@ -285,14 +369,17 @@ __global__ void __launch_bounds__(NW * 32, 4)
     const int tile = (b * a.n_ut + ut) * a.n_chunks + c;
 
     for (int k = a.k_first; k <= a.k_last; ++k) {
-        float Jr[SEG], A, Bv;
+        float2 J2[HALF];
+        float A_lo, B_lo, A, Bv;
         if (FUSED && k == 1 && !load_h) {
-            if (general) warp_pairs<TS, true, true, true>(Pv, r0, lane, G, hb, hm, nvalid, prm, Jr, A, Bv);
-            else warp_pairs<TS, true, false, true>(Pv, r0, lane, G, hb, hm, nvalid, prm, Jr, A, Bv);
+            if (general)
+                warp_pairs<TS, true, true, true>(Pv, warp, lane, G, hb, hm, nvalid, prm2, J2, A_lo, B_lo, A, Bv);
+            else
+                warp_pairs<TS, true, false, true>(Pv, warp, lane, G, hb, hm, nvalid, prm2, J2, A_lo, B_lo, A, Bv);
         } else if (general) {
-            warp_pairs<TS, FUSED, true>(Pv, r0, lane, G, hb, hm, nvalid, prm, Jr, A, Bv);
+            warp_pairs<TS, FUSED, true>(Pv, warp, lane, G, hb, hm, nvalid, prm2, J2, A_lo, B_lo, A, Bv);
         } else {
-            warp_pairs<TS, FUSED, false>(Pv, r0, lane, G, hb, hm, nvalid, prm, Jr, A, Bv);
+            warp_pairs<TS, FUSED, false>(Pv, warp, lane, G, hb, hm, nvalid, prm2, J2, A_lo, B_lo, A, Bv);
         }
         s_aggA[warp][lane] = A;
         s_aggB[warp][lane] = Bv;
@@ -324,13 +411,15 @@ __global__ void __launch_bounds__(NW * 32, 4)
         }
         __syncthreads();
 
-        // H^(k) of this warp's rows from H^(k) at row r0 - 1
-        float h = fmaf(s_aggA[warp][lane], s_C[lane], s_aggB[warp][lane]);
+        // H^(k) of this warp's rows from H^(k) at row r0 - 1 (first half) and at
+        // row r0 + HALF - 1 (second half, through the first half's map)
+        const float h = fmaf(s_aggA[warp][lane], s_C[lane], s_aggB[warp][lane]);
         hb = FUSED ? h : round_to<TS>(h);
+        float2 h2 = make_float2(h, fmaf(A_lo, h, B_lo));
 #pragma unroll
-        for (int i = 0; i < SEG; ++i) {
-            h = fmaf(Jr[i], h, G[i]);
-            G[i] = FUSED ? h : round_to<TS>(h);
+        for (int j = 0; j < HALF; ++j) {
+            h2 = fma2(J2[j], h2, G[j]);
+            G[j] = FUSED ? h2 : make_float2(round_to<TS>(h2.x), round_to<TS>(h2.y));
         }
     }
 
@@ -338,28 +427,14 @@ __global__ void __launch_bounds__(NW * 32, 4)
     if (a.last && a.residual_bits != nullptr) {
         // each warp read only its own prefix slot in the apply step: reuse the
         // slots for the last row of each warp
-        s_aggA[warp][lane] = round_to<TS>(G[SEG - 1]);
+        s_aggA[warp][lane] = round_to<TS>(G[HALF - 1].y);
         __syncthreads();
-        float m = 0.f;
-        float hprev = (warp == 0) ? round_to<TS>(hb) : s_aggA[warp - 1][lane];
-#pragma unroll
-        for (int i = 0; i < SEG; ++i) {
-            const int r = r0 + i;
-            float sz, sr, sc;
-            if (FUSED) {
-                sz = Pf[(0 * L + r) * U + lane];
-                sr = Pf[(1 * L + r) * U + lane];
-                sc = Pf[(2 * L + r) * U + lane];
-            } else {
-                scale_preact(to_f32(Pt[(0 * L + r) * U + lane]), to_f32(Pt[(1 * L + r) * U + lane]),
-                             to_f32(Pt[(2 * L + r) * U + lane]), prm, sz, sr, sc);
-            }
-            const bool head = (hm >> i) & 1u;
-            const float hq = round_to<TS>(G[i]);
-            const float f = cell_f_scaled(head ? 0.f : hprev, sz, sr, sc, prm);
-            if (uok && i < nvalid) m = fmaxf(m, abs_residual(hq - f));
-            hprev = hq;
-        }
+        const float2 prev = make_float2((warp == 0) ? round_to<TS>(hb) : s_aggA[warp - 1][lane],
+                                        round_to<TS>(G[HALF - 1].x));
+        float m = general ? residual_rows<TS, FUSED, true>(Pf, Pt, warp, lane, G, prev, hm, nvalid, prm2)
+                          : residual_rows<TS, FUSED, false>(Pf, Pt, warp, lane, G, prev, hm, nvalid, prm2);
+        if (!uok) m = 0.f;
+        m = abs_residual(m);   // NaN counts as +inf
         const uint32_t v = __reduce_max_sync(FULL_MASK, __float_as_uint(m));
         if (lane == 0) s_red[warp] = v;
         __syncthreads();
@@ -374,9 +449,12 @@ __global__ void __launch_bounds__(NW * 32, 4)
     if (uok) {
         TS *o = reinterpret_cast<TS *>(a.H_next) +
                 (static_cast<size_t>(b) * a.T + t0 + r0) * a.d_h + u;
+        const size_t half_off = static_cast<size_t>(HALF) * a.d_h;
 #pragma unroll
-        for (int i = 0; i < SEG; ++i, o += a.d_h)
-            if (i < nvalid) *o = from_f32<TS>(G[i]);
+        for (int j = 0; j < HALF; ++j, o += a.d_h) {
+            if (j < nvalid) o[0] = from_f32<TS>(G[j].x);
+            if (j + HALF < nvalid) o[half_off] = from_f32<TS>(G[j].y);
+        }
     }
 }
 
@@ -486,15 +564,13 @@ size_t smem_bytes_for(bool with_h) {
 template <typename TS, bool FUSED>
 cudaError_t launch_one(const CUtensorMap &tmP, const CUtensorMap &tmH, const NewtonArgs &a,
                        int64_t n_ctas, cudaStream_t stream) {
-    static bool configured = false;
+    static std::atomic<unsigned long long> configured{0};
     const size_t smem = smem_bytes_for<TS, FUSED>(a.H_prev != nullptr);
-    if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(k_newton<TS, FUSED>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(smem_bytes_for<TS, FUSED>(true)));
-        if (e != cudaSuccess) return e;
-        configured = true;
-    }
+    cudaError_t e = once_per_device(configured, [](int) {
+        return cudaFuncSetAttribute(k_newton<TS, FUSED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    static_cast<int>(smem_bytes_for<TS, FUSED>(true)));
+    });
+    if (e != cudaSuccess) return e;
     k_newton<TS, FUSED><<<static_cast<unsigned>(n_ctas), NW * 32, smem, stream>>>(tmP, tmH, tmP,
                                                                                 tmP, a);
     return cudaGetLastError();
@@ -502,16 +578,14 @@ cudaError_t launch_one(const CUtensorMap &tmP, const CUtensorMap &tmH, const New
 
 cudaError_t launch_x(const CUtensorMap &tmX, const CUtensorMap &tmW, const NewtonArgs &a,
                      int64_t n_ctas, cudaStream_t stream) {
-    static bool configured = false;
-    const size_t smem = 2 * XP_STAGE_BYTES + 1024;   // stages alias the P' tile; + alignment
+    static std::atomic<unsigned long long> configured{0};
+    constexpr size_t smem = 2 * XP_STAGE_BYTES + 1024;   // stages alias the P' tile; + alignment
     static_assert(2 * XP_STAGE_BYTES >= 3 * L * U * 4, "P' tile must fit in the stage ring");
-    if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(k_newton<__nv_bfloat16, true, true>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(smem));
-        if (e != cudaSuccess) return e;
-        configured = true;
-    }
+    cudaError_t e = once_per_device(configured, [](int) {
+        return cudaFuncSetAttribute(k_newton<__nv_bfloat16, true, true>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    });
+    if (e != cudaSuccess) return e;
     k_newton<__nv_bfloat16, true, true><<<static_cast<unsigned>(n_ctas), NW * 32, smem, stream>>>(
         tmX, tmX, tmX, tmW, a);
     return cudaGetLastError();

@@ -47,6 +47,12 @@ __device__ __forceinline__ float min_nan(float a, float b) {
     asm("min.NaN.f32 %0, %1, %2;" : "=f"(y) : "f"(a), "f"(b));
     return y;
 }
+// max that propagates NaN (a NaN residual must reach the gate)
+__device__ __forceinline__ float max_nan(float a, float b) {
+    float y;
+    asm("max.NaN.f32 %0, %1, %2;" : "=f"(y) : "f"(a), "f"(b));
+    return y;
+}
 __device__ __forceinline__ uint64_t globaltimer_ns() {
     uint64_t t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
@@ -263,6 +269,113 @@ __device__ __forceinline__ float cell_f_scaled(float h, float sz, float sr, floa
     float z, r, c;
     gates_scaled(h, sz, sr, sc, p, z, r, c);
     return fmaf(z, c - h, h);
+}
+
+// ------------------------------------------------ the cell on pairs of steps
+// sm_100 and later execute fma / mul / add on a pair of fp32 values as one
+// instruction (f32x2: two FMA lanes for one issue slot).  The Newton kernel
+// evaluates two independent time steps per thread with them; ex2 / rcp and the
+// clamps stay scalar.  Each lane of a pair computes exactly what the scalar
+// formulas below compute, up to the order of a few roundings.
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) { return __fmul2_rn(a, b); }
+__device__ __forceinline__ float2 add2(float2 a, float2 b) { return __fadd2_rn(a, b); }
+__device__ __forceinline__ float2 splat2(float v) { return make_float2(v, v); }
+__device__ __forceinline__ float2 ex2_2(float2 x) {
+    return make_float2(ex2_approx(x.x), ex2_approx(x.y));
+}
+__device__ __forceinline__ float2 rcp_2(float2 x) {
+    return make_float2(rcp_approx(x.x), rcp_approx(x.y));
+}
+__device__ __forceinline__ float2 clamp2(float2 x) {
+    return make_float2(min_nan(x.x, EXP2_CLAMP), min_nan(x.y, EXP2_CLAMP));
+}
+
+struct ScaledParams2 {
+    float2 na_z, na_r, a_c2;   // state coefficients of the exponent-2 gate arguments
+    float2 a_z, a_r, a_c4;     // Jacobian: a_z, a_r, 4 a_c
+    float2 nb_z, nb_r, b_c2;   // scaled biases (raw preactivations only)
+};
+
+__device__ __forceinline__ ScaledParams2 pair_params(const ScaledParams &p) {
+    ScaledParams2 q;
+    q.na_z = splat2(p.na_z);
+    q.na_r = splat2(p.na_r);
+    q.a_c2 = splat2(p.a_c2);
+    q.a_z = splat2(p.a_z);
+    q.a_r = splat2(p.a_r);
+    q.a_c4 = splat2(4.0f * p.a_c);
+    q.nb_z = splat2(p.nb_z);
+    q.nb_r = splat2(p.nb_r);
+    q.b_c2 = splat2(p.b_c2);
+    return q;
+}
+
+// pre-scaled arguments of a pair of steps from raw preactivations
+__device__ __forceinline__ void scale_preact2(float2 pz, float2 pr, float2 pc,
+                                              const ScaledParams2 &p, float2 &sz, float2 &sr,
+                                              float2 &sc) {
+    sz = fma2(pz, splat2(-LOG2E), p.nb_z);
+    sr = fma2(pr, splat2(-LOG2E), p.nb_r);
+    sc = fma2(pc, splat2(2.0f * LOG2E), p.b_c2);
+}
+
+// gates at a pair of states (gates_scaled on each lane); q = 1 / (1 + 2^(arg_c)),
+// so that c = 1 - 2 q and 1 - c^2 = 4 q (1 - q)
+__device__ __forceinline__ void gates2(float2 h, float2 sz, float2 sr, float2 sc,
+                                       const ScaledParams2 &p, float2 &z, float2 &r, float2 &c,
+                                       float2 &q) {
+    const float2 one = splat2(1.0f);
+    const float2 dz = add2(ex2_2(clamp2(fma2(p.na_z, h, sz))), one);
+    r = rcp_2(add2(ex2_2(fma2(p.na_r, h, sr)), one));
+    const float2 dc = add2(ex2_2(clamp2(fma2(p.a_c2, mul2(r, h), sc))), one);
+    const float2 inv = rcp_2(mul2(dz, dc));
+    z = mul2(dc, inv);
+    q = mul2(dz, inv);
+    c = fma2(splat2(-2.0f), q, one);
+}
+
+// J = df/dh and the Newton pair's offset g = f(h) - J h for a pair of shifted
+// states.  With inner = (1 - z) a_z (c - h) + (1 - c^2) a_c d(rh)/dh one has
+// J = (1 - z) + z inner and f - J h = z (c - h inner).
+__device__ __forceinline__ void cell_jg2(float2 h, float2 sz, float2 sr, float2 sc,
+                                         const ScaledParams2 &p, float2 &J, float2 &g) {
+    float2 z, r, c, q;
+    gates2(h, sz, sr, sc, p, z, r, c, q);
+    const float2 one = splat2(1.0f), mone = splat2(-1.0f);
+    const float2 nh = mul2(h, mone);
+    const float2 cmh = add2(c, nh);
+    const float2 omz = fma2(z, mone, one);
+    const float2 dq = fma2(mul2(mul2(h, p.a_r), fma2(r, mone, one)), r, r);   // d(r h)/dh
+    const float2 t3 = mul2(mul2(mul2(q, p.a_c4), fma2(q, mone, one)), dq);    // (1 - c^2) a_c dq
+    const float2 inner = fma2(mul2(omz, p.a_z), cmh, t3);
+    J = fma2(z, inner, omz);
+    g = mul2(z, fma2(nh, inner, c));
+}
+
+// the same at the zero state: g = f(0) = z c, J = (1 - z) + z ((1 - z) a_z c + (1 - c^2) a_c r)
+__device__ __forceinline__ void cell_jg2_at_zero(float2 sz, float2 sr, float2 sc,
+                                                 const ScaledParams2 &p, float2 &J, float2 &g) {
+    const float2 one = splat2(1.0f), mone = splat2(-1.0f);
+    const float2 dz = add2(ex2_2(clamp2(sz)), one);
+    const float2 r = rcp_2(add2(ex2_2(sr), one));
+    const float2 dc = add2(ex2_2(clamp2(sc)), one);
+    const float2 inv = rcp_2(mul2(dz, dc));
+    const float2 z = mul2(dc, inv);
+    const float2 q = mul2(dz, inv);
+    const float2 c = fma2(splat2(-2.0f), q, one);
+    const float2 omz = fma2(z, mone, one);
+    const float2 t3 = mul2(mul2(mul2(q, p.a_c4), fma2(q, mone, one)), r);
+    J = fma2(z, fma2(mul2(omz, p.a_z), c, t3), omz);
+    g = mul2(z, c);
+}
+
+// f(h) for a pair of states
+__device__ __forceinline__ float2 cell_f2(float2 h, float2 sz, float2 sr, float2 sc,
+                                          const ScaledParams2 &p) {
+    float2 z, r, c, q;
+    gates2(h, sz, sr, sc, p, z, r, c, q);
+    return fma2(z, fma2(h, splat2(-1.0f), c), h);
 }
 
 // |F| for the residual gate; NaN counts as +inf

@@ -6,7 +6,24 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <atomic>
+
 namespace nrnn {
+
+// Runs configure(device) for the current device unless it already succeeded
+// there (kernel attributes are per device).  Ordinals >= 64 configure on every
+// call.
+template <typename Fn>
+inline cudaError_t once_per_device(std::atomic<unsigned long long> &done, Fn &&configure) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const unsigned long long bit = dev < 64 ? (1ull << dev) : 0ull;
+    if (bit != 0 && (done.load(std::memory_order_acquire) & bit) != 0) return cudaSuccess;
+    e = configure(dev);
+    if (e == cudaSuccess) done.fetch_or(bit, std::memory_order_acq_rel);
+    return e;
+}
 
 // Tile of one Newton CTA: 32 hidden units (one per lane) x L time steps,
 // L = NW warps x SEG steps per warp.

@@ -252,20 +252,25 @@ template <bool F32>
 cudaError_t launch_tc(const CUtensorMap &tmA, const CUtensorMap &tmB, int64_t rows, int d_in,
                       int n_out, void *P, cudaStream_t stream) {
     using C = ProjCfg<F32>;
-    static bool configured = false;
-    static int sms = 0;
-    const size_t smem = static_cast<size_t>(C::STAGES) * C::STAGE_BYTES + 1024;
-    if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(k_projection_tc<F32>,
+    static std::atomic<unsigned long long> configured{0};
+    static int sms_of[64];
+    constexpr size_t smem = static_cast<size_t>(C::STAGES) * C::STAGE_BYTES + 1024;
+    cudaError_t e = once_per_device(configured, [](int dev) {
+        cudaError_t r = cudaFuncSetAttribute(k_projection_tc<F32>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              static_cast<int>(smem));
-        if (e != cudaSuccess) return e;
-        int dev = 0;
-        e = cudaGetDevice(&dev);
-        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-        if (e != cudaSuccess) return e;
-        configured = true;
-    }
+        int n = 0;
+        if (r == cudaSuccess) r = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        if (r == cudaSuccess && dev < 64) sms_of[dev] = n;
+        return r;
+    });
+    if (e != cudaSuccess) return e;
+    int dev = 0, sms = 0;
+    e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 64) sms = sms_of[dev];
+    else e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess || sms <= 0) return e != cudaSuccess ? e : cudaErrorInvalidValue;
     const int64_t n_tiles = ((rows + C::BM - 1) / C::BM) * ((n_out + C::BN - 1) / C::BN);
     const int64_t grid = n_tiles < sms ? n_tiles : sms;
     k_projection_tc<F32><<<static_cast<unsigned>(grid), C::THREADS, smem, stream>>>(
