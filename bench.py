@@ -141,11 +141,14 @@ def workload_bytes(w, algo):
     return [4 * w.d_h * s * tok]          # fused: read P once, write H once
 
 
-# XU (MUFU) operations per cell evaluation in the Newton kernels (three
-# exp2, one reciprocal for r, one shared reciprocal for z and tanh), and the
-# XU issue rate of an SM (16 results per clock).
-XU_PER_EVAL = 5
-XU_PER_CLK_PER_SM = 16
+# Special-function (MUFU) work per cell evaluation in the Newton kernels:
+# three ex2 (one per gate) and two rcp (one for r, one shared by z and the
+# tanh).  The roof is the SM's measured MUFU rate (nrnn_probe_xu_rates, run
+# live): an rcp occupies the unit for ex2_rate / rcp_rate ex2 slots, so the
+# work is counted in ex2-equivalent operations.
+EX2_PER_EVAL = 3
+RCP_PER_EVAL = 2
+SM_MAX_MHZ = 2070.0
 
 
 def time_steps(torch, fn, steps, flush, stream, nvtx=True):
@@ -201,6 +204,7 @@ def run_ours(args, w, rank, world, local):
         return lambda: (g.replay(), res)[1]
 
     newton = graphed(algo) if args.graph else newton_call
+    xu_rates = nr.probe_xu_rates(dev)   # live denominator of the fused kernel's ALU roof
 
     for _ in range(args.warmup):
         flush.fill_(1.0)
@@ -242,14 +246,19 @@ def run_ours(args, w, rank, world, local):
            "peak_src": pk["src"] + " (MEASURED_PEAKS.json hbm_gbs)"}
     if fused:
         # one launch runs K iterations plus the residual evaluation
-        xu_ops = XU_PER_EVAL * (w.K + 1) * tokens * w.d_h
+        ex2_rate, rcp_rate = xu_rates
+        per_eval = EX2_PER_EVAL + RCP_PER_EVAL * ex2_rate / rcp_rate
+        xu_ops = per_eval * (w.K + 1) * tokens * w.d_h
         xu_achieved = xu_ops / (ms * 1e-3) / 1e9
-        xu_peak = XU_PER_CLK_PER_SM * props.multi_processor_count * 2070e6 / 1e9
-        roof = {"bound": "alu", "achieved": xu_achieved, "peak": xu_peak, "unit": "Gop/s (XU)",
+        mhz = clocks.get("sm_max_mhz") or SM_MAX_MHZ
+        xu_peak = ex2_rate * props.multi_processor_count * mhz * 1e6 / 1e9
+        roof = {"bound": "alu", "achieved": xu_achieved, "peak": xu_peak,
+                "unit": "Gop/s (MUFU, ex2-equivalent)",
                 "frac": xu_achieved / xu_peak, "traffic": load_traffic(w, algo), "kernel": kname,
                 "algorithmic_ops_per_launch": xu_ops,
-                "peak_src": f"{XU_PER_CLK_PER_SM} XU results/clk/SM x {props.multi_processor_count} SMs "
-                            "x 2070 MHz (maximum SM clock)",
+                "peak_src": f"measured {ex2_rate:.2f} ex2 and {rcp_rate:.2f} rcp results/clk/SM "
+                            f"(nrnn_probe_xu_rates) x {props.multi_processor_count} SMs x {mhz:.0f} MHz "
+                            "(maximum SM clock); per evaluation 3 ex2 + 2 rcp",
                 "hbm": {k: hbm[k] for k in ("achieved", "peak", "unit", "frac",
                                             "algorithmic_bytes_per_launch")}}
     else:

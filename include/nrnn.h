@@ -316,6 +316,21 @@ int64_t nrnn_debug_withhold_publish(int64_t tile);
  */
 uint64_t nrnn_set_wait_limit_ns(uint64_t ns);
 
+/*
+ * Measures the special-function unit throughput of the current device, the
+ * denominator of the fused Newton kernel's ALU roofline (each cell evaluation
+ * issues three ex2.approx and two rcp.approx; the pages give no hardware
+ * figure for it, so the library measures it).  One CTA per SM runs independent
+ * chains of each instruction and times itself with the SM cycle counter.
+ *   ex2_per_clk, rcp_per_clk  host, 1 float each: median over SMs of results
+ *                             per SM clock cycle
+ *   stream                    cudaStream_t to run on (NULL: legacy stream);
+ *                             the call synchronises it
+ * Allocates and frees a small device buffer; takes about a millisecond.
+ * Returns NRNN_OK, NRNN_ERR_INVALID_ARG (null output) or NRNN_ERR_CUDA.
+ */
+int nrnn_probe_xu_rates(float *ex2_per_clk, float *rcp_per_clk, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -25,6 +25,7 @@ from ._binding import (  # noqa: F401
     newton_forward_x,
     params_tensor,
     picard,
+    probe_xu_rates,
     residual,
     sequential_forward,
     set_wait_limit_ns,

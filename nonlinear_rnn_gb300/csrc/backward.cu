@@ -10,8 +10,8 @@
 // crosses a segment boundary).  Then dL/dP_{t,g} = lambda_t df/dP_g and the
 // parameter gradients are sums over (b, t) of lambda_t df/d(a_g, b_g).
 //
-// Same tiling as the Newton kernel (32 units x 128 steps, 8 warps x 16 steps)
-// run backwards in time: tiles of P, H and gH land in shared memory by TMA;
+// Same tiling as the Newton kernel (32 units x NEWTON_L steps, NEWTON_NW warps
+// x 16 steps) run backwards in time: tiles of P, H and gH land in shared memory by TMA;
 // each thread composes the maps nu_{t+1} -> nu_t = (J_t, J_t gH_t) of its rows
 // from the last upwards; warp aggregates meet in shared memory; warp 0
 // publishes the chunk aggregate and completes a decoupled look-back over
@@ -32,7 +32,7 @@ constexpr int L = NEWTON_L;
 constexpr int U = TILE_U;
 
 template <typename TS>
-__global__ void __launch_bounds__(NW * 32, 2)
+__global__ void __launch_bounds__(NW * 32, 4)
     k_backward(const __grid_constant__ CUtensorMap tmP, const __grid_constant__ CUtensorMap tmH,
                const __grid_constant__ CUtensorMap tmG, const BackwardArgs a) {
     extern __shared__ __align__(128) unsigned char dsmem[];
@@ -44,17 +44,21 @@ __global__ void __launch_bounds__(NW * 32, 2)
     __shared__ float s_red[6][NW][32];
     __shared__ uint32_t s_heads[L / 32];
     __shared__ __align__(8) uint64_t s_bar;
-    __shared__ uint32_t s_ticket;
+    __shared__ int s_tile[3];   // chunk, batch row, unit tile of this CTA's ticket
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    if (tid == 0) s_ticket = atomicAdd(a.ticket, 1u);
+    if (tid == 0) {
+        const uint32_t ticket = atomicAdd(a.ticket, 1u);
+        const uint32_t per_chunk = static_cast<uint32_t>(a.B) * a.n_ut;
+        const uint32_t rem = ticket % per_chunk;
+        s_tile[0] = a.n_chunks - 1 - static_cast<int>(ticket / per_chunk);   // last chunk first
+        s_tile[1] = static_cast<int>(rem / a.n_ut);
+        s_tile[2] = static_cast<int>(rem % a.n_ut);
+    }
     if (tid < L / 32) s_heads[tid] = 0u;
     __syncthreads();
 
-    const uint32_t per_chunk = static_cast<uint32_t>(a.B) * a.n_ut;
-    const int c = a.n_chunks - 1 - static_cast<int>(s_ticket / per_chunk);   // last chunk first
-    const int rem = static_cast<int>(s_ticket % per_chunk);
-    const int b = rem / a.n_ut, ut = rem - (rem / a.n_ut) * a.n_ut;
+    const int c = s_tile[0], b = s_tile[1], ut = s_tile[2];
     const int t0 = c * L, u0 = ut * U;
 
     if (tid == 0) {
@@ -183,11 +187,13 @@ __global__ void __launch_bounds__(NW * 32, 2)
     s_red[4][warp][lane] = g_br;
     s_red[5][warp][lane] = g_bc;
     __syncthreads();
-    if (warp < 6 && uok) {   // warp g sums gate-parameter g over the 8 warps
-        float s = 0.f;
+    if (uok) {   // warp w sums gate-parameters w, w + NW, ... over the NW warps
+        for (int g = warp; g < 6; g += NW) {
+            float s = 0.f;
 #pragma unroll
-        for (int w = 0; w < NW; ++w) s += s_red[warp][w][lane];
-        atomicAdd(a.gparams + warp * a.d_h + u, s);
+            for (int w = 0; w < NW; ++w) s += s_red[g][w][lane];
+            atomicAdd(a.gparams + g * a.d_h + u, s);
+        }
     }
 }
 

@@ -1,15 +1,17 @@
 // Parallel Newton forward of the diagonal-mix GRU (sm_103a).
 //
-// One CTA owns a tile of 32 hidden units (one per lane) x L = 128 time steps
-// of one batch row; warp w owns rows [16 w, 16 w + 16).  Per Newton iteration
+// One CTA owns a tile of 32 hidden units (one per lane) x L = 64 time steps
+// of one batch row (4 warps; 8 CTAs fill an SM's registers); warp w owns rows
+// [16 w, 16 w + 16), which each thread runs as two halves of 8 rows in the
+// lanes of packed f32x2 arithmetic.  Per Newton iteration
 //   1. each thread evaluates the cell at the shifted trajectory for its 16
 //      steps, F_t = H_t - f(H_{t-1}, P_t) and J_t = df/dh (J = 0 and shifted
 //      state 0 at segment heads; pararnn-torch shapes_layout, "cu_seqlens"),
 //      and composes the affine maps delta -> J_t delta - F_t serially;
-//   2. the 8 warp aggregates meet in shared memory (one barrier): each warp
-//      takes its exclusive prefix, warp 0 the chunk aggregate, which it
-//      publishes and then completes by a decoupled look-back over earlier
-//      chunks (one lane per unit, 4 predecessors read per round);
+//   2. the warp aggregates meet in shared memory (one barrier): warp 0 hands
+//      every warp its exclusive prefix, publishes the chunk aggregate and
+//      completes it by a decoupled look-back over earlier chunks (one lane per
+//      unit, 4 predecessors read per round);
 //   3. after a second barrier every thread applies the carry:
 //      delta_t = J_t delta_{t-1} - F_t, H <- H + delta.
 // Each warp advances the shifted state at its first row itself
@@ -175,7 +177,7 @@ __device__ __forceinline__ float residual_rows(const float *Pf, const TS *Pt, in
 // (tcgen05.ld: lane = unit, registers = time), round to bf16 as a stored
 // preactivation would be, and write the pre-scaled arguments.
 template <typename TS, bool FUSED, bool XPROJ = false>
-__global__ void __launch_bounds__(NW * 32, 4)
+__global__ void __launch_bounds__(NW * 32, 8)
     k_newton(const __grid_constant__ CUtensorMap tmP, const __grid_constant__ CUtensorMap tmH,
              const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
              const NewtonArgs a) {
@@ -200,18 +202,24 @@ __global__ void __launch_bounds__(NW * 32, 4)
     __shared__ __align__(8) uint64_t s_bar;
     __shared__ __align__(8) uint64_t s_xfull[2], s_xempty[2], s_xacc;   // XPROJ only
     __shared__ uint32_t s_tmem;                                         // XPROJ only
-    __shared__ uint32_t s_ticket;
+    __shared__ int s_tile[3];   // chunk, batch row, unit tile of this CTA's ticket
     __shared__ uint32_t s_red[NW];
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    if (tid == 0) s_ticket = atomicAdd(a.ticket, 1u);
+    if (tid == 0) {
+        // tickets run chunk-major: every chunk this tile's look-back waits for
+        // belongs to a CTA that has already started
+        const uint32_t ticket = atomicAdd(a.ticket, 1u);
+        const uint32_t per_chunk = static_cast<uint32_t>(a.B) * a.n_ut;
+        const uint32_t cc = ticket / per_chunk, rem = ticket - cc * per_chunk;
+        s_tile[0] = static_cast<int>(cc);
+        s_tile[1] = static_cast<int>(rem / a.n_ut);
+        s_tile[2] = static_cast<int>(rem % a.n_ut);
+    }
     if (tid < L / 32) s_heads[tid] = 0u;
     __syncthreads();
 
-    const uint32_t per_chunk = static_cast<uint32_t>(a.B) * a.n_ut;
-    const int c = static_cast<int>(s_ticket / per_chunk);
-    const int rem = static_cast<int>(s_ticket - static_cast<uint32_t>(c) * per_chunk);
-    const int b = rem / a.n_ut, ut = rem - (rem / a.n_ut) * a.n_ut;
+    const int c = s_tile[0], b = s_tile[1], ut = s_tile[2];
     const int t0 = c * L, u0 = ut * U;
     const bool load_h = a.H_prev != nullptr;   // H^(k-1) (per-iteration) or H^(0) (fused)
 
@@ -460,7 +468,7 @@ __global__ void __launch_bounds__(NW * 32, 4)
 
 // Residual of a given trajectory (G == null: the zero trajectory).
 template <typename TS>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(NW * 32)
     k_residual(const TS *__restrict__ P, const float *__restrict__ params,
                const TS *__restrict__ G, int T, int d_h, const int32_t *cu, int S,
                uint32_t *residual_bits) {
@@ -503,7 +511,7 @@ __global__ void __launch_bounds__(256)
 // One Picard sweep G_out_t = f(G_in_{t-1}, P_t) for every t (G_in == null: the
 // zero trajectory; shifted state 0 at t = 0 and at segment heads).
 template <typename TS>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(NW * 32)
     k_picard(const TS *__restrict__ P, const float *__restrict__ params,
              const TS *__restrict__ G_in, TS *__restrict__ G_out, int T, int d_h,
              const int32_t *cu, int S) {
@@ -618,11 +626,11 @@ cudaError_t launch_residual(int dtype, const void *P, const float *params, const
                             cudaStream_t stream) {
     const dim3 grid((d_h + U - 1) / U, (T + L - 1) / L, B);
     if (dtype == 1)
-        k_residual<__nv_bfloat16><<<grid, 256, 0, stream>>>(
+        k_residual<__nv_bfloat16><<<grid, NW * 32, 0, stream>>>(
             static_cast<const __nv_bfloat16 *>(P), params, static_cast<const __nv_bfloat16 *>(G), T,
             d_h, cu, S, residual_bits);
     else
-        k_residual<float><<<grid, 256, 0, stream>>>(static_cast<const float *>(P), params,
+        k_residual<float><<<grid, NW * 32, 0, stream>>>(static_cast<const float *>(P), params,
                                                     static_cast<const float *>(G), T, d_h, cu, S,
                                                     residual_bits);
     return cudaGetLastError();
@@ -633,11 +641,11 @@ cudaError_t launch_picard(int dtype, const void *P, const float *params, const v
                           cudaStream_t stream) {
     const dim3 grid((d_h + U - 1) / U, (T + L - 1) / L, B);
     if (dtype == 1)
-        k_picard<__nv_bfloat16><<<grid, 256, 0, stream>>>(
+        k_picard<__nv_bfloat16><<<grid, NW * 32, 0, stream>>>(
             static_cast<const __nv_bfloat16 *>(P), params, static_cast<const __nv_bfloat16 *>(G_in),
             static_cast<__nv_bfloat16 *>(G_out), T, d_h, cu, S);
     else
-        k_picard<float><<<grid, 256, 0, stream>>>(static_cast<const float *>(P), params,
+        k_picard<float><<<grid, NW * 32, 0, stream>>>(static_cast<const float *>(P), params,
                                                   static_cast<const float *>(G_in),
                                                   static_cast<float *>(G_out), T, d_h, cu, S);
     return cudaGetLastError();

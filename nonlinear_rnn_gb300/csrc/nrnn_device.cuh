@@ -119,11 +119,25 @@ __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map) {
 }
 
 // Bounded wait on an mbarrier phase; sets *error bit 2 and returns false on timeout.
+// try_wait that suspends the thread until the phase completes or about
+// hint_ns nanoseconds pass (no issue slots spent spinning)
+__device__ __forceinline__ bool mbar_try_wait_hint(uint64_t *bar, uint32_t parity, uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity,
                                                   uint64_t limit_ns, uint32_t *error) {
     if (mbar_try_wait(bar, parity)) return true;
+    const uint32_t hint = static_cast<uint32_t>(limit_ns < 1000000u ? limit_ns : 1000000u);
     const uint64_t t0 = globaltimer_ns();
-    while (!mbar_try_wait(bar, parity)) {
+    while (!mbar_try_wait_hint(bar, parity, hint)) {
         if (globaltimer_ns() - t0 > limit_ns) {
             atomicOr(error, 2u);
             return false;

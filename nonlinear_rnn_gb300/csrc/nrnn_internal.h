@@ -28,7 +28,7 @@ inline cudaError_t once_per_device(std::atomic<unsigned long long> &done, Fn &&c
 // Tile of one Newton CTA: 32 hidden units (one per lane) x L time steps,
 // L = NW warps x SEG steps per warp.
 constexpr int TILE_U = 32;
-constexpr int NEWTON_NW = 8;
+constexpr int NEWTON_NW = 4;
 constexpr int NEWTON_SEG = 16;
 constexpr int NEWTON_L = NEWTON_NW * NEWTON_SEG;
 

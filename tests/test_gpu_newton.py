@@ -60,7 +60,7 @@ def test_golden_tiny(nr, algo):
 @pytest.mark.parametrize("algo", ["fused", "per_iter"])
 @pytest.mark.parametrize("K", [1, 2, 3, 6])
 def test_newton_matches_oracle_small(nr, dtype, algo, K):
-    # 3 rows x 300 steps (2 full 128-step tiles + a ragged tail) x 40 units
+    # 3 rows x 300 steps (several full time tiles + a ragged tail) x 40 units
     # (one full 32-unit tile + a ragged 8)
     w = syn.small_workload(B=3, T=300, d_h=40, dtype=dtype, seed=20 + K)
     P = syn.direct_preact(w)
@@ -260,7 +260,7 @@ def test_input_projection_matches_oracle(nr, dtype, shape):
 def test_lookback_timeout_is_reported_and_context_survives(nr, algo):
     """A tile that never publishes makes its successors' bounded waits run out:
     the call terminates, reports NRNN_ERR_TIMEOUT, and the next call is correct."""
-    w = syn.small_workload(B=1, T=1000, d_h=16, seed=90)    # one column of 8 chunks
+    w = syn.small_workload(B=1, T=1000, d_h=16, seed=90)    # one column of chunks
     P = syn.direct_preact(w)
     prm = syn.make_params(w)
     old_limit = nr.set_wait_limit_ns(2_000_000)               # 2 ms
@@ -275,3 +275,11 @@ def test_lookback_timeout_is_reported_and_context_survives(nr, algo):
     Href, _ = oracle.newton(P, prm, 2)
     H, _ = nr.newton_forward(dev(P), prm, K=2, algo=algo)
     assert np.max(np.abs(host(H) - Href)) <= 2e-5
+
+
+def test_probe_xu_rates(nr):
+    # special-function throughput per SM clock: a power-of-two rate on every
+    # NVIDIA part so far; ex2 at least as fast as rcp
+    ex2, rcp = nr.probe_xu_rates()
+    assert 4.0 < ex2 < 80.0 and 2.0 < rcp < 80.0
+    assert ex2 >= 0.9 * rcp
