@@ -103,7 +103,8 @@ size_t nrnn_newton_workspace_bytes(int64_t B, int64_t T, int64_t d_h, int dtype,
  *   K             Newton iterations, 0 <= K <= 64 (K = 0: H = 0)
  *   residual_fail divergence threshold (the pages' default is 1.0)
  *   algo          nrnn_algo
- *   H_out         device, (B, T, d_h) of dtype: H^(K)
+ *   H_out         device, (B, T, d_h) of dtype: H^(K); 16-byte aligned, must
+ *                 not overlap preact (NRNN_ERR_INVALID_ARG)
  *   residual_dev  device, 1 float: rho = max|F(H^(K))|, +inf if any F is NaN
  *   residual_host NULL: fully asynchronous, no gate, no timeout report.
  *                 Non-NULL: the call synchronises the stream, stores rho

@@ -24,11 +24,12 @@ size_t elem_size(int dtype) { return dtype == NRNN_BF16 ? 2 : 4; }
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-bool overlaps(const void *a, const void *b, size_t bytes) {
-    if (a == nullptr || b == nullptr || bytes == 0) return false;
+bool ranges_overlap(const void *a, size_t a_bytes, const void *b, size_t b_bytes) {
+    if (a == nullptr || b == nullptr || a_bytes == 0 || b_bytes == 0) return false;
     const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
-    return x < y + bytes && y < x + bytes;
+    return x < y + b_bytes && y < x + a_bytes;
 }
+bool overlaps(const void *a, const void *b, size_t bytes) { return ranges_overlap(a, bytes, b, bytes); }
 
 // Workspace: [counters (K+1) u32 | error u32] zeroed per call, then
 // [slots K x n_tiles x 32 u64] set to all-ones bytes per call, then
@@ -226,6 +227,10 @@ int nrnn_newton_forward_init(const void *preact, int dtype, const float *params,
     if (K < 0 || K > MAX_K || residual_dev == nullptr) return NRNN_ERR_INVALID_ARG;
     if (algo < NRNN_ALGO_AUTO || algo > NRNN_ALGO_FUSED) return NRNN_ERR_INVALID_ARG;
     if (B * T > 0 && (H_out == nullptr || !aligned16(H_out))) return NRNN_ERR_INVALID_ARG;
+    {
+        const size_t hb = elem_size(dtype) * static_cast<size_t>(B * T * d_h);
+        if (ranges_overlap(preact, 3 * hb, H_out, hb)) return NRNN_ERR_INVALID_ARG;
+    }
     const bool fused = algo != NRNN_ALGO_PER_ITER;
     const SyncLayout ly = layout(B, T, d_h, dtype, K, fused);
     if (workspace == nullptr || ws_bytes < ly.total ||
@@ -281,7 +286,9 @@ int nrnn_newton_forward_init(const void *preact, int dtype, const float *params,
                 a.k_last = K;
                 a.last = 1;
                 a.ticket = counters;
-                e = launch_newton(dtype, true, tmP, tmH, a, ly.n_tiles, stream);
+                CUtensorMap tmO;
+                if (!make_map(&tmO, H_out, dtype, d_h, T, B)) return NRNN_ERR_CUDA;
+                e = launch_newton(dtype, true, tmP, tmH, tmO, a, ly.n_tiles, stream);
                 if (e != cudaSuccess) return NRNN_ERR_CUDA;
             } else {
                 void *hbuf = ws + ly.hbuf_off;
@@ -289,15 +296,16 @@ int nrnn_newton_forward_init(const void *preact, int dtype, const float *params,
                 for (int k = 1; k <= K; ++k) {
                     // iteration K lands in H_out; earlier ones alternate with hbuf
                     void *dst = ((K - k) % 2 == 0) ? H_out : hbuf;
-                    CUtensorMap tmH = tmP;
+                    CUtensorMap tmH = tmP, tmO;
                     if (prev != nullptr && !make_map(&tmH, prev, dtype, d_h, T, B))
                         return NRNN_ERR_CUDA;
+                    if (!make_map(&tmO, dst, dtype, d_h, T, B)) return NRNN_ERR_CUDA;
                     a.H_prev = prev;
                     a.H_next = dst;
                     a.k_first = a.k_last = k;
                     a.last = (k == K) ? 1 : 0;
                     a.ticket = counters + k;
-                    e = launch_newton(dtype, false, tmP, tmH, a, ly.n_tiles, stream);
+                    e = launch_newton(dtype, false, tmP, tmH, tmO, a, ly.n_tiles, stream);
                     if (e != cudaSuccess) return NRNN_ERR_CUDA;
                     prev = dst;
                 }
@@ -356,7 +364,9 @@ int nrnn_newton_forward_x(const void *x, const void *W_x, int dtype, const float
         a.k_last = K;
         a.last = 1;
         a.ticket = reinterpret_cast<uint32_t *>(ws + ly.counters_off);
-        if (launch_newton_x(tmX, tmW, a, ly.n_tiles, stream) != cudaSuccess) return NRNN_ERR_CUDA;
+        CUtensorMap tmO;
+        if (!make_map(&tmO, H_out, dtype, d_h, T, B)) return NRNN_ERR_CUDA;
+        if (launch_newton_x(tmX, tmW, tmO, a, ly.n_tiles, stream) != cudaSuccess) return NRNN_ERR_CUDA;
     }
     return gate_residual(residual_dev, residual_host, err, residual_fail, stream);
 }

@@ -179,8 +179,8 @@ __device__ __forceinline__ float residual_rows(const float *Pf, const TS *Pt, in
 template <typename TS, bool FUSED, bool XPROJ = false>
 __global__ void __launch_bounds__(NW * 32, 8)
     k_newton(const __grid_constant__ CUtensorMap tmP, const __grid_constant__ CUtensorMap tmH,
-             const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
-             const NewtonArgs a) {
+             const __grid_constant__ CUtensorMap tmO, const __grid_constant__ CUtensorMap tmX,
+             const __grid_constant__ CUtensorMap tmW, const NewtonArgs a) {
     extern __shared__ __align__(128) unsigned char dsmem_raw[];
     // the 128-byte swizzle of the XPROJ stages needs a 1024-byte aligned base
     unsigned char *dsmem = XPROJ ? reinterpret_cast<unsigned char *>(
@@ -335,31 +335,29 @@ __global__ void __launch_bounds__(NW * 32, 8)
     }
 
     if (FUSED && !XPROJ) {
-        // pre-scale the tile once, P' = scale (P + b) per gate, into pair order:
-        // this thread takes row pairs p = warp + NW m (owner warp p / HALF,
-        // j = p mod HALF) of its lane's unit
-        constexpr int PER = HALF;   // NW * HALF row pairs over NW warps
-        float2 v[3][PER];
+        // each warp pre-scales its own rows once, P' = scale (P + b) per gate,
+        // into pair order; for fp32 the tile is rewritten in place inside the
+        // warp's own rows, for bf16 the source tile overlaps other warps'
+        // destinations
+        float2 v[3][HALF];
+        const TS *src = Pt + r0 * U + lane;
 #pragma unroll
-        for (int m = 0; m < PER; ++m) {
-            const int pr = warp + NW * m;
-            const int lo = ((pr / HALF) * SEG + pr % HALF) * U + lane, hi = lo + HALF * U;
+        for (int j = 0; j < HALF; ++j)
 #pragma unroll
             for (int g = 0; g < 3; ++g)
-                v[g][m] = make_float2(to_f32(Pt[g * L * U + lo]), to_f32(Pt[g * L * U + hi]));
-        }
-        __syncthreads();   // the pair-ordered destination overlaps the tile as loaded
+                v[g][j] = make_float2(to_f32(src[g * L * U + j * U]), to_f32(src[g * L * U + (j + HALF) * U]));
+        if (sizeof(TS) == 2) __syncthreads();
+        else __syncwarp();
         float2 *P2 = reinterpret_cast<float2 *>(Pf);
 #pragma unroll
-        for (int m = 0; m < PER; ++m) {
-            const int pr = warp + NW * m;
+        for (int j = 0; j < HALF; ++j) {
             float2 sz, sr, sc;
-            scale_preact2(v[0][m], v[1][m], v[2][m], prm2, sz, sr, sc);
-            P2[pf2_index(0, pr / HALF, pr % HALF, lane)] = sz;
-            P2[pf2_index(1, pr / HALF, pr % HALF, lane)] = sr;
-            P2[pf2_index(2, pr / HALF, pr % HALF, lane)] = sc;
+            scale_preact2(v[0][j], v[1][j], v[2][j], prm2, sz, sr, sc);
+            P2[pf2_index(0, warp, j, lane)] = sz;
+            P2[pf2_index(1, warp, j, lane)] = sr;
+            P2[pf2_index(2, warp, j, lane)] = sc;
         }
-        __syncthreads();
+        __syncwarp();
     }
 
     float2 G[HALF];   // H of this warp's rows (between iterations) / g_t (inside), in pairs
@@ -454,15 +452,20 @@ __global__ void __launch_bounds__(NW * 32, 8)
         }
     }
 
-    if (uok) {
-        TS *o = reinterpret_cast<TS *>(a.H_next) +
-                (static_cast<size_t>(b) * a.T + t0 + r0) * a.d_h + u;
-        const size_t half_off = static_cast<size_t>(HALF) * a.d_h;
+    // H^(K) of the tile -> shared memory (the P tile's space: every read of it
+    // lies behind the last barrier) -> one TMA store, which clips rows past T
+    // and units past d_h
+    TS *Hst = reinterpret_cast<TS *>(dsmem);   // [L][U]
 #pragma unroll
-        for (int j = 0; j < HALF; ++j, o += a.d_h) {
-            if (j < nvalid) o[0] = from_f32<TS>(G[j].x);
-            if (j + HALF < nvalid) o[half_off] = from_f32<TS>(G[j].y);
-        }
+    for (int j = 0; j < HALF; ++j) {
+        Hst[(r0 + j) * U + lane] = from_f32<TS>(G[j].x);
+        Hst[(r0 + HALF + j) * U + lane] = from_f32<TS>(G[j].y);
+    }
+    fence_proxy_async_smem();
+    __syncthreads();
+    if (tid == 0) {
+        tma_store_3d(&tmO, Hst, u0, t0, b);
+        bulk_commit_and_wait_read();
     }
 }
 
@@ -570,8 +573,8 @@ size_t smem_bytes_for(bool with_h) {
 }
 
 template <typename TS, bool FUSED>
-cudaError_t launch_one(const CUtensorMap &tmP, const CUtensorMap &tmH, const NewtonArgs &a,
-                       int64_t n_ctas, cudaStream_t stream) {
+cudaError_t launch_one(const CUtensorMap &tmP, const CUtensorMap &tmH, const CUtensorMap &tmO,
+                       const NewtonArgs &a, int64_t n_ctas, cudaStream_t stream) {
     static std::atomic<unsigned long long> configured{0};
     const size_t smem = smem_bytes_for<TS, FUSED>(a.H_prev != nullptr);
     cudaError_t e = once_per_device(configured, [](int) {
@@ -579,13 +582,13 @@ cudaError_t launch_one(const CUtensorMap &tmP, const CUtensorMap &tmH, const New
                                     static_cast<int>(smem_bytes_for<TS, FUSED>(true)));
     });
     if (e != cudaSuccess) return e;
-    k_newton<TS, FUSED><<<static_cast<unsigned>(n_ctas), NW * 32, smem, stream>>>(tmP, tmH, tmP,
-                                                                                tmP, a);
+    k_newton<TS, FUSED><<<static_cast<unsigned>(n_ctas), NW * 32, smem, stream>>>(tmP, tmH, tmO,
+                                                                                tmP, tmP, a);
     return cudaGetLastError();
 }
 
-cudaError_t launch_x(const CUtensorMap &tmX, const CUtensorMap &tmW, const NewtonArgs &a,
-                     int64_t n_ctas, cudaStream_t stream) {
+cudaError_t launch_x(const CUtensorMap &tmX, const CUtensorMap &tmW, const CUtensorMap &tmO,
+                     const NewtonArgs &a, int64_t n_ctas, cudaStream_t stream) {
     static std::atomic<unsigned long long> configured{0};
     constexpr size_t smem = 2 * XP_STAGE_BYTES + 1024;   // stages alias the P' tile; + alignment
     static_assert(2 * XP_STAGE_BYTES >= 3 * L * U * 4, "P' tile must fit in the stage ring");
@@ -595,7 +598,7 @@ cudaError_t launch_x(const CUtensorMap &tmX, const CUtensorMap &tmW, const Newto
     });
     if (e != cudaSuccess) return e;
     k_newton<__nv_bfloat16, true, true><<<static_cast<unsigned>(n_ctas), NW * 32, smem, stream>>>(
-        tmX, tmX, tmX, tmW, a);
+        tmX, tmX, tmO, tmX, tmW, a);
     return cudaGetLastError();
 }
 
@@ -608,17 +611,18 @@ size_t newton_smem_bytes(int dtype, bool fused) {
 }
 
 cudaError_t launch_newton(int dtype, bool fused, const CUtensorMap &tmP, const CUtensorMap &tmH,
-                          const NewtonArgs &a, int64_t n_ctas, cudaStream_t stream) {
+                          const CUtensorMap &tmO, const NewtonArgs &a, int64_t n_ctas,
+                          cudaStream_t stream) {
     if (dtype == 1)
-        return fused ? launch_one<__nv_bfloat16, true>(tmP, tmH, a, n_ctas, stream)
-                     : launch_one<__nv_bfloat16, false>(tmP, tmH, a, n_ctas, stream);
-    return fused ? launch_one<float, true>(tmP, tmH, a, n_ctas, stream)
-                 : launch_one<float, false>(tmP, tmH, a, n_ctas, stream);
+        return fused ? launch_one<__nv_bfloat16, true>(tmP, tmH, tmO, a, n_ctas, stream)
+                     : launch_one<__nv_bfloat16, false>(tmP, tmH, tmO, a, n_ctas, stream);
+    return fused ? launch_one<float, true>(tmP, tmH, tmO, a, n_ctas, stream)
+                 : launch_one<float, false>(tmP, tmH, tmO, a, n_ctas, stream);
 }
 
-cudaError_t launch_newton_x(const CUtensorMap &tmX, const CUtensorMap &tmW, const NewtonArgs &a,
-                            int64_t n_ctas, cudaStream_t stream) {
-    return launch_x(tmX, tmW, a, n_ctas, stream);
+cudaError_t launch_newton_x(const CUtensorMap &tmX, const CUtensorMap &tmW, const CUtensorMap &tmO,
+                            const NewtonArgs &a, int64_t n_ctas, cudaStream_t stream) {
+    return launch_x(tmX, tmW, tmO, a, n_ctas, stream);
 }
 
 cudaError_t launch_residual(int dtype, const void *P, const float *params, const void *G, int B,

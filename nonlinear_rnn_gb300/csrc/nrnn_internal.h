@@ -82,14 +82,17 @@ struct SyncLayout {
 
 size_t newton_smem_bytes(int dtype, bool fused);
 
+// tmP over P (3 d_h, T, B), tmH over the H^(k-1) or H^(0) input, tmO over the
+// H output, all with a TILE_U x NEWTON_L x 1 box
 cudaError_t launch_newton(int dtype, bool fused, const CUtensorMap &tmP, const CUtensorMap &tmH,
-                          const NewtonArgs &a, int64_t n_ctas, cudaStream_t stream);
+                          const CUtensorMap &tmO, const NewtonArgs &a, int64_t n_ctas,
+                          cudaStream_t stream);
 
 // fused algorithm with the input projection computed in-kernel (bf16): tmX over
-// x (d_in, T, B) with a 64 x 128 x 1 box, tmW over W_x (d_in, 3 d_h) with a
-// 64 x 32 box, both with the 128-byte swizzle
-cudaError_t launch_newton_x(const CUtensorMap &tmX, const CUtensorMap &tmW, const NewtonArgs &a,
-                            int64_t n_ctas, cudaStream_t stream);
+// x (d_in, T, B) with a 64 x NEWTON_L x 1 box, tmW over W_x (d_in, 3 d_h) with
+// a 64 x 32 box, both with the 128-byte swizzle; tmO over the H output
+cudaError_t launch_newton_x(const CUtensorMap &tmX, const CUtensorMap &tmW, const CUtensorMap &tmO,
+                            const NewtonArgs &a, int64_t n_ctas, cudaStream_t stream);
 
 cudaError_t launch_residual(int dtype, const void *P, const float *params, const void *G,
                             int B, int T, int d_h, const int32_t *cu, int S,

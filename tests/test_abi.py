@@ -72,8 +72,9 @@ def test_forward_rejects_bad_arguments_before_any_launch():
     lib = nr.load()
     fake = ctypes.c_void_p(256)   # never dereferenced: checks fail first
     res = ctypes.c_void_p(512)
+    hout = ctypes.c_void_p(1 << 24)   # apart from preact
     args = dict(pre=fake, dtype=0, prm=fake, B=1, T=8, d=16, cu=None, S=0, K=3, fail=1.0, algo=0,
-                H=fake, rd=res, rh=None, ws=fake, wsb=1 << 20, st=None)
+                H=hout, rd=res, rh=None, ws=fake, wsb=1 << 20, st=None)
 
     def call(**kw):
         a = dict(args, **kw)
@@ -86,6 +87,7 @@ def test_forward_rejects_bad_arguments_before_any_launch():
     assert call(K=65) == -1
     assert call(algo=9) == -1
     assert call(B=2, cu=fake, S=2) == -2          # packs need B == 1
+    assert call(H=ctypes.c_void_p(256 + 3 * 8 * 16 * 4 - 16)) == -1   # H_out overlaps preact
     assert call(wsb=16) == -7                     # workspace too small
     assert call(ws=ctypes.c_void_p(256 + 16)) == -7   # workspace misaligned
     assert call(pre=ctypes.c_void_p(260)) == -1   # preact misaligned
