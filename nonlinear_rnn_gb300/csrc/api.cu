@@ -31,9 +31,9 @@ bool ranges_overlap(const void *a, size_t a_bytes, const void *b, size_t b_bytes
 }
 bool overlaps(const void *a, const void *b, size_t bytes) { return ranges_overlap(a, bytes, b, bytes); }
 
-// Workspace: [counters (K+1) u32 | error u32] zeroed per call, then
-// [slots K x n_tiles x 32 u64] set to all-ones bytes per call, then
-// (per-iteration, K > 1) one H buffer.
+// Workspace: [counters (K+1) u32 | error u32], then [slots K x n_tiles x 32
+// u64], both cleared by one memset per call, then (per-iteration, K > 1) one
+// H buffer.
 SyncLayout layout(int64_t B, int64_t T, int64_t d_h, int dtype, int K, bool fused) {
     SyncLayout s{};
     const int64_t n_ut = (d_h + TILE_U - 1) / TILE_U;
@@ -42,10 +42,10 @@ SyncLayout layout(int64_t B, int64_t T, int64_t d_h, int dtype, int K, bool fuse
     s.n_tiles = B * n_ut * n_chunks;
     s.counters_off = 0;
     s.error_off = sizeof(uint32_t) * (kk + 1);
-    s.zero_bytes = align_up(s.error_off + sizeof(uint32_t), 16);
-    s.slots_off = align_up(s.zero_bytes, 256);
+    s.slots_off = align_up(s.error_off + sizeof(uint32_t), 256);
     s.slots_bytes = sizeof(unsigned long long) * 32 * kk * s.n_tiles;
-    size_t end = s.slots_off + s.slots_bytes;
+    s.zero_bytes = s.slots_off + s.slots_bytes;
+    size_t end = s.zero_bytes;
     s.hbuf_off = align_up(end, 256);
     if (!fused && K > 1) end = s.hbuf_off + elem_size(dtype) * B * T * d_h;
     s.total = align_up(end, 256);
@@ -242,9 +242,9 @@ int nrnn_newton_forward_init(const void *preact, int dtype, const float *params,
     uint32_t *err = reinterpret_cast<uint32_t *>(ws + ly.error_off);
     const int S = static_cast<int>(cu_seqlens ? num_segments : 0);
 
+    // one memset clears counters, error word and slots; rho accumulates by
+    // atomicMax into residual_dev
     cudaError_t e = cudaMemsetAsync(ws, 0, ly.zero_bytes, stream);
-    if (e == cudaSuccess && K > 0 && ly.slots_bytes > 0)
-        e = cudaMemsetAsync(ws + ly.slots_off, 0xff, ly.slots_bytes, stream);
     if (e == cudaSuccess) e = cudaMemsetAsync(residual_dev, 0, sizeof(float), stream);
     if (e != cudaSuccess) return NRNN_ERR_CUDA;
 
@@ -335,7 +335,6 @@ int nrnn_newton_forward_x(const void *x, const void *W_x, int dtype, const float
     unsigned char *ws = static_cast<unsigned char *>(workspace);
     uint32_t *err = reinterpret_cast<uint32_t *>(ws + ly.error_off);
     cudaError_t e = cudaMemsetAsync(ws, 0, ly.zero_bytes, stream);
-    if (e == cudaSuccess) e = cudaMemsetAsync(ws + ly.slots_off, 0xff, ly.slots_bytes, stream);
     if (e == cudaSuccess) e = cudaMemsetAsync(residual_dev, 0, sizeof(float), stream);
     if (e != cudaSuccess) return NRNN_ERR_CUDA;
     if (B * T > 0) {
@@ -391,7 +390,6 @@ int nrnn_newton_backward(const void *preact, int dtype, const float *params, int
     if (e != cudaSuccess) return NRNN_ERR_CUDA;
     if (B * T == 0) return NRNN_OK;
     e = cudaMemsetAsync(ws, 0, ly.zero_bytes, stream);
-    if (e == cudaSuccess) e = cudaMemsetAsync(ws + ly.slots_off, 0xff, ly.slots_bytes, stream);
     if (e != cudaSuccess) return NRNN_ERR_CUDA;
     CUtensorMap tmP, tmH, tmG;
     if (!make_map(&tmP, preact, dtype, 3 * d_h, T, B) || !make_map(&tmH, H, dtype, d_h, T, B) ||

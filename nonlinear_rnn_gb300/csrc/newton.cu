@@ -430,7 +430,7 @@ __global__ void __launch_bounds__(NW * 32, 8)
     }
 
     // residual max|F(H^(K))| at the values as stored
-    if (a.last && a.residual_bits != nullptr) {
+    if (a.last) {
         // each warp read only its own prefix slot in the apply step: reuse the
         // slots for the last row of each warp
         s_aggA[warp][lane] = round_to<TS>(G[HALF - 1].y);

@@ -458,18 +458,19 @@ __device__ __forceinline__ float pair_b(unsigned long long v) {
 
 // ------------------------------------------------- decoupled look-back slots
 // One 64-bit word per (chunk, unit) holds the chunk's affine pair (A, b) and is
-// its own ready flag: SLOT_EMPTY (all ones, written by a per-call memset)
-// means not yet published.  Published pairs never take that value (arithmetic
-// NaNs are 0x7fffffff; publish() remaps the one colliding pattern).  Because
-// a 64-bit aligned access is single-copy atomic, a reader sees either
-// SLOT_EMPTY, the chunk aggregate, or the inclusive prefix (A = 0), and the
-// latter two both compose correctly: no fence is needed on either side.
-constexpr unsigned long long SLOT_EMPTY = 0xffffffffffffffffull;
+// its own ready flag: SLOT_EMPTY (all zero bits, from the one per-call memset
+// that also clears the counters) means not yet published.  Published pairs
+// never take that value: publish() writes the pair (+0, +0) as (+0, -0),
+// which composes identically.  Because a 64-bit aligned access is single-copy
+// atomic, a reader sees either SLOT_EMPTY, the chunk aggregate, or the
+// inclusive prefix (A = 0), and the latter two both compose correctly: no
+// fence is needed on either side.
+constexpr unsigned long long SLOT_EMPTY = 0ull;
 constexpr int LOOKBACK_WIN = 4;   // neighbours read in parallel per round
 
 __device__ __forceinline__ void publish(unsigned long long *slot, float A, float b) {
     unsigned long long v = pack_pair(A, b);
-    if (v == SLOT_EMPTY) v = pack_pair(__int_as_float(0x7fffffff), b);
+    if (v == SLOT_EMPTY) v = pack_pair(0.f, -0.f);
     st_relaxed_u64(slot, v);
 }
 
@@ -495,7 +496,7 @@ __device__ __forceinline__ float lookback_lane(const unsigned long long *slot, i
             const int qi = c + dir * (d + i);
             v[i] = (qi >= 0 && qi < n_chunks)
                        ? ld_relaxed_u64(slot + static_cast<ptrdiff_t>(dir) * (d + i) * 32)
-                       : pack_pair(0.f, 0.f);
+                       : pack_pair(0.f, -0.f);   // before the first chunk: closed, zero
         }
         int folded = 0;
 #pragma unroll

@@ -45,7 +45,7 @@ struct NewtonArgs {
     int last;                     // this launch ends with H^(K): compute the residual
     unsigned long long *slots;    // [K][n_tiles][32] packed (A, b); all-ones = not published
     uint32_t *ticket;             // this launch's CTA ticket counter
-    uint32_t *residual_bits;      // float bits of rho (atomicMax), or null
+    uint32_t *residual_bits;      // float bits of rho (atomicMax), cleared by the caller
     uint32_t *error;              // error word (bit 0: look-back timeout, bit 1: TMA timeout)
     unsigned long long wait_ns;   // limit of every bounded wait
     int withhold_tile;            // debug: this tile never publishes its look-back slot (-1: none)
@@ -72,8 +72,9 @@ cudaError_t launch_backward(int dtype, const CUtensorMap &tmP, const CUtensorMap
                             const CUtensorMap &tmG, const BackwardArgs &a, int64_t n_ctas,
                             cudaStream_t stream);
 
-// Workspace of one call: [counters | error] zeroed, [slots] set to all-ones
-// bytes, then (per-iteration variant, K > 1) one H buffer.
+// Workspace of one call: [counters | error] and [slots], cleared together by
+// one memset (zero_bytes from the start), then (per-iteration variant, K > 1)
+// one H buffer.
 struct SyncLayout {
     size_t counters_off, error_off, zero_bytes;
     size_t slots_off, slots_bytes, hbuf_off, total;
