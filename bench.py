@@ -141,13 +141,13 @@ def workload_bytes(w, algo):
     return [4 * w.d_h * s * tok]          # fused: read P once, write H once
 
 
-# Special-function (MUFU) work per cell evaluation in the Newton kernels:
-# three ex2 (one per gate) and two rcp (one for r, one shared by z and the
-# tanh).  The roof is the SM's measured MUFU rate (nrnn_probe_xu_rates, run
-# live): an rcp occupies the unit for ex2_rate / rcp_rate ex2 slots, so the
-# work is counted in ex2-equivalent operations.
-EX2_PER_EVAL = 3
-RCP_PER_EVAL = 2
+# Special-function (MUFU) work per cell evaluation in the Newton kernels: for
+# fp32 storage three ex2 (one per gate) and two rcp (one for r, one shared by
+# z and the tanh); for bf16 storage three tanh.approx.  The roof is the SM's
+# measured MUFU rate (nrnn_probe_xu_rates, run live): an rcp or tanh occupies
+# the unit for ex2_rate / its rate ex2 slots, so the work is counted in
+# ex2-equivalent operations.
+MUFU_PER_EVAL = {"f32": {"ex2": 3, "rcp": 2}, "bf16": {"tanh": 3}}
 SM_MAX_MHZ = 2070.0
 
 
@@ -246,8 +246,10 @@ def run_ours(args, w, rank, world, local):
            "peak_src": pk["src"] + " (MEASURED_PEAKS.json hbm_gbs)"}
     if fused:
         # one launch runs K iterations plus the residual evaluation
-        ex2_rate, rcp_rate = xu_rates
-        per_eval = EX2_PER_EVAL + RCP_PER_EVAL * ex2_rate / rcp_rate
+        rates = dict(zip(("ex2", "rcp", "tanh"), xu_rates))
+        mix = MUFU_PER_EVAL[w.dtype]
+        per_eval = sum(n * rates["ex2"] / rates[op] for op, n in mix.items())
+        ex2_rate = rates["ex2"]
         xu_ops = per_eval * (w.K + 1) * tokens * w.d_h
         xu_achieved = xu_ops / (ms * 1e-3) / 1e9
         mhz = clocks.get("sm_max_mhz") or SM_MAX_MHZ
@@ -256,9 +258,10 @@ def run_ours(args, w, rank, world, local):
                 "unit": "Gop/s (MUFU, ex2-equivalent)",
                 "frac": xu_achieved / xu_peak, "traffic": load_traffic(w, algo), "kernel": kname,
                 "algorithmic_ops_per_launch": xu_ops,
-                "peak_src": f"measured {ex2_rate:.2f} ex2 and {rcp_rate:.2f} rcp results/clk/SM "
-                            f"(nrnn_probe_xu_rates) x {props.multi_processor_count} SMs x {mhz:.0f} MHz "
-                            "(maximum SM clock); per evaluation 3 ex2 + 2 rcp",
+                "peak_src": "measured " + ", ".join(f"{rates[k]:.2f} {k}" for k in rates)
+                            + f" results/clk/SM (nrnn_probe_xu_rates) x {props.multi_processor_count} "
+                            f"SMs x {mhz:.0f} MHz (maximum SM clock); per evaluation "
+                            + " + ".join(f"{n} {op}" for op, n in mix.items()),
                 "hbm": {k: hbm[k] for k in ("achieved", "peak", "unit", "frac",
                                             "algorithmic_bytes_per_launch")}}
     else:

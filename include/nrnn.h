@@ -320,17 +320,21 @@ uint64_t nrnn_set_wait_limit_ns(uint64_t ns);
 /*
  * Measures the special-function unit throughput of the current device, the
  * denominator of the fused Newton kernel's ALU roofline (each cell evaluation
- * issues three ex2.approx and two rcp.approx; the pages give no hardware
- * figure for it, so the library measures it).  One CTA per SM runs independent
- * chains of each instruction and times itself with the SM cycle counter.
- *   ex2_per_clk, rcp_per_clk  host, 1 float each: median over SMs of results
- *                             per SM clock cycle
- *   stream                    cudaStream_t to run on (NULL: legacy stream);
- *                             the call synchronises it
- * Allocates and frees a small device buffer; takes about a millisecond.
+ * issues three ex2.approx and two rcp.approx for fp32 storage, three
+ * tanh.approx for bf16 storage; the pages give no hardware figure for it, so
+ * the library measures it).  No counterpart in the pages.  One CTA per SM runs
+ * independent chains of each instruction and times itself with the SM cycle
+ * counter.
+ *   ex2_per_clk, rcp_per_clk, tanh_per_clk
+ *                 host, 1 float each: median over SMs of results per SM
+ *                 clock cycle
+ *   stream        cudaStream_t to run on (NULL: legacy stream); the call
+ *                 synchronises it
+ * Allocates and frees a small device buffer; takes a few milliseconds.
  * Returns NRNN_OK, NRNN_ERR_INVALID_ARG (null output) or NRNN_ERR_CUDA.
  */
-int nrnn_probe_xu_rates(float *ex2_per_clk, float *rcp_per_clk, void *stream);
+int nrnn_probe_xu_rates(float *ex2_per_clk, float *rcp_per_clk, float *tanh_per_clk,
+                        void *stream);
 
 #ifdef __cplusplus
 }

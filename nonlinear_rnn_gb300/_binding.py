@@ -51,7 +51,7 @@ _SIGNATURES = {
     "nrnn_debug_bounded_wait": ([_vp, _u64, _vp, _vp], _int),
     "nrnn_set_wait_limit_ns": ([_u64], _u64),
     "nrnn_debug_withhold_publish": ([_i64], _i64),
-    "nrnn_probe_xu_rates": ([ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_float), _vp], _int),
+    "nrnn_probe_xu_rates": ([ctypes.POINTER(ctypes.c_float)] * 3 + [_vp], _int),
     "nrnn_newton_forward_noalloc": ([_vp, _int, _vp, _i64, _i64, _i64, _vp, _i64, _int, _f, _vp,
                                      _vp, _vp, _vp], _int),
 }
@@ -466,13 +466,14 @@ def verify_agreement(preact, params, K: int = 3, cu_seqlens=None, atol: float | 
     return rep
 
 
-def probe_xu_rates(device="cuda") -> tuple[float, float]:
-    """(ex2, rcp) results per SM clock cycle on `device`, measured by the
+def probe_xu_rates(device="cuda") -> tuple[float, float, float]:
+    """(ex2, rcp, tanh) results per SM clock cycle on `device`, measured by the
     library's special-function throughput probe."""
     lib = load()
     dev = torch.device(device)
-    e2, rc = ctypes.c_float(0.0), ctypes.c_float(0.0)
+    e2, rc, th = ctypes.c_float(0.0), ctypes.c_float(0.0), ctypes.c_float(0.0)
     with torch.cuda.device(dev):
-        st = lib.nrnn_probe_xu_rates(ctypes.byref(e2), ctypes.byref(rc), _stream(dev))
+        st = lib.nrnn_probe_xu_rates(ctypes.byref(e2), ctypes.byref(rc), ctypes.byref(th),
+                                     _stream(dev))
     _raise(st, "probe_xu_rates")
-    return float(e2.value), float(rc.value)
+    return float(e2.value), float(rc.value), float(th.value)

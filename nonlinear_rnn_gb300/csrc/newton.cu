@@ -76,8 +76,10 @@ __device__ __forceinline__ int pf2_index(int g, int warp, int j, int lane) {
 template <typename TS, bool SCALED, bool GENERAL, bool ZERO = false>
 __device__ __forceinline__ void warp_pairs(const void *Pv, int warp, int lane,
                                            float2 (&G)[HALF], float hb, uint32_t hm, int nvalid,
-                                           const ScaledParams2 &prm, float2 (&J2)[HALF],
-                                           float &A_lo, float &B_lo, float &A, float &Bv) {
+                                           const typename CellOf<TS>::type::Params &prm,
+                                           float2 (&J2)[HALF], float &A_lo, float &B_lo, float &A,
+                                           float &Bv) {
+    using Cell = typename CellOf<TS>::type;
     const int r0 = warp * SEG;
     float2 A2 = splat2(1.f), B2 = splat2(0.f);
     float2 prev = make_float2(hb, G[HALF - 1].x);   // H^(k-1) at rows r0 - 1, r0 + HALF - 1
@@ -92,22 +94,22 @@ __device__ __forceinline__ void warp_pairs(const void *Pv, int warp, int lane,
         } else {
             const TS *P = static_cast<const TS *>(Pv);
             const int lo = (r0 + j) * U + lane, hi = lo + HALF * U;
-            scale_preact2(make_float2(to_f32(P[lo]), to_f32(P[hi])),
-                          make_float2(to_f32(P[L * U + lo]), to_f32(P[L * U + hi])),
-                          make_float2(to_f32(P[2 * L * U + lo]), to_f32(P[2 * L * U + hi])), prm,
-                          sz, sr, sc);
+            Cell::scale(make_float2(to_f32(P[lo]), to_f32(P[hi])),
+                        make_float2(to_f32(P[L * U + lo]), to_f32(P[L * U + hi])),
+                        make_float2(to_f32(P[2 * L * U + lo]), to_f32(P[2 * L * U + hi])), prm, sz,
+                        sr, sc);
         }
         const bool head_lo = GENERAL && ((hm >> j) & 1u);
         const bool head_hi = GENERAL && ((hm >> (j + HALF)) & 1u);
         const float2 cur = G[j];
         float2 J, g;
         if (ZERO) {
-            cell_jg2_at_zero(sz, sr, sc, prm, J, g);
+            Cell::jg_zero(sz, sr, sc, prm, J, g);
         } else {
             float2 hs = prev;
             if (head_lo) hs.x = 0.f;
             if (head_hi) hs.y = 0.f;
-            cell_jg2(hs, sz, sr, sc, prm, J, g);
+            Cell::jg(hs, sz, sr, sc, prm, J, g);
         }
         if (GENERAL) {
             if (head_lo) J.x = 0.f;
@@ -133,7 +135,9 @@ __device__ __forceinline__ void warp_pairs(const void *Pv, int warp, int lane,
 template <typename TS, bool FUSED, bool GENERAL>
 __device__ __forceinline__ float residual_rows(const float *Pf, const TS *Pt, int warp, int lane,
                                                const float2 (&G)[HALF], float2 prev, uint32_t hm,
-                                               int nvalid, const ScaledParams2 &prm) {
+                                               int nvalid,
+                                               const typename CellOf<TS>::type::Params &prm) {
+    using Cell = typename CellOf<TS>::type;
     const int r0 = warp * SEG;
     float m = 0.f;
 #pragma unroll
@@ -146,10 +150,10 @@ __device__ __forceinline__ float residual_rows(const float *Pf, const TS *Pt, in
             sc = P2[pf2_index(2, warp, j, lane)];
         } else {
             const int lo = (r0 + j) * U + lane, hi = lo + HALF * U;
-            scale_preact2(make_float2(to_f32(Pt[lo]), to_f32(Pt[hi])),
-                          make_float2(to_f32(Pt[L * U + lo]), to_f32(Pt[L * U + hi])),
-                          make_float2(to_f32(Pt[2 * L * U + lo]), to_f32(Pt[2 * L * U + hi])),
-                          prm, sz, sr, sc);
+            Cell::scale(make_float2(to_f32(Pt[lo]), to_f32(Pt[hi])),
+                        make_float2(to_f32(Pt[L * U + lo]), to_f32(Pt[L * U + hi])),
+                        make_float2(to_f32(Pt[2 * L * U + lo]), to_f32(Pt[2 * L * U + hi])), prm,
+                        sz, sr, sc);
         }
         const float2 hq = make_float2(round_to<TS>(G[j].x), round_to<TS>(G[j].y));
         float2 hs = prev;
@@ -157,7 +161,7 @@ __device__ __forceinline__ float residual_rows(const float *Pf, const TS *Pt, in
             if ((hm >> j) & 1u) hs.x = 0.f;
             if ((hm >> (j + HALF)) & 1u) hs.y = 0.f;
         }
-        const float2 F = fma2(cell_f2(hs, sz, sr, sc, prm), splat2(-1.0f), hq);
+        const float2 F = fma2(Cell::f(hs, sz, sr, sc, prm), splat2(-1.0f), hq);
         float fx = fabsf(F.x), fy = fabsf(F.y);
         if (GENERAL) {
             if (j >= nvalid) fx = 0.f;
@@ -255,8 +259,9 @@ __global__ void __launch_bounds__(NW * 32, 8)
     }
     const int u = u0 + lane;
     const bool uok = u < a.d_h;
-    const ScaledParams prm = scale_params(load_unit_params(a.params, a.d_h, u, uok));
-    const ScaledParams2 prm2 = pair_params(prm);
+    using Cell = typename CellOf<TS>::type;
+    const UnitParams up = load_unit_params(a.params, a.d_h, u, uok);
+    const typename Cell::Params prm2 = Cell::make(up);
     const int r0 = warp * SEG;
     // shifted state at this warp's first row: H^(k-1) at row r0 - 1
     float hb = 0.f;
@@ -303,8 +308,8 @@ __global__ void __launch_bounds__(NW * 32, 8)
         if (warp < 3) {
             // lane = unit of gate `warp`, registers = 32 time steps per load
             // (two warps' rows), written in pair order
-            const float mul = warp == 2 ? 2.0f * LOG2E : -LOG2E;
-            const float add = warp == 0 ? prm.nb_z : (warp == 1 ? prm.nb_r : prm.b_c2);
+            float mul, add;
+            Cell::gate_affine(warp, up, mul, add);
             float2 *P2 = reinterpret_cast<float2 *>(Pf);
 #pragma unroll 1
             for (int cc = 0; cc < L / 32; ++cc) {
@@ -352,7 +357,7 @@ __global__ void __launch_bounds__(NW * 32, 8)
 #pragma unroll
         for (int j = 0; j < HALF; ++j) {
             float2 sz, sr, sc;
-            scale_preact2(v[0][j], v[1][j], v[2][j], prm2, sz, sr, sc);
+            Cell::scale(v[0][j], v[1][j], v[2][j], prm2, sz, sr, sc);
             P2[pf2_index(0, warp, j, lane)] = sz;
             P2[pf2_index(1, warp, j, lane)] = sr;
             P2[pf2_index(2, warp, j, lane)] = sc;

@@ -410,6 +410,121 @@ __device__ __forceinline__ float2 cell_f2(float2 h, float2 sz, float2 sr, float2
     return fma2(z, fma2(h, splat2(-1.0f), c), h);
 }
 
+// --------------------------------------------- cell formulations per storage
+// ExpCell (fp32 storage): the exponent-2 form above, ex2.approx and
+// rcp.approx, a few ulp.  TanhCell (bf16 storage): sig(x) = (1 + tanh(x/2))/2
+// and tanh on tanh.approx.f32 (max relative error about 2^-11, four times
+// below the bf16 storage step), three MUFU operations per evaluation and no
+// clamps (tanh saturates).  Both present the same interface to the kernels:
+// pre-scaled gate arguments, (J, g) of a pair of steps, f of a pair.
+__device__ __forceinline__ float tanh_approx(float x) {
+    float y;
+    asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+__device__ __forceinline__ float2 tanh_2(float2 x) {
+    return make_float2(tanh_approx(x.x), tanh_approx(x.y));
+}
+
+struct ExpCell {
+    using Params = ScaledParams2;
+    __device__ static Params make(const UnitParams &p) { return pair_params(scale_params(p)); }
+    // pre-scaled argument of gate g from a raw preactivation: p * mul + add
+    __device__ static void gate_affine(int g, const UnitParams &p, float &mul, float &add) {
+        mul = g == 2 ? 2.0f * LOG2E : -LOG2E;
+        add = g == 0 ? -LOG2E * p.b_z : (g == 1 ? -LOG2E * p.b_r : 2.0f * LOG2E * p.b_c);
+    }
+    __device__ static void scale(float2 pz, float2 pr, float2 pc, const Params &q, float2 &sz,
+                                 float2 &sr, float2 &sc) {
+        scale_preact2(pz, pr, pc, q, sz, sr, sc);
+    }
+    __device__ static void jg(float2 h, float2 sz, float2 sr, float2 sc, const Params &q, float2 &J,
+                              float2 &g) {
+        cell_jg2(h, sz, sr, sc, q, J, g);
+    }
+    __device__ static void jg_zero(float2 sz, float2 sr, float2 sc, const Params &q, float2 &J,
+                                   float2 &g) {
+        cell_jg2_at_zero(sz, sr, sc, q, J, g);
+    }
+    __device__ static float2 f(float2 h, float2 sz, float2 sr, float2 sc, const Params &q) {
+        return cell_f2(h, sz, sr, sc, q);
+    }
+};
+
+struct TanhCell {
+    struct Params {
+        float2 hz, hr;           // a_z / 2, a_r / 2: state terms of the halved z, r arguments
+        float2 a_c, na_c;        // a_c, -a_c
+        float2 a_z, a_r;         // Jacobian
+        float2 bz, br, bc;       // b_z / 2, b_r / 2, b_c
+    };
+    __device__ static Params make(const UnitParams &p) {
+        Params q;
+        q.hz = splat2(0.5f * p.a_z);
+        q.hr = splat2(0.5f * p.a_r);
+        q.a_c = splat2(p.a_c);
+        q.na_c = splat2(-p.a_c);
+        q.a_z = splat2(p.a_z);
+        q.a_r = splat2(p.a_r);
+        q.bz = splat2(0.5f * p.b_z);
+        q.br = splat2(0.5f * p.b_r);
+        q.bc = splat2(p.b_c);
+        return q;
+    }
+    __device__ static void gate_affine(int g, const UnitParams &p, float &mul, float &add) {
+        mul = g == 2 ? 1.0f : 0.5f;
+        add = g == 0 ? 0.5f * p.b_z : (g == 1 ? 0.5f * p.b_r : p.b_c);
+    }
+    __device__ static void scale(float2 pz, float2 pr, float2 pc, const Params &q, float2 &sz,
+                                 float2 &sr, float2 &sc) {
+        sz = fma2(pz, splat2(0.5f), q.bz);
+        sr = fma2(pr, splat2(0.5f), q.br);
+        sc = add2(pc, q.bc);
+    }
+    // tz = tanh(arg_z / 2 ...): z = (1 + tz) / 2, 1 - z = (1 - tz) / 2; likewise r
+    __device__ static void gates(float2 h, float2 sz, float2 sr, float2 sc, const Params &q,
+                                 float2 &tz, float2 &tr, float2 &r, float2 &c) {
+        tz = tanh_2(fma2(q.hz, h, sz));
+        tr = tanh_2(fma2(q.hr, h, sr));
+        r = fma2(splat2(0.5f), tr, splat2(0.5f));
+        c = tanh_2(fma2(q.a_c, mul2(r, h), sc));
+    }
+    __device__ static void jg(float2 h, float2 sz, float2 sr, float2 sc, const Params &q, float2 &J,
+                              float2 &g) {
+        float2 tz, tr, r, c;
+        gates(h, sz, sr, sc, q, tz, tr, r, c);
+        const float2 half = splat2(0.5f), mhalf = splat2(-0.5f), mone = splat2(-1.0f);
+        const float2 z = fma2(half, tz, half), omz = fma2(mhalf, tz, half);
+        const float2 omr = fma2(mhalf, tr, half);
+        const float2 nh = mul2(h, mone);
+        const float2 cmh = add2(c, nh);
+        const float2 dq = fma2(mul2(mul2(h, q.a_r), omr), r, r);      // d(r h)/dh
+        const float2 t2 = fma2(mul2(c, q.na_c), c, q.a_c);            // a_c (1 - c^2)
+        const float2 inner = fma2(mul2(omz, q.a_z), cmh, mul2(t2, dq));
+        J = fma2(z, inner, omz);
+        g = mul2(z, fma2(nh, inner, c));
+    }
+    __device__ static void jg_zero(float2 sz, float2 sr, float2 sc, const Params &q, float2 &J,
+                                   float2 &g) {
+        const float2 half = splat2(0.5f), mhalf = splat2(-0.5f);
+        const float2 tz = tanh_2(sz), tr = tanh_2(sr), c = tanh_2(sc);
+        const float2 z = fma2(half, tz, half), omz = fma2(mhalf, tz, half);
+        const float2 r = fma2(half, tr, half);
+        const float2 t2 = fma2(mul2(c, q.na_c), c, q.a_c);
+        J = fma2(z, fma2(mul2(omz, q.a_z), c, mul2(t2, r)), omz);
+        g = mul2(z, c);
+    }
+    __device__ static float2 f(float2 h, float2 sz, float2 sr, float2 sc, const Params &q) {
+        float2 tz, tr, r, c;
+        gates(h, sz, sr, sc, q, tz, tr, r, c);
+        const float2 z = fma2(splat2(0.5f), tz, splat2(0.5f));
+        return fma2(z, fma2(h, splat2(-1.0f), c), h);
+    }
+};
+
+template <typename TS> struct CellOf { using type = ExpCell; };
+template <> struct CellOf<__nv_bfloat16> { using type = TanhCell; };
+
 // |F| for the residual gate; NaN counts as +inf
 __device__ __forceinline__ float abs_residual(float F) {
     const float a = fabsf(F);

@@ -1,6 +1,6 @@
 // Special-function (MUFU) throughput of the GPU the library runs on: the
 // denominator of the fused Newton kernel's ALU roofline, whose work is three
-// ex2 and two rcp per cell evaluation.  One CTA of 1024 threads per SM (the
+// ex2 and two rcp per cell evaluation (fp32 storage) or three tanh (bf16).  One CTA of 1024 threads per SM (the
 // dynamic shared memory request keeps a second CTA off the SM) runs eight
 // independent chains of the instruction per thread and times itself with the
 // SM cycle counter, so the rate comes out per SM clock, independent of the
@@ -23,7 +23,7 @@ constexpr size_t PROBE_SMEM = 160 * 1024;
 
 // OP 0: x <- ex2(-x) (stays in [0.5, 1)); OP 1: x <- 0.5 rcp(x) + 0.75 (stays
 // in [1, 1.25]; the fma keeps the compiler from pairing reciprocals away and
-// runs on another pipe)
+// runs on another pipe); OP 2: x <- tanh(x) + 0.5 (stays in [0.5, 1.5])
 template <int OP>
 __global__ void __launch_bounds__(PROBE_THREADS, 1)
     k_xu_probe(int iters, long long *cycles, float *sink) {
@@ -37,6 +37,10 @@ __global__ void __launch_bounds__(PROBE_THREADS, 1)
         for (int j = 0; j < PROBE_CHAINS; ++j) {
             if (OP == 0) {
                 asm volatile("ex2.approx.ftz.f32 %0, %1;" : "=f"(x[j]) : "f"(-x[j]));
+            } else if (OP == 2) {
+                float y;
+                asm volatile("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x[j]));
+                x[j] = y + 0.5f;
             } else {
                 float y;
                 asm volatile("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x[j]));
@@ -76,8 +80,10 @@ int run(int sms, long long *cycles_dev, float *sink, cudaStream_t stream, float 
 
 }  // namespace nrnn
 
-extern "C" int nrnn_probe_xu_rates(float *ex2_per_clk, float *rcp_per_clk, void *stream_) {
-    if (ex2_per_clk == nullptr || rcp_per_clk == nullptr) return NRNN_ERR_INVALID_ARG;
+extern "C" int nrnn_probe_xu_rates(float *ex2_per_clk, float *rcp_per_clk, float *tanh_per_clk,
+                                   void *stream_) {
+    if (ex2_per_clk == nullptr || rcp_per_clk == nullptr || tanh_per_clk == nullptr)
+        return NRNN_ERR_INVALID_ARG;
     cudaStream_t stream = static_cast<cudaStream_t>(stream_);
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
@@ -92,6 +98,7 @@ extern "C" int nrnn_probe_xu_rates(float *ex2_per_clk, float *rcp_per_clk, void 
     }
     int st = nrnn::run<0>(sms, cycles, sink, stream, ex2_per_clk);
     if (st == NRNN_OK) st = nrnn::run<1>(sms, cycles, sink, stream, rcp_per_clk);
+    if (st == NRNN_OK) st = nrnn::run<2>(sms, cycles, sink, stream, tanh_per_clk);
     cudaStreamSynchronize(stream);
     cudaFree(cycles);
     cudaFree(sink);

@@ -280,6 +280,6 @@ def test_lookback_timeout_is_reported_and_context_survives(nr, algo):
 def test_probe_xu_rates(nr):
     # special-function throughput per SM clock: a power-of-two rate on every
     # NVIDIA part so far; ex2 at least as fast as rcp
-    ex2, rcp = nr.probe_xu_rates()
-    assert 4.0 < ex2 < 80.0 and 2.0 < rcp < 80.0
+    ex2, rcp, tanh = nr.probe_xu_rates()
+    assert 4.0 < ex2 < 80.0 and 2.0 < rcp < 80.0 and 2.0 < tanh < 80.0
     assert ex2 >= 0.9 * rcp
