@@ -325,7 +325,7 @@ __device__ __forceinline__ float2 clamp2(float2 x) {
 
 struct ScaledParams2 {
     float2 na_z, na_r, a_c2;   // state coefficients of the exponent-2 gate arguments
-    float2 a_z, a_r, a_c4;     // Jacobian: a_z, a_r, 4 a_c
+    float2 a_z, ma_z, a_r, a_c4;   // Jacobian: a_z, -a_z, a_r, 4 a_c
     float2 nb_z, nb_r, b_c2;   // scaled biases (raw preactivations only)
 };
 
@@ -335,6 +335,7 @@ __device__ __forceinline__ ScaledParams2 pair_params(const ScaledParams &p) {
     q.na_r = splat2(p.na_r);
     q.a_c2 = splat2(p.a_c2);
     q.a_z = splat2(p.a_z);
+    q.ma_z = splat2(-p.a_z);
     q.a_r = splat2(p.a_r);
     q.a_c4 = splat2(4.0f * p.a_c);
     q.nb_z = splat2(p.nb_z);
@@ -369,7 +370,8 @@ __device__ __forceinline__ void gates2(float2 h, float2 sz, float2 sr, float2 sc
 
 // J = df/dh and the Newton pair's offset g = f(h) - J h for a pair of shifted
 // states.  With inner = (1 - z) a_z (c - h) + (1 - c^2) a_c d(rh)/dh one has
-// J = (1 - z) + z inner and f - J h = z (c - h inner).
+// J = (1 - z) + z inner = 1 + z (inner - 1) and f - J h = z (c - h inner)
+// = z ((c - h) - h (inner - 1)); the kernels use inner - 1 directly.
 __device__ __forceinline__ void cell_jg2(float2 h, float2 sz, float2 sr, float2 sc,
                                          const ScaledParams2 &p, float2 &J, float2 &g) {
     float2 z, r, c, q;
@@ -377,12 +379,11 @@ __device__ __forceinline__ void cell_jg2(float2 h, float2 sz, float2 sr, float2 
     const float2 one = splat2(1.0f), mone = splat2(-1.0f);
     const float2 nh = mul2(h, mone);
     const float2 cmh = add2(c, nh);
-    const float2 omz = fma2(z, mone, one);
     const float2 dq = fma2(mul2(mul2(h, p.a_r), fma2(r, mone, one)), r, r);   // d(r h)/dh
-    const float2 t3 = mul2(mul2(mul2(q, p.a_c4), fma2(q, mone, one)), dq);    // (1 - c^2) a_c dq
-    const float2 inner = fma2(mul2(omz, p.a_z), cmh, t3);
-    J = fma2(z, inner, omz);
-    g = mul2(z, fma2(nh, inner, c));
+    const float2 t3m1 = fma2(mul2(mul2(q, p.a_c4), fma2(q, mone, one)), dq, mone);   // (1 - c^2) a_c dq - 1
+    const float2 im1 = fma2(fma2(z, p.ma_z, p.a_z), cmh, t3m1);           // inner - 1
+    J = fma2(z, im1, one);
+    g = mul2(z, fma2(nh, im1, cmh));
 }
 
 // the same at the zero state: g = f(0) = z c, J = (1 - z) + z ((1 - z) a_z c + (1 - c^2) a_c r)
@@ -396,9 +397,8 @@ __device__ __forceinline__ void cell_jg2_at_zero(float2 sz, float2 sr, float2 sc
     const float2 z = mul2(dc, inv);
     const float2 q = mul2(dz, inv);
     const float2 c = fma2(splat2(-2.0f), q, one);
-    const float2 omz = fma2(z, mone, one);
-    const float2 t3 = mul2(mul2(mul2(q, p.a_c4), fma2(q, mone, one)), r);
-    J = fma2(z, fma2(mul2(omz, p.a_z), c, t3), omz);
+    const float2 t3m1 = fma2(mul2(mul2(q, p.a_c4), fma2(q, mone, one)), r, mone);
+    J = fma2(z, fma2(fma2(z, p.ma_z, p.a_z), c, t3m1), one);
     g = mul2(z, c);
 }
 
