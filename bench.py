@@ -362,13 +362,30 @@ def run_ours(args, w, rank, world, local):
     return out
 
 
+# Sources whose change invalidates the recorded DRAM counters of the Newton kernel.
+TRAFFIC_SOURCES = ("nonlinear_rnn_gb300/csrc/newton.cu", "nonlinear_rnn_gb300/csrc/nrnn_device.cuh",
+                   "nonlinear_rnn_gb300/csrc/nrnn_internal.h")
+
+
+def kernel_sources_digest():
+    import hashlib
+    h = hashlib.sha256()
+    for rel in TRAFFIC_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
 def load_traffic(w, algo):
-    """DRAM bytes per launch of the dominant kernel from a committed ncu summary, if any."""
+    """DRAM bytes per launch of the dominant kernel from the committed ncu summary,
+    or None when there is none or the kernel sources changed since it was taken."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
     with open(p) as fh:
         d = json.load(fh)
+    if d.get("_kernel_sources_sha256") != kernel_sources_digest():
+        return None
     return d.get(f"{w.name}|{algo}")
 
 

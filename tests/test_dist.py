@@ -45,3 +45,15 @@ def test_two_rank_max_timing_and_token_total():
         assert w == 2 and lr == r
         assert ms == 2.0            # the slowest rank's time
         assert total == 2000        # weak scaling: every rank runs a full replica
+
+
+def test_traffic_record_is_tied_to_the_kernel_sources(monkeypatch):
+    import bench
+    import synthetic as syn
+    w = syn.WORKLOADS[1]
+    with open(os.path.join(bench.ROOT, "profiles", "traffic.json")) as fh:
+        rec = __import__("json").load(fh)
+    if rec.get("_kernel_sources_sha256") == bench.kernel_sources_digest():
+        assert bench.load_traffic(w, "fused") == rec[f"{w.name}|fused"]
+    monkeypatch.setattr(bench, "kernel_sources_digest", lambda: "changed")
+    assert bench.load_traffic(w, "fused") is None
