@@ -289,17 +289,17 @@ def run_ours(args, w, rank, world, local):
     seq_ms, _ = time_steps(torch, lambda: nr.sequential_forward(P, prm, cu_seqlens=cu, out=H), 3,
                            flush, stream, nvtx=False)
 
-    # end to end through the public call with host buffers
+    # end to end through the C-ABI call on host buffers (nrnn_newton_forward_host:
+    # blocks of rows or segments, copies overlapped with the kernels)
     P_host = P.cpu().pin_memory()
     H_host = torch.empty(H.shape, dtype=H.dtype).pin_memory()
-    rho_host = torch.empty((), dtype=torch.float32).pin_memory()
+    cu_host = None if inp["cu_seqlens"] is None else inp["cu_seqlens"]
+    staging = torch.empty(nr.host_staging_bytes(w.B, w.T, w.d_h, tdt, w.K, cu_seqlens=cu_host),
+                          dtype=torch.uint8, device=dev)
 
     def e2e_step():
-        Pd = P_host.to(dev, non_blocking=True)
-        Hd, r = nr.newton_forward(Pd, prm, cu_seqlens=cu, K=w.K, algo=algo, check=False,
-                                  workspace=ws)
-        H_host.copy_(Hd, non_blocking=True)
-        rho_host.copy_(r, non_blocking=True)
+        nr.newton_forward_host(P_host, prm, cu_seqlens=cu_host, K=w.K, out=H_host,
+                               staging=staging, device=dev, check=False)
     e2e_step()
     e2e, _ = time_steps(torch, e2e_step, max(3, min(args.steps, 10)), flush, stream, nvtx=False)
     e2e_ms = statistics.median(e2e)

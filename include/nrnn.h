@@ -268,6 +268,46 @@ int nrnn_debug_bounded_wait(const uint32_t *flag_dev, uint64_t wait_ns, uint32_t
                             void *stream);
 
 /*
+ * Newton forward on host buffers, with the host-device copies overlapped
+ * with the computation (the pages run the forward on device tensors only;
+ * this is the library's end-to-end entry point for data that lives on the
+ * host).  The problem is cut into blocks that need nothing from one another
+ * -- groups of batch rows, or for a pack groups of whole segments -- of about
+ * tokens_per_block tokens each (0: about six blocks).  Each block is copied
+ * in on a library stream, run through nrnn_newton_forward (fused algorithm)
+ * on `stream`, and copied out on a second library stream, on one of three
+ * slots of `staging`, so that one block's copies overlap another's kernels.
+ * The library streams and their events are created on the calling host
+ * thread's first call on a device and kept for that thread's lifetime.
+ *   preact_host    host, (B, T, 3 d_h) of dtype; page-locked memory lets the
+ *                  copies run asynchronously (pageable memory works, slower)
+ *   params         device, (6, d_h) fp32, as for nrnn_newton_forward
+ *   cu_seqlens_host host, (num_segments + 1) int32 or NULL; validated as by
+ *                  nrnn_validate_cu_seqlens; B must be 1
+ *   H_host         host, (B, T, d_h) of dtype: H^(K)
+ *   residual_host  host, 1 float (required): rho = max over blocks of
+ *                  max|F(H^(K))|, +inf if any F is NaN
+ *   staging        device, staging_bytes >= nrnn_newton_host_staging_bytes(
+ *                  same shape, cu_seqlens_host, tokens_per_block); 256-byte
+ *                  aligned; scratch
+ * Synchronous: returns once H_host and *residual_host hold the result.
+ * Returns NRNN_OK, NRNN_ERR_TIMEOUT (a bounded device wait gave up),
+ * NRNN_ERR_DIVERGED (rho > residual_fail or not finite; H_host written),
+ * NRNN_ERR_WORKSPACE (staging too small or misaligned), NRNN_ERR_CU_SEQLENS,
+ * NRNN_ERR_UNSUPPORTED, NRNN_ERR_INVALID_ARG or NRNN_ERR_CUDA.  Results equal
+ * nrnn_newton_forward up to the composition order of the look-back (a pack's
+ * blocks start their time chunks at their own first token).
+ */
+size_t nrnn_newton_host_staging_bytes(int64_t B, int64_t T, int64_t d_h, int dtype, int K,
+                                      const int32_t *cu_seqlens_host, int64_t num_segments,
+                                      int64_t tokens_per_block);
+int nrnn_newton_forward_host(const void *preact_host, int dtype, const float *params, int64_t B,
+                             int64_t T, int64_t d_h, const int32_t *cu_seqlens_host,
+                             int64_t num_segments, int K, float residual_fail, void *H_host,
+                             float *residual_host, void *staging, size_t staging_bytes,
+                             int64_t tokens_per_block, void *stream);
+
+/*
  * Size of the device scratch array that nrnn_newton_forward_noalloc uses
  * (64 MiB on every GPU where the library is used, held until process exit).
  */
@@ -302,7 +342,7 @@ int nrnn_newton_forward_noalloc(const void *preact, int dtype, const float *para
 
 /*
  * Debug: from the next call on, the Newton tile with index `tile` (tile =
- * (b * ceil(d_h / 32) + unit_tile) * ceil(T / 128) + chunk) never publishes
+ * (b * ceil(d_h / 32) + unit_tile) * ceil(T / 64) + chunk) never publishes
  * its look-back slot, so that the later chunks of its column wait for it
  * until their bounded wait gives up.  The call then still terminates and,
  * with residual_host non-NULL, returns NRNN_ERR_TIMEOUT (H_out is invalid).

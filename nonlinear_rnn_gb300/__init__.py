@@ -17,11 +17,13 @@ from ._binding import (  # noqa: F401
     decode_step,
     default_agreement_atol,
     head_mask,
+    host_staging_bytes,
     input_projection,
     lib_path,
     load,
     newton_backward,
     newton_forward,
+    newton_forward_host,
     newton_forward_x,
     params_tensor,
     picard,

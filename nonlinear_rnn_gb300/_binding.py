@@ -52,6 +52,9 @@ _SIGNATURES = {
     "nrnn_set_wait_limit_ns": ([_u64], _u64),
     "nrnn_debug_withhold_publish": ([_i64], _i64),
     "nrnn_probe_xu_rates": ([ctypes.POINTER(ctypes.c_float)] * 3 + [_vp], _int),
+    "nrnn_newton_host_staging_bytes": ([_i64, _i64, _i64, _int, _int, _vp, _i64, _i64], _sz),
+    "nrnn_newton_forward_host": ([_vp, _int, _vp, _i64, _i64, _i64, _vp, _i64, _int, _f, _vp, _vp,
+                                  _vp, _sz, _i64, _vp], _int),
     "nrnn_newton_forward_noalloc": ([_vp, _int, _vp, _i64, _i64, _i64, _vp, _i64, _int, _f, _vp,
                                      _vp, _vp, _vp], _int),
 }
@@ -232,6 +235,64 @@ def newton_forward(preact: torch.Tensor, params, cu_seqlens=None, K: int = 3,
                                           _ptr(workspace), workspace.numel(), _stream(dev))
     _raise(st, "newton_forward", H=H, residual=(host.value if host is not None else None))
     return H, rho
+
+
+def host_staging_bytes(B, T, d_h, dtype=torch.float32, K=3, cu_seqlens=None,
+                       tokens_per_block: int = 0) -> int:
+    code = F32 if dtype == torch.float32 else BF16
+    cu32 = None if cu_seqlens is None else validate_cu_seqlens(cu_seqlens, T)
+    return int(load().nrnn_newton_host_staging_bytes(
+        B, T, d_h, code, int(K), None if cu32 is None else cu32.ctypes.data_as(ctypes.c_void_p),
+        0 if cu32 is None else cu32.size - 1, int(tokens_per_block)))
+
+
+def newton_forward_host(preact: torch.Tensor, params, cu_seqlens=None, K: int = 3,
+                        residual_fail: float = 1.0, out: torch.Tensor | None = None,
+                        staging: torch.Tensor | None = None, tokens_per_block: int = 0,
+                        device="cuda", check: bool = True):
+    """Newton forward on host tensors with the copies overlapped with the
+    kernels (nrnn_newton_forward_host).  preact (B, T, 3 d_h) float32/bfloat16
+    CPU tensor, ideally pinned; returns (H, residual): H a CPU tensor (`out`
+    if given, else a new pinned one) and residual a Python float.  With
+    check=True a residual above residual_fail raises NewtonDivergenceError."""
+    lib = load()
+    if preact.device.type != "cpu":
+        raise ValueError("preact must be a host tensor; use newton_forward for device tensors")
+    if not preact.is_contiguous():
+        preact = preact.contiguous()
+    if preact.dim() != 3 or preact.shape[2] % 3:
+        raise ValueError("preact must have shape (B, T, 3 d_h)")
+    B, T, d_h = preact.shape[0], preact.shape[1], preact.shape[2] // 3
+    code = _dtype_code(preact)
+    dev = torch.device(device)
+    prm = params_tensor(params, d_h, dev)
+    cu32 = None
+    if cu_seqlens is not None:
+        if B != 1:
+            raise ValueError("cu_seqlens requires batch 1 (x of shape (1, N, d))")
+        cu32 = validate_cu_seqlens(cu_seqlens, T)
+    H = out if out is not None else torch.empty((B, T, d_h), dtype=preact.dtype).pin_memory()
+    if tuple(H.shape) != (B, T, d_h) or H.dtype != preact.dtype or not H.is_contiguous() \
+            or H.device.type != "cpu":
+        raise ValueError("out must be a contiguous host tensor of shape (B, T, d_h) and preact's dtype")
+    cu_ptr = None if cu32 is None else cu32.ctypes.data_as(ctypes.c_void_p)
+    S = 0 if cu32 is None else cu32.size - 1
+    nbytes = lib.nrnn_newton_host_staging_bytes(B, T, d_h, code, int(K), cu_ptr, S,
+                                                int(tokens_per_block))
+    if nbytes == 0:
+        raise ValueError("invalid shape or K")
+    if staging is None or staging.numel() < nbytes:
+        staging = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    rho = ctypes.c_float(0.0)
+    with torch.cuda.device(dev):
+        st = lib.nrnn_newton_forward_host(_ptr(preact), code, _ptr(prm), B, T, d_h, cu_ptr, S,
+                                          int(K), float(residual_fail), _ptr(H),
+                                          ctypes.byref(rho), _ptr(staging), staging.numel(),
+                                          int(tokens_per_block), _stream(dev))
+    if st == -5 and not check:
+        return H, float(rho.value)
+    _raise(st, "newton_forward_host", H=H, residual=float(rho.value))
+    return H, float(rho.value)
 
 
 def newton_forward_x(x: torch.Tensor, W_x: torch.Tensor, params, cu_seqlens=None, K: int = 3,

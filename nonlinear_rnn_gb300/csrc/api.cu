@@ -141,6 +141,10 @@ int cuda_status(cudaError_t e) { return e == cudaSuccess ? NRNN_OK : NRNN_ERR_CU
 
 }  // namespace
 
+namespace nrnn {
+size_t newton_error_offset(int K) { return layout(0, 0, 8, NRNN_F32, K, true).error_off; }
+}  // namespace nrnn
+
 // Synchronous tail of the forward entry points: copies rho and the error word
 // to the host, then applies the timeout and residual gates.  With no host
 // pointer the call stays asynchronous and returns NRNN_OK.

@@ -83,6 +83,9 @@ struct SyncLayout {
 
 size_t newton_smem_bytes(int dtype, bool fused);
 
+// byte offset of the error word in a Newton forward's workspace
+size_t newton_error_offset(int K);
+
 // tmP over P (3 d_h, T, B), tmH over the H^(k-1) or H^(0) input, tmO over the
 // H output, all with a TILE_U x NEWTON_L x 1 box
 cudaError_t launch_newton(int dtype, bool fused, const CUtensorMap &tmP, const CUtensorMap &tmH,
