@@ -15,12 +15,13 @@
 //   warps 8..11 (fp32 only) split each staged tile in place for split-TF32
 // bf16: kind::f16, 128 x 256 tiles, 64-wide K slices, 4 stages, fp32
 // accumulation rounded to bf16.  fp32: split-TF32 ("3xTF32") -- each fp32
-// operand x becomes hi = x rounded to the nearest TF32 value (low 13 mantissa
-// bits cleared after adding half their range; exactly representable, so the
-// tensor core reads it unchanged) and lo = x - hi (exact, |lo| <= 2^-11 |x|), and
+// operand x is read by kind::tf32 as hi = x with its low 13 mantissa bits
+// dropped (the tensor core ignores them, so the staged tile serves as hi
+// unchanged), and the splitter warps write lo = x - hi (exact, |lo| < 2^-10
+// |x|) beside it, and
 //   A B ~ A_hi B_hi + A_hi B_lo + A_lo B_hi
-// with kind::tf32 (the dropped A_lo B_lo and the TF32 reading of lo are of
-// order 2^-21 relative), 128 x 128 tiles, 32-wide K slices, 3 stages.
+// (the dropped A_lo B_lo and the TF32 reading of lo are of order 2^-20
+// relative), 128 x 128 tiles, 32-wide K slices, 3 stages.
 // Out-of-range rows, columns and K are zero-filled by TMA and masked on
 // store.  Every wait is bounded; a wait that gives up sets
 // g_projection_tc_error and the epilogue writes NaN, which the Newton residual
@@ -202,14 +203,12 @@ __global__ void __launch_bounds__(ProjCfg<F32>::THREADS, 1)
             for (int kt = 0; kt < kt_count; ++kt, ++it) {
                 const int s = it % C::STAGES;
                 mbar_wait_bounded(&full_bar[s], (it / C::STAGES) & 1, TC_WAIT_NS, error);
-                uint32_t *hi = reinterpret_cast<uint32_t *>(smem + s * C::STAGE_BYTES);
+                const uint32_t *raw = reinterpret_cast<const uint32_t *>(smem + s * C::STAGE_BYTES);
                 float *lo = reinterpret_cast<float *>(smem + s * C::STAGE_BYTES + C::A_BYTES + C::B_BYTES);
 #pragma unroll 4
                 for (int e = t; e < (C::A_BYTES + C::B_BYTES) / 4; e += SPLIT_THREADS) {
-                    const uint32_t bits = hi[e];
-                    const uint32_t hb = (bits + 0x1000u) & 0xffffe000u;
-                    lo[e] = __uint_as_float(bits) - __uint_as_float(hb);
-                    hi[e] = hb;
+                    const uint32_t bits = raw[e];
+                    lo[e] = __uint_as_float(bits) - __uint_as_float(bits & 0xffffe000u);
                 }
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                 mbar_arrive(&split_bar[s]);
