@@ -520,8 +520,9 @@ int nrnn_input_projection(const void *x, const void *W_x, int dtype, int64_t row
     }
     if (!aligned16(x) || !aligned16(W_x) || !aligned16(preact)) return NRNN_ERR_INVALID_ARG;
     CUtensorMap tmA, tmB;
-    if (!make_map_2d_sw128(&tmA, x, d_in, rows, PROJ_T3_BOX_K, PROJ_T3_BOX_MN, NRNN_F32) ||
-        !make_map_2d_sw128(&tmB, W_x, d_in, 3 * d_h, PROJ_T3_BOX_K, PROJ_T3_BOX_MN, NRNN_F32))
+    const int bn = projection_tf32x3_bn(static_cast<int>(3 * d_h));
+    if (!make_map_2d_sw128(&tmA, x, d_in, rows, PROJ_T3_BOX_K, PROJ_T3_BOX_M, NRNN_F32) ||
+        !make_map_2d_sw128(&tmB, W_x, d_in, 3 * d_h, PROJ_T3_BOX_K, bn, NRNN_F32))
         return NRNN_ERR_CUDA;
     return cuda_status(launch_projection_tf32x3(tmA, tmB, rows, static_cast<int>(d_in),
                                                 static_cast<int>(3 * d_h),

@@ -127,9 +127,11 @@ constexpr int PROJ_TC_BOX_K = 64, PROJ_TC_BOX_M = 128, PROJ_TC_BOX_N = 256;
 cudaError_t launch_projection_tc(const CUtensorMap &tmA, const CUtensorMap &tmB, int64_t rows,
                                  int d_in, int n_out, void *P, cudaStream_t stream);
 
-// fp32 split-TF32 tensor-core projection: tmA over x (d_in, rows), tmB over W_x
-// (d_in, n_out), both fp32 with a 32 x 128 box and the 128-byte swizzle.
-constexpr int PROJ_T3_BOX_K = 32, PROJ_T3_BOX_MN = 128;   // box of both operands
+// fp32 split-TF32 tensor-core projection: tmA over x (d_in, rows) with a
+// 32 x 128 box, tmB over W_x (d_in, n_out) with a 32 x projection_tf32x3_bn(n_out)
+// box, both fp32 with the 128-byte swizzle.
+constexpr int PROJ_T3_BOX_K = 32, PROJ_T3_BOX_M = 128;
+int projection_tf32x3_bn(int n_out);
 cudaError_t launch_projection_tf32x3(const CUtensorMap &tmA, const CUtensorMap &tmB, int64_t rows,
                                      int d_in, int n_out, float *P, cudaStream_t stream);
 

@@ -40,9 +40,13 @@ constexpr uint64_t TC_WAIT_NS = 2000000000ull;
 
 __device__ uint32_t g_projection_tc_error;
 
-template <bool F32> struct ProjCfg;
+// MODE 0: bf16; MODE 1: fp32 split-TF32, 128-column tiles; MODE 2: fp32
+// split-TF32, 256-column tiles (half the A-operand traffic per product, two
+// stages)
+template <int MODE> struct ProjCfg;
 
-template <> struct ProjCfg<false> {   // bf16
+template <> struct ProjCfg<0> {   // bf16
+    static constexpr bool F32 = false;
     static constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
     static constexpr int A_BYTES = BM * BK * 2, B_BYTES = BN * BK * 2;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
@@ -52,15 +56,18 @@ template <> struct ProjCfg<false> {   // bf16
     static constexpr uint32_t IDESC = idesc_kmajor<false>(BM, BN);
 };
 
-template <> struct ProjCfg<true> {    // fp32 split-TF32
-    static constexpr int BM = 128, BN = 128, BK = 32, STAGES = 3;
+template <int BN_, int STAGES_> struct ProjCfgTf32 {   // fp32 split-TF32
+    static constexpr bool F32 = true;
+    static constexpr int BM = 128, BN = BN_, BK = 32, STAGES = STAGES_;
     static constexpr int A_BYTES = BM * BK * 4, B_BYTES = BN * BK * 4;
-    static constexpr int STAGE_BYTES = 2 * (A_BYTES + B_BYTES);   // hi A | hi B | lo A | lo B
+    static constexpr int STAGE_BYTES = 2 * (A_BYTES + B_BYTES);   // A | B | lo A | lo B
     static constexpr int THREADS = 384;
     static constexpr int MMA_K = 8;    // elements per instruction (32 bytes)
     // D fp32, A and B TF32, both K-major, N = BN, M = BM
     static constexpr uint32_t IDESC = idesc_kmajor<true>(BM, BN);
 };
+template <> struct ProjCfg<1> : ProjCfgTf32<128, 3> {};
+template <> struct ProjCfg<2> : ProjCfgTf32<256, 2> {};
 
 constexpr int SPLIT_THREADS = 128;
 constexpr int EPI_THREADS = 128;
@@ -99,11 +106,12 @@ __device__ __forceinline__ void store_row_chunk(float *dst, int col0, int N,
     }
 }
 
-template <bool F32>
-__global__ void __launch_bounds__(ProjCfg<F32>::THREADS, 1)
+template <int MODE>
+__global__ void __launch_bounds__(ProjCfg<MODE>::THREADS, 1)
     k_projection_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     int64_t rows, int K, int N, void *Pv) {
-    using C = ProjCfg<F32>;
+    using C = ProjCfg<MODE>;
+    constexpr bool F32 = C::F32;
     using Out = typename std::conditional<F32, float, __nv_bfloat16>::type;
     constexpr uint32_t TMEM_COLS = 2 * C::BN;   // two accumulators
     uint32_t *error = &g_projection_tc_error;
@@ -247,15 +255,15 @@ __global__ void __launch_bounds__(ProjCfg<F32>::THREADS, 1)
     }
 }
 
-template <bool F32>
+template <int MODE>
 cudaError_t launch_tc(const CUtensorMap &tmA, const CUtensorMap &tmB, int64_t rows, int d_in,
                       int n_out, void *P, cudaStream_t stream) {
-    using C = ProjCfg<F32>;
+    using C = ProjCfg<MODE>;
     static std::atomic<unsigned long long> configured{0};
     static int sms_of[64];
     constexpr size_t smem = static_cast<size_t>(C::STAGES) * C::STAGE_BYTES + 1024;
     cudaError_t e = once_per_device(configured, [](int dev) {
-        cudaError_t r = cudaFuncSetAttribute(k_projection_tc<F32>,
+        cudaError_t r = cudaFuncSetAttribute(k_projection_tc<MODE>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              static_cast<int>(smem));
         int n = 0;
@@ -272,7 +280,7 @@ cudaError_t launch_tc(const CUtensorMap &tmA, const CUtensorMap &tmB, int64_t ro
     if (e != cudaSuccess || sms <= 0) return e != cudaSuccess ? e : cudaErrorInvalidValue;
     const int64_t n_tiles = ((rows + C::BM - 1) / C::BM) * ((n_out + C::BN - 1) / C::BN);
     const int64_t grid = n_tiles < sms ? n_tiles : sms;
-    k_projection_tc<F32><<<static_cast<unsigned>(grid), C::THREADS, smem, stream>>>(
+    k_projection_tc<MODE><<<static_cast<unsigned>(grid), C::THREADS, smem, stream>>>(
         tmA, tmB, rows, d_in, n_out, P);
     return cudaGetLastError();
 }
@@ -281,12 +289,15 @@ cudaError_t launch_tc(const CUtensorMap &tmA, const CUtensorMap &tmB, int64_t ro
 
 cudaError_t launch_projection_tc(const CUtensorMap &tmA, const CUtensorMap &tmB, int64_t rows,
                                  int d_in, int n_out, void *P, cudaStream_t stream) {
-    return launch_tc<false>(tmA, tmB, rows, d_in, n_out, P, stream);
+    return launch_tc<0>(tmA, tmB, rows, d_in, n_out, P, stream);
 }
+
+int projection_tf32x3_bn(int n_out) { return n_out >= 512 ? 256 : 128; }
 
 cudaError_t launch_projection_tf32x3(const CUtensorMap &tmA, const CUtensorMap &tmB, int64_t rows,
                                      int d_in, int n_out, float *P, cudaStream_t stream) {
-    return launch_tc<true>(tmA, tmB, rows, d_in, n_out, P, stream);
+    if (projection_tf32x3_bn(n_out) == 256) return launch_tc<2>(tmA, tmB, rows, d_in, n_out, P, stream);
+    return launch_tc<1>(tmA, tmB, rows, d_in, n_out, P, stream);
 }
 
 }  // namespace nrnn
