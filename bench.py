@@ -306,6 +306,43 @@ def run_ours(args, w, rank, world, local):
 
     proj = statistics.median(proj_ms)
 
+    # NEXT rows, each against the HBM roof: the backward (adjoint) scan at the
+    # forward's trajectory (reads P, H, dL/dH, writes dL/dP: 8 d_h s bytes per
+    # token) and one decode step for a batch of slots (reads P and h, writes h':
+    # 5 d_h s per slot; fused projection: x and h in, h' out, W_x once)
+    s_el = 2 if w.dtype == "bf16" else 4
+    nxt = {}
+    if not args.skip_next:
+        gH = H.clone()
+        bw_ms, _ = time_steps(torch, lambda: nr.newton_backward(P, prm, H, gH, cu_seqlens=cu), 3,
+                              flush, stream, nvtx=False)
+        bw = statistics.median(bw_ms)
+        bw_bytes = 8 * w.d_h * s_el * tokens
+        nxt["backward"] = {"ms": bw, "bytes": bw_bytes, "achieved_gbs": bw_bytes / (bw * 1e-3) / 1e9,
+                           "frac": bw_bytes / (bw * 1e-3) / 1e9 / pk["hbm_gbs"]}
+        del gH
+        def decode_leg(name, slots, with_x):
+            Pd = P.reshape(-1, 3 * w.d_h)[:slots]
+            hd = H.reshape(-1, w.d_h)[:slots]
+            xd = x.reshape(-1, w.d_in)[:slots]
+            hout = torch.empty_like(hd)
+            if with_x:   # W_x read once; x and h in, h' out
+                fn = lambda: nr.decode_step(prm, hd, x=xd, W_x=W, out=hout)
+                nbytes = (w.d_in + 2 * w.d_h) * s_el * slots + 3 * w.d_h * w.d_in * s_el
+            else:
+                fn = lambda: nr.decode_step(prm, hd, preact=Pd, out=hout)
+                nbytes = 5 * w.d_h * s_el * slots
+            dms, _ = time_steps(torch, fn, 5, flush, stream, nvtx=False)
+            dm = statistics.median(dms)
+            nxt[name] = {"slots": slots, "ms": dm, "bytes": nbytes,
+                         "achieved_gbs": nbytes / (dm * 1e-3) / 1e9,
+                         "frac": nbytes / (dm * 1e-3) / 1e9 / pk["hbm_gbs"]}
+
+        big = min(8192, tokens)
+        decode_leg("decode", big, False)
+        decode_leg("decode_x", big, True)                       # projection, then the step
+        decode_leg("decode_x_small", min(64, tokens), True)     # fused kernel
+
     # bf16: the projection fused into the Newton kernel (P never written)
     fused_x = None
     if w.dtype == "bf16" and w.K > 0:
@@ -355,6 +392,7 @@ def run_ours(args, w, rank, world, local):
                             "fused_in_kernel": fused_x},
         "sequential_gpu": {"ms": statistics.median(seq_ms),
                            "tokens_per_s": tokens / (statistics.median(seq_ms) * 1e-3)},
+        "next_rows": nxt or None,
         "residual": float(rho.item()),
         "wall_s": t_wall,
         "clocks": clocks,
@@ -443,6 +481,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--preroll-s", type=float, default=1.0)
+    ap.add_argument("--skip-next", action="store_true",
+                    help="skip the backward and decode legs")
     ap.add_argument("--skip-per-iter", action="store_true")
     ap.add_argument("--no-graph", dest="graph", action="store_false",
                     help="launch each forward eagerly instead of replaying a CUDA graph")

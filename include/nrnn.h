@@ -229,11 +229,17 @@ int nrnn_decode_step(const void *preact, int dtype, const float *params, int64_t
 
 /*
  * Decode step with the input projection fused in (FAQs: "decode_wx +
- * decode_step"): P_s = W_x x_s (fp32 accumulation, rounded to dtype as the
- * stored preactivation would be), then h_out = f(h_in, P).
- *   x       device, (slots, d_in) of dtype;  W_x device, (3 d_h, d_in) of dtype
+ * decode_step"): P_s = W_x x_s (fp32 accumulation on the CUDA cores, rounded
+ * to dtype as the stored preactivation would be), then h_out = f(h_in, P).
+ * A batched matrix-vector product per step, meant for small slot counts: each
+ * W_x row is read once per group of 8 slots.  For hundreds of slots and more,
+ * nrnn_input_projection into a (slots, 3 d_h) buffer followed by
+ * nrnn_decode_step runs the product on the tensor cores instead (the Python
+ * binding switches above 64 slots).
+ *   x       device, (slots, d_in) of dtype, 16-byte aligned
+ *   W_x     device, (3 d_h, d_in) of dtype, 16-byte aligned
  *   h_in    device (slots, d_h) or NULL;  h_out device (slots, d_h), may be h_in
- *   slots <= 262140.
+ *   slots <= 524280; d_in a multiple of 8 (else NRNN_ERR_UNSUPPORTED).
  */
 int nrnn_decode_step_x(const void *x, const void *W_x, int dtype, const float *params,
                        int64_t slots, int64_t d_in, int64_t d_h, const void *h_in, void *h_out,

@@ -394,6 +394,11 @@ def sequential_forward(preact: torch.Tensor, params, cu_seqlens=None,
     return H
 
 
+# above this many slots decode_step(x=, W_x=) projects on the tensor cores
+# (nrnn_input_projection) and then steps (nrnn_decode_step)
+DECODE_X_MAX_SLOTS = 64
+
+
 def decode_step(params, h: torch.Tensor | None = None, preact: torch.Tensor | None = None,
                 x: torch.Tensor | None = None, W_x: torch.Tensor | None = None,
                 out: torch.Tensor | None = None) -> torch.Tensor:
@@ -420,8 +425,15 @@ def decode_step(params, h: torch.Tensor | None = None, preact: torch.Tensor | No
                                       _ptr(H), _stream(dev))
         else:
             W_x = _device_tensor(W_x, "W_x")
-            st = lib.nrnn_decode_step_x(_ptr(src), _ptr(W_x), _dtype_code(src), _ptr(prm), slots,
-                                        src.shape[1], d_h, _ptr(h), _ptr(H), _stream(dev))
+            if slots > DECODE_X_MAX_SLOTS:
+                # large batches: the projection on the tensor cores, then the step
+                P = input_projection(src, W_x)
+                st = lib.nrnn_decode_step(_ptr(P), _dtype_code(P), _ptr(prm), slots, d_h, _ptr(h),
+                                          _ptr(H), _stream(dev))
+            else:
+                st = lib.nrnn_decode_step_x(_ptr(src), _ptr(W_x), _dtype_code(src), _ptr(prm),
+                                            slots, src.shape[1], d_h, _ptr(h), _ptr(H),
+                                            _stream(dev))
     _raise(st, "decode_step")
     return H
 

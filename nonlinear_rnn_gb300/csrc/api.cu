@@ -463,7 +463,8 @@ int nrnn_decode_step(const void *preact, int dtype, const float *params, int64_t
     if (slots == 0) return NRNN_OK;
     if (preact == nullptr || params == nullptr || h_out == nullptr) return NRNN_ERR_INVALID_ARG;
     if (slots * d_h > INT32_MAX || d_h > INT32_MAX / 3) return NRNN_ERR_UNSUPPORTED;
-    if (overlaps(h_out, preact, elem_size(dtype) * static_cast<size_t>(slots * 3 * d_h)))
+    if (ranges_overlap(h_out, elem_size(dtype) * static_cast<size_t>(slots * d_h), preact,
+                       elem_size(dtype) * static_cast<size_t>(slots * 3 * d_h)))
         return NRNN_ERR_INVALID_ARG;
     return cuda_status(launch_decode_step(dtype, preact, params, h_in, h_out,
                                           static_cast<int>(slots), static_cast<int>(d_h),
@@ -478,7 +479,9 @@ int nrnn_decode_step_x(const void *x, const void *W_x, int dtype, const float *p
     if (slots == 0) return NRNN_OK;
     if (x == nullptr || W_x == nullptr || params == nullptr || h_out == nullptr)
         return NRNN_ERR_INVALID_ARG;
-    if (slots > 4 * 65535 || d_h > INT32_MAX / 3 || d_in > INT32_MAX) return NRNN_ERR_UNSUPPORTED;
+    if (slots > 8 * 65535 || d_h > INT32_MAX / 3 || d_in > INT32_MAX || d_in % 8 != 0)
+        return NRNN_ERR_UNSUPPORTED;
+    if (!aligned16(x) || !aligned16(W_x)) return NRNN_ERR_INVALID_ARG;
     return cuda_status(launch_decode_step_x(dtype, x, W_x, params, h_in, h_out,
                                             static_cast<int>(slots), static_cast<int>(d_in),
                                             static_cast<int>(d_h),

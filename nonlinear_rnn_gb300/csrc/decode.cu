@@ -4,10 +4,8 @@
 // size (slots, d_h), prefill then decode_wx + decode_step(..., out=) per token).
 //
 // k_decode_step: h_out = f(h_in, P) elementwise from given preactivations.
-// k_decode_step_x: the same step with the input projection fused in: warp w of
-// a CTA takes slot s = 4 blockIdx.y + w and unit j = blockIdx.x; its lanes
-// split d_in for the three dot products x_s . W_x[g d_h + j] (fp32
-// accumulation, shuffle reduction), and lane 0 applies the cell.
+// k_decode_step_x: the same step with the input projection fused in, for
+// small slot counts (a batched matrix-vector product per step; see below).
 #include "nrnn_device.cuh"
 #include "nrnn_internal.h"
 
@@ -28,41 +26,96 @@ __global__ void __launch_bounds__(256)
     h_out[i] = from_f32<TS>(cell_f(h, to_f32(p[0]), to_f32(p[d_h]), to_f32(p[2 * d_h]), prm));
 }
 
-constexpr int DEC_WARPS = 4;
+// k_decode_step_x: a CTA takes DX_UNITS units (one warp each) and a group of
+// DX_SLOTS slots whose x rows it stages in shared memory once (or reads from
+// global memory when they do not fit); each lane accumulates 16-byte slices of
+// d_in for the three gate rows of its warp's unit against every slot of the
+// group, so a W_x row is read once per slot group, not once per slot.  After
+// the shuffle reduction lane s applies the cell to slot s.
+constexpr int DX_UNITS = 8;
+constexpr int DX_SLOTS = 8;
+constexpr size_t DX_SMEM_MAX = 48 * 1024;
+
+__device__ __forceinline__ void unpack16(const uint4 &v, float (&o)[4]) {
+    o[0] = __uint_as_float(v.x);
+    o[1] = __uint_as_float(v.y);
+    o[2] = __uint_as_float(v.z);
+    o[3] = __uint_as_float(v.w);
+}
+__device__ __forceinline__ void unpack16(const uint4 &v, float (&o)[8]) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        o[2 * i] = __uint_as_float(w[i] << 16);
+        o[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+    }
+}
 
 template <typename TS>
-__global__ void __launch_bounds__(DEC_WARPS * 32)
+__global__ void __launch_bounds__(DX_UNITS * 32)
     k_decode_step_x(const TS *__restrict__ x, const TS *__restrict__ W, const float *__restrict__ params,
                     const TS *__restrict__ h_in, TS *__restrict__ h_out, int slots, int d_in,
-                    int d_h) {
+                    int d_h, int stage_x) {
+    constexpr int VEC = 16 / sizeof(TS);   // elements per 16-byte load
+    extern __shared__ __align__(16) unsigned char dx_smem[];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int j = blockIdx.x;
-    const int s = blockIdx.y * DEC_WARPS + warp;
-    if (s >= slots) return;
-    const TS *xs = x + static_cast<int64_t>(s) * d_in;
-    const TS *wz = W + static_cast<int64_t>(j) * d_in;
-    const TS *wr = W + static_cast<int64_t>(d_h + j) * d_in;
-    const TS *wc = W + static_cast<int64_t>(2 * d_h + j) * d_in;
-    float az = 0.f, ar = 0.f, ac = 0.f;
-    for (int k = lane; k < d_in; k += 32) {
-        const float xv = to_f32(xs[k]);
-        az = fmaf(xv, to_f32(wz[k]), az);
-        ar = fmaf(xv, to_f32(wr[k]), ar);
-        ac = fmaf(xv, to_f32(wc[k]), ac);
+    const int j = blockIdx.x * DX_UNITS + warp;
+    const int s0 = blockIdx.y * DX_SLOTS;
+    const int ns = min(DX_SLOTS, slots - s0);
+    const TS *xg = x + static_cast<int64_t>(s0) * d_in;
+    const TS *xs = xg;
+    if (stage_x) {
+        uint4 *dst = reinterpret_cast<uint4 *>(dx_smem);
+        const uint4 *src = reinterpret_cast<const uint4 *>(xg);
+        const int nvec = ns * d_in / VEC;
+        for (int i = threadIdx.x; i < nvec; i += blockDim.x) dst[i] = src[i];
+        __syncthreads();
+        xs = reinterpret_cast<const TS *>(dx_smem);
+    }
+    if (j >= d_h) return;
+    float acc[3][DX_SLOTS];
+#pragma unroll
+    for (int g = 0; g < 3; ++g)
+#pragma unroll
+        for (int s = 0; s < DX_SLOTS; ++s) acc[g][s] = 0.f;
+    const TS *wr[3] = {W + static_cast<int64_t>(j) * d_in, W + static_cast<int64_t>(d_h + j) * d_in,
+                       W + static_cast<int64_t>(2 * d_h + j) * d_in};
+    for (int k = lane * VEC; k < d_in; k += 32 * VEC) {
+        float wv[3][VEC];
+#pragma unroll
+        for (int g = 0; g < 3; ++g) unpack16(__ldg(reinterpret_cast<const uint4 *>(wr[g] + k)), wv[g]);
+#pragma unroll
+        for (int s = 0; s < DX_SLOTS; ++s) {
+            if (s >= ns) break;
+            float xv[VEC];
+            unpack16(*reinterpret_cast<const uint4 *>(xs + s * d_in + k), xv);
+#pragma unroll
+            for (int e = 0; e < VEC; ++e)
+#pragma unroll
+                for (int g = 0; g < 3; ++g) acc[g][s] = fmaf(xv[e], wv[g][e], acc[g][s]);
+        }
     }
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        az += __shfl_xor_sync(FULL_MASK, az, o);
-        ar += __shfl_xor_sync(FULL_MASK, ar, o);
-        ac += __shfl_xor_sync(FULL_MASK, ac, o);
-    }
-    if (lane == 0) {
-        // the preactivation is stored in TS before the cell reads it, as on the
-        // projection path (decode_wx then decode_step)
-        const float pz = round_to<TS>(az), pr = round_to<TS>(ar), pc = round_to<TS>(ac);
-        const int64_t i = static_cast<int64_t>(s) * d_h + j;
+    for (int g = 0; g < 3; ++g)
+#pragma unroll
+        for (int s = 0; s < DX_SLOTS; ++s)
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) acc[g][s] += __shfl_xor_sync(FULL_MASK, acc[g][s], o);
+    // lane s applies the cell to slot s0 + s; the preactivation is stored in TS
+    // before the cell reads it, as on the projection path
+    float pz = 0.f, pr = 0.f, pc = 0.f;
+#pragma unroll
+    for (int s = 0; s < DX_SLOTS; ++s)
+        if (lane == s) {
+            pz = acc[0][s];
+            pr = acc[1][s];
+            pc = acc[2][s];
+        }
+    if (lane < ns) {
+        const int64_t i = static_cast<int64_t>(s0 + lane) * d_h + j;
         const float h = (h_in != nullptr) ? to_f32(h_in[i]) : 0.f;
-        h_out[i] = from_f32<TS>(cell_f(h, pz, pr, pc, load_unit_params(params, d_h, j, true)));
+        h_out[i] = from_f32<TS>(cell_f(h, round_to<TS>(pz), round_to<TS>(pr), round_to<TS>(pc),
+                                       load_unit_params(params, d_h, j, true)));
     }
 }
 
@@ -88,16 +141,19 @@ cudaError_t launch_decode_step_x(int dtype, const void *x, const void *W, const 
                                  const void *h_in, void *h_out, int slots, int d_in, int d_h,
                                  cudaStream_t stream) {
     if (slots == 0) return cudaSuccess;
-    const dim3 grid(d_h, (slots + DEC_WARPS - 1) / DEC_WARPS);
+    const dim3 grid((d_h + DX_UNITS - 1) / DX_UNITS, (slots + DX_SLOTS - 1) / DX_SLOTS);
+    const size_t xbytes = static_cast<size_t>(DX_SLOTS) * d_in * (dtype == 1 ? 2 : 4);
+    const int stage = xbytes <= DX_SMEM_MAX ? 1 : 0;
+    const size_t smem = stage ? xbytes : 0;
     if (dtype == 1)
-        k_decode_step_x<__nv_bfloat16><<<grid, DEC_WARPS * 32, 0, stream>>>(
+        k_decode_step_x<__nv_bfloat16><<<grid, DX_UNITS * 32, smem, stream>>>(
             static_cast<const __nv_bfloat16 *>(x), static_cast<const __nv_bfloat16 *>(W), params,
             static_cast<const __nv_bfloat16 *>(h_in), static_cast<__nv_bfloat16 *>(h_out), slots,
-            d_in, d_h);
+            d_in, d_h, stage);
     else
-        k_decode_step_x<float><<<grid, DEC_WARPS * 32, 0, stream>>>(
+        k_decode_step_x<float><<<grid, DX_UNITS * 32, smem, stream>>>(
             static_cast<const float *>(x), static_cast<const float *>(W), params,
-            static_cast<const float *>(h_in), static_cast<float *>(h_out), slots, d_in, d_h);
+            static_cast<const float *>(h_in), static_cast<float *>(h_out), slots, d_in, d_h, stage);
     return cudaGetLastError();
 }
 

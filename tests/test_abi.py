@@ -7,6 +7,7 @@ import re
 
 import numpy as np
 import pytest
+import torch
 
 import nonlinear_rnn_gb300 as nr
 
@@ -92,3 +93,20 @@ def test_forward_rejects_bad_arguments_before_any_launch():
     assert call(ws=ctypes.c_void_p(256 + 16)) == -7   # workspace misaligned
     assert call(pre=ctypes.c_void_p(260)) == -1   # preact misaligned
     assert call(rd=None) == -1
+
+
+def test_decode_overlap_check_uses_each_buffer_size():
+    # h_out (slots x d_h) ending right before preact (slots x 3 d_h) does not
+    # overlap it; h_out inside preact does.  Fake pointers: the overlap check
+    # runs before anything touches them (the GPU-less call then fails on CUDA).
+    lib = nr.load()
+    slots, d_h = 300, 40
+    pre = 1 << 24
+    h_before = pre - slots * d_h * 4
+    if not torch.cuda.is_available():   # with a GPU this call would launch on fake pointers
+        st = lib.nrnn_decode_step(ctypes.c_void_p(pre), 0, ctypes.c_void_p(256), slots, d_h, None,
+                                  ctypes.c_void_p(h_before), None)
+        assert st != -1
+    st = lib.nrnn_decode_step(ctypes.c_void_p(pre), 0, ctypes.c_void_p(256), slots, d_h, None,
+                              ctypes.c_void_p(pre + 64), None)
+    assert st == -1

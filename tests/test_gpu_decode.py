@@ -55,3 +55,26 @@ def test_decode_step_with_fused_projection(dtype):
     ref = oracle.decode_step(P, prm, h0)
     h = nr.decode_step(prm, h=dev(h0, tdt), x=dev(x, tdt), W_x=dev(W, tdt))
     assert np.max(np.abs(host(h) - ref)) <= (2e-6 if dtype == "f32" else 1.6e-2)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("slots,d_in,d_h", [(64, 2048, 16), (300, 136, 40), (8, 8, 8)])
+def test_decode_step_with_projection_at_other_sizes(dtype, slots, d_in, d_h):
+    # 64 slots x d_in 2048: the fused kernel reading x from global memory (it
+    # does not fit the staging buffer); 300 slots: the binding's
+    # projection-then-step path; 8 x 8: the smallest shape
+    import nonlinear_rnn_gb300 as nr
+    tdt = torch.float32 if dtype == "f32" else torch.bfloat16
+    rng = np.random.default_rng(slots + d_in)
+    x = rng.normal(size=(slots, d_in)).astype(np.float32)
+    W = (rng.uniform(-1, 1, size=(3 * d_h, d_in)) / math.sqrt(d_in)).astype(np.float32)
+    h0 = rng.uniform(-0.5, 0.5, size=(slots, d_h)).astype(np.float32)
+    if dtype == "bf16":
+        x, W, h0 = syn.round_bf16(x), syn.round_bf16(W), syn.round_bf16(h0)
+    prm = syn.make_params(syn.small_workload(d_h=d_h, seed=64))
+    P = oracle.input_projection(x, W)
+    if dtype == "bf16":
+        P = syn.round_bf16(P.astype(np.float32))
+    ref = oracle.decode_step(P, prm, h0)
+    h = nr.decode_step(prm, h=dev(h0, tdt), x=dev(x, tdt), W_x=dev(W, tdt))
+    assert np.max(np.abs(host(h) - ref)) <= (1e-5 if dtype == "f32" else 1.6e-2)
