@@ -132,6 +132,9 @@ int check_common(const void *preact, int dtype, const float *params, int64_t B, 
     if (B > INT32_MAX || T > INT32_MAX || d_h > (1 << 24) || S > INT32_MAX - 1)
         return NRNN_ERR_UNSUPPORTED;
     if (d_h % 8 != 0) return NRNN_ERR_UNSUPPORTED;
+    // tile indices and CTA tickets are 32-bit
+    if (B * ((d_h + TILE_U - 1) / TILE_U) * ((T + NEWTON_L - 1) / NEWTON_L) > INT32_MAX)
+        return NRNN_ERR_UNSUPPORTED;
     if (cu != nullptr && (B != 1 || S < 1)) return NRNN_ERR_CU_SEQLENS;
     if (preact != nullptr && !aligned16(preact)) return NRNN_ERR_INVALID_ARG;
     return NRNN_OK;

@@ -84,6 +84,7 @@ def test_forward_rejects_bad_arguments_before_any_launch():
                                        a["rd"], a["rh"], a["ws"], a["wsb"], a["st"])
     assert call(dtype=7) == -1
     assert call(d=12) == -3                       # d_h % 8 != 0
+    assert call(B=1 << 20, T=1 << 20, d=64) == -3   # more than 2^31 tiles
     assert call(K=-1) == -1
     assert call(K=65) == -1
     assert call(algo=9) == -1
