@@ -184,11 +184,14 @@ int nrnn_newton_backward(const void *preact, int dtype, const float *params, int
  * "try Picard warm-start (picard_iters)"; read as fixed-point sweeps):
  * from G = 0, each sweep sets G_t = f(G_{t-1}, P_t) for all t at once from
  * the previous sweep (shifted state 0 at t = 0 and at segment heads).  Sweep
- * s makes steps 1..s exact.  One elementwise launch per sweep, no scan.
+ * s makes steps 1..s exact.  One elementwise launch per sweep, no scan.  The
+ * cell runs in the storage type's formulation (bf16: tanh.approx, as in the
+ * Newton kernels).
  *   sweeps  >= 0 (0: H_out = 0)
- *   H_out   device, (B, T, d_h) of dtype: the last sweep
- *   H_tmp   device scratch of the same size, needed when sweeps >= 2; must
- *           not overlap H_out
+ *   H_out   device, (B, T, d_h) of dtype, 16-byte aligned: the last sweep
+ *   H_tmp   device scratch of the same size and alignment, needed when
+ *           sweeps >= 2; must not overlap H_out
+ * Neither may overlap preact (NRNN_ERR_INVALID_ARG).
  */
 int nrnn_picard(const void *preact, int dtype, const float *params, int64_t B, int64_t T,
                 int64_t d_h, const int32_t *cu_seqlens, int64_t num_segments, int sweeps,

@@ -431,6 +431,10 @@ int nrnn_picard(const void *preact, int dtype, const float *params, int64_t B, i
     if (sweeps < 0 || (B * T > 0 && H_out == nullptr)) return NRNN_ERR_INVALID_ARG;
     if (sweeps >= 2 && B * T > 0 && (H_tmp == nullptr || overlaps(H_tmp, H_out, hbytes)))
         return NRNN_ERR_INVALID_ARG;
+    if (B * T > 0 && (!aligned16(H_out) || (sweeps >= 2 && !aligned16(H_tmp)) ||
+                      ranges_overlap(preact, 3 * hbytes, H_out, hbytes) ||
+                      (sweeps >= 2 && ranges_overlap(preact, 3 * hbytes, H_tmp, hbytes))))
+        return NRNN_ERR_INVALID_ARG;
     if (B * T == 0) return NRNN_OK;
     cudaStream_t stream = static_cast<cudaStream_t>(stream_);
     if (sweeps == 0) return cuda_status(cudaMemsetAsync(H_out, 0, hbytes, stream));

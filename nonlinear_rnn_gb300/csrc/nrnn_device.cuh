@@ -525,6 +525,21 @@ struct TanhCell {
 template <typename TS> struct CellOf { using type = ExpCell; };
 template <> struct CellOf<__nv_bfloat16> { using type = TanhCell; };
 
+// f(h, P) from raw preactivations in the storage type's formulation: the
+// ex2/rcp form for fp32, tanh.approx for bf16 (sig(x) = (1 + tanh(x/2))/2)
+template <typename TS>
+__device__ __forceinline__ float cell_f_storage(float h, float pz, float pr, float pc,
+                                                const UnitParams &p) {
+    if constexpr (sizeof(TS) == 2) {
+        const float z = fmaf(0.5f, tanh_approx(0.5f * fmaf(p.a_z, h, pz + p.b_z)), 0.5f);
+        const float r = fmaf(0.5f, tanh_approx(0.5f * fmaf(p.a_r, h, pr + p.b_r)), 0.5f);
+        const float c = tanh_approx(fmaf(p.a_c, r * h, pc + p.b_c));
+        return fmaf(z, c - h, h);
+    } else {
+        return cell_f(h, pz, pr, pc, p);
+    }
+}
+
 // |F| for the residual gate; NaN counts as +inf
 __device__ __forceinline__ float abs_residual(float F) {
     const float a = fabsf(F);
