@@ -78,10 +78,9 @@ bool make_plan(int64_t B, int64_t T, int64_t d_h, int dtype, int K, const int32_
         off += pl.p_bytes + pl.h_bytes + pl.ws_bytes;
     }
     const size_t nblk = pl.blocks.size();
-    pl.res_off = off;
-    off = align_up(off + sizeof(float) * nblk);
-    pl.err_off = off;
-    off = align_up(off + sizeof(uint32_t) * nblk);
+    pl.res_off = off;                                   // residuals, then error words:
+    pl.err_off = off + sizeof(float) * nblk;            // one copy brings both home
+    off = align_up(pl.err_off + sizeof(uint32_t) * nblk);
     pl.cu_off = off;
     off = align_up(off + sizeof(int32_t) * static_cast<size_t>(pl.cu_ints));
     pl.total = off;
@@ -193,6 +192,9 @@ int nrnn_newton_forward_host(const void *preact_host, int dtype, const float *pa
         if (e != cudaSuccess) return NRNN_ERR_CUDA;
     }
 
+    // one block: everything on the caller's stream, no cross-stream events
+    const bool single = nblk == 1;
+    cudaStream_t s_in = single ? stream : ln->in, s_out = single ? stream : ln->out;
     int call_status = NRNN_OK;
     for (size_t i = 0; i < nblk && e == cudaSuccess && call_status == NRNN_OK; ++i) {
         const int s = static_cast<int>(i % NSLOT);
@@ -206,10 +208,10 @@ int nrnn_newton_forward_host(const void *preact_host, int dtype, const float *pa
         const unsigned char *src = static_cast<const unsigned char *>(preact_host) + first * 3 * d_h * es;
         unsigned char *dst = static_cast<unsigned char *>(H_host) + first * d_h * es;
 
-        if (i >= NSLOT) e = cudaStreamWaitEvent(ln->in, ln->computed[s], 0);   // P slot read
-        if (e == cudaSuccess) e = cudaMemcpyAsync(P, src, n * 3 * d_h * es, cudaMemcpyHostToDevice, ln->in);
-        if (e == cudaSuccess) e = cudaEventRecord(ln->loaded[s], ln->in);
-        if (e == cudaSuccess) e = cudaStreamWaitEvent(stream, ln->loaded[s], 0);
+        if (i >= NSLOT) e = cudaStreamWaitEvent(s_in, ln->computed[s], 0);   // P slot read
+        if (e == cudaSuccess) e = cudaMemcpyAsync(P, src, n * 3 * d_h * es, cudaMemcpyHostToDevice, s_in);
+        if (e == cudaSuccess && !single) e = cudaEventRecord(ln->loaded[s], s_in);
+        if (e == cudaSuccess && !single) e = cudaStreamWaitEvent(stream, ln->loaded[s], 0);
         if (e == cudaSuccess && i >= NSLOT) e = cudaStreamWaitEvent(stream, ln->drained[s], 0);
         if (e != cudaSuccess) break;
         call_status = nrnn_newton_forward(P, dtype, params, bk.nb, bk.nt, d_h,
@@ -219,24 +221,21 @@ int nrnn_newton_forward_host(const void *preact_host, int dtype, const float *pa
                                           stream_);
         if (call_status != NRNN_OK) break;
         e = cudaMemcpyAsync(err + i, ws + err_word, sizeof(uint32_t), cudaMemcpyDeviceToDevice, stream);
-        if (e == cudaSuccess) e = cudaEventRecord(ln->computed[s], stream);
-        if (e == cudaSuccess) e = cudaStreamWaitEvent(ln->out, ln->computed[s], 0);
-        if (e == cudaSuccess) e = cudaMemcpyAsync(dst, H, n * d_h * es, cudaMemcpyDeviceToHost, ln->out);
-        if (e == cudaSuccess) e = cudaEventRecord(ln->drained[s], ln->out);
+        if (e == cudaSuccess && !single) e = cudaEventRecord(ln->computed[s], stream);
+        if (e == cudaSuccess && !single) e = cudaStreamWaitEvent(s_out, ln->computed[s], 0);
+        if (e == cudaSuccess) e = cudaMemcpyAsync(dst, H, n * d_h * es, cudaMemcpyDeviceToHost, s_out);
+        if (e == cudaSuccess && !single) e = cudaEventRecord(ln->drained[s], s_out);
     }
     // join: the caller's stream waits for every slot's last copy out, then
-    // brings the per-block residuals and error words home
-    std::vector<float> res_h(nblk, 0.f);
-    std::vector<uint32_t> err_h(nblk, 0u);
-    for (int s = 0; s < NSLOT && static_cast<size_t>(s) < nblk; ++s)
-        if (cudaStreamWaitEvent(stream, ln->drained[s], 0) != cudaSuccess) e = cudaErrorUnknown;
-    if (e == cudaSuccess && call_status == NRNN_OK) {
-        e = cudaMemcpyAsync(res_h.data(), res, sizeof(float) * nblk, cudaMemcpyDeviceToHost, stream);
-        if (e == cudaSuccess)
-            e = cudaMemcpyAsync(err_h.data(), err, sizeof(uint32_t) * nblk, cudaMemcpyDeviceToHost, stream);
-    }
-    const cudaError_t es1 = cudaStreamSynchronize(ln->in);
-    const cudaError_t es2 = cudaStreamSynchronize(ln->out);
+    // brings the per-block residuals and error words home in one copy
+    std::vector<uint32_t> tail(2 * nblk, 0u);   // nblk residual bit patterns, nblk error words
+    if (!single)
+        for (int s = 0; s < NSLOT && static_cast<size_t>(s) < nblk; ++s)
+            if (cudaStreamWaitEvent(stream, ln->drained[s], 0) != cudaSuccess) e = cudaErrorUnknown;
+    if (e == cudaSuccess && call_status == NRNN_OK)
+        e = cudaMemcpyAsync(tail.data(), res, sizeof(uint32_t) * 2 * nblk, cudaMemcpyDeviceToHost, stream);
+    const cudaError_t es1 = single ? cudaSuccess : cudaStreamSynchronize(ln->in);
+    const cudaError_t es2 = single ? cudaSuccess : cudaStreamSynchronize(ln->out);
     const cudaError_t es3 = cudaStreamSynchronize(stream);
     if (call_status != NRNN_OK) return call_status;
     if (e != cudaSuccess || es1 != cudaSuccess || es2 != cudaSuccess || es3 != cudaSuccess)
@@ -244,8 +243,9 @@ int nrnn_newton_forward_host(const void *preact_host, int dtype, const float *pa
     float rho = 0.f;
     bool timeout = false;
     for (size_t i = 0; i < nblk; ++i) {
-        timeout = timeout || err_h[i] != 0u;
-        const float r = res_h[i];
+        timeout = timeout || tail[nblk + i] != 0u;
+        float r;
+        std::memcpy(&r, &tail[i], sizeof(float));
         rho = (r != r || r > rho) ? r : rho;   // NaN stays
         if (rho != rho) break;
     }
