@@ -194,21 +194,6 @@ __device__ __forceinline__ float tanh_f(float x) {
     return fmaf(-2.0f, rcp_approx(1.0f + ex2_approx((2.0f * LOG2E) * x)), 1.0f);
 }
 
-// f(h, P) and df/dh
-__device__ __forceinline__ void cell_fj(float h, float pz, float pr, float pc,
-                                        const UnitParams &p, float &f, float &J) {
-    const float z = sigmoid_f(fmaf(p.a_z, h, pz + p.b_z));
-    const float r = sigmoid_f(fmaf(p.a_r, h, pr + p.b_r));
-    const float c = tanh_f(fmaf(p.a_c, r * h, pc + p.b_c));
-    const float cmh = c - h;
-    f = fmaf(z, cmh, h);
-    const float omz = 1.0f - z;
-    const float dz = z * omz * p.a_z;               // dz/dh
-    const float dq = fmaf(h, fmaf(-r, r, r) * p.a_r, r);  // d(r h)/dh
-    const float dc = fmaf(-c, c, 1.0f) * p.a_c * dq;      // dc/dh
-    J = fmaf(dz, cmh, fmaf(z, dc, omz));
-}
-
 // f(h, P) only
 __device__ __forceinline__ float cell_f(float h, float pz, float pr, float pc,
                                         const UnitParams &p) {
@@ -266,41 +251,6 @@ __device__ __forceinline__ void gates_scaled(float h, float sz, float sr, float 
     const float inv = rcp_approx(dz * dc);
     z = dc * inv;
     c = fmaf(-2.0f, dz * inv, 1.0f);
-}
-
-// f(h) and J = df/dh from pre-scaled arguments
-__device__ __forceinline__ void cell_fj_scaled(float h, float sz, float sr, float sc,
-                                               const ScaledParams &p, float &f, float &J) {
-    float z, r, c;
-    gates_scaled(h, sz, sr, sc, p, z, r, c);
-    const float omz = 1.0f - z;
-    const float cmh = c - h;
-    f = fmaf(z, cmh, h);
-    const float dq = fmaf(h * p.a_r, fmaf(-r, r, r), r);          // d(r h)/dh
-    const float t2 = fmaf(-c, c, 1.0f) * p.a_c * dq;               // (1 - c^2) a_c d(rh)/dh
-    J = fmaf(z, fmaf(omz * p.a_z, cmh, t2), omz);
-}
-
-// f(0) and J at the zero state: z = sig(P_z + b_z), r = sig(P_r + b_r),
-// c = tanh(P_c + b_c), f = z c, J = (1 - z) + z ((1 - z) a_z c + (1 - c^2) a_c r)
-__device__ __forceinline__ void cell_fj_scaled_at_zero(float sz, float sr, float sc,
-                                                       const ScaledParams &p, float &f, float &J) {
-    const float dz = 1.0f + ex2_approx(min_nan(sz, EXP2_CLAMP));
-    const float r = rcp_approx(1.0f + ex2_approx(sr));
-    const float dc = 1.0f + ex2_approx(min_nan(sc, EXP2_CLAMP));
-    const float inv = rcp_approx(dz * dc);
-    const float z = dc * inv;
-    const float c = fmaf(-2.0f, dz * inv, 1.0f);
-    const float omz = 1.0f - z;
-    f = z * c;
-    J = fmaf(z, fmaf(omz * p.a_z, c, fmaf(-c, c, 1.0f) * p.a_c * r), omz);
-}
-
-__device__ __forceinline__ float cell_f_scaled(float h, float sz, float sr, float sc,
-                                               const ScaledParams &p) {
-    float z, r, c;
-    gates_scaled(h, sz, sr, sc, p, z, r, c);
-    return fmaf(z, c - h, h);
 }
 
 // ------------------------------------------------ the cell on pairs of steps
