@@ -522,7 +522,7 @@ int nrnn_input_projection(const void *x, const void *W_x, int dtype, int64_t row
         if (!aligned16(x) || !aligned16(W_x) || !aligned16(preact)) return NRNN_ERR_INVALID_ARG;
         CUtensorMap tmA, tmB;
         if (!make_map_2d_sw128(&tmA, x, d_in, rows, PROJ_TC_BOX_K, PROJ_TC_BOX_M) ||
-            !make_map_2d_sw128(&tmB, W_x, d_in, 3 * d_h, PROJ_TC_BOX_K, PROJ_TC_BOX_N))
+            !make_map_2d_sw128(&tmB, W_x, d_in, 3 * d_h, PROJ_TC_BOX_K, projection_tc_b_box(rows)))
             return NRNN_ERR_CUDA;
         return cuda_status(launch_projection_tc(tmA, tmB, rows, static_cast<int>(d_in),
                                                 static_cast<int>(3 * d_h), preact,

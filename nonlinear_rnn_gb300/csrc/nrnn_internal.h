@@ -121,9 +121,11 @@ cudaError_t launch_head_mask(const int32_t *cu, int S, int64_t N, uint8_t *mask,
 cudaError_t launch_bounded_wait(const uint32_t *flag, uint64_t wait_ns, uint32_t *result,
                                 cudaStream_t stream);
 
-// bf16 tensor-core projection: tmA over x (d_in, rows), tmB over W_x (d_in, n_out),
-// both bf16 with a 64 x 128 / 64 x 256 box and the 128-byte swizzle.
+// bf16 tensor-core projection: tmA over x (d_in, rows) with a 64 x 128 box,
+// tmB over W_x (d_in, n_out) with a 64 x projection_tc_b_box(rows) box, both
+// bf16 with the 128-byte swizzle (a 128-row box: two CTAs share each W_x tile).
 constexpr int PROJ_TC_BOX_K = 64, PROJ_TC_BOX_M = 128, PROJ_TC_BOX_N = 256;
+int projection_tc_b_box(int64_t rows);
 cudaError_t launch_projection_tc(const CUtensorMap &tmA, const CUtensorMap &tmB, int64_t rows,
                                  int d_in, int n_out, void *P, cudaStream_t stream);
 

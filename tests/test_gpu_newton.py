@@ -231,7 +231,7 @@ def test_bounded_wait_gives_up_and_context_survives(nr):
     assert torch.ones(4, device="cuda").sum().item() == 4.0  # context still usable
 
 
-PROJ_SHAPES = [(1000, 136, 72), (128, 8, 16), (4097, 512, 256), (300, 1024, 344)]
+PROJ_SHAPES = [(1000, 136, 72), (128, 8, 16), (4097, 512, 256), (300, 1024, 344), (2000, 64, 40)]
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
