@@ -253,7 +253,9 @@ int nrnn_decode_step_x(const void *x, const void *W_x, int dtype, const float *p
  * (B, T, d_in)); x (rows, d_in), W_x (3 d_h, d_in), preact (rows, 3 d_h), all
  * of dtype, fp32 accumulation.  NRNN_F32 keeps fp32 accuracy (no TF32
  * rounding of the operands); NRNN_BF16 uses the bf16 tensor-core path and
- * rounds the fp32 accumulator to bf16.  d_in must be a multiple of 8.
+ * rounds the fp32 accumulator to bf16.  d_in and d_h must be multiples of 8
+ * and rows < 2^31 (else NRNN_ERR_UNSUPPORTED); x, W_x and preact 16-byte
+ * aligned (else NRNN_ERR_INVALID_ARG).
  */
 int nrnn_input_projection(const void *x, const void *W_x, int dtype, int64_t rows,
                           int64_t d_in, int64_t d_h, void *preact, void *stream);

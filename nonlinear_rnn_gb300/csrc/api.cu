@@ -86,9 +86,10 @@ bool make_map(CUtensorMap *m, const void *base, int dtype, int64_t width, int64_
 }
 
 // 2-D map over a (outer, inner) row-major bf16 or fp32 array, box
-// (box_inner x box_outer), 128-byte swizzle (box_inner * elem must be 128 bytes).
-bool make_map_2d_sw128(CUtensorMap *m, const void *base, int64_t inner, int64_t outer,
-                       uint32_t box_inner, uint32_t box_outer, int dtype = NRNN_BF16) {
+// (box_inner x box_outer) with the given swizzle (box_inner * elem must not
+// exceed the swizzle span).
+bool make_map_2d(CUtensorMap *m, const void *base, int64_t inner, int64_t outer,
+                 uint32_t box_inner, uint32_t box_outer, int dtype, CUtensorMapSwizzle swizzle) {
     auto fn = encode_fn();
     if (fn == nullptr) return false;
     const size_t es = elem_size(dtype);
@@ -100,9 +101,15 @@ bool make_map_2d_sw128(CUtensorMap *m, const void *base, int64_t inner, int64_t 
                                                 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
                           2, const_cast<void *>(base), dims,
                           strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
+}
+// the same with the 128-byte swizzle (box_inner * elem must be 128 bytes)
+bool make_map_2d_sw128(CUtensorMap *m, const void *base, int64_t inner, int64_t outer,
+                       uint32_t box_inner, uint32_t box_outer, int dtype = NRNN_BF16) {
+    return make_map_2d(m, base, inner, outer, box_inner, box_outer, dtype,
+                       CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 // 3-D bf16 map over x (B, T, d_in) row-major: dims (d_in, T, B), box (64, rows, 1),
@@ -515,29 +522,31 @@ int nrnn_input_projection(const void *x, const void *W_x, int dtype, int64_t row
     if (dtype != NRNN_F32 && dtype != NRNN_BF16) return NRNN_ERR_INVALID_ARG;
     if (rows < 0 || d_in <= 0 || d_h <= 0) return NRNN_ERR_INVALID_ARG;
     if (rows > 0 && (x == nullptr || W_x == nullptr || preact == nullptr)) return NRNN_ERR_INVALID_ARG;
-    if (d_in % 8 != 0 || d_h % 8 != 0 || d_in > INT32_MAX || 3 * d_h > INT32_MAX)
+    if (d_in % 8 != 0 || d_h % 8 != 0 || d_in > INT32_MAX || 3 * d_h > INT32_MAX ||
+        rows > INT32_MAX)
         return NRNN_ERR_UNSUPPORTED;
     if (rows == 0) return NRNN_OK;
-    if (dtype == NRNN_BF16) {
-        if (!aligned16(x) || !aligned16(W_x) || !aligned16(preact)) return NRNN_ERR_INVALID_ARG;
-        CUtensorMap tmA, tmB;
-        if (!make_map_2d_sw128(&tmA, x, d_in, rows, PROJ_TC_BOX_K, PROJ_TC_BOX_M) ||
-            !make_map_2d_sw128(&tmB, W_x, d_in, 3 * d_h, PROJ_TC_BOX_K, projection_tc_b_box(rows)))
-            return NRNN_ERR_CUDA;
-        return cuda_status(launch_projection_tc(tmA, tmB, rows, static_cast<int>(d_in),
-                                                static_cast<int>(3 * d_h), preact,
-                                                static_cast<cudaStream_t>(stream)));
-    }
     if (!aligned16(x) || !aligned16(W_x) || !aligned16(preact)) return NRNN_ERR_INVALID_ARG;
-    CUtensorMap tmA, tmB;
-    const int bn = projection_tf32x3_bn(static_cast<int>(3 * d_h));
+    CUtensorMap tmA, tmB, tmP;
+    const int64_t n_out = 3 * d_h;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (dtype == NRNN_BF16) {
+        if (!make_map_2d_sw128(&tmA, x, d_in, rows, PROJ_TC_BOX_K, PROJ_TC_BOX_M) ||
+            !make_map_2d_sw128(&tmB, W_x, d_in, n_out, PROJ_TC_BOX_K, projection_tc_b_box(rows)) ||
+            !make_map_2d(&tmP, preact, n_out, rows, PROJ_OUT_BOX, PROJ_OUT_BOX, NRNN_BF16,
+                         CU_TENSOR_MAP_SWIZZLE_64B))
+            return NRNN_ERR_CUDA;
+        return cuda_status(launch_projection_tc(tmA, tmB, tmP, rows, static_cast<int>(d_in),
+                                                static_cast<int>(n_out), st));
+    }
+    const int bn = projection_tf32x3_bn(static_cast<int>(n_out));
     if (!make_map_2d_sw128(&tmA, x, d_in, rows, PROJ_T3_BOX_K, PROJ_T3_BOX_M, NRNN_F32) ||
-        !make_map_2d_sw128(&tmB, W_x, d_in, 3 * d_h, PROJ_T3_BOX_K, bn, NRNN_F32))
+        !make_map_2d_sw128(&tmB, W_x, d_in, n_out, PROJ_T3_BOX_K, bn, NRNN_F32) ||
+        !make_map_2d(&tmP, preact, n_out, rows, PROJ_OUT_BOX, PROJ_OUT_BOX, NRNN_F32,
+                     CU_TENSOR_MAP_SWIZZLE_128B))
         return NRNN_ERR_CUDA;
-    return cuda_status(launch_projection_tf32x3(tmA, tmB, rows, static_cast<int>(d_in),
-                                                static_cast<int>(3 * d_h),
-                                                static_cast<float *>(preact),
-                                                static_cast<cudaStream_t>(stream)));
+    return cuda_status(launch_projection_tf32x3(tmA, tmB, tmP, rows, static_cast<int>(d_in),
+                                                static_cast<int>(n_out), st));
 }
 
 int nrnn_debug_head_mask(const int32_t *cu_seqlens, int64_t num_segments, int64_t N,

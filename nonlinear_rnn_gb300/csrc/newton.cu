@@ -314,7 +314,7 @@ __global__ void __launch_bounds__(NW * 32, 8)
 #pragma unroll 1
             for (int cc = 0; cc < L / 32; ++cc) {
                 uint32_t v[32];
-                tmem_ld_32cols(tmem + (static_cast<uint32_t>(warp * 32) << 16) + cc * 32, v);
+                tmem_ld_cols<32>(tmem + (static_cast<uint32_t>(warp * 32) << 16) + cc * 32, v);
 #pragma unroll
                 for (int i = 0; i < 32; ++i) {
                     if ((i % SEG) >= HALF) continue;

@@ -123,18 +123,24 @@ cudaError_t launch_bounded_wait(const uint32_t *flag, uint64_t wait_ns, uint32_t
 
 // bf16 tensor-core projection: tmA over x (d_in, rows) with a 64 x 128 box,
 // tmB over W_x (d_in, n_out) with a 64 x projection_tc_b_box(rows) box, both
-// bf16 with the 128-byte swizzle (a 128-row box: two CTAs share each W_x tile).
+// bf16 with the 128-byte swizzle (a 128-row box: two CTAs share each W_x tile);
+// tmP over P (n_out, rows) with a PROJ_OUT_BOX x PROJ_OUT_BOX box and the
+// 64-byte swizzle.
 constexpr int PROJ_TC_BOX_K = 64, PROJ_TC_BOX_M = 128, PROJ_TC_BOX_N = 256;
+constexpr int PROJ_OUT_BOX = 32;
 int projection_tc_b_box(int64_t rows);
-cudaError_t launch_projection_tc(const CUtensorMap &tmA, const CUtensorMap &tmB, int64_t rows,
-                                 int d_in, int n_out, void *P, cudaStream_t stream);
+cudaError_t launch_projection_tc(const CUtensorMap &tmA, const CUtensorMap &tmB,
+                                 const CUtensorMap &tmP, int64_t rows, int d_in, int n_out,
+                                 cudaStream_t stream);
 
 // fp32 split-TF32 tensor-core projection: tmA over x (d_in, rows) with a
 // 32 x 128 box, tmB over W_x (d_in, n_out) with a 32 x projection_tf32x3_bn(n_out)
-// box, both fp32 with the 128-byte swizzle.
+// box, both fp32 with the 128-byte swizzle; tmP over P (n_out, rows) with a
+// PROJ_OUT_BOX x PROJ_OUT_BOX box and the 128-byte swizzle.
 constexpr int PROJ_T3_BOX_K = 32, PROJ_T3_BOX_M = 128;
 int projection_tf32x3_bn(int n_out);
-cudaError_t launch_projection_tf32x3(const CUtensorMap &tmA, const CUtensorMap &tmB, int64_t rows,
-                                     int d_in, int n_out, float *P, cudaStream_t stream);
+cudaError_t launch_projection_tf32x3(const CUtensorMap &tmA, const CUtensorMap &tmB,
+                                     const CUtensorMap &tmP, int64_t rows, int d_in, int n_out,
+                                     cudaStream_t stream);
 
 }  // namespace nrnn

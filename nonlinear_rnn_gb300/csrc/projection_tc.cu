@@ -10,8 +10,9 @@
 //               accumulators, tcgen05.commit returns stages and hands a
 //               finished accumulator to the epilogue
 //   warp 2      owns the tensor-memory allocation
-//   warps 4..7  epilogue: tcgen05.ld of their 32-lane quarter, store, then
-//               release the accumulator; it overlaps the next tile's K loop
+//   warps 4..7  epilogue: tcgen05.ld of their 32-lane quarter, 32 x 32
+//               blocks staged in shared memory and sent out by TMA stores,
+//               then release the accumulator; it overlaps the next K loop
 //   warps 8..11 (fp32 only) split each staged tile in place for split-TF32
 // bf16: kind::f16, 128 x 256 tiles, 64-wide K slices, 4 stages, fp32
 // accumulation rounded to bf16.  fp32: split-TF32 ("3xTF32") -- each fp32
@@ -22,8 +23,8 @@
 //   A B ~ A_hi B_hi + A_hi B_lo + A_lo B_hi
 // (the dropped A_lo B_lo and the TF32 reading of lo are of order 2^-20
 // relative), 128 x 128 tiles, 32-wide K slices, 3 stages.
-// Out-of-range rows, columns and K are zero-filled by TMA and masked on
-// store.  Every wait is bounded; a wait that gives up sets
+// Out-of-range rows, columns and K are zero-filled by TMA loads and clipped
+// by TMA stores.  Every wait is bounded; a wait that gives up sets
 // g_projection_tc_error and the epilogue writes NaN, which the Newton residual
 // gate downstream reports as divergence.
 #include <type_traits>
@@ -78,44 +79,49 @@ template <> struct ProjCfg<2> : ProjCfgTf32<256, 2> {};
 constexpr int SPLIT_THREADS = 128;
 constexpr int EPI_THREADS = 128;
 
-// 32 accumulator columns of one row -> output (bf16: 4 x 16-byte stores; fp32: 8)
-__device__ __forceinline__ void store_row_chunk(__nv_bfloat16 *dst, int col0, int N,
-                                                const uint32_t (&v)[32], bool ok) {
+// The epilogue writes each 32 x 32 block of the accumulator, converted to the
+// output type, into a shared-memory buffer in the layout of a TMA box with the
+// 64-byte (bf16: 64-byte rows) or 128-byte (fp32: 128-byte rows) swizzle, and
+// one TMA store sends it to P in whole lines: the row-per-thread layout of
+// tcgen05.ld would otherwise store 16-byte pieces of 32 different rows.  The
+// swizzle moves 16-byte piece q of row r to q ^ ((r >> 1) & 3) (64-byte) or
+// q ^ (r & 7) (128-byte), so the 32 row-writes of a warp hit distinct banks.
+constexpr int OUT_BOX = PROJ_OUT_BOX;   // rows and columns of one stored block
+
+// this thread's row (32 accumulator columns) -> the staged block
+__device__ __forceinline__ void stage_row(unsigned char *blk, int r, const uint32_t (&v)[32],
+                                          bool ok, __nv_bfloat16 *) {
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
-        if (col0 + q * 8 + 8 <= N) {
-            uint4 pk;
-            uint32_t *w = reinterpret_cast<uint32_t *>(&pk);
+        uint4 pk;
+        uint32_t *w = reinterpret_cast<uint32_t *>(&pk);
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const float lo = ok ? __uint_as_float(v[q * 8 + 2 * e]) : __int_as_float(0x7fffffff);
-                const float hi = ok ? __uint_as_float(v[q * 8 + 2 * e + 1]) : __int_as_float(0x7fffffff);
-                const __nv_bfloat162 h2 = __floats2bfloat162_rn(lo, hi);
-                w[e] = *reinterpret_cast<const uint32_t *>(&h2);
-            }
-            *reinterpret_cast<uint4 *>(dst + q * 8) = pk;
+        for (int e = 0; e < 4; ++e) {
+            const float lo = ok ? __uint_as_float(v[q * 8 + 2 * e]) : __int_as_float(0x7fffffff);
+            const float hi = ok ? __uint_as_float(v[q * 8 + 2 * e + 1]) : __int_as_float(0x7fffffff);
+            const __nv_bfloat162 h2 = __floats2bfloat162_rn(lo, hi);
+            w[e] = *reinterpret_cast<const uint32_t *>(&h2);
         }
+        *reinterpret_cast<uint4 *>(blk + r * 64 + 16 * (q ^ ((r >> 1) & 3))) = pk;
     }
 }
-__device__ __forceinline__ void store_row_chunk(float *dst, int col0, int N,
-                                                const uint32_t (&v)[32], bool ok) {
+__device__ __forceinline__ void stage_row(unsigned char *blk, int r, const uint32_t (&v)[32],
+                                          bool ok, float *) {
 #pragma unroll
     for (int q = 0; q < 8; ++q) {
-        if (col0 + q * 4 + 4 <= N) {
-            float4 o;
-            o.x = ok ? __uint_as_float(v[4 * q + 0]) : __int_as_float(0x7fffffff);
-            o.y = ok ? __uint_as_float(v[4 * q + 1]) : __int_as_float(0x7fffffff);
-            o.z = ok ? __uint_as_float(v[4 * q + 2]) : __int_as_float(0x7fffffff);
-            o.w = ok ? __uint_as_float(v[4 * q + 3]) : __int_as_float(0x7fffffff);
-            *reinterpret_cast<float4 *>(dst + q * 4) = o;
-        }
+        uint4 o;
+        o.x = ok ? v[4 * q + 0] : 0x7fffffffu;
+        o.y = ok ? v[4 * q + 1] : 0x7fffffffu;
+        o.z = ok ? v[4 * q + 2] : 0x7fffffffu;
+        o.w = ok ? v[4 * q + 3] : 0x7fffffffu;
+        *reinterpret_cast<uint4 *>(blk + r * 128 + 16 * (q ^ (r & 7))) = o;
     }
 }
 
 template <int MODE>
 __global__ void __launch_bounds__(ProjCfg<MODE>::THREADS, 1)
     k_projection_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                    int64_t rows, int K, int N, void *Pv) {
+                    const __grid_constant__ CUtensorMap tmP, int64_t rows, int K, int N) {
     using C = ProjCfg<MODE>;
     constexpr bool F32 = C::F32;
     using Out = typename std::conditional<F32, float, __nv_bfloat16>::type;
@@ -154,6 +160,7 @@ __global__ void __launch_bounds__(ProjCfg<MODE>::THREADS, 1)
         fence_mbar_init();
         prefetch_tensormap(&tmA);
         prefetch_tensormap(&tmB);
+        prefetch_tensormap(&tmP);
     }
     if (warp == 2) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -259,7 +266,10 @@ __global__ void __launch_bounds__(ProjCfg<MODE>::THREADS, 1)
     } else if (warp >= 4 && warp < 8) {
         // --------------------------------------------------------------- epilogue
         const int quarter = warp & 3;
-        Out *P = static_cast<Out *>(Pv);
+        constexpr int BLK_BYTES = OUT_BOX * OUT_BOX * static_cast<int>(sizeof(Out));
+        // two staged blocks per warp: one is filled while the other is stored
+        unsigned char *stage_out = smem + C::STAGES * C::STAGE_BYTES + quarter * 2 * BLK_BYTES;
+        int nblk = 0;
         int j = 0;
         for (int64_t u = unit0; u < n_units; u += unit_step, ++j) {
             const int buf = j & 1;
@@ -267,16 +277,28 @@ __global__ void __launch_bounds__(ProjCfg<MODE>::THREADS, 1)
             const int n0 = static_cast<int>(u % tiles_n) * C::BN;
             const bool ok = mbar_wait_bounded(&accf_bar[buf], (j >> 1) & 1, TC_WAIT_NS, error);
             asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-            const int64_t row = m0 + quarter * 32 + lane;
+            const int64_t row0 = m0 + quarter * 32;
 #pragma unroll 1
-            for (int c = 0; c < C::BN / 32; ++c) {
+            for (int c = 0; c < C::BN; c += OUT_BOX) {
                 uint32_t v[32];
-                tmem_ld_32cols(tmem + (static_cast<uint32_t>(quarter * 32) << 16) + buf * C::BN + c * 32, v);
-                if (row < rows) store_row_chunk(P + row * N + n0 + c * 32, n0 + c * 32, N, v, ok);
+                tmem_ld_cols<32>(tmem + (static_cast<uint32_t>(quarter * 32) << 16) + buf * C::BN + c, v);
+                if (row0 >= rows || n0 + c >= N) continue;   // block wholly outside P
+                unsigned char *blk = stage_out + (nblk & 1) * BLK_BYTES;
+                if (lane == 0) bulk_wait_read<1>();   // this buffer's previous store has read it
+                __syncwarp();
+                stage_row(blk, lane, v, ok, static_cast<Out *>(nullptr));
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    tma_store_2d(&tmP, blk, n0 + c, static_cast<int>(row0));
+                    bulk_commit();
+                }
+                ++nblk;
             }
             asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
             mbar_arrive(&acce_bar[buf]);
         }
+        if (lane == 0) bulk_wait_all();   // the stores are done before the CTA exits
     }
     __syncwarp();
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
@@ -291,13 +313,15 @@ __global__ void __launch_bounds__(ProjCfg<MODE>::THREADS, 1)
 }
 
 template <int MODE>
-cudaError_t launch_tc(const CUtensorMap &tmA, const CUtensorMap &tmB, int64_t rows, int d_in,
-                      int n_out, void *P, cudaStream_t stream) {
+cudaError_t launch_tc(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUtensorMap &tmP,
+                      int64_t rows, int d_in, int n_out, cudaStream_t stream) {
     using C = ProjCfg<MODE>;
     constexpr int CL = C::CLUSTER;
     static std::atomic<unsigned long long> configured{0};
     static int groups_of[64];   // co-resident CTAs (CL == 1) or clusters per device
-    constexpr size_t smem = static_cast<size_t>(C::STAGES) * C::STAGE_BYTES + 1024;
+    // operand ring + two staged output blocks per epilogue warp + alignment slack
+    constexpr size_t smem = static_cast<size_t>(C::STAGES) * C::STAGE_BYTES +
+                            (EPI_THREADS / 32) * 2 * OUT_BOX * OUT_BOX * (C::F32 ? 4 : 2) + 1024;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
     cfg.blockDim = dim3(C::THREADS);
@@ -339,7 +363,7 @@ cudaError_t launch_tc(const CUtensorMap &tmA, const CUtensorMap &tmB, int64_t ro
     const int64_t grid = (n_units < groups ? n_units : groups) * CL;
     cfg.gridDim = dim3(static_cast<unsigned>(grid));
     if (CL == 1) cfg.numAttrs = 0;
-    return cudaLaunchKernelEx(&cfg, k_projection_tc<MODE>, tmA, tmB, rows, d_in, n_out, P);
+    return cudaLaunchKernelEx(&cfg, k_projection_tc<MODE>, tmA, tmB, tmP, rows, d_in, n_out);
 }
 
 }  // namespace
@@ -348,19 +372,21 @@ int projection_tc_b_box(int64_t rows) {
     return rows > PROJ_TC_BOX_M ? PROJ_TC_BOX_N / 2 : PROJ_TC_BOX_N;
 }
 
-cudaError_t launch_projection_tc(const CUtensorMap &tmA, const CUtensorMap &tmB, int64_t rows,
-                                 int d_in, int n_out, void *P, cudaStream_t stream) {
+cudaError_t launch_projection_tc(const CUtensorMap &tmA, const CUtensorMap &tmB,
+                                 const CUtensorMap &tmP, int64_t rows, int d_in, int n_out,
+                                 cudaStream_t stream) {
     if (projection_tc_b_box(rows) != PROJ_TC_BOX_N)
-        return launch_tc<3>(tmA, tmB, rows, d_in, n_out, P, stream);
-    return launch_tc<0>(tmA, tmB, rows, d_in, n_out, P, stream);
+        return launch_tc<3>(tmA, tmB, tmP, rows, d_in, n_out, stream);
+    return launch_tc<0>(tmA, tmB, tmP, rows, d_in, n_out, stream);
 }
 
 int projection_tf32x3_bn(int n_out) { return n_out >= 512 ? 256 : 128; }
 
-cudaError_t launch_projection_tf32x3(const CUtensorMap &tmA, const CUtensorMap &tmB, int64_t rows,
-                                     int d_in, int n_out, float *P, cudaStream_t stream) {
-    if (projection_tf32x3_bn(n_out) == 256) return launch_tc<2>(tmA, tmB, rows, d_in, n_out, P, stream);
-    return launch_tc<1>(tmA, tmB, rows, d_in, n_out, P, stream);
+cudaError_t launch_projection_tf32x3(const CUtensorMap &tmA, const CUtensorMap &tmB,
+                                     const CUtensorMap &tmP, int64_t rows, int d_in, int n_out,
+                                     cudaStream_t stream) {
+    if (projection_tf32x3_bn(n_out) == 256) return launch_tc<2>(tmA, tmB, tmP, rows, d_in, n_out, stream);
+    return launch_tc<1>(tmA, tmB, tmP, rows, d_in, n_out, stream);
 }
 
 }  // namespace nrnn
