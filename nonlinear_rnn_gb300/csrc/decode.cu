@@ -3,7 +3,9 @@
 // FAQs, "How do I pass recurrent state between decode steps?": a carry of
 // size (slots, d_h), prefill then decode_wx + decode_step(..., out=) per token).
 //
-// k_decode_step: h_out = f(h_in, P) elementwise from given preactivations.
+// k_decode_step: h_out = f(h_in, P) elementwise from given preactivations
+// (k_decode_step_vec: the same on 16-byte vectors when shapes and alignment
+// allow).
 // k_decode_step_x: the same step with the input projection fused in, for
 // small slot counts (a batched matrix-vector product per step; see below).
 #include "nrnn_device.cuh"
@@ -26,16 +28,6 @@ __global__ void __launch_bounds__(256)
     h_out[i] = from_f32<TS>(cell_f(h, to_f32(p[0]), to_f32(p[d_h]), to_f32(p[2 * d_h]), prm));
 }
 
-// k_decode_step_x: a CTA takes DX_UNITS units (one warp each) and a group of
-// DX_SLOTS slots whose x rows it stages in shared memory once (or reads from
-// global memory when they do not fit); each lane accumulates 16-byte slices of
-// d_in for the three gate rows of its warp's unit against every slot of the
-// group, so a W_x row is read once per slot group, not once per slot.  After
-// the shuffle reduction lane s applies the cell to slot s.
-constexpr int DX_UNITS = 8;
-constexpr int DX_SLOTS = 8;
-constexpr size_t DX_SMEM_MAX = 48 * 1024;
-
 __device__ __forceinline__ void unpack16(const uint4 &v, float (&o)[4]) {
     o[0] = __uint_as_float(v.x);
     o[1] = __uint_as_float(v.y);
@@ -50,6 +42,63 @@ __device__ __forceinline__ void unpack16(const uint4 &v, float (&o)[8]) {
         o[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
     }
 }
+
+// The same step with 16 bytes per load: a thread takes the 16 / sizeof(TS)
+// adjacent units of one slot (4 fp32 or 8 bf16), so each thread has four
+// 16-byte loads in flight instead of four scalar ones.  Needs d_h a multiple
+// of that width and 16-byte aligned P, params, h_in and h_out.
+template <typename TS>
+__global__ void __launch_bounds__(256)
+    k_decode_step_vec(const TS *__restrict__ P, const float *__restrict__ params,
+                      const TS *__restrict__ h_in, TS *__restrict__ h_out, int slots, int d_h) {
+    constexpr int VEC = 16 / sizeof(TS);
+    const int groups = d_h / VEC;
+    const int64_t v = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (v >= static_cast<int64_t>(slots) * groups) return;
+    const int s = static_cast<int>(v / groups);
+    const int j0 = static_cast<int>(v - static_cast<int64_t>(s) * groups) * VEC;
+    const TS *p = P + static_cast<int64_t>(s) * 3 * d_h + j0;
+    const int64_t i0 = static_cast<int64_t>(s) * d_h + j0;
+    float z[VEC], r[VEC], c[VEC], h[VEC];
+    unpack16(*reinterpret_cast<const uint4 *>(p), z);
+    unpack16(*reinterpret_cast<const uint4 *>(p + d_h), r);
+    unpack16(*reinterpret_cast<const uint4 *>(p + 2 * d_h), c);
+    if (h_in != nullptr) {
+        unpack16(*reinterpret_cast<const uint4 *>(h_in + i0), h);
+    } else {
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) h[e] = 0.f;
+    }
+    // parameters of the VEC units: 6 rows of params, VEC floats each
+    float prm[6][VEC];
+#pragma unroll
+    for (int g = 0; g < 6; ++g)
+#pragma unroll
+        for (int q = 0; q < VEC / 4; ++q) {
+            const float4 w = *reinterpret_cast<const float4 *>(params + g * d_h + j0 + 4 * q);
+            prm[g][4 * q] = w.x;
+            prm[g][4 * q + 1] = w.y;
+            prm[g][4 * q + 2] = w.z;
+            prm[g][4 * q + 3] = w.w;
+        }
+    __align__(16) TS o[VEC];
+#pragma unroll
+    for (int e = 0; e < VEC; ++e) {
+        const UnitParams up{prm[0][e], prm[1][e], prm[2][e], prm[3][e], prm[4][e], prm[5][e]};
+        o[e] = from_f32<TS>(cell_f(h[e], z[e], r[e], c[e], up));
+    }
+    *reinterpret_cast<uint4 *>(h_out + i0) = *reinterpret_cast<const uint4 *>(o);
+}
+
+// k_decode_step_x: a CTA takes DX_UNITS units (one warp each) and a group of
+// DX_SLOTS slots whose x rows it stages in shared memory once (or reads from
+// global memory when they do not fit); each lane accumulates 16-byte slices of
+// d_in for the three gate rows of its warp's unit against every slot of the
+// group, so a W_x row is read once per slot group, not once per slot.  After
+// the shuffle reduction lane s applies the cell to slot s.
+constexpr int DX_UNITS = 8;
+constexpr int DX_SLOTS = 8;
+constexpr size_t DX_SMEM_MAX = 48 * 1024;
 
 template <typename TS>
 __global__ void __launch_bounds__(DX_UNITS * 32)
@@ -125,6 +174,21 @@ cudaError_t launch_decode_step(int dtype, const void *P, const float *params, co
                                void *h_out, int slots, int d_h, cudaStream_t stream) {
     const int64_t n = static_cast<int64_t>(slots) * d_h;
     if (n == 0) return cudaSuccess;
+    const int vec = dtype == 1 ? 8 : 4;
+    const auto a16 = [](const void *q) { return (reinterpret_cast<uintptr_t>(q) & 15u) == 0; };
+    if (d_h % vec == 0 && a16(P) && a16(params) && a16(h_out) && (h_in == nullptr || a16(h_in))) {
+        const unsigned vblocks = static_cast<unsigned>((n / vec + 255) / 256);
+        if (dtype == 1)
+            k_decode_step_vec<__nv_bfloat16><<<vblocks, 256, 0, stream>>>(
+                static_cast<const __nv_bfloat16 *>(P), params,
+                static_cast<const __nv_bfloat16 *>(h_in), static_cast<__nv_bfloat16 *>(h_out),
+                slots, d_h);
+        else
+            k_decode_step_vec<float><<<vblocks, 256, 0, stream>>>(
+                static_cast<const float *>(P), params, static_cast<const float *>(h_in),
+                static_cast<float *>(h_out), slots, d_h);
+        return cudaGetLastError();
+    }
     const unsigned blocks = static_cast<unsigned>((n + 255) / 256);
     if (dtype == 1)
         k_decode_step<__nv_bfloat16><<<blocks, 256, 0, stream>>>(

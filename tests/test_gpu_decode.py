@@ -38,6 +38,30 @@ def test_decode_step_matches_oracle_and_carries_state(dtype):
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("d_h, offset", [(6, 0), (16, 0), (40, 0), (16, 1)])
+def test_decode_step_vector_and_scalar_paths(dtype, d_h, offset):
+    # d_h a multiple of the 16-byte width with aligned buffers takes the vector
+    # kernel; d_h = 6 (and 40 for bf16) or an output one element off alignment
+    # takes the scalar one; both against the oracle, h_in given
+    import nonlinear_rnn_gb300 as nr
+    tdt = torch.float32 if dtype == "f32" else torch.bfloat16
+    slots = 333
+    w = syn.small_workload(B=slots, T=1, d_h=d_h, dtype=dtype, seed=64 + d_h)
+    P = syn.direct_preact(w)[:, 0]
+    prm = syn.make_params(w)
+    rng = np.random.default_rng(65 + d_h)
+    h0 = rng.uniform(-0.9, 0.9, size=(slots, d_h)).astype(np.float32)
+    if dtype == "bf16":
+        P, h0 = syn.round_bf16(P), syn.round_bf16(h0)
+    buf = torch.full((slots * d_h + offset,), float("nan"), dtype=tdt, device="cuda")
+    out = buf[offset:].view(slots, d_h)
+    h = nr.decode_step(prm, h=dev(h0, tdt), preact=dev(P, tdt), out=out)
+    assert h.data_ptr() == out.data_ptr()
+    ref = oracle.decode_step(P, prm, h0)
+    assert np.max(np.abs(host(h) - ref)) <= (1e-6 if dtype == "f32" else 4e-3)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
 def test_decode_step_with_fused_projection(dtype):
     import nonlinear_rnn_gb300 as nr
     tdt = torch.float32 if dtype == "f32" else torch.bfloat16
