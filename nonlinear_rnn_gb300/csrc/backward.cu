@@ -31,6 +31,70 @@ constexpr int SEG = NEWTON_SEG;
 constexpr int L = NEWTON_L;
 constexpr int U = TILE_U;
 
+constexpr int HALF = SEG / 2;
+
+// Gates of a pair of steps in the storage type's formulation (the forward's:
+// ex2/rcp for fp32, tanh.approx for bf16), from raw preactivations.
+template <typename TS> struct BwCell;
+template <> struct BwCell<float> {
+    using Params = ScaledParams2;
+    __device__ static Params make(const UnitParams &p) { return pair_params(scale_params(p)); }
+    __device__ static void scale(float2 pz, float2 pr, float2 pc, const Params &q, float2 &sz,
+                                 float2 &sr, float2 &sc) {
+        scale_preact2(pz, pr, pc, q, sz, sr, sc);
+    }
+    __device__ static void gates(float2 h, float2 sz, float2 sr, float2 sc, const Params &q,
+                                 float2 &z, float2 &omz, float2 &r, float2 &c) {
+        float2 qc;
+        gates2(h, sz, sr, sc, q, z, r, c, qc);
+        omz = fma2(z, splat2(-1.0f), splat2(1.0f));
+    }
+};
+template <> struct BwCell<__nv_bfloat16> {
+    using Params = TanhCell::Params;
+    __device__ static Params make(const UnitParams &p) { return TanhCell::make(p); }
+    __device__ static void scale(float2 pz, float2 pr, float2 pc, const Params &q, float2 &sz,
+                                 float2 &sr, float2 &sc) {
+        TanhCell::scale(pz, pr, pc, q, sz, sr, sc);
+    }
+    __device__ static void gates(float2 h, float2 sz, float2 sr, float2 sc, const Params &q,
+                                 float2 &z, float2 &omz, float2 &r, float2 &c) {
+        float2 tz, tr;
+        TanhCell::gates(h, sz, sr, sc, q, tz, tr, r, c);
+        z = fma2(splat2(0.5f), tz, splat2(0.5f));
+        omz = fma2(splat2(-0.5f), tz, splat2(0.5f));
+    }
+};
+
+// The derivatives of a pair of steps at shifted states hs: J = df/dh and the
+// factors of df/dP_g and df/d(a_g) that the gradient loop scales by lambda:
+//   df/dP_z = z (1 - z) (c - h),  df/dP_c = z (1 - c^2),
+//   df/dP_r = z (1 - c^2) a_c h r (1 - r),  df/da_g = df/dP_g * (h, h, r h)
+struct Derivs2 {
+    float2 J, dz, dr, dc, rh;
+};
+template <typename TS>
+__device__ __forceinline__ Derivs2 derivs2(float2 hs, float2 pz, float2 pr, float2 pc,
+                                           const typename BwCell<TS>::Params &q, float2 a_z,
+                                           float2 a_r, float2 a_c) {
+    const float2 one = splat2(1.0f), mone = splat2(-1.0f);
+    float2 sz, sr, sc, z, omz, r, c;
+    BwCell<TS>::scale(pz, pr, pc, q, sz, sr, sc);
+    BwCell<TS>::gates(hs, sz, sr, sc, q, z, omz, r, c);
+    const float2 cmh = fma2(hs, mone, c);
+    const float2 omc2 = fma2(mul2(c, mone), c, one);       // 1 - c^2
+    const float2 rr = fma2(mul2(r, mone), r, r);           // r (1 - r)
+    const float2 dq = fma2(mul2(hs, a_r), rr, r);          // d(r h)/dh
+    const float2 t3 = mul2(mul2(omc2, a_c), dq);
+    Derivs2 d;
+    d.J = fma2(z, fma2(mul2(omz, a_z), cmh, t3), omz);
+    d.dz = mul2(mul2(z, omz), cmh);
+    d.dc = mul2(z, omc2);
+    d.dr = mul2(mul2(d.dc, a_c), mul2(hs, rr));
+    d.rh = mul2(r, hs);
+    return d;
+}
+
 template <typename TS>
 __global__ void __launch_bounds__(NW * 32, 4)
     k_backward(const __grid_constant__ CUtensorMap tmP, const __grid_constant__ CUtensorMap tmH,
@@ -74,7 +138,8 @@ __global__ void __launch_bounds__(NW * 32, 4)
     const int u = u0 + lane;
     const bool uok = u < a.d_h;
     const UnitParams up = load_unit_params(a.params, a.d_h, u, uok);
-    const ScaledParams prm = scale_params(up);
+    const typename BwCell<TS>::Params q = BwCell<TS>::make(up);
+    const float2 a_z = splat2(up.a_z), a_r = splat2(up.a_r), a_c = splat2(up.a_c);
     const int r0 = warp * SEG;
     float hb = 0.f;   // H at row r0 - 1
     if (warp == 0 && t0 > 0 && uok)
@@ -85,47 +150,43 @@ __global__ void __launch_bounds__(NW * 32, 4)
     const uint32_t hm = (s_heads[r0 >> 5] >> (r0 & 31)) & ((1u << SEG) - 1u);
     const int nvalid = min(SEG, a.T - (t0 + r0));
 
-    // per-row derivatives at (h~ = H_{t-1}, P_t)
-    float Jr[SEG], dz[SEG], dr[SEG], dc[SEG], rh[SEG];
-    {
-        float hprev = hb;
+    // Each thread takes its 16 rows as 8 pairs (i, i + 8) on packed f32x2
+    // arithmetic: .x the lower half of the warp's rows, .y the upper half.
+    // Shifted state of row r (0 at a head); H at row r0 - 1 is hb.
+    auto shifted = [&](int i) {
+        if ((hm >> i) & 1u) return 0.f;
+        return i == 0 ? hb : to_f32(Hs[(r0 + i - 1) * U + lane]);
+    };
+    // per-row derivatives at (h~ = H_{t-1}, P_t); J = 0 at a head and past the end
+    float2 Jr[HALF], dz[HALF], dr[HALF], dc[HALF], rh[HALF];
 #pragma unroll
-        for (int i = 0; i < SEG; ++i) {
-            const int r = r0 + i;
-            const bool head = (hm >> i) & 1u;
-            const float hs = head ? 0.f : hprev;
-            float sz, sr, sc;
-            scale_preact(to_f32(Ps[(0 * L + r) * U + lane]), to_f32(Ps[(1 * L + r) * U + lane]),
-                         to_f32(Ps[(2 * L + r) * U + lane]), prm, sz, sr, sc);
-            float z, rg, cg;
-            gates_scaled(hs, sz, sr, sc, prm, z, rg, cg);
-            const float omz = 1.0f - z;
-            const float cmh = cg - hs;
-            const float omc2 = fmaf(-cg, cg, 1.0f);
-            const float dPc = z * omc2;
-            const float rr = fmaf(-rg, rg, rg);
-            const float dq = fmaf(hs * up.a_r, rr, rg);
-            float J = fmaf(z, fmaf(omz * up.a_z, cmh, omc2 * up.a_c * dq), omz);
-            if (head || i >= nvalid) J = 0.f;   // no flow across a head or past the end
-            Jr[i] = J;
-            dz[i] = z * omz * cmh;
-            dc[i] = dPc;
-            dr[i] = dPc * up.a_c * hs * rr;
-            rh[i] = rg * hs;
-            hprev = to_f32(Hs[r * U + lane]);
-        }
+    for (int i = 0; i < HALF; ++i) {
+        const int rl = r0 + i, ru = rl + HALF;
+        const float2 hs = make_float2(shifted(i), shifted(i + HALF));
+        const float2 pz = make_float2(to_f32(Ps[(0 * L + rl) * U + lane]), to_f32(Ps[(0 * L + ru) * U + lane]));
+        const float2 pr = make_float2(to_f32(Ps[(1 * L + rl) * U + lane]), to_f32(Ps[(1 * L + ru) * U + lane]));
+        const float2 pc = make_float2(to_f32(Ps[(2 * L + rl) * U + lane]), to_f32(Ps[(2 * L + ru) * U + lane]));
+        const Derivs2 d = derivs2<TS>(hs, pz, pr, pc, q, a_z, a_r, a_c);
+        Jr[i] = make_float2(((hm >> i) & 1u) || i >= nvalid ? 0.f : d.J.x,
+                            ((hm >> (i + HALF)) & 1u) || i + HALF >= nvalid ? 0.f : d.J.y);
+        dz[i] = d.dz;
+        dr[i] = d.dr;
+        dc[i] = d.dc;
+        rh[i] = d.rh;
     }
 
-    // compose nu_{t+1} -> nu_t = J_t nu_{t+1} + J_t gH_t over this warp's rows, last first
-    float A = 1.f, Bv = 0.f;
+    // compose nu_{t+1} -> nu_t = J_t nu_{t+1} + J_t gH_t over each half, last
+    // row first, then the lower half after the upper one
+    float2 A2 = splat2(1.0f), B2 = splat2(0.0f);
 #pragma unroll
-    for (int i = SEG - 1; i >= 0; --i) {
-        const float gh = (i < nvalid) ? to_f32(Gs[(r0 + i) * U + lane]) : 0.f;
-        Bv = fmaf(Jr[i], Bv, Jr[i] * gh);
-        A *= Jr[i];
+    for (int i = HALF - 1; i >= 0; --i) {
+        const float2 gh = make_float2(i < nvalid ? to_f32(Gs[(r0 + i) * U + lane]) : 0.f,
+                                      i + HALF < nvalid ? to_f32(Gs[(r0 + i + HALF) * U + lane]) : 0.f);
+        B2 = fma2(Jr[i], B2, mul2(Jr[i], gh));
+        A2 = mul2(A2, Jr[i]);
     }
-    s_aggA[warp][lane] = A;
-    s_aggB[warp][lane] = Bv;
+    s_aggA[warp][lane] = A2.x * A2.y;
+    s_aggB[warp][lane] = fmaf(A2.x, B2.y, B2.x);
     __syncthreads();
 
     // carry into this warp from the later warps of the chunk
@@ -155,37 +216,49 @@ __global__ void __launch_bounds__(NW * 32, 4)
     }
     __syncthreads();
 
-    // lambda_t = gH_t + nu_{t+1}; nu_t = J_t lambda_t; gradients
-    float nu = fmaf(eA, s_C[lane], eB);
-    float g_az = 0.f, g_ar = 0.f, g_ac = 0.f, g_bz = 0.f, g_br = 0.f, g_bc = 0.f;
+    // lambda_t = gH_t + nu_{t+1}; nu_t = J_t lambda_t; gradients.  nu enters the
+    // upper half from the later warps and the lower half from the upper half.
+    const float nu_hi = fmaf(eA, s_C[lane], eB);
+    float2 nu = make_float2(fmaf(A2.y, nu_hi, B2.y), nu_hi);
+    float2 g_az = splat2(0.f), g_ar = splat2(0.f), g_ac = splat2(0.f);
+    float2 g_bz = splat2(0.f), g_br = splat2(0.f), g_bc = splat2(0.f);
     TS *gP = reinterpret_cast<TS *>(a.gP);
 #pragma unroll
-    for (int i = SEG - 1; i >= 0; --i) {
-        if (i >= nvalid) continue;
-        const int r = r0 + i;
-        const float lam = to_f32(Gs[r * U + lane]) + nu;
-        nu = Jr[i] * lam;
-        const float hs = ((hm >> i) & 1u) ? 0.f : (i == 0 ? hb : to_f32(Hs[(r - 1) * U + lane]));
-        const float gz = lam * dz[i], gr = lam * dr[i], gc = lam * dc[i];
-        g_bz += gz;
-        g_br += gr;
-        g_bc += gc;
-        g_az = fmaf(gz, hs, g_az);
-        g_ar = fmaf(gr, hs, g_ar);
-        g_ac = fmaf(gc, rh[i], g_ac);
+    for (int i = HALF - 1; i >= 0; --i) {
+        const bool vl = i < nvalid, vu = i + HALF < nvalid;
+        const float2 lam = make_float2(vl ? to_f32(Gs[(r0 + i) * U + lane]) + nu.x : 0.f,
+                                       vu ? to_f32(Gs[(r0 + i + HALF) * U + lane]) + nu.y : 0.f);
+        nu = mul2(Jr[i], lam);
+        const float2 hs = make_float2(shifted(i), shifted(i + HALF));
+        const float2 gz = mul2(lam, dz[i]), gr = mul2(lam, dr[i]), gc = mul2(lam, dc[i]);
+        g_bz = add2(g_bz, gz);
+        g_br = add2(g_br, gr);
+        g_bc = add2(g_bc, gc);
+        g_az = fma2(gz, hs, g_az);
+        g_ar = fma2(gr, hs, g_ar);
+        g_ac = fma2(gc, rh[i], g_ac);
         if (uok) {
-            TS *o = gP + (static_cast<size_t>(b) * a.T + t0 + r) * 3 * a.d_h + u;
-            o[0] = from_f32<TS>(gz);
-            o[a.d_h] = from_f32<TS>(gr);
-            o[2 * a.d_h] = from_f32<TS>(gc);
+            const size_t row = static_cast<size_t>(b) * a.T + t0 + r0 + i;
+            if (vl) {
+                TS *o = gP + row * 3 * a.d_h + u;
+                o[0] = from_f32<TS>(gz.x);
+                o[a.d_h] = from_f32<TS>(gr.x);
+                o[2 * a.d_h] = from_f32<TS>(gc.x);
+            }
+            if (vu) {
+                TS *o = gP + (row + HALF) * 3 * a.d_h + u;
+                o[0] = from_f32<TS>(gz.y);
+                o[a.d_h] = from_f32<TS>(gr.y);
+                o[2 * a.d_h] = from_f32<TS>(gc.y);
+            }
         }
     }
-    s_red[0][warp][lane] = g_az;
-    s_red[1][warp][lane] = g_ar;
-    s_red[2][warp][lane] = g_ac;
-    s_red[3][warp][lane] = g_bz;
-    s_red[4][warp][lane] = g_br;
-    s_red[5][warp][lane] = g_bc;
+    s_red[0][warp][lane] = g_az.x + g_az.y;
+    s_red[1][warp][lane] = g_ar.x + g_ar.y;
+    s_red[2][warp][lane] = g_ac.x + g_ac.y;
+    s_red[3][warp][lane] = g_bz.x + g_bz.y;
+    s_red[4][warp][lane] = g_br.x + g_br.y;
+    s_red[5][warp][lane] = g_bc.x + g_bc.y;
     __syncthreads();
     if (uok) {   // warp w sums gate-parameters w, w + NW, ... over the NW warps
         for (int g = warp; g < 6; g += NW) {
