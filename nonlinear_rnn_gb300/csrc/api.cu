@@ -85,6 +85,27 @@ bool make_map(CUtensorMap *m, const void *base, int dtype, int64_t width, int64_
     return r == CUDA_SUCCESS;
 }
 
+// 4-D map over a (B, T, 3 d_h) preactivation-shaped array seen as (d_h, gate,
+// T, B), box (TILE_U x 1 x NEWTON_L x 1): one gate block of a tile, clipped at
+// d_h so that a partial unit tile never reaches into the next gate's columns.
+bool make_map_gates(CUtensorMap *m, const void *base, int dtype, int64_t d_h, int64_t T, int64_t B) {
+    auto fn = encode_fn();
+    if (fn == nullptr) return false;
+    const size_t es = elem_size(dtype);
+    cuuint64_t dims[4] = {static_cast<cuuint64_t>(d_h), 3, static_cast<cuuint64_t>(T),
+                          static_cast<cuuint64_t>(B)};
+    cuuint64_t strides[3] = {static_cast<cuuint64_t>(d_h * es), static_cast<cuuint64_t>(3 * d_h * es),
+                             static_cast<cuuint64_t>(3 * d_h * es * T)};
+    cuuint32_t box[4] = {TILE_U, 1, NEWTON_L, 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    const CUresult r = fn(m, dtype == NRNN_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+                          4, const_cast<void *>(base), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 // 2-D map over a (outer, inner) row-major bf16 or fp32 array, box
 // (box_inner x box_outer) with the given swizzle (box_inner * elem must not
 // exceed the swizzle span).
@@ -405,14 +426,13 @@ int nrnn_newton_backward(const void *preact, int dtype, const float *params, int
     if (B * T == 0) return NRNN_OK;
     e = cudaMemsetAsync(ws, 0, ly.zero_bytes, stream);
     if (e != cudaSuccess) return NRNN_ERR_CUDA;
-    CUtensorMap tmP, tmH, tmG;
+    CUtensorMap tmP, tmH, tmG, tmGP;
     if (!make_map(&tmP, preact, dtype, 3 * d_h, T, B) || !make_map(&tmH, H, dtype, d_h, T, B) ||
-        !make_map(&tmG, gH, dtype, d_h, T, B))
+        !make_map(&tmG, gH, dtype, d_h, T, B) || !make_map_gates(&tmGP, gP, dtype, d_h, T, B))
         return NRNN_ERR_CUDA;
     BackwardArgs a{};
     a.H = H;
     a.gH = gH;
-    a.gP = gP;
     a.gparams = gparams;
     a.params = params;
     a.cu = cu_seqlens;
@@ -426,7 +446,7 @@ int nrnn_newton_backward(const void *preact, int dtype, const float *params, int
     a.ticket = reinterpret_cast<uint32_t *>(ws + ly.counters_off);
     a.error = reinterpret_cast<uint32_t *>(ws + ly.error_off);
     a.wait_ns = g_wait_ns.load();
-    return cuda_status(launch_backward(dtype, tmP, tmH, tmG, a, ly.n_tiles, stream));
+    return cuda_status(launch_backward(dtype, tmP, tmH, tmG, tmGP, a, ly.n_tiles, stream));
 }
 
 int nrnn_picard(const void *preact, int dtype, const float *params, int64_t B, int64_t T,

@@ -21,6 +21,7 @@
 // with one atomicAdd per (gate, unit).  Every wait is bounded.
 #include "nrnn_device.cuh"
 #include "nrnn_internal.h"
+#include "tcgen05.cuh"
 
 namespace nrnn {
 
@@ -32,6 +33,17 @@ constexpr int L = NEWTON_L;
 constexpr int U = TILE_U;
 
 constexpr int HALF = SEG / 2;
+
+// shared -> global store of one gate block of dL/dP through the 4-D map
+// (d_h, gate, T, B); units past d_h and steps past T are not written
+__device__ __forceinline__ void tma_store_4d(const CUtensorMap *map, const void *src, int x, int y,
+                                             int z, int w) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.global.shared::cta.bulk_group [%0, {%2, %3, %4, %5}], [%1];" ::"l"(
+            reinterpret_cast<uint64_t>(map)),
+        "r"(smem_u32(src)), "r"(x), "r"(y), "r"(z), "r"(w)
+        : "memory");
+}
 
 // Gates of a pair of steps in the storage type's formulation (the forward's:
 // ex2/rcp for fp32, tanh.approx for bf16), from raw preactivations.
@@ -98,7 +110,8 @@ __device__ __forceinline__ Derivs2 derivs2(float2 hs, float2 pz, float2 pr, floa
 template <typename TS>
 __global__ void __launch_bounds__(NW * 32, 4)
     k_backward(const __grid_constant__ CUtensorMap tmP, const __grid_constant__ CUtensorMap tmH,
-               const __grid_constant__ CUtensorMap tmG, const BackwardArgs a) {
+               const __grid_constant__ CUtensorMap tmG, const __grid_constant__ CUtensorMap tmGP,
+               const BackwardArgs a) {
     extern __shared__ __align__(128) unsigned char dsmem[];
     TS *Ps = reinterpret_cast<TS *>(dsmem);   // [3][L][U]
     TS *Hs = Ps + 3 * L * U;                  // [L][U] trajectory
@@ -222,7 +235,6 @@ __global__ void __launch_bounds__(NW * 32, 4)
     float2 nu = make_float2(fmaf(A2.y, nu_hi, B2.y), nu_hi);
     float2 g_az = splat2(0.f), g_ar = splat2(0.f), g_ac = splat2(0.f);
     float2 g_bz = splat2(0.f), g_br = splat2(0.f), g_bc = splat2(0.f);
-    TS *gP = reinterpret_cast<TS *>(a.gP);
 #pragma unroll
     for (int i = HALF - 1; i >= 0; --i) {
         const bool vl = i < nvalid, vu = i + HALF < nvalid;
@@ -237,21 +249,15 @@ __global__ void __launch_bounds__(NW * 32, 4)
         g_az = fma2(gz, hs, g_az);
         g_ar = fma2(gr, hs, g_ar);
         g_ac = fma2(gc, rh[i], g_ac);
-        if (uok) {
-            const size_t row = static_cast<size_t>(b) * a.T + t0 + r0 + i;
-            if (vl) {
-                TS *o = gP + row * 3 * a.d_h + u;
-                o[0] = from_f32<TS>(gz.x);
-                o[a.d_h] = from_f32<TS>(gr.x);
-                o[2 * a.d_h] = from_f32<TS>(gc.x);
-            }
-            if (vu) {
-                TS *o = gP + (row + HALF) * 3 * a.d_h + u;
-                o[0] = from_f32<TS>(gz.y);
-                o[a.d_h] = from_f32<TS>(gr.y);
-                o[2 * a.d_h] = from_f32<TS>(gc.y);
-            }
-        }
+        // dL/dP of both rows goes into the P tile, whose values are no longer
+        // read (rows past T and units past d_h are clipped by the store)
+        const int rl = r0 + i, ru = rl + HALF;
+        Ps[(0 * L + rl) * U + lane] = from_f32<TS>(gz.x);
+        Ps[(1 * L + rl) * U + lane] = from_f32<TS>(gr.x);
+        Ps[(2 * L + rl) * U + lane] = from_f32<TS>(gc.x);
+        Ps[(0 * L + ru) * U + lane] = from_f32<TS>(gz.y);
+        Ps[(1 * L + ru) * U + lane] = from_f32<TS>(gr.y);
+        Ps[(2 * L + ru) * U + lane] = from_f32<TS>(gc.y);
     }
     s_red[0][warp][lane] = g_az.x + g_az.y;
     s_red[1][warp][lane] = g_ar.x + g_ar.y;
@@ -259,7 +265,13 @@ __global__ void __launch_bounds__(NW * 32, 4)
     s_red[3][warp][lane] = g_bz.x + g_bz.y;
     s_red[4][warp][lane] = g_br.x + g_br.y;
     s_red[5][warp][lane] = g_bc.x + g_bc.y;
+    fence_proxy_async_smem();   // the staged dL/dP is visible to the TMA store
     __syncthreads();
+    if (tid == 0) {
+#pragma unroll
+        for (int g = 0; g < 3; ++g) tma_store_4d(&tmGP, Ps + g * L * U, u0, g, t0, b);
+        bulk_commit();
+    }
     if (uok) {   // warp w sums gate-parameters w, w + NW, ... over the NW warps
         for (int g = warp; g < 6; g += NW) {
             float s = 0.f;
@@ -268,11 +280,13 @@ __global__ void __launch_bounds__(NW * 32, 4)
             atomicAdd(a.gparams + g * a.d_h + u, s);
         }
     }
+    if (tid == 0) bulk_wait_read<0>();   // the tile outlives the store's reads
 }
 
 template <typename TS>
 cudaError_t launch_bw(const CUtensorMap &tmP, const CUtensorMap &tmH, const CUtensorMap &tmG,
-                      const BackwardArgs &a, int64_t n_ctas, cudaStream_t stream) {
+                      const CUtensorMap &tmGP, const BackwardArgs &a, int64_t n_ctas,
+                      cudaStream_t stream) {
     static std::atomic<unsigned long long> configured{0};
     constexpr size_t smem = static_cast<size_t>(5) * L * U * sizeof(TS);
     cudaError_t e = once_per_device(configured, [](int) {
@@ -280,17 +294,17 @@ cudaError_t launch_bw(const CUtensorMap &tmP, const CUtensorMap &tmH, const CUte
                                     static_cast<int>(smem));
     });
     if (e != cudaSuccess) return e;
-    k_backward<TS><<<static_cast<unsigned>(n_ctas), NW * 32, smem, stream>>>(tmP, tmH, tmG, a);
+    k_backward<TS><<<static_cast<unsigned>(n_ctas), NW * 32, smem, stream>>>(tmP, tmH, tmG, tmGP, a);
     return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_backward(int dtype, const CUtensorMap &tmP, const CUtensorMap &tmH,
-                            const CUtensorMap &tmG, const BackwardArgs &a, int64_t n_ctas,
-                            cudaStream_t stream) {
-    if (dtype == 1) return launch_bw<__nv_bfloat16>(tmP, tmH, tmG, a, n_ctas, stream);
-    return launch_bw<float>(tmP, tmH, tmG, a, n_ctas, stream);
+                            const CUtensorMap &tmG, const CUtensorMap &tmGP, const BackwardArgs &a,
+                            int64_t n_ctas, cudaStream_t stream) {
+    if (dtype == 1) return launch_bw<__nv_bfloat16>(tmP, tmH, tmG, tmGP, a, n_ctas, stream);
+    return launch_bw<float>(tmP, tmH, tmG, tmGP, a, n_ctas, stream);
 }
 
 }  // namespace nrnn

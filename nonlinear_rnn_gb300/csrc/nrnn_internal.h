@@ -55,7 +55,6 @@ struct NewtonArgs {
 struct BackwardArgs {
     const void *H;                // (B, T, d_h) trajectory the derivatives are taken at
     const void *gH;               // (B, T, d_h) dL/dH
-    void *gP;                     // (B, T, 3 d_h) dL/dP (out)
     float *gparams;               // (6, d_h) dL/d(params), accumulated (zeroed by the caller)
     const float *params;
     const int32_t *cu;
@@ -68,9 +67,11 @@ struct BackwardArgs {
     unsigned long long wait_ns;
 };
 
+// tmP, tmH, tmG: load maps as for the Newton kernel (tile boxes of P, H, dL/dH);
+// tmGP: 4-D store map over dL/dP as (d_h, 3, T, B) with a (32, 1, 64, 1) box.
 cudaError_t launch_backward(int dtype, const CUtensorMap &tmP, const CUtensorMap &tmH,
-                            const CUtensorMap &tmG, const BackwardArgs &a, int64_t n_ctas,
-                            cudaStream_t stream);
+                            const CUtensorMap &tmG, const CUtensorMap &tmGP, const BackwardArgs &a,
+                            int64_t n_ctas, cudaStream_t stream);
 
 // Workspace of one call: [counters | error] and [slots], cleared together by
 // one memset (zero_bytes from the start), then (per-iteration variant, K > 1)
