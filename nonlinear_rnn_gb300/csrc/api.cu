@@ -52,6 +52,28 @@ SyncLayout layout(int64_t B, int64_t T, int64_t d_h, int dtype, int K, bool fuse
     return s;
 }
 
+// The per-call clears of a forward or backward as one kernel instead of two
+// memset nodes: the workspace's synchronisation area (counters, error word,
+// look-back slots; bytes a multiple of 16) and a small output (the residual
+// word, or the parameter gradients; bytes a multiple of 4).
+__global__ void k_clear(uint4 *ws, size_t ws16, uint32_t *out, size_t out4) {
+    const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
+    const size_t i0 = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    for (size_t i = i0; i < ws16; i += stride) ws[i] = make_uint4(0u, 0u, 0u, 0u);
+    for (size_t i = i0; i < out4; i += stride) out[i] = 0u;
+}
+
+cudaError_t clear_for_call(void *ws, size_t ws_bytes, void *out, size_t out_bytes,
+                           cudaStream_t stream) {
+    const size_t ws16 = ws_bytes / 16, out4 = out_bytes / 4;
+    const size_t n = ws16 > out4 ? ws16 : out4;
+    if (n == 0) return cudaSuccess;
+    const size_t blocks = (n + 255) / 256;
+    k_clear<<<static_cast<unsigned>(blocks < 1216 ? blocks : 1216), 256, 0, stream>>>(
+        static_cast<uint4 *>(ws), ws16, static_cast<uint32_t *>(out), out4);
+    return cudaGetLastError();
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
     static std::once_flag once;
@@ -279,8 +301,7 @@ int nrnn_newton_forward_init(const void *preact, int dtype, const float *params,
 
     // one memset clears counters, error word and slots; rho accumulates by
     // atomicMax into residual_dev
-    cudaError_t e = cudaMemsetAsync(ws, 0, ly.zero_bytes, stream);
-    if (e == cudaSuccess) e = cudaMemsetAsync(residual_dev, 0, sizeof(float), stream);
+    cudaError_t e = clear_for_call(ws, ly.zero_bytes, residual_dev, sizeof(float), stream);
     if (e != cudaSuccess) return NRNN_ERR_CUDA;
 
     if (B * T > 0) {
@@ -369,8 +390,7 @@ int nrnn_newton_forward_x(const void *x, const void *W_x, int dtype, const float
     cudaStream_t stream = static_cast<cudaStream_t>(stream_);
     unsigned char *ws = static_cast<unsigned char *>(workspace);
     uint32_t *err = reinterpret_cast<uint32_t *>(ws + ly.error_off);
-    cudaError_t e = cudaMemsetAsync(ws, 0, ly.zero_bytes, stream);
-    if (e == cudaSuccess) e = cudaMemsetAsync(residual_dev, 0, sizeof(float), stream);
+    cudaError_t e = clear_for_call(ws, ly.zero_bytes, residual_dev, sizeof(float), stream);
     if (e != cudaSuccess) return NRNN_ERR_CUDA;
     if (B * T > 0) {
         CUtensorMap tmX, tmW;
@@ -421,10 +441,9 @@ int nrnn_newton_backward(const void *preact, int dtype, const float *params, int
         return NRNN_ERR_WORKSPACE;
     cudaStream_t stream = static_cast<cudaStream_t>(stream_);
     unsigned char *ws = static_cast<unsigned char *>(workspace);
-    cudaError_t e = cudaMemsetAsync(gparams, 0, sizeof(float) * 6 * d_h, stream);
-    if (e != cudaSuccess) return NRNN_ERR_CUDA;
-    if (B * T == 0) return NRNN_OK;
-    e = cudaMemsetAsync(ws, 0, ly.zero_bytes, stream);
+    if (B * T == 0)
+        return cuda_status(cudaMemsetAsync(gparams, 0, sizeof(float) * 6 * d_h, stream));
+    cudaError_t e = clear_for_call(ws, ly.zero_bytes, gparams, sizeof(float) * 6 * d_h, stream);
     if (e != cudaSuccess) return NRNN_ERR_CUDA;
     CUtensorMap tmP, tmH, tmG, tmGP;
     if (!make_map(&tmP, preact, dtype, 3 * d_h, T, B) || !make_map(&tmH, H, dtype, d_h, T, B) ||
