@@ -195,7 +195,8 @@ def run_ours(args, w, rank, world, local):
                                  out=H, workspace=ws)
 
     def graphed(a):
-        """The forward (per-call memsets + kernels) captured once as a CUDA graph."""
+        """The forward (the per-call clear kernel + the Newton kernels) captured once as a
+        CUDA graph."""
         newton_call(a)
         torch.cuda.synchronize()
         g = torch.cuda.CUDAGraph()
@@ -408,7 +409,8 @@ def run_ours(args, w, rank, world, local):
         "e2e": {"value": tokens * world / (e2e_ms * 1e-3), "unit": "tokens/s",
                 "h2d_bytes_per_step": P.numel() * P.element_size(),
                 "d2h_bytes_per_step": H.numel() * H.element_size() + 4},
-        "gpu_launches": launches * args.steps,
+        # per step: the clear kernel of the call's workspace, then the Newton launch(es)
+        "gpu_launches": (launches + 1) * args.steps,
         "with_projection": {"projection_ms": proj,
                             "tokens_per_s": tokens * world / ((ms + proj) * 1e-3),
                             "fused_in_kernel": fused_x},

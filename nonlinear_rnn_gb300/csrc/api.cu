@@ -32,7 +32,7 @@ bool ranges_overlap(const void *a, size_t a_bytes, const void *b, size_t b_bytes
 bool overlaps(const void *a, const void *b, size_t bytes) { return ranges_overlap(a, bytes, b, bytes); }
 
 // Workspace: [counters (K+1) u32 | error u32], then [slots K x n_tiles x 32
-// u64], both cleared by one memset per call, then (per-iteration, K > 1) one
+// u64], both cleared by one kernel per call, then (per-iteration, K > 1) one
 // H buffer.
 SyncLayout layout(int64_t B, int64_t T, int64_t d_h, int dtype, int K, bool fused) {
     SyncLayout s{};
@@ -299,7 +299,7 @@ int nrnn_newton_forward_init(const void *preact, int dtype, const float *params,
     uint32_t *err = reinterpret_cast<uint32_t *>(ws + ly.error_off);
     const int S = static_cast<int>(cu_seqlens ? num_segments : 0);
 
-    // one memset clears counters, error word and slots; rho accumulates by
+    // one kernel clears counters, error word, slots and rho; rho accumulates by
     // atomicMax into residual_dev
     cudaError_t e = clear_for_call(ws, ly.zero_bytes, residual_dev, sizeof(float), stream);
     if (e != cudaSuccess) return NRNN_ERR_CUDA;

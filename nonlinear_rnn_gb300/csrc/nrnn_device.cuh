@@ -538,8 +538,8 @@ __device__ __forceinline__ float pair_b(unsigned long long v) {
 
 // ------------------------------------------------- decoupled look-back slots
 // One 64-bit word per (chunk, unit) holds the chunk's affine pair (A, b) and is
-// its own ready flag: SLOT_EMPTY (all zero bits, from the one per-call memset
-// that also clears the counters) means not yet published.  Published pairs
+// its own ready flag: SLOT_EMPTY (all zero bits, from the per-call clear that
+// also zeroes the counters) means not yet published.  Published pairs
 // never take that value: publish() writes the pair (+0, +0) as (+0, -0),
 // which composes identically.  Because a 64-bit aligned access is single-copy
 // atomic, a reader sees either SLOT_EMPTY, the chunk aggregate, or the

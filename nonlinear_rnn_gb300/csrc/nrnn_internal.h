@@ -73,9 +73,9 @@ cudaError_t launch_backward(int dtype, const CUtensorMap &tmP, const CUtensorMap
                             const CUtensorMap &tmG, const CUtensorMap &tmGP, const BackwardArgs &a,
                             int64_t n_ctas, cudaStream_t stream);
 
-// Workspace of one call: [counters | error] and [slots], cleared together by
-// one memset (zero_bytes from the start), then (per-iteration variant, K > 1)
-// one H buffer.
+// Workspace of one call: [counters | error] and [slots], cleared together at
+// the start of every call (zero_bytes from the start), then (per-iteration
+// variant, K > 1) one H buffer.
 struct SyncLayout {
     size_t counters_off, error_off, zero_bytes;
     size_t slots_off, slots_bytes, hbuf_off, total;
