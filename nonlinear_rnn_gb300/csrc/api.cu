@@ -57,6 +57,9 @@ SyncLayout layout(int64_t B, int64_t T, int64_t d_h, int dtype, int K, bool fuse
 // look-back slots; bytes a multiple of 16) and a small output (the residual
 // word, or the parameter gradients; bytes a multiple of 4).
 __global__ void k_clear(uint4 *ws, size_t ws16, uint32_t *out, size_t out4) {
+    // the Newton kernel that follows may be scheduled now; it waits for this
+    // grid's completion (griddepcontrol.wait) before it touches memory
+    asm volatile("griddepcontrol.launch_dependents;");
     const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
     const size_t i0 = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     for (size_t i = i0; i < ws16; i += stride) ws[i] = make_uint4(0u, 0u, 0u, 0u);

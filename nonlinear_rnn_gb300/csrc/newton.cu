@@ -193,8 +193,8 @@ __global__ void __launch_bounds__(NW * 32, 8)
                                  : dsmem_raw;
     // FUSED: [3][L][U] fp32 pre-scaled arguments (a bf16 tile lands by TMA in
     // the upper half and is widened in place), then, with an initial iterate,
-    // its [L][U] tile.  Per-iteration: [3][L][U] raw preactivations followed by
-    // the [L][U] tile of H^(k-1), both of type TS.
+    // its [L][U] tile.  Per-iteration: [3][L][U] raw preactivations of type TS,
+    // then (bf16) the [L][U] tile of H^(k-1); fp32 reads H^(k-1) into registers.
     float *Pf = reinterpret_cast<float *>(dsmem);
     TS *Pt = FUSED ? reinterpret_cast<TS *>(dsmem + (sizeof(TS) == 2 ? 3 * L * U * 2 : 0))
                    : reinterpret_cast<TS *>(dsmem);
@@ -210,6 +210,13 @@ __global__ void __launch_bounds__(NW * 32, 8)
     __shared__ uint32_t s_red[NW];
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    constexpr bool REG_H = !FUSED && sizeof(TS) == 4;   // H^(k-1) in registers, not a tile
+    // launched as a dependent of the kernel before it on the stream (the
+    // workspace clear, or the previous iteration): every access to memory lies
+    // behind the wait; the next iteration's CTAs may be scheduled as soon as
+    // all of this grid's have started, and wait for its completion in turn
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;");
     if (tid == 0) {
         // tickets run chunk-major: every chunk this tile's look-back waits for
         // belongs to a CTA that has already started
@@ -238,12 +245,14 @@ __global__ void __launch_bounds__(NW * 32, 8)
         } else {
             mbar_init(&s_bar, 1);
             fence_mbar_init();
-            const uint32_t bytes = (3u + (load_h ? 1u : 0u)) * L * U * sizeof(TS);
+            // the fp32 per-iteration kernel reads H^(k-1) straight into registers
+            const bool tile_h = !REG_H && load_h;
+            const uint32_t bytes = (3u + (tile_h ? 1u : 0u)) * L * U * sizeof(TS);
             mbar_arrive_expect_tx(&s_bar, bytes);
 #pragma unroll
             for (int g = 0; g < 3; ++g)
                 tma_load_3d(Pt + g * L * U, &tmP, &s_bar, g * a.d_h + u0, t0, b);
-            if (load_h) tma_load_3d(Hs, &tmH, &s_bar, u0, t0, b);
+            if (tile_h) tma_load_3d(Hs, &tmH, &s_bar, u0, t0, b);
         }
         mark_heads(a.cu, a.S, t0, L, s_heads);
     }
@@ -268,6 +277,28 @@ __global__ void __launch_bounds__(NW * 32, 8)
     if (load_h && warp == 0 && t0 > 0 && uok)
         hb = to_f32(reinterpret_cast<const TS *>(a.H_prev)[(static_cast<size_t>(b) * a.T + t0 - 1) *
                                                                a.d_h + u]);
+    // fp32 per-iteration: H^(k-1) of this warp's rows goes straight into
+    // registers (one 128-byte row per warp load), in flight together with the
+    // P tile's TMA; rows past T and units past d_h read as 0.  Keeping it out
+    // of shared memory leaves room for 8 CTAs per SM (bf16 tiles fit 8 with
+    // it, and its 2-byte loads were slower than the TMA tile).
+    float2 Hreg[HALF];
+    if constexpr (REG_H) {
+#pragma unroll
+        for (int j = 0; j < HALF; ++j) Hreg[j] = splat2(0.f);
+        if (load_h && uok) {
+            const TS *Hp = reinterpret_cast<const TS *>(a.H_prev) +
+                           (static_cast<size_t>(b) * a.T + t0) * a.d_h + u;
+            const int rows = a.T - t0;   // rows of this chunk inside the sequence
+#pragma unroll
+            for (int j = 0; j < HALF; ++j) {
+                if (r0 + j < rows) Hreg[j].x = to_f32(Hp[static_cast<size_t>(r0 + j) * a.d_h]);
+                if (r0 + HALF + j < rows)
+                    Hreg[j].y = to_f32(Hp[static_cast<size_t>(r0 + HALF + j) * a.d_h]);
+            }
+            if (warp > 0 && r0 - 1 < rows) hb = to_f32(Hp[static_cast<size_t>(r0 - 1) * a.d_h]);
+        }
+    }
     __syncthreads();   // barriers initialised, head bits visible
     if constexpr (XPROJ) {
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
@@ -368,9 +399,10 @@ __global__ void __launch_bounds__(NW * 32, 8)
     float2 G[HALF];   // H of this warp's rows (between iterations) / g_t (inside), in pairs
 #pragma unroll
     for (int j = 0; j < HALF; ++j)
-        G[j] = load_h ? make_float2(to_f32(Hs[(r0 + j) * U + lane]), to_f32(Hs[(r0 + HALF + j) * U + lane]))
-                      : splat2(0.f);
-    if (load_h && warp > 0) hb = to_f32(Hs[(r0 - 1) * U + lane]);
+        G[j] = REG_H ? Hreg[j]
+               : load_h ? make_float2(to_f32(Hs[(r0 + j) * U + lane]), to_f32(Hs[(r0 + HALF + j) * U + lane]))
+                        : splat2(0.f);
+    if (!REG_H && load_h && warp > 0) hb = to_f32(Hs[(r0 - 1) * U + lane]);
     const uint32_t hm = (s_heads[r0 >> 5] >> (r0 & 31)) & ((1u << SEG) - 1u);
     const int nvalid = min(SEG, a.T - (t0 + r0));
     const bool general = (hm != 0u) || (nvalid < SEG);
@@ -382,11 +414,11 @@ __global__ void __launch_bounds__(NW * 32, 8)
     for (int k = a.k_first; k <= a.k_last; ++k) {
         float2 J2[HALF];
         float A_lo, B_lo, A, Bv;
-        if (FUSED && k == 1 && !load_h) {
+        if (k == 1 && !load_h) {   // from H^(0) = 0: every shifted state is 0
             if (general)
-                warp_pairs<TS, true, true, true>(Pv, warp, lane, G, hb, hm, nvalid, prm2, J2, A_lo, B_lo, A, Bv);
+                warp_pairs<TS, FUSED, true, true>(Pv, warp, lane, G, hb, hm, nvalid, prm2, J2, A_lo, B_lo, A, Bv);
             else
-                warp_pairs<TS, true, false, true>(Pv, warp, lane, G, hb, hm, nvalid, prm2, J2, A_lo, B_lo, A, Bv);
+                warp_pairs<TS, FUSED, false, true>(Pv, warp, lane, G, hb, hm, nvalid, prm2, J2, A_lo, B_lo, A, Bv);
         } else if (general) {
             warp_pairs<TS, FUSED, true>(Pv, warp, lane, G, hb, hm, nvalid, prm2, J2, A_lo, B_lo, A, Bv);
         } else {
@@ -543,7 +575,7 @@ __global__ void k_bounded_wait(const uint32_t *flag, uint64_t wait_ns, uint32_t 
 template <typename TS, bool FUSED>
 size_t smem_bytes_for(bool with_h) {
     return FUSED ? static_cast<size_t>(3) * L * U * sizeof(float) + (with_h ? L * U * sizeof(TS) : 0)
-                 : static_cast<size_t>(4) * L * U * sizeof(TS);
+                 : static_cast<size_t>(sizeof(TS) == 4 ? 3 : 4) * L * U * sizeof(TS);
 }
 
 template <typename TS, bool FUSED>
@@ -556,9 +588,8 @@ cudaError_t launch_one(const CUtensorMap &tmP, const CUtensorMap &tmH, const CUt
                                     static_cast<int>(smem_bytes_for<TS, FUSED>(true)));
     });
     if (e != cudaSuccess) return e;
-    k_newton<TS, FUSED><<<static_cast<unsigned>(n_ctas), NW * 32, smem, stream>>>(tmP, tmH, tmO,
-                                                                                tmP, tmP, a);
-    return cudaGetLastError();
+    return launch_dependent(k_newton<TS, FUSED>, static_cast<unsigned>(n_ctas), NW * 32, smem, stream,
+                            tmP, tmH, tmO, tmP, tmP, a);
 }
 
 cudaError_t launch_x(const CUtensorMap &tmX, const CUtensorMap &tmW, const CUtensorMap &tmO,
@@ -571,9 +602,8 @@ cudaError_t launch_x(const CUtensorMap &tmX, const CUtensorMap &tmW, const CUten
                                     cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     });
     if (e != cudaSuccess) return e;
-    k_newton<__nv_bfloat16, true, true><<<static_cast<unsigned>(n_ctas), NW * 32, smem, stream>>>(
-        tmX, tmX, tmO, tmX, tmW, a);
-    return cudaGetLastError();
+    return launch_dependent(k_newton<__nv_bfloat16, true, true>, static_cast<unsigned>(n_ctas),
+                            NW * 32, smem, stream, tmX, tmX, tmO, tmX, tmW, a);
 }
 
 }  // namespace

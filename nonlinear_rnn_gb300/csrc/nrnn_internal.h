@@ -13,6 +13,27 @@ namespace nrnn {
 // Runs configure(device) for the current device unless it already succeeded
 // there (kernel attributes are per device).  Ordinals >= 64 configure on every
 // call.
+// Launch with programmatic stream serialization: the kernel may be scheduled
+// while the kernel before it on the stream finishes (once that kernel's CTAs
+// have all executed griddepcontrol.launch_dependents, or exited); it executes
+// griddepcontrol.wait, which returns when that kernel has completed and its
+// writes are visible, before touching memory.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_dependent(void (*kernel)(KArgs...), unsigned grid, unsigned block,
+                                    size_t smem, cudaStream_t stream, Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(block);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args &&>(args)...);
+}
+
 template <typename Fn>
 inline cudaError_t once_per_device(std::atomic<unsigned long long> &done, Fn &&configure) {
     int dev = 0;
