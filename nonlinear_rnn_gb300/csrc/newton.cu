@@ -180,8 +180,13 @@ __device__ __forceinline__ float residual_rows(const float *Pf, const TS *Pt, in
 // TMA ring that aliases the P' tile; warps 0..2 then read their gate's lanes
 // (tcgen05.ld: lane = unit, registers = time), round to bf16 as a stored
 // preactivation would be, and write the pre-scaled arguments.
+// CTAs per SM: 8 (64 registers); the bf16 per-iteration kernel runs 9 (56
+// registers, a few spills in its prologue), which measured faster than 8
+template <typename TS, bool FUSED>
+constexpr int newton_min_blocks() { return (!FUSED && sizeof(TS) == 2) ? 9 : 8; }
+
 template <typename TS, bool FUSED, bool XPROJ = false>
-__global__ void __launch_bounds__(NW * 32, 8)
+__global__ void __launch_bounds__(NW * 32, newton_min_blocks<TS, FUSED>())
     k_newton(const __grid_constant__ CUtensorMap tmP, const __grid_constant__ CUtensorMap tmH,
              const __grid_constant__ CUtensorMap tmO, const __grid_constant__ CUtensorMap tmX,
              const __grid_constant__ CUtensorMap tmW, const NewtonArgs a) {
