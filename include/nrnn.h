@@ -168,7 +168,8 @@ int nrnn_newton_forward_x(const void *x, const void *W_x, int dtype, const float
  * derivatives taken at (H_{t-1}, P_t) (H_{-1} = 0 at heads).  Solved by the
  * same chunked decoupled look-back scan as the forward, in reverse time.
  *   H, gH     device, (B, T, d_h) of dtype, 16-byte aligned
- *   gP        device, (B, T, 3 d_h) of dtype (out)
+ *   gP        device, (B, T, 3 d_h) of dtype, 16-byte aligned (out; written by
+ *             TMA stores of whole gate blocks)
  *   gparams   device, fp32 (6, d_h) (out; overwritten)
  *   workspace >= nrnn_newton_workspace_bytes(B, T, d_h, dtype, 1, NRNN_ALGO_FUSED)
  * Results are accumulated with atomics: within float rounding, not bitwise
@@ -225,7 +226,9 @@ int nrnn_residual(const void *preact, int dtype, const float *params, int64_t B,
  *   h_in    device, (slots, d_h) of dtype, or NULL for the zero state
  *   h_out   device, (slots, d_h) of dtype; may be h_in (in place), must not
  *           overlap preact
- * No alignment or d_h restriction.
+ * No alignment or d_h restriction; with d_h a multiple of 4 (fp32) or 8
+ * (bf16) and preact, params, h_in, h_out 16-byte aligned the step runs on
+ * 16-byte vectors, else one element per thread (same results).
  */
 int nrnn_decode_step(const void *preact, int dtype, const float *params, int64_t slots,
                      int64_t d_h, const void *h_in, void *h_out, void *stream);
