@@ -12,13 +12,15 @@
 //
 // Same tiling as the Newton kernel (32 units x NEWTON_L steps, NEWTON_NW warps
 // x 16 steps) run backwards in time: tiles of P, H and gH land in shared memory by TMA;
-// each thread composes the maps nu_{t+1} -> nu_t = (J_t, J_t gH_t) of its rows
-// from the last upwards; warp aggregates meet in shared memory; warp 0
-// publishes the chunk aggregate and completes a decoupled look-back over
+// each thread takes its rows as pairs (i, i + 8) on packed f32x2 arithmetic with
+// the storage type's cell and composes the maps nu_{t+1} -> nu_t = (J_t, J_t gH_t)
+// of each half from the last row upwards; warp aggregates meet in shared memory;
+// warp 0 publishes the chunk aggregate and completes a decoupled look-back over
 // LATER chunks (tickets are handed out from the last chunk backwards, so every
-// chunk waited for has started); the carry nu at the chunk end is then applied
-// and dL/dP written.  Parameter gradients are reduced over the CTA and added
-// with one atomicAdd per (gate, unit).  Every wait is bounded.
+// chunk waited for has started); the carry nu at the chunk end is then applied,
+// dL/dP staged in the P tile and stored by TMA.  Parameter gradients are reduced
+// over the CTA and added with one atomicAdd per (gate, unit).  Every wait is
+// bounded.
 #include "nrnn_device.cuh"
 #include "nrnn_internal.h"
 #include "tcgen05.cuh"
