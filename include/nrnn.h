@@ -25,7 +25,12 @@
  *     Parameters are always fp32.
  *   - params: device, fp32, shape (6, d_h): rows a_z, a_r, a_c, b_z, b_r, b_c.
  *   - stream: a cudaStream_t (NULL = legacy default stream).  Calls are
- *     asynchronous on that stream unless stated otherwise.
+ *     asynchronous on that stream unless stated otherwise.  The Newton
+ *     kernels are launched with programmatic stream serialization and signal
+ *     their dependents early: a kernel the caller launches after them with
+ *     that launch attribute must execute griddepcontrol.wait (as programmatic
+ *     dependent launch requires) before it reads their outputs.  Ordinary
+ *     launches, copies and events after a call are ordered as usual.
  *   - cu_seqlens (nullable): device int32 array of num_segments + 1 offsets
  *     for a ragged pack; then B must be 1 and T is the packed length N.  The
  *     offsets must satisfy cu[0] = 0, cu[i] <= cu[i+1], cu[S] = N; check
