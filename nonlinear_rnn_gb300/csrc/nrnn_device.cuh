@@ -318,19 +318,38 @@ __device__ __forceinline__ void gates2(float2 h, float2 sz, float2 sr, float2 sc
     c = fma2(splat2(-2.0f), q, one);
 }
 
+// gates2 with two signs folded in, for the Jacobian below: z, mr = -r, c and
+// mq = -q.  -(1 + 2^x) costs the same one fma as 1 + 2^x, and the negated
+// values save the (1 - r), (1 - q) steps of the derivative (r (1 - r) =
+// -(mr + mr^2), q (1 - q) = -(mq + mq^2)).  nh = -h.
+__device__ __forceinline__ void gates2_neg(float2 h, float2 nh, float2 sz, float2 sr, float2 sc,
+                                           const ScaledParams2 &p, float2 &z, float2 &mr,
+                                           float2 &c, float2 &mq) {
+    const float2 one = splat2(1.0f), mone = splat2(-1.0f);
+    const float2 dz = add2(ex2_2(clamp2(fma2(p.na_z, h, sz))), one);
+    mr = rcp_2(fma2(ex2_2(fma2(p.na_r, h, sr)), mone, mone));
+    const float2 mdc = fma2(ex2_2(clamp2(fma2(p.a_c2, mul2(mr, nh), sc))), mone, mone);
+    const float2 minv = rcp_2(mul2(dz, mdc));   // -1 / (dz dc)
+    z = mul2(mdc, minv);
+    mq = mul2(dz, minv);
+    c = fma2(splat2(2.0f), mq, one);
+}
+
 // J = df/dh and the Newton pair's offset g = f(h) - J h for a pair of shifted
 // states.  With inner = (1 - z) a_z (c - h) + (1 - c^2) a_c d(rh)/dh one has
 // J = (1 - z) + z inner = 1 + z (inner - 1) and f - J h = z (c - h inner)
-// = z ((c - h) - h (inner - 1)); the kernels use inner - 1 directly.
+// = z ((c - h) - h (inner - 1)); the kernels use inner - 1 directly.  With
+// D = -d(rh)/dh = mr + h a_r (mr + mr^2) and 1 - c^2 = 4 q (1 - q):
+// (1 - c^2) a_c d(rh)/dh = 4 a_c (mq + mq^2) D.
 __device__ __forceinline__ void cell_jg2(float2 h, float2 sz, float2 sr, float2 sc,
                                          const ScaledParams2 &p, float2 &J, float2 &g) {
-    float2 z, r, c, q;
-    gates2(h, sz, sr, sc, p, z, r, c, q);
     const float2 one = splat2(1.0f), mone = splat2(-1.0f);
     const float2 nh = mul2(h, mone);
+    float2 z, mr, c, mq;
+    gates2_neg(h, nh, sz, sr, sc, p, z, mr, c, mq);
     const float2 cmh = add2(c, nh);
-    const float2 dq = fma2(mul2(mul2(h, p.a_r), fma2(r, mone, one)), r, r);   // d(r h)/dh
-    const float2 t3m1 = fma2(mul2(mul2(q, p.a_c4), fma2(q, mone, one)), dq, mone);   // (1 - c^2) a_c dq - 1
+    const float2 D = fma2(mul2(h, p.a_r), fma2(mr, mr, mr), mr);
+    const float2 t3m1 = fma2(mul2(p.a_c4, fma2(mq, mq, mq)), D, mone);   // (1 - c^2) a_c dq - 1
     const float2 im1 = fma2(fma2(z, p.ma_z, p.a_z), cmh, t3m1);           // inner - 1
     J = fma2(z, im1, one);
     g = mul2(z, fma2(nh, im1, cmh));
@@ -341,13 +360,13 @@ __device__ __forceinline__ void cell_jg2_at_zero(float2 sz, float2 sr, float2 sc
                                                  const ScaledParams2 &p, float2 &J, float2 &g) {
     const float2 one = splat2(1.0f), mone = splat2(-1.0f);
     const float2 dz = add2(ex2_2(clamp2(sz)), one);
-    const float2 r = rcp_2(add2(ex2_2(sr), one));
-    const float2 dc = add2(ex2_2(clamp2(sc)), one);
-    const float2 inv = rcp_2(mul2(dz, dc));
-    const float2 z = mul2(dc, inv);
-    const float2 q = mul2(dz, inv);
-    const float2 c = fma2(splat2(-2.0f), q, one);
-    const float2 t3m1 = fma2(mul2(mul2(q, p.a_c4), fma2(q, mone, one)), r, mone);
+    const float2 mr = rcp_2(fma2(ex2_2(sr), mone, mone));
+    const float2 mdc = fma2(ex2_2(clamp2(sc)), mone, mone);
+    const float2 minv = rcp_2(mul2(dz, mdc));
+    const float2 z = mul2(mdc, minv);
+    const float2 mq = mul2(dz, minv);
+    const float2 c = fma2(splat2(2.0f), mq, one);
+    const float2 t3m1 = fma2(mul2(p.a_c4, fma2(mq, mq, mq)), mr, mone);   // (1 - c^2) a_c r - 1
     J = fma2(z, fma2(fma2(z, p.ma_z, p.a_z), c, t3m1), one);
     g = mul2(z, c);
 }
