@@ -5,15 +5,19 @@ python bench.py [--gpus N] [--steps K] [--warmup W] [--workload I] [--algo A]
 
 A step is one Newton forward over one batch of the workload: K iterations of
 cell + Jacobian + residual + affine scan and the final residual gate
-(nrnn_newton_forward), preactivations resident in HBM.  The input projection
-is timed beside it (``with_projection``).  Prints one JSON line on rank 0.
+(nrnn_newton_forward), preactivations resident in HBM.  The default workload
+is the largest single-GPU configuration (diagonal GRU, bf16 storage with fp32
+math, B16 T16384 d_in = d_h = 1024, K = 3; the ragged N262144 d512 fp32 pack
+moves the same bytes and is timed beside it under ``other_workloads``).  The
+input projection is timed beside the forward (``with_projection``).  Prints
+one JSON line on rank 0.
 
 Under torchrun each rank runs its own replica of the workload on its own GPU
 (the batch rows are independent; there is no collective on the data path):
 weak scaling, value = tokens of all ranks / max over ranks of the time.
 
-``--impl reference`` times the float64 CPU oracle (the reference
-implementation of this method here) on a bounded sample of the same
+``--impl reference`` times the float64 CPU oracle's sequential unroll (the
+definition the Newton forward must reproduce) on a bounded sample of the same
 workload on the host cores, rank 0 only.
 """
 from __future__ import annotations
@@ -149,6 +153,75 @@ def workload_bytes(w, algo):
 # ex2-equivalent operations.
 MUFU_PER_EVAL = {"f32": {"ex2": 3, "rcp": 2}, "bf16": {"tanh": 3}}
 SM_MAX_MHZ = 2070.0
+DEFAULT_WORKLOAD = 3
+CPU_SAMPLE_BYTES = 256 << 20
+
+
+def mhz_of(clocks):
+    return clocks.get("sm_mhz") or clocks.get("sm_max_mhz") or SM_MAX_MHZ
+
+
+def xu_work(w, rates):
+    """ex2-equivalent MUFU operations of one fused forward."""
+    mix = MUFU_PER_EVAL[w.dtype]
+    per_eval = sum(n * rates["ex2"] / rates[op] for op, n in mix.items())
+    return per_eval * (w.K + 1) * w.B * w.T * w.d_h
+
+
+def time_workload(torch, nr, w, args, dev, flush, stream, xu_rates, props, mhz):
+    """Fused and per-iteration forward of workload w (CUDA-graph replays, L2
+    flushed between steps): ms, tokens/s, the fused kernel's MUFU fraction and
+    the per-iteration kernel's HBM fraction."""
+    P = syn.preact_uniform_torch(w, device=dev)
+    inp = syn.make_inputs(w, with_x=False)
+    prm = nr.params_tensor(inp["params"], w.d_h, dev)
+    cu = None if inp["cu_seqlens"] is None else nr.DeviceCuSeqlens(inp["cu_seqlens"], w.T, dev)
+    tdt = P.dtype
+    H = torch.empty((w.B, w.T, w.d_h), dtype=tdt, device=dev)
+    ws = torch.empty(max(nr.workspace_bytes(w.B, w.T, w.d_h, tdt, w.K, a) for a in ("fused", "per_iter")),
+                     dtype=torch.uint8, device=dev)
+    res = {"B": w.B, "T": w.T, "d_h": w.d_h, "K": w.K, "dtype": w.dtype,
+           "input": "preact drawn directly, U(-1, 1)"}
+    rates = dict(zip(("ex2", "rcp", "tanh"), xu_rates))
+    pk = peaks()
+    for algo in ("fused", "per_iter"):
+        def call(a=algo):
+            return nr.newton_forward(P, prm, cu_seqlens=cu, K=w.K, algo=a, check=False, out=H,
+                                     workspace=ws)
+        call()
+        torch.cuda.synchronize()
+        if args.graph:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                call()
+            step = g.replay
+        else:
+            step = call
+        for _ in range(args.warmup):
+            flush.fill_(1.0)
+            step()
+        ms_l, _ = time_steps(torch, step, max(3, min(args.steps, 10)), flush, stream, nvtx=False)
+        ms = sum(ms_l) / len(ms_l)
+        entry = {"ms": ms, "tokens_per_s": w.B * w.T / (ms * 1e-3)}
+        if algo == "fused":
+            peak = rates["ex2"] * props.multi_processor_count * mhz * 1e6 / 1e9
+            entry["alu_frac"] = xu_work(w, rates) / (ms * 1e-3) / 1e9 / peak
+            entry["hbm_frac"] = sum(workload_bytes(w, algo)) / (ms * 1e-3) / 1e9 / pk["hbm_gbs"]
+        else:
+            b = workload_bytes(w, algo)
+            entry["hbm_frac"] = (sum(b) / len(b)) / (ms / len(b) * 1e-3) / 1e9 / pk["hbm_gbs"]
+        res[algo] = entry
+    del P, H, ws
+    return res
+
+
+def bench_config(w, args, world):
+    """The workload and launch configuration (identical in both arms' lines)."""
+    return {"workload": w.name, "B": w.B, "T": w.T, "d_in": w.d_in, "d_h": w.d_h,
+            "K": w.K, "segments": w.segments, "algo": args.algo,
+            "parallelism": f"replica x{world}",
+            "launch": "CUDA graph replay of one forward" if args.graph else "eager launches",
+            "l2": f"flushed between steps ({L2_FLUSH_BYTES >> 20} MiB write, untimed)"}
 
 
 def time_steps(torch, fn, steps, flush, stream, nvtx=True):
@@ -265,7 +338,9 @@ def run_ours(args, w, rank, world, local):
         ex2_rate = rates["ex2"]
         xu_ops = per_eval * (w.K + 1) * tokens * w.d_h
         xu_achieved = xu_ops / (ms * 1e-3) / 1e9
-        mhz = clocks.get("sm_max_mhz") or SM_MAX_MHZ
+        # the SM clock the timed steps ran at (median of the samples taken
+        # during them), else the maximum clock
+        mhz = clocks.get("sm_mhz") or clocks.get("sm_max_mhz") or SM_MAX_MHZ
         xu_peak = ex2_rate * props.multi_processor_count * mhz * 1e6 / 1e9
         roof = {"bound": "alu", "achieved": xu_achieved, "peak": xu_peak,
                 "unit": "Gop/s (MUFU, ex2-equivalent)",
@@ -273,7 +348,7 @@ def run_ours(args, w, rank, world, local):
                 "algorithmic_ops_per_launch": xu_ops,
                 "peak_src": "measured " + ", ".join(f"{rates[k]:.2f} {k}" for k in rates)
                             + f" results/clk/SM (nrnn_probe_xu_rates) x {props.multi_processor_count} "
-                            f"SMs x {mhz:.0f} MHz (maximum SM clock); per evaluation "
+                            f"SMs x {mhz:.0f} MHz (median sampled SM clock); per evaluation "
                             + " + ".join(f"{n} {op}" for op, n in mix.items()),
                 "hbm": {k: hbm[k] for k in ("achieved", "peak", "unit", "frac",
                                             "algorithmic_bytes_per_launch")}}
@@ -386,6 +461,16 @@ def run_ours(args, w, rank, world, local):
         fx_ms, _ = time_steps(torch, fx_step, max(3, min(args.steps, 10)), flush, stream, nvtx=False)
         fused_x = {"ms": statistics.median(fx_ms),
                    "tokens_per_s": tokens * world / (statistics.median(fx_ms) * 1e-3)}
+    # the other multi-megabyte workloads, timed the same way on preactivations
+    # drawn directly on the device (U(-1, 1), the variance of x W_x^T)
+    others = {}
+    if not args.skip_others:
+        for oi in args.others:
+            if oi == args.workload:
+                continue
+            others[syn.WORKLOADS[oi].name] = time_workload(
+                torch, nr, syn.WORKLOADS[oi], args, dev, flush, stream, xu_rates, props, mhz_of(clocks))
+
     out = {
         "metric": METRIC,
         "value": tokens_all_ranks(tokens, world) / (ms * 1e-3),
@@ -399,11 +484,7 @@ def run_ours(args, w, rank, world, local):
         "vs_baseline": None,
         "dtype": w.dtype,
         "data": "synthetic (seeded SplitMix64: x~N(0,1), W_x~U(+-1/sqrt(d_in)), a~U(+-1), b=0)",
-        "config": {"workload": w.name, "B": w.B, "T": w.T, "d_in": w.d_in, "d_h": w.d_h,
-                   "K": w.K, "segments": w.segments, "algo": algo,
-                   "parallelism": f"replica x{world}",
-                   "launch": "CUDA graph replay of one forward" if args.graph else "eager launches",
-                   "l2": f"flushed between steps ({L2_FLUSH_BYTES >> 20} MiB write, untimed)"},
+        "config": bench_config(w, args, world),
         "roofline": roof,
         "per_iter_roofline": per_iter,
         "e2e": {"value": tokens * world / (e2e_ms * 1e-3), "unit": "tokens/s",
@@ -417,6 +498,7 @@ def run_ours(args, w, rank, world, local):
         "sequential_gpu": {"ms": statistics.median(seq_ms),
                            "tokens_per_s": tokens / (statistics.median(seq_ms) * 1e-3)},
         "next_rows": nxt or None,
+        "other_workloads": others or None,
         "residual": float(rho.item()),
         "wall_s": t_wall,
         "clocks": clocks,
@@ -452,10 +534,13 @@ def load_traffic(w, algo):
 
 
 def cpu_baseline(w, budget_s=10.0, steps=1):
-    """Times the float64 oracle (as it stands) on a bounded sample of the workload
-    on all host cores: whole rows of T steps for a subset of hidden units (units
-    are independent), as many rows and units as fit in about budget_s per pass.
-    Returns tokens/s scaled to full tokens (d_h units per token)."""
+    """Times the float64 oracle's sequential unroll h_t = f(h_{t-1}, P_t) (the
+    definition the Newton forward must reproduce; numerics contract,
+    "Invariant") as it stands, on all host cores, on a bounded sample of the
+    workload: whole rows of T steps (every segment of a pack, each from h = 0)
+    for a subset of hidden units, which are independent, as many rows and
+    units as fit in about budget_s per pass.  Returns tokens/s scaled to full
+    tokens (d_h units per token)."""
     import oracle
 
     cores = os.cpu_count() or 1
@@ -464,34 +549,38 @@ def cpu_baseline(w, budget_s=10.0, steps=1):
     cu = inp["cu_seqlens"]
     n0 = min(w.d_h, cores)
     units = np.arange(n0)
-    Pc = syn.preact_uniform_columns(w, units, rows=[0])
+    Pc = syn.preact_uniform_columns(w, units, rows=[0]).astype(np.float64)
     t = time.perf_counter()
-    oracle.newton(Pc, prm[:, units], w.K, cu_seqlens=cu, threads=cores)
+    oracle.sequential(Pc, prm[:, units], cu_seqlens=cu, threads=cores)
     t_unit_row = max(time.perf_counter() - t, 1e-4)     # one unit per core, one row
     waves = lambda n: -(-n // cores)                      # noqa: E731
+    # sample: whole rows, at most SAMPLE_BYTES of float64 preactivations
     n_units, n_rows = w.d_h, w.B
-    while n_rows > 1 and t_unit_row * waves(n_units) * n_rows > budget_s:
+    fits = lambda nu, nr: (t_unit_row * waves(nu) * nr <= budget_s and        # noqa: E731
+                           nu * nr * w.T * 3 * 8 <= CPU_SAMPLE_BYTES)
+    while n_rows > 1 and not fits(n_units, n_rows):
         n_rows -= 1
-    while n_units > 1 and t_unit_row * waves(n_units) * n_rows > budget_s:
+    while n_units > 1 and not fits(n_units, n_rows):
         n_units = max(1, n_units // 2)
     units = np.arange(n_units)
     rows = list(range(n_rows))
-    Pc = syn.preact_uniform_columns(w, units, rows=rows)
+    Pc = syn.preact_uniform_columns(w, units, rows=rows).astype(np.float64)
     pp = prm[:, units]
     reps = max(1, int(budget_s / max(t_unit_row * waves(n_units) * n_rows, 1e-3)))
+    threads = min(cores, n_units)
     times = []
     for _ in range(steps):
         t = time.perf_counter()
         for _ in range(reps):
-            oracle.newton(Pc, pp, w.K, cu_seqlens=cu, threads=cores)
+            oracle.sequential(Pc, pp, cu_seqlens=cu, threads=threads)
         times.append((time.perf_counter() - t) / reps)
     sec = statistics.mean(times)
     unit_tokens = n_units * n_rows * w.T
-    return {"value": unit_tokens / w.d_h / sec, "unit": "tokens/s", "cores": min(cores, n_units),
+    return {"value": unit_tokens / w.d_h / sec, "unit": "tokens/s", "cores": threads,
             "kind": "oracle",
-            "sample": f"oracle.newton float64 K={w.K} on {n_units} of {w.d_h} units x {n_rows} of "
-                      f"{w.B} rows x T={w.T} (uniform preact), {sec:.3f} s per pass, "
-                      f"{reps} passes per step",
+            "sample": f"oracle.sequential (float64 unroll) on {n_units} of {w.d_h} units x "
+                      f"{n_rows} of {w.B} rows x T={w.T} (uniform preact), {threads} threads, "
+                      f"{sec:.3f} s per pass, {reps} passes per step",
             "seconds": sec}
 
 
@@ -500,7 +589,7 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--workload", type=int, default=1)
+    ap.add_argument("--workload", type=int, default=DEFAULT_WORKLOAD)
     ap.add_argument("--algo", default="auto", choices=["auto", "fused", "per_iter"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -508,6 +597,10 @@ def main():
     ap.add_argument("--skip-next", action="store_true",
                     help="skip the backward and decode legs")
     ap.add_argument("--skip-per-iter", action="store_true")
+    ap.add_argument("--skip-others", action="store_true",
+                    help="skip the fused / per-iteration timings of the other workloads")
+    ap.add_argument("--others", type=int, nargs="*", default=[1, 2, 3, 4],
+                    help="workloads timed under other_workloads (the headline one is skipped)")
     ap.add_argument("--no-graph", dest="graph", action="store_false",
                     help="launch each forward eagerly instead of replaying a CUDA graph")
     ap.add_argument("--batch", type=int, default=0,
@@ -522,14 +615,13 @@ def main():
     if args.impl == "reference":
         if rank != 0:
             return
-        cb = cpu_baseline(w, budget_s=max(1.0, 90.0 / max(args.steps, 1)), steps=args.steps)
+        cb = cpu_baseline(w, budget_s=max(1.0, 60.0 / max(args.steps, 1)), steps=args.steps)
         out = {"impl": "reference", "metric": METRIC, "value": cb["value"], "unit": "tokens/s",
                "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
                "ms_per_step": 1e3 * w.B * w.T / cb["value"], "higher_is_better": True,
                "scaling": "weak", "vs_baseline": None, "dtype": "f64",
                "data": "synthetic (seeded SplitMix64)",
-               "config": {"workload": w.name, "B": w.B, "T": w.T, "d_in": w.d_in, "d_h": w.d_h,
-                          "K": w.K, "segments": w.segments},
+               "config": bench_config(w, args, world),
                "cpu_baseline": {k: cb[k] for k in ("value", "unit", "cores", "kind", "sample")},
                "e2e": {"value": cb["value"], "unit": "tokens/s", "h2d_bytes_per_step": 0,
                        "d2h_bytes_per_step": 0}}

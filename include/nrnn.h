@@ -18,7 +18,11 @@
  *           the divergence signal (NewtonDivergenceError on the pages).
  *
  * Conventions shared by every entry point
- *   - Every buffer is caller-owned.  The library allocates no memory.
+ *   - Every buffer is caller-owned.  No entry point of the computation
+ *     allocates device memory.  Two exceptions, both outside it:
+ *     nrnn_probe_xu_rates (a throughput measurement) allocates and frees a
+ *     small buffer, and nrnn_newton_forward_host creates two streams and a
+ *     few events per device on its first call and keeps them.
  *   - Device buffers are contiguous, row-major, 16-byte aligned.
  *   - dtype selects the storage type of preact, x, W_x and H: NRNN_F32 or
  *     NRNN_BF16 (bfloat16 storage; all arithmetic inside the kernels is fp32).
@@ -347,8 +351,10 @@ int nrnn_newton_forward_host(const void *preact_host, int dtype, const float *pa
  *     NRNN_ALGO_FUSED) exceeds NRNN_NOALLOC_SCRATCH_BYTES return
  *     NRNN_ERR_WORKSPACE before any CUDA call.
  *   - The first call on a device looks up the array's device address with
- *     that device current (cudaGetSymbolAddress) and caches it; make that
- *     first call before any stream capture on the device.
+ *     that device current (cudaGetSymbolAddress) and keeps it for the
+ *     device's context; make that first call before any stream capture on
+ *     the device.  After cudaDeviceReset the next call looks the address up
+ *     again (again: outside any stream capture).
  *   - Every call on a device shares the one array; each call re-initialises
  *     the parts that must start cleared.  Calls that overlap on the GPU
  *     (different streams, no ordering between them) race on it: serialise them.

@@ -574,7 +574,7 @@ int nrnn_input_projection(const void *x, const void *W_x, int dtype, int64_t row
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (dtype == NRNN_BF16) {
         if (!make_map_2d_sw128(&tmA, x, d_in, rows, PROJ_TC_BOX_K, PROJ_TC_BOX_M) ||
-            !make_map_2d_sw128(&tmB, W_x, d_in, n_out, PROJ_TC_BOX_K, projection_tc_b_box(rows)) ||
+            !make_map_2d_sw128(&tmB, W_x, d_in, n_out, PROJ_TC_BOX_K, PROJ_TC_BOX_N) ||
             !make_map_2d(&tmP, preact, n_out, rows, PROJ_OUT_BOX, PROJ_OUT_BOX, NRNN_BF16,
                          CU_TENSOR_MAP_SWIZZLE_64B))
             return NRNN_ERR_CUDA;

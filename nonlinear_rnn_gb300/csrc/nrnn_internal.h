@@ -64,7 +64,7 @@ struct NewtonArgs {
     int n_ut, n_chunks;           // unit tiles, time chunks
     int k_first, k_last;          // iterations this launch runs (1-based, inclusive)
     int last;                     // this launch ends with H^(K): compute the residual
-    unsigned long long *slots;    // [K][n_tiles][32] packed (A, b); all-ones = not published
+    unsigned long long *slots;    // [K][n_tiles][32] packed (A, b); all-zero bits = not published
     uint32_t *ticket;             // this launch's CTA ticket counter
     uint32_t *residual_bits;      // float bits of rho (atomicMax), cleared by the caller
     uint32_t *error;              // error word (bit 0: look-back timeout, bit 1: TMA timeout)
@@ -144,13 +144,11 @@ cudaError_t launch_bounded_wait(const uint32_t *flag, uint64_t wait_ns, uint32_t
                                 cudaStream_t stream);
 
 // bf16 tensor-core projection: tmA over x (d_in, rows) with a 64 x 128 box,
-// tmB over W_x (d_in, n_out) with a 64 x projection_tc_b_box(rows) box, both
-// bf16 with the 128-byte swizzle (a 128-row box: two CTAs share each W_x tile);
-// tmP over P (n_out, rows) with a PROJ_OUT_BOX x PROJ_OUT_BOX box and the
-// 64-byte swizzle.
+// tmB over W_x (d_in, n_out) with a 64 x 256 box, both bf16 with the 128-byte
+// swizzle; tmP over P (n_out, rows) with a PROJ_OUT_BOX x PROJ_OUT_BOX box and
+// the 64-byte swizzle.
 constexpr int PROJ_TC_BOX_K = 64, PROJ_TC_BOX_M = 128, PROJ_TC_BOX_N = 256;
 constexpr int PROJ_OUT_BOX = 32;
-int projection_tc_b_box(int64_t rows);
 cudaError_t launch_projection_tc(const CUtensorMap &tmA, const CUtensorMap &tmB,
                                  const CUtensorMap &tmP, int64_t rows, int d_in, int n_out,
                                  cudaStream_t stream);

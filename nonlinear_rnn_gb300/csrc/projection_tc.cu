@@ -43,14 +43,11 @@ __device__ uint32_t g_projection_tc_error;
 
 // MODE 0: bf16; MODE 1: fp32 split-TF32, 128-column tiles; MODE 2: fp32
 // split-TF32, 256-column tiles (half the A-operand traffic per product, two
-// stages); MODE 3: bf16 in clusters of two CTAs that take vertically adjacent
-// tiles of the same gate columns and share the W_x tile: each loads one half
-// of it and multicasts it to both, a third less load traffic per CTA
+// stages)
 template <int MODE> struct ProjCfg;
 
-template <int CLUSTER_> struct ProjCfgBf16 {
+template <> struct ProjCfg<0> {
     static constexpr bool F32 = false;
-    static constexpr int CLUSTER = CLUSTER_;
     static constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
     static constexpr int A_BYTES = BM * BK * 2, B_BYTES = BN * BK * 2;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
@@ -59,12 +56,9 @@ template <int CLUSTER_> struct ProjCfgBf16 {
     // D fp32, A and B bf16, both K-major, N = BN, M = BM
     static constexpr uint32_t IDESC = idesc_kmajor<false>(BM, BN);
 };
-template <> struct ProjCfg<0> : ProjCfgBf16<1> {};
-template <> struct ProjCfg<3> : ProjCfgBf16<2> {};
 
 template <int BN_, int STAGES_> struct ProjCfgTf32 {   // fp32 split-TF32
     static constexpr bool F32 = true;
-    static constexpr int CLUSTER = 1;
     static constexpr int BM = 128, BN = BN_, BK = 32, STAGES = STAGES_;
     static constexpr int A_BYTES = BM * BK * 4, B_BYTES = BN * BK * 4;
     static constexpr int STAGE_BYTES = 2 * (A_BYTES + B_BYTES);   // A | B | lo A | lo B
@@ -135,23 +129,19 @@ __global__ void __launch_bounds__(ProjCfg<MODE>::THREADS, 1)
         empty_bar[C::STAGES], accf_bar[2], acce_bar[2];
     __shared__ uint32_t s_tmem;
 
-    constexpr int CL = C::CLUSTER;
-    constexpr uint16_t CL_MASK = static_cast<uint16_t>((1u << CL) - 1u);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int tiles_n = (N + C::BN - 1) / C::BN;
     const int64_t tiles_m = (rows + C::BM - 1) / C::BM;
     const int kt_count = (K + C::BK - 1) / C::BK;
-    // work unit: a column of CL vertically adjacent tiles of the same gate
-    // columns, one per CTA of the cluster (gate columns fastest)
-    const int64_t n_units = ((tiles_m + CL - 1) / CL) * tiles_n;
-    const int64_t unit0 = blockIdx.x / CL, unit_step = gridDim.x / CL;
-    const int64_t rank = CL > 1 ? static_cast<int64_t>(cluster_ctarank()) : 0;
+    // tiles in order, gate columns fastest, round-robin over the CTAs
+    const int64_t n_tiles = tiles_m * tiles_n;
+    const int64_t tile0 = blockIdx.x, tile_step = gridDim.x;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::STAGES; ++s) {
             mbar_init(&full_bar[s], 1);
             mbar_init(&split_bar[s], SPLIT_THREADS);
-            mbar_init(&empty_bar[s], CL);   // one commit from each CTA's MMA issuer
+            mbar_init(&empty_bar[s], 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&accf_bar[b], 1);
@@ -170,50 +160,30 @@ __global__ void __launch_bounds__(ProjCfg<MODE>::THREADS, 1)
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-    if (CL > 1) cluster_sync();   // the peers' barriers are initialised before any multicast
-    else __syncthreads();
+    __syncthreads();
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
     const uint32_t tmem = s_tmem;
 
     if (warp == 0 && lane == 0) {
         // ---------------------------------------------------------- TMA producer
-        // with CL > 1, CTA r loads rows [r BN/CL, (r+1) BN/CL) of the W_x tile
-        // into every CTA of the cluster, so a stage is refilled only after the
-        // MMA issuers of all of them have released it; a part of a tile that
-        // lies wholly outside the matrix is not loaded (its accumulator rows
-        // or columns are never stored)
-        constexpr int B_PART = C::B_BYTES / CL, N_PART = C::BN / CL;
         int it = 0;
-        for (int64_t u = unit0; u < n_units; u += unit_step) {
-            const int64_t mt = (u / tiles_n) * CL + rank;
+        for (int64_t u = tile0; u < n_tiles; u += tile_step) {
+            const int64_t m0 = (u / tiles_n) * C::BM;
             const int n0 = static_cast<int>(u % tiles_n) * C::BN;
-            const bool a_in = mt < tiles_m;
-            uint32_t bytes = a_in ? C::A_BYTES : 0;
-            for (int r = 0; r < CL; ++r)
-                if (n0 + r * N_PART < N) bytes += B_PART;
-            const bool b_in = n0 + static_cast<int>(rank) * N_PART < N;
             for (int kt = 0; kt < kt_count; ++kt, ++it) {
                 const int s = it % C::STAGES;
                 if (it >= C::STAGES)
                     mbar_wait_bounded(&empty_bar[s], ((it / C::STAGES) - 1) & 1, TC_WAIT_NS, error);
                 unsigned char *st = smem + s * C::STAGE_BYTES;
-                mbar_arrive_expect_tx(&full_bar[s], bytes);
-                if (a_in) tma_load_2d(st, &tmA, &full_bar[s], kt * C::BK, static_cast<int>(mt * C::BM));
-                if (CL == 1)
-                    tma_load_2d(st + C::A_BYTES, &tmB, &full_bar[s], kt * C::BK, n0);
-                else if (b_in)
-                    tma_load_2d_multicast(st + C::A_BYTES + rank * B_PART, &tmB, &full_bar[s],
-                                          kt * C::BK, n0 + static_cast<int>(rank) * N_PART, CL_MASK);
+                mbar_arrive_expect_tx(&full_bar[s], C::A_BYTES + C::B_BYTES);
+                tma_load_2d(st, &tmA, &full_bar[s], kt * C::BK, static_cast<int>(m0));
+                tma_load_2d(st + C::A_BYTES, &tmB, &full_bar[s], kt * C::BK, n0);
             }
         }
-        // the peers' last commits land on this CTA's barriers before it may exit
-        if (CL > 1)
-            for (int q = it > C::STAGES ? it - C::STAGES : 0; q < it; ++q)
-                mbar_wait_bounded(&empty_bar[q % C::STAGES], (q / C::STAGES) & 1, TC_WAIT_NS, error);
     } else if (warp == 1 && lane == 0) {
         // ------------------------------------------------------------ MMA issuer
         int it = 0, j = 0;
-        for (int64_t u = unit0; u < n_units; u += unit_step, ++j) {
+        for (int64_t u = tile0; u < n_tiles; u += tile_step, ++j) {
             const int buf = j & 1;
             if (j >= 2) mbar_wait_bounded(&acce_bar[buf], ((j >> 1) - 1) & 1, TC_WAIT_NS, error);
             asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
@@ -239,8 +209,7 @@ __global__ void __launch_bounds__(ProjCfg<MODE>::THREADS, 1)
                         mma<F32, C::IDESC>(d, sw128_desc(a_hi + o), sw128_desc(b_hi + o), acc);
                     }
                 }
-                if (CL > 1) mma_commit_multicast(&empty_bar[s], CL_MASK);
-                else mma_commit(&empty_bar[s]);
+                mma_commit(&empty_bar[s]);
             }
             mma_commit(&accf_bar[buf]);
         }
@@ -248,7 +217,7 @@ __global__ void __launch_bounds__(ProjCfg<MODE>::THREADS, 1)
         // ------------------------------------------- split-TF32 operand splitter
         const int t = threadIdx.x - 8 * 32;
         int it = 0;
-        for (int64_t u = unit0; u < n_units; u += unit_step) {
+        for (int64_t u = tile0; u < n_tiles; u += tile_step) {
             for (int kt = 0; kt < kt_count; ++kt, ++it) {
                 const int s = it % C::STAGES;
                 mbar_wait_bounded(&full_bar[s], (it / C::STAGES) & 1, TC_WAIT_NS, error);
@@ -271,9 +240,9 @@ __global__ void __launch_bounds__(ProjCfg<MODE>::THREADS, 1)
         unsigned char *stage_out = smem + C::STAGES * C::STAGE_BYTES + quarter * 2 * BLK_BYTES;
         int nblk = 0;
         int j = 0;
-        for (int64_t u = unit0; u < n_units; u += unit_step, ++j) {
+        for (int64_t u = tile0; u < n_tiles; u += tile_step, ++j) {
             const int buf = j & 1;
-            const int64_t m0 = ((u / tiles_n) * CL + rank) * C::BM;
+            const int64_t m0 = (u / tiles_n) * C::BM;
             const int n0 = static_cast<int>(u % tiles_n) * C::BN;
             const bool ok = mbar_wait_bounded(&accf_bar[buf], (j >> 1) & 1, TC_WAIT_NS, error);
             asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
@@ -302,8 +271,7 @@ __global__ void __launch_bounds__(ProjCfg<MODE>::THREADS, 1)
     }
     __syncwarp();
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-    if (CL > 1) cluster_sync();   // no peer still writes to this CTA's shared memory
-    else __syncthreads();
+    __syncthreads();
     if (warp == 2) {
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
@@ -316,40 +284,19 @@ template <int MODE>
 cudaError_t launch_tc(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUtensorMap &tmP,
                       int64_t rows, int d_in, int n_out, cudaStream_t stream) {
     using C = ProjCfg<MODE>;
-    constexpr int CL = C::CLUSTER;
     static std::atomic<unsigned long long> configured{0};
-    static int groups_of[64];   // co-resident CTAs (CL == 1) or clusters per device
+    static int sms_of[64];   // SMs per device: one persistent CTA each
     // operand ring + two staged output blocks per epilogue warp + alignment slack
     constexpr size_t smem = static_cast<size_t>(C::STAGES) * C::STAGE_BYTES +
                             (EPI_THREADS / 32) * 2 * OUT_BOX * OUT_BOX * (C::F32 ? 4 : 2) + 1024;
-    cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
-    cfg.blockDim = dim3(C::THREADS);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = stream;
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = CL;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    cudaError_t e = once_per_device(configured, [&cfg](int dev) {
+    cudaError_t e = once_per_device(configured, [](int dev) {
         cudaError_t r = cudaFuncSetAttribute(k_projection_tc<MODE>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              static_cast<int>(smem));
         int n = 0;
-        if (r == cudaSuccess && CL == 1)
-            r = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-        if (r == cudaSuccess && CL > 1) {
-            // clusters are placed within one GPC: ask how many fit at once
-            cudaLaunchConfig_t q = cfg;
-            int sms = 0;
-            r = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-            q.gridDim = dim3(static_cast<unsigned>(sms / CL * CL));
-            if (r == cudaSuccess) r = cudaOccupancyMaxActiveClusters(&n, k_projection_tc<MODE>, &q);
-        }
+        if (r == cudaSuccess) r = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
         if (r == cudaSuccess && n <= 0) r = cudaErrorInvalidConfiguration;
-        if (r == cudaSuccess && dev < 64) groups_of[dev] = n;
+        if (r == cudaSuccess && dev < 64) sms_of[dev] = n;
         return r;
     });
     if (e != cudaSuccess) return e;
@@ -357,26 +304,18 @@ cudaError_t launch_tc(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUte
     e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev >= 64) return cudaErrorInvalidDevice;
-    const int groups = groups_of[dev];
-    const int64_t tiles_m = (rows + C::BM - 1) / C::BM;
-    const int64_t n_units = ((tiles_m + CL - 1) / CL) * ((n_out + C::BN - 1) / C::BN);
-    const int64_t grid = (n_units < groups ? n_units : groups) * CL;
-    cfg.gridDim = dim3(static_cast<unsigned>(grid));
-    if (CL == 1) cfg.numAttrs = 0;
-    return cudaLaunchKernelEx(&cfg, k_projection_tc<MODE>, tmA, tmB, tmP, rows, d_in, n_out);
+    const int64_t n_tiles = ((rows + C::BM - 1) / C::BM) * ((n_out + C::BN - 1) / C::BN);
+    const int64_t grid = n_tiles < sms_of[dev] ? n_tiles : sms_of[dev];
+    k_projection_tc<MODE><<<static_cast<unsigned>(grid), C::THREADS, smem, stream>>>(
+        tmA, tmB, tmP, rows, d_in, n_out);
+    return cudaGetLastError();
 }
 
 }  // namespace
 
-int projection_tc_b_box(int64_t rows) {
-    return rows > PROJ_TC_BOX_M ? PROJ_TC_BOX_N / 2 : PROJ_TC_BOX_N;
-}
-
 cudaError_t launch_projection_tc(const CUtensorMap &tmA, const CUtensorMap &tmB,
                                  const CUtensorMap &tmP, int64_t rows, int d_in, int n_out,
                                  cudaStream_t stream) {
-    if (projection_tc_b_box(rows) != PROJ_TC_BOX_N)
-        return launch_tc<3>(tmA, tmB, tmP, rows, d_in, n_out, stream);
     return launch_tc<0>(tmA, tmB, tmP, rows, d_in, n_out, stream);
 }
 

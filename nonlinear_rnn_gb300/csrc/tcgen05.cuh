@@ -27,18 +27,6 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, u
         : "memory");
 }
 
-// the same load delivered to the same shared-memory offset, and signalled on
-// the same mbarrier offset, of every CTA of the cluster named in cta_mask
-__device__ __forceinline__ void tma_load_2d_multicast(void *dst, const CUtensorMap *map,
-                                                      uint64_t *bar, int x, int y,
-                                                      uint16_t cta_mask) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
-        ".multicast::cluster [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "h"(cta_mask)
-        : "memory");
-}
-
 // shared -> global tile store; elements outside the tensor are not written
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, const void *src, int x, int y) {
     asm volatile(
@@ -58,19 +46,6 @@ __device__ __forceinline__ void bulk_wait_all() {
 template <int N>
 __device__ __forceinline__ void bulk_wait_read() {
     asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
-}
-
-__device__ __forceinline__ uint32_t cluster_ctarank() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-
-// every thread of every CTA of the cluster; orders shared-memory writes
-// (mbarrier initialisation included) before the peers' later accesses
-__device__ __forceinline__ void cluster_sync() {
-    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
-    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
 template <bool F32, uint32_t IDESC>
@@ -96,16 +71,6 @@ __device__ __forceinline__ void mma_commit(uint64_t *bar) {
     asm volatile(
         "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
             smem_u32(bar))
-        : "memory");
-}
-
-// arrive once on the mbarrier at this offset in every CTA named in cta_mask
-// when this thread's earlier tcgen05.mma have completed
-__device__ __forceinline__ void mma_commit_multicast(uint64_t *bar, uint16_t cta_mask) {
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-        " [%0], %1;" ::"r"(smem_u32(bar)),
-        "h"(cta_mask)
         : "memory");
 }
 

@@ -24,6 +24,7 @@ and returns ``cu_seqlens`` as the exclusive prefix sum (int32, length S + 1).
 from __future__ import annotations
 
 import math
+import os
 from dataclasses import dataclass, field
 
 import numpy as np
@@ -71,12 +72,26 @@ def uniform64(seed: int, stream: int, n: int, start: int = 0) -> np.ndarray:
     return out
 
 
+def _blocks(fn, n_blocks: int) -> None:
+    """Runs fn(i) for every block index; blocks write disjoint slices, and numpy
+    releases the GIL inside its array operations, so large draws use threads."""
+    if n_blocks <= 1:
+        for i in range(n_blocks):
+            fn(i)
+        return
+    from concurrent.futures import ThreadPoolExecutor
+    with ThreadPoolExecutor(min(n_blocks, os.cpu_count() or 1)) as ex:
+        list(ex.map(fn, range(n_blocks)))
+
+
 def normal64(seed: int, stream: int, n: int) -> np.ndarray:
     """n standard normals (Box-Muller on uniform pairs), float64."""
     out = np.empty(n, dtype=np.float64)
     pairs = (n + 1) // 2
     blk = _BLOCK // 2
-    for o in range(0, pairs, blk):
+
+    def one(i):
+        o = i * blk
         m = min(blk, pairs - o)
         u = uniform64(seed, stream, 2 * m, start=2 * o)
         u1 = 1.0 - u[0::2]            # (0, 1]: log is finite
@@ -89,6 +104,8 @@ def normal64(seed: int, stream: int, n: int) -> np.ndarray:
         lo = 2 * o
         hi = min(n, lo + 2 * m)
         out[lo:hi] = seg[: hi - lo]
+
+    _blocks(one, -(-pairs // blk))
     return out
 
 
@@ -153,17 +170,24 @@ def small_workload(B=2, T=300, d_in=8, d_h=40, K=3, dtype="f32", seed=11,
                     segments=segments, seg_lo=seg_lo, seg_hi=seg_hi, seed=seed)
 
 
-def round_bf16(a: np.ndarray) -> np.ndarray:
-    """Round float32 values to bfloat16 (round to nearest even), returned as float32."""
-    a = np.ascontiguousarray(a, dtype=np.float32)
+def _round_bf16_flat(a: np.ndarray, r: np.ndarray) -> None:
     u = a.view(np.uint32).astype(np.uint64)
     lsb = (u >> np.uint64(16)) & np.uint64(1)
-    r = ((u + np.uint64(0x7FFF) + lsb) >> np.uint64(16)) << np.uint64(16)
-    r = r.astype(np.uint32)
+    r[:] = (((u + np.uint64(0x7FFF) + lsb) >> np.uint64(16)) << np.uint64(16)).astype(np.uint32)
     nan = np.isnan(a)
     if nan.any():
         r[nan] = np.uint32(0x7FC00000)
-    return r.view(np.float32)
+
+
+def round_bf16(a: np.ndarray) -> np.ndarray:
+    """Round float32 values to bfloat16 (round to nearest even), returned as float32."""
+    a = np.ascontiguousarray(a, dtype=np.float32)
+    flat = a.reshape(-1)
+    r = np.empty(flat.shape, dtype=np.uint32)
+    _blocks(lambda i: _round_bf16_flat(flat[i * _BLOCK:(i + 1) * _BLOCK],
+                                       r[i * _BLOCK:(i + 1) * _BLOCK]),
+            -(-flat.size // _BLOCK))
+    return r.view(np.float32).reshape(a.shape)
 
 
 def make_params(w: Workload) -> dict:
@@ -189,7 +213,12 @@ def make_inputs(w: Workload, with_x: bool = True) -> dict:
     W = uniform_pm(s, STREAM_WX, 3 * w.d_h * w.d_in, 1.0 / math.sqrt(w.d_in))
     W = W.astype(np.float32).reshape(3 * w.d_h, w.d_in)
     if with_x:
-        x = normal64(s, STREAM_X, w.B * w.T * w.d_in).astype(np.float32)
+        n = w.B * w.T * w.d_in
+        x64 = normal64(s, STREAM_X, n)
+        x = np.empty(n, dtype=np.float32)
+        _blocks(lambda i: np.copyto(x[i * _BLOCK:(i + 1) * _BLOCK], x64[i * _BLOCK:(i + 1) * _BLOCK],
+                                    casting="same_kind"), -(-n // _BLOCK))
+        del x64
         x = x.reshape(w.B, w.T, w.d_in)
     else:
         x = None

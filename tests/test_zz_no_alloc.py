@@ -11,6 +11,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 import synthetic as syn
 
 pytestmark = pytest.mark.gpu
@@ -42,9 +43,12 @@ def test_noalloc_matches_workspace_entry_point_on_two_calls(dtype, ragged):
     else:
         w = syn.small_workload(B=3, T=700, d_h=72, dtype=dtype, seed=32)
         cu_np, cu, S = None, None, 0
-    P = torch.from_numpy(syn.direct_preact(w)).cuda().to(tdt)
+    P_host = syn.direct_preact(w)
+    P = torch.from_numpy(P_host).cuda().to(tdt)
     prm = nr.params_tensor(syn.make_params(w), w.d_h, "cuda")
     H_ref, rho_ref = nr.newton_forward(P, prm, cu_seqlens=cu_np, K=3, algo="fused", check=False)
+    # the float64 oracle on the same stored preactivations
+    H_orc, rho_orc = oracle.newton(P_host, syn.make_params(w), 3, cu_seqlens=cu_np)
     tol = 1e-4 if dtype == "f32" else 5e-2
     for _ in range(2):   # the second call finds the first call's scratch contents
         H = torch.full_like(H_ref, float("nan"))
@@ -54,6 +58,8 @@ def test_noalloc_matches_workspace_entry_point_on_two_calls(dtype, ragged):
         assert not torch.isnan(H).any()
         assert (H.float() - H_ref.float()).abs().max().item() <= tol
         assert abs(rho.item() - rho_ref.item()) <= tol
+        assert float(np.max(np.abs(H.double().cpu().numpy() - H_orc))) <= tol
+        assert abs(rho.item() - rho_orc) <= tol
 
 
 def test_noalloc_rejects_requests_beyond_its_scratch():
