@@ -224,7 +224,7 @@ __global__ void __launch_bounds__(NW * 32, 4)
             publish(slot, 0.f, tB);
         } else {
             publish(slot, tA, tB);
-            C = lookback_lane(slot, c, +1, a.n_chunks, a.wait_ns, a.error);
+            C = lookback_lane<4>(slot, c, +1, a.n_chunks, a.wait_ns, a.error);
             publish(slot, 0.f, fmaf(tA, C, tB));
         }
         s_C[lane] = C;

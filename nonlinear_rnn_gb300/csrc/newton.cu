@@ -40,6 +40,8 @@ constexpr int NW = NEWTON_NW;
 constexpr int SEG = NEWTON_SEG;
 constexpr int L = NEWTON_L;
 constexpr int U = TILE_U;
+// early look-back reads when at most this many chunks per column are resident
+constexpr int EARLY_LOOKBACK_CHUNKS = 4;
 
 // fused-projection prologue (XPROJ): bf16 operands, 64-wide K slices
 constexpr int XP_BK = 64;
@@ -185,7 +187,9 @@ __device__ __forceinline__ float residual_rows(const float *Pf, const TS *Pt, in
 template <typename TS, bool FUSED>
 constexpr int newton_min_blocks() { return (!FUSED && sizeof(TS) == 2) ? 9 : 8; }
 
-template <typename TS, bool FUSED, bool XPROJ = false>
+// EARLY: warp 0 reads the nearest predecessors' look-back slots before the
+// CTA barrier (see with_lookback_mode)
+template <typename TS, bool FUSED, bool XPROJ = false, bool EARLY = false>
 __global__ void __launch_bounds__(NW * 32, newton_min_blocks<TS, FUSED>())
     k_newton(const __grid_constant__ CUtensorMap tmP, const __grid_constant__ CUtensorMap tmH,
              const __grid_constant__ CUtensorMap tmO, const __grid_constant__ CUtensorMap tmX,
@@ -429,6 +433,16 @@ __global__ void __launch_bounds__(NW * 32, newton_min_blocks<TS, FUSED>())
         } else {
             warp_pairs<TS, FUSED, false>(Pv, warp, lane, G, hb, hm, nvalid, prm2, J2, A_lo, B_lo, A, Bv);
         }
+        // when few chunks of a column run at once, the nearest predecessors
+        // have usually published by now: warp 0 reads their slots before the
+        // barrier, so that the L2 round trip overlaps the other warps' rows
+        unsigned long long *slot =
+            a.slots + (static_cast<size_t>(k - 1) * n_tiles + tile) * 32 + lane;
+        unsigned long long pre1 = SLOT_EMPTY, pre2 = SLOT_EMPTY;
+        if (EARLY && warp == 0) {
+            if (c > 0) pre1 = ld_relaxed_u64(slot - 32);
+            if (c > 1) pre2 = ld_relaxed_u64(slot - 64);
+        }
         s_aggA[warp][lane] = A;
         s_aggB[warp][lane] = Bv;
         __syncthreads();
@@ -444,15 +458,14 @@ __global__ void __launch_bounds__(NW * 32, newton_min_blocks<TS, FUSED>())
                 tB = fmaf(wa, tB, wb);
                 tA *= wa;
             }
-            unsigned long long *slot =
-                a.slots + (static_cast<size_t>(k - 1) * n_tiles + tile) * 32 + lane;
             float C = 0.f;   // H^(k) at t0 - 1 (0 before the first step)
             const bool pub = tile != a.withhold_tile;
             if (c == 0) {
                 if (pub) publish(slot, 0.f, tB);
             } else {
                 if (pub) publish(slot, tA, tB);
-                C = lookback_lane(slot, c, -1, a.n_chunks, a.wait_ns, a.error);
+                C = lookback_lane<EARLY ? 2 : 4>(slot, c, -1, a.n_chunks, a.wait_ns, a.error, pre1,
+                                                  pre2);
                 if (pub) publish(slot, 0.f, fmaf(tA, C, tB));
             }
             s_C[lane] = C;
@@ -583,18 +596,42 @@ size_t smem_bytes_for(bool with_h) {
                  : static_cast<size_t>(sizeof(TS) == 4 ? 3 : 4) * L * U * sizeof(TS);
 }
 
-template <typename TS, bool FUSED>
+// Early look-back reads pay when few chunks of each column (batch row x unit
+// tile) are resident at once: then the nearest predecessor has usually
+// published its inclusive prefix by the time a tile has its own aggregate.
+// With many resident chunks per column (long sequences of few columns) the
+// early read mostly finds a predecessor still at work.
+bool early_lookback(const NewtonArgs &a, int ctas_per_sm) {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return false;
+    const int64_t resident = static_cast<int64_t>(sms) * ctas_per_sm;
+    const int64_t columns = static_cast<int64_t>(a.B) * a.n_ut;
+    return resident <= EARLY_LOOKBACK_CHUNKS * columns;
+}
+
+template <typename TS, bool FUSED, bool EARLY>
 cudaError_t launch_one(const CUtensorMap &tmP, const CUtensorMap &tmH, const CUtensorMap &tmO,
                        const NewtonArgs &a, int64_t n_ctas, cudaStream_t stream) {
     static std::atomic<unsigned long long> configured{0};
     const size_t smem = smem_bytes_for<TS, FUSED>(a.H_prev != nullptr);
     cudaError_t e = once_per_device(configured, [](int) {
-        return cudaFuncSetAttribute(k_newton<TS, FUSED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        return cudaFuncSetAttribute(k_newton<TS, FUSED, false, EARLY>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     static_cast<int>(smem_bytes_for<TS, FUSED>(true)));
     });
     if (e != cudaSuccess) return e;
-    return launch_dependent(k_newton<TS, FUSED>, static_cast<unsigned>(n_ctas), NW * 32, smem, stream,
-                            tmP, tmH, tmO, tmP, tmP, a);
+    return launch_dependent(k_newton<TS, FUSED, false, EARLY>, static_cast<unsigned>(n_ctas),
+                            NW * 32, smem, stream, tmP, tmH, tmO, tmP, tmP, a);
+}
+
+template <typename TS, bool FUSED>
+cudaError_t launch_one(const CUtensorMap &tmP, const CUtensorMap &tmH, const CUtensorMap &tmO,
+                       const NewtonArgs &a, int64_t n_ctas, cudaStream_t stream) {
+    return early_lookback(a, newton_min_blocks<TS, FUSED>())
+               ? launch_one<TS, FUSED, true>(tmP, tmH, tmO, a, n_ctas, stream)
+               : launch_one<TS, FUSED, false>(tmP, tmH, tmO, a, n_ctas, stream);
 }
 
 cudaError_t launch_x(const CUtensorMap &tmX, const CUtensorMap &tmW, const CUtensorMap &tmO,

@@ -565,7 +565,6 @@ __device__ __forceinline__ float pair_b(unsigned long long v) {
 // inclusive prefix (A = 0), and the latter two both compose correctly: no
 // fence is needed on either side.
 constexpr unsigned long long SLOT_EMPTY = 0ull;
-constexpr int LOOKBACK_WIN = 4;   // neighbours read in parallel per round
 
 __device__ __forceinline__ void publish(unsigned long long *slot, float A, float b) {
     unsigned long long v = pack_pair(A, b);
@@ -577,21 +576,39 @@ __device__ __forceinline__ void publish(unsigned long long *slot, float A, float
 // of chunks c + dir, c + 2 dir, ... (dir = -1: earlier chunks, forward scan;
 // dir = +1: later chunks, reverse scan) until a closed prefix (A = 0) or the
 // end of the sequence, and returns the carry into chunk c.  `slot` is this
-// lane's slot of chunk c; chunk c + dir d has slot + dir d 32.  Up to
-// LOOKBACK_WIN neighbours are read per round with independent loads; while
-// nothing is ready only the nearest is polled.  Bounded: gives up after
-// wait_ns without progress, sets bit 0 of *error and returns the partial
-// prefix.
+// lane's slot of chunk c; chunk c + dir d has slot + dir d 32.  Up to WIN
+// neighbours are read per round with independent loads; while nothing is
+// ready only the nearest is polled.  pre1, pre2: the slots of chunks c + dir
+// and c + 2 dir as the caller read them earlier (SLOT_EMPTY if it did not,
+// or if they were not published then): what they hold is folded first, so a
+// caller that issues those loads before waiting for other work hides their
+// latency.  Bounded: gives up after wait_ns without progress, sets bit 0 of
+// *error and returns the partial prefix.
+template <int WIN>
 __device__ __forceinline__ float lookback_lane(const unsigned long long *slot, int c, int dir,
-                                               int n_chunks, uint64_t wait_ns, uint32_t *error) {
+                                               int n_chunks, uint64_t wait_ns, uint32_t *error,
+                                               unsigned long long pre1 = SLOT_EMPTY,
+                                               unsigned long long pre2 = SLOT_EMPTY) {
     float cA = 1.f, cB = 0.f;
     int d = 1;   // distance of the next neighbour to fold
+    if (pre1 != SLOT_EMPTY) {
+        cB = pair_b(pre1);
+        cA = pair_A(pre1);
+        d = 2;
+        if (cA == 0.f) return cB;
+        if (pre2 != SLOT_EMPTY) {
+            cB = fmaf(cA, pair_b(pre2), cB);
+            cA *= pair_A(pre2);
+            d = 3;
+            if (cA == 0.f) return cB;
+        }
+    }
     for (;;) {
         const int q = c + dir * d;
         if (q < 0 || q >= n_chunks) break;
-        unsigned long long v[LOOKBACK_WIN];
+        unsigned long long v[WIN];
 #pragma unroll
-        for (int i = 0; i < LOOKBACK_WIN; ++i) {
+        for (int i = 0; i < WIN; ++i) {
             const int qi = c + dir * (d + i);
             v[i] = (qi >= 0 && qi < n_chunks)
                        ? ld_relaxed_u64(slot + static_cast<ptrdiff_t>(dir) * (d + i) * 32)
@@ -599,7 +616,7 @@ __device__ __forceinline__ float lookback_lane(const unsigned long long *slot, i
         }
         int folded = 0;
 #pragma unroll
-        for (int i = 0; i < LOOKBACK_WIN; ++i) {
+        for (int i = 0; i < WIN; ++i) {
             if (folded < i || v[i] == SLOT_EMPTY) break;
             cB = fmaf(cA, pair_b(v[i]), cB);
             cA *= pair_A(v[i]);
