@@ -211,8 +211,41 @@ def time_workload(torch, nr, w, args, dev, flush, stream, xu_rates, props, mhz):
             b = workload_bytes(w, algo)
             entry["hbm_frac"] = (sum(b) / len(b)) / (ms / len(b) * 1e-3) / 1e9 / pk["hbm_gbs"]
         res[algo] = entry
+    if not args.skip_routes:
+        res["routes_to_tau"] = routes_to_tau(torch, nr, w, P, prm, cu, args, flush, stream)
     del P, H, ws
     return res
+
+
+def time_graph(torch, fn, args, flush, stream):
+    """Median ms of fn as a CUDA-graph replay (eager launches with --no-graph),
+    L2 flushed between steps."""
+    fn()
+    torch.cuda.synchronize()
+    step = fn
+    if args.graph:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            fn()
+        step = g.replay
+    for _ in range(args.warmup):
+        flush.fill_(1.0)
+        step()
+    ms, _ = time_steps(torch, step, max(3, min(args.steps, 10)), flush, stream, nvtx=False)
+    return statistics.median(ms)
+
+
+def routes_to_tau(torch, nr, w, P, prm, cu, args, flush, stream):
+    """Two routes past the configured K's method error (FAQs, "How many Newton
+    iterations should I use?"): one more Newton iteration, or two Picard
+    sweeps and then K Newton iterations from their result.  ms of each; their
+    max-abs against the float64 unroll is checked by the GPU tests."""
+    H = torch.empty((w.B, w.T, w.d_h), dtype=P.dtype, device=P.device)
+    k1 = time_graph(torch, lambda: nr.newton_forward(P, prm, cu_seqlens=cu, K=w.K + 1,
+                                                     check=False, out=H), args, flush, stream)
+    pk = time_graph(torch, lambda: nr.newton_forward(P, prm, cu_seqlens=cu, K=w.K, check=False,
+                                                     out=H, picard_iters=2), args, flush, stream)
+    return {f"newton_K{w.K + 1}_ms": k1, f"picard2_newton_K{w.K}_ms": pk}
 
 
 def bench_config(w, args, world):
@@ -372,7 +405,10 @@ def run_ours(args, w, rank, world, local):
                     "algorithmic_bytes_per_launch": sum(pb) / len(pb)}
 
     # projection and the GPU sequential unroll beside it
-    proj_ms, _ = time_steps(torch, replay_of(lambda: nr.input_projection(x, W, out=P)), max(3, min(args.steps, 10)),
+    pws = torch.empty(max(1, nr.projection_workspace_bytes(tdt, w.d_in, w.d_h)), dtype=torch.uint8,
+                      device=dev)
+    proj_ms, _ = time_steps(torch, replay_of(lambda: nr.input_projection(x, W, out=P, workspace=pws)),
+                            max(3, min(args.steps, 10)),
                             flush, stream, nvtx=False)
     seq_ms, _ = time_steps(torch, replay_of(lambda: nr.sequential_forward(P, prm, cu_seqlens=cu, out=H)), 3,
                            flush, stream, nvtx=False)
@@ -461,6 +497,9 @@ def run_ours(args, w, rank, world, local):
         fx_ms, _ = time_steps(torch, fx_step, max(3, min(args.steps, 10)), flush, stream, nvtx=False)
         fused_x = {"ms": statistics.median(fx_ms),
                    "tokens_per_s": tokens * world / (statistics.median(fx_ms) * 1e-3)}
+    routes = None if args.skip_routes else routes_to_tau(torch, nr, w, P, prm, cu, args, flush,
+                                                         stream)
+
     # the other multi-megabyte workloads, timed the same way on preactivations
     # drawn directly on the device (U(-1, 1), the variance of x W_x^T)
     others = {}
@@ -498,6 +537,7 @@ def run_ours(args, w, rank, world, local):
         "sequential_gpu": {"ms": statistics.median(seq_ms),
                            "tokens_per_s": tokens / (statistics.median(seq_ms) * 1e-3)},
         "next_rows": nxt or None,
+        "routes_to_tau": routes,
         "other_workloads": others or None,
         "residual": float(rho.item()),
         "wall_s": t_wall,
@@ -597,6 +637,8 @@ def main():
     ap.add_argument("--skip-next", action="store_true",
                     help="skip the backward and decode legs")
     ap.add_argument("--skip-per-iter", action="store_true")
+    ap.add_argument("--skip-routes", action="store_true",
+                    help="skip the K+1 and Picard-warm-start timings")
     ap.add_argument("--skip-others", action="store_true",
                     help="skip the fused / per-iteration timings of the other workloads")
     ap.add_argument("--others", type=int, nargs="*", default=[1, 2, 3, 4],

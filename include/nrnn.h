@@ -264,13 +264,21 @@ int nrnn_decode_step_x(const void *x, const void *W_x, int dtype, const float *p
  * Input projection P = x W_x^T (shapes_layout page: "W_x" reads x of layout
  * (B, T, d_in)); x (rows, d_in), W_x (3 d_h, d_in), preact (rows, 3 d_h), all
  * of dtype, fp32 accumulation.  NRNN_F32 keeps fp32 accuracy (no TF32
- * rounding of the operands); NRNN_BF16 uses the bf16 tensor-core path and
- * rounds the fp32 accumulator to bf16.  d_in and d_h must be multiples of 8
- * and rows < 2^31 (else NRNN_ERR_UNSUPPORTED); x, W_x and preact 16-byte
- * aligned (else NRNN_ERR_INVALID_ARG).
+ * rounding of the operands: three TF32 products of a high/low split of each
+ * operand); NRNN_BF16 uses the bf16 tensor-core path and rounds the fp32
+ * accumulator to bf16.  d_in and d_h must be multiples of 8 and rows < 2^31
+ * (else NRNN_ERR_UNSUPPORTED); x, W_x and preact 16-byte aligned (else
+ * NRNN_ERR_INVALID_ARG).
+ *   workspace  device, caller-owned, 256-byte aligned, at least
+ *              nrnn_input_projection_workspace_bytes(dtype, d_in, d_h) bytes
+ *              (NRNN_F32: the low part of W_x, written by this call; may be
+ *              NULL when that size is 0); too small or misaligned returns
+ *              NRNN_ERR_WORKSPACE
  */
+size_t nrnn_input_projection_workspace_bytes(int dtype, int64_t d_in, int64_t d_h);
 int nrnn_input_projection(const void *x, const void *W_x, int dtype, int64_t rows,
-                          int64_t d_in, int64_t d_h, void *preact, void *stream);
+                          int64_t d_in, int64_t d_h, void *preact, void *workspace,
+                          size_t ws_bytes, void *stream);
 
 /*
  * Debug export of the segment-head mask the Newton kernels use

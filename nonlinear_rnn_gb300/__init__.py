@@ -28,6 +28,7 @@ from ._binding import (  # noqa: F401
     params_tensor,
     picard,
     probe_xu_rates,
+    projection_workspace_bytes,
     residual,
     sequential_forward,
     set_wait_limit_ns,

@@ -46,7 +46,8 @@ _SIGNATURES = {
     "nrnn_decode_step_x": ([_vp, _vp, _int, _vp, _i64, _i64, _i64, _vp, _vp, _vp], _int),
     "nrnn_sequential_forward": ([_vp, _int, _vp, _i64, _i64, _i64, _vp, _i64, _vp, _vp], _int),
     "nrnn_residual": ([_vp, _int, _vp, _i64, _i64, _i64, _vp, _i64, _vp, _vp, _vp], _int),
-    "nrnn_input_projection": ([_vp, _vp, _int, _i64, _i64, _i64, _vp, _vp], _int),
+    "nrnn_input_projection_workspace_bytes": ([_int, _i64, _i64], _sz),
+    "nrnn_input_projection": ([_vp, _vp, _int, _i64, _i64, _i64, _vp, _vp, _sz, _vp], _int),
     "nrnn_debug_head_mask": ([_vp, _i64, _i64, _vp, _vp], _int),
     "nrnn_debug_bounded_wait": ([_vp, _u64, _vp, _vp], _int),
     "nrnn_set_wait_limit_ns": ([_u64], _u64),
@@ -457,8 +458,16 @@ def residual(preact: torch.Tensor, params, G: torch.Tensor, cu_seqlens=None) -> 
     return rho
 
 
-def input_projection(x: torch.Tensor, W_x: torch.Tensor, out: torch.Tensor | None = None):
-    """P = x W_x^T: x (..., d_in), W_x (3 d_h, d_in) -> (..., 3 d_h), same dtype."""
+def projection_workspace_bytes(dtype, d_in: int, d_h: int) -> int:
+    """Workspace bytes nrnn_input_projection needs (fp32: the low part of W_x)."""
+    code = F32 if dtype == torch.float32 else BF16 if dtype == torch.bfloat16 else -1
+    return int(load().nrnn_input_projection_workspace_bytes(code, int(d_in), int(d_h)))
+
+
+def input_projection(x: torch.Tensor, W_x: torch.Tensor, out: torch.Tensor | None = None,
+                     workspace: torch.Tensor | None = None):
+    """P = x W_x^T: x (..., d_in), W_x (3 d_h, d_in) -> (..., 3 d_h), same dtype.
+    fp32 needs a workspace (the low part of W_x; allocated here if not given)."""
     lib = load()
     x = _device_tensor(x, "x")
     W_x = _device_tensor(W_x, "W_x")
@@ -470,9 +479,14 @@ def input_projection(x: torch.Tensor, W_x: torch.Tensor, out: torch.Tensor | Non
         raise ValueError("W_x must have shape (3 d_h, d_in)")
     rows = x.numel() // d_in
     P = out if out is not None else torch.empty((*x.shape[:-1], n_out), dtype=x.dtype, device=x.device)
+    code = _dtype_code(x)
+    nbytes = lib.nrnn_input_projection_workspace_bytes(code, d_in, n_out // 3)
+    if nbytes > 0 and (workspace is None or workspace.numel() < nbytes):
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=x.device)
     with torch.cuda.device(x.device):
-        st = lib.nrnn_input_projection(_ptr(x), _ptr(W_x), _dtype_code(x), rows, d_in, n_out // 3,
-                                       _ptr(P), _stream(x.device))
+        st = lib.nrnn_input_projection(_ptr(x), _ptr(W_x), code, rows, d_in, n_out // 3, _ptr(P),
+                                       _ptr(workspace) if nbytes > 0 else None, int(nbytes),
+                                       _stream(x.device))
     _raise(st, "input_projection")
     return P
 

@@ -559,8 +559,17 @@ int nrnn_residual(const void *preact, int dtype, const float *params, int64_t B,
                                        reinterpret_cast<uint32_t *>(residual_dev), stream));
 }
 
+size_t nrnn_input_projection_workspace_bytes(int dtype, int64_t d_in, int64_t d_h) {
+    if (dtype == NRNN_BF16 && d_in > 0 && d_h > 0) return 0;
+    if (dtype != NRNN_F32 || d_in <= 0 || d_h <= 0 || d_in > INT32_MAX || 3 * d_h > INT32_MAX)
+        return 0;
+    // the low part of W_x, (3 d_h, d_in) fp32
+    return sizeof(float) * static_cast<size_t>(3 * d_h) * static_cast<size_t>(d_in);
+}
+
 int nrnn_input_projection(const void *x, const void *W_x, int dtype, int64_t rows, int64_t d_in,
-                          int64_t d_h, void *preact, void *stream) {
+                          int64_t d_h, void *preact, void *workspace, size_t ws_bytes,
+                          void *stream) {
     if (dtype != NRNN_F32 && dtype != NRNN_BF16) return NRNN_ERR_INVALID_ARG;
     if (rows < 0 || d_in <= 0 || d_h <= 0) return NRNN_ERR_INVALID_ARG;
     if (rows > 0 && (x == nullptr || W_x == nullptr || preact == nullptr)) return NRNN_ERR_INVALID_ARG;
@@ -568,6 +577,10 @@ int nrnn_input_projection(const void *x, const void *W_x, int dtype, int64_t row
         rows > INT32_MAX)
         return NRNN_ERR_UNSUPPORTED;
     if (rows == 0) return NRNN_OK;
+    const size_t need = nrnn_input_projection_workspace_bytes(dtype, d_in, d_h);
+    if (need > 0 && (workspace == nullptr || ws_bytes < need ||
+                     (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0))
+        return NRNN_ERR_WORKSPACE;
     if (!aligned16(x) || !aligned16(W_x) || !aligned16(preact)) return NRNN_ERR_INVALID_ARG;
     CUtensorMap tmA, tmB, tmP;
     const int64_t n_out = 3 * d_h;
@@ -581,13 +594,19 @@ int nrnn_input_projection(const void *x, const void *W_x, int dtype, int64_t row
         return cuda_status(launch_projection_tc(tmA, tmB, tmP, rows, static_cast<int>(d_in),
                                                 static_cast<int>(n_out), st));
     }
+    // split-TF32: the static operand W_x is split once per call (its low part
+    // into the workspace); the kernel splits the x tiles as they arrive
     const int bn = projection_tf32x3_bn(static_cast<int>(n_out));
+    CUtensorMap tmBlo;
     if (!make_map_2d_sw128(&tmA, x, d_in, rows, PROJ_T3_BOX_K, PROJ_T3_BOX_M, NRNN_F32) ||
         !make_map_2d_sw128(&tmB, W_x, d_in, n_out, PROJ_T3_BOX_K, bn, NRNN_F32) ||
+        !make_map_2d_sw128(&tmBlo, workspace, d_in, n_out, PROJ_T3_BOX_K, bn, NRNN_F32) ||
         !make_map_2d(&tmP, preact, n_out, rows, PROJ_OUT_BOX, PROJ_OUT_BOX, NRNN_F32,
                      CU_TENSOR_MAP_SWIZZLE_128B))
         return NRNN_ERR_CUDA;
-    return cuda_status(launch_projection_tf32x3(tmA, tmB, tmP, rows, static_cast<int>(d_in),
+    cudaError_t e = launch_split_low(W_x, workspace, n_out * d_in, st);
+    if (e != cudaSuccess) return NRNN_ERR_CUDA;
+    return cuda_status(launch_projection_tf32x3(tmA, tmB, tmBlo, tmP, rows, static_cast<int>(d_in),
                                                 static_cast<int>(n_out), st));
 }
 

@@ -154,13 +154,16 @@ cudaError_t launch_projection_tc(const CUtensorMap &tmA, const CUtensorMap &tmB,
                                  cudaStream_t stream);
 
 // fp32 split-TF32 tensor-core projection: tmA over x (d_in, rows) with a
-// 32 x 128 box, tmB over W_x (d_in, n_out) with a 32 x projection_tf32x3_bn(n_out)
-// box, both fp32 with the 128-byte swizzle; tmP over P (n_out, rows) with a
-// PROJ_OUT_BOX x PROJ_OUT_BOX box and the 128-byte swizzle.
+// 32 x 128 box, tmB over W_x and tmBlo over its low part (both (d_in, n_out))
+// with a 32 x projection_tf32x3_bn(n_out) box, all fp32 with the 128-byte
+// swizzle; tmP over P (n_out, rows) with a PROJ_OUT_BOX x PROJ_OUT_BOX box and
+// the 128-byte swizzle.
 constexpr int PROJ_T3_BOX_K = 32, PROJ_T3_BOX_M = 128;
 int projection_tf32x3_bn(int n_out);
 cudaError_t launch_projection_tf32x3(const CUtensorMap &tmA, const CUtensorMap &tmB,
-                                     const CUtensorMap &tmP, int64_t rows, int d_in, int n_out,
-                                     cudaStream_t stream);
+                                     const CUtensorMap &tmBlo, const CUtensorMap &tmP,
+                                     int64_t rows, int d_in, int n_out, cudaStream_t stream);
+// lo[i] = w[i] - (w[i] with its low 13 mantissa bits cleared), n fp32 values
+cudaError_t launch_split_low(const void *w, void *lo, int64_t n, cudaStream_t stream);
 
 }  // namespace nrnn

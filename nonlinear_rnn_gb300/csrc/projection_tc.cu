@@ -13,16 +13,19 @@
 //   warps 4..7  epilogue: tcgen05.ld of their 32-lane quarter, 32 x 32
 //               blocks staged in shared memory and sent out by TMA stores,
 //               then release the accumulator; it overlaps the next K loop
-//   warps 8..11 (fp32 only) split each staged tile in place for split-TF32
+//   warps 8..15 (fp32 only) split each staged x tile for split-TF32
 // bf16: kind::f16, 128 x 256 tiles, 64-wide K slices, 4 stages, fp32
 // accumulation rounded to bf16.  fp32: split-TF32 ("3xTF32") -- each fp32
-// operand x is read by kind::tf32 as hi = x with its low 13 mantissa bits
-// dropped (the tensor core ignores them, so the staged tile serves as hi
-// unchanged), and the splitter warps write lo = x - hi (exact, |lo| < 2^-10
-// |x|) beside it, and
+// operand v is read by kind::tf32 as hi = v with its low 13 mantissa bits
+// dropped (the tensor core ignores them, so a staged tile serves as hi
+// unchanged), lo = v - hi is exact with |lo| < 2^-10 |v|, and
 //   A B ~ A_hi B_hi + A_hi B_lo + A_lo B_hi
 // (the dropped A_lo B_lo and the TF32 reading of lo are of order 2^-20
-// relative), 128 x 128 tiles, 32-wide K slices, 3 stages.
+// relative).  The low part of the static operand W_x is computed once per
+// call into global memory (k_split_low) and staged by TMA like its high part;
+// the splitter warps write the low part of each staged x tile beside it with
+// 16-byte accesses.  128 x 128 tiles in 3 stages, or 128 x 256 in 2, with
+// 32-wide K slices.
 // Out-of-range rows, columns and K are zero-filled by TMA loads and clipped
 // by TMA stores.  Every wait is bounded; a wait that gives up sets
 // g_projection_tc_error and the epilogue writes NaN, which the Newton residual
@@ -62,7 +65,7 @@ template <int BN_, int STAGES_> struct ProjCfgTf32 {   // fp32 split-TF32
     static constexpr int BM = 128, BN = BN_, BK = 32, STAGES = STAGES_;
     static constexpr int A_BYTES = BM * BK * 4, B_BYTES = BN * BK * 4;
     static constexpr int STAGE_BYTES = 2 * (A_BYTES + B_BYTES);   // A | B | lo A | lo B
-    static constexpr int THREADS = 384;
+    static constexpr int THREADS = 512;
     static constexpr int MMA_K = 8;    // elements per instruction (32 bytes)
     // D fp32, A and B TF32, both K-major, N = BN, M = BM
     static constexpr uint32_t IDESC = idesc_kmajor<true>(BM, BN);
@@ -70,7 +73,18 @@ template <int BN_, int STAGES_> struct ProjCfgTf32 {   // fp32 split-TF32
 template <> struct ProjCfg<1> : ProjCfgTf32<128, 3> {};
 template <> struct ProjCfg<2> : ProjCfgTf32<256, 2> {};
 
-constexpr int SPLIT_THREADS = 128;
+constexpr int SPLIT_THREADS = 256;
+
+// v - (v with its low 13 mantissa bits cleared): what kind::tf32 drops, exact
+__device__ __forceinline__ float low_part(uint32_t bits) {
+    return __uint_as_float(bits) - __uint_as_float(bits & 0xffffe000u);
+}
+
+__global__ void k_split_low(const uint32_t *__restrict__ w, float *__restrict__ lo, int64_t n) {
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n; i += stride)
+        lo[i] = low_part(w[i]);
+}
 constexpr int EPI_THREADS = 128;
 
 // The epilogue writes each 32 x 32 block of the accumulator, converted to the
@@ -115,7 +129,8 @@ __device__ __forceinline__ void stage_row(unsigned char *blk, int r, const uint3
 template <int MODE>
 __global__ void __launch_bounds__(ProjCfg<MODE>::THREADS, 1)
     k_projection_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                    const __grid_constant__ CUtensorMap tmP, int64_t rows, int K, int N) {
+                    const __grid_constant__ CUtensorMap tmBlo, const __grid_constant__ CUtensorMap tmP,
+                    int64_t rows, int K, int N) {
     using C = ProjCfg<MODE>;
     constexpr bool F32 = C::F32;
     using Out = typename std::conditional<F32, float, __nv_bfloat16>::type;
@@ -150,6 +165,7 @@ __global__ void __launch_bounds__(ProjCfg<MODE>::THREADS, 1)
         fence_mbar_init();
         prefetch_tensormap(&tmA);
         prefetch_tensormap(&tmB);
+        if (F32) prefetch_tensormap(&tmBlo);
         prefetch_tensormap(&tmP);
     }
     if (warp == 2) {
@@ -175,9 +191,12 @@ __global__ void __launch_bounds__(ProjCfg<MODE>::THREADS, 1)
                 if (it >= C::STAGES)
                     mbar_wait_bounded(&empty_bar[s], ((it / C::STAGES) - 1) & 1, TC_WAIT_NS, error);
                 unsigned char *st = smem + s * C::STAGE_BYTES;
-                mbar_arrive_expect_tx(&full_bar[s], C::A_BYTES + C::B_BYTES);
+                // stage layout: A | B | lo A | lo B
+                mbar_arrive_expect_tx(&full_bar[s], C::A_BYTES + (F32 ? 2 : 1) * C::B_BYTES);
                 tma_load_2d(st, &tmA, &full_bar[s], kt * C::BK, static_cast<int>(m0));
                 tma_load_2d(st + C::A_BYTES, &tmB, &full_bar[s], kt * C::BK, n0);
+                if (F32)
+                    tma_load_2d(st + 2 * C::A_BYTES + C::B_BYTES, &tmBlo, &full_bar[s], kt * C::BK, n0);
             }
         }
     } else if (warp == 1 && lane == 0) {
@@ -221,12 +240,12 @@ __global__ void __launch_bounds__(ProjCfg<MODE>::THREADS, 1)
             for (int kt = 0; kt < kt_count; ++kt, ++it) {
                 const int s = it % C::STAGES;
                 mbar_wait_bounded(&full_bar[s], (it / C::STAGES) & 1, TC_WAIT_NS, error);
-                const uint32_t *raw = reinterpret_cast<const uint32_t *>(smem + s * C::STAGE_BYTES);
-                float *lo = reinterpret_cast<float *>(smem + s * C::STAGE_BYTES + C::A_BYTES + C::B_BYTES);
+                const uint4 *raw = reinterpret_cast<const uint4 *>(smem + s * C::STAGE_BYTES);
+                float4 *lo = reinterpret_cast<float4 *>(smem + s * C::STAGE_BYTES + C::A_BYTES + C::B_BYTES);
 #pragma unroll 4
-                for (int e = t; e < (C::A_BYTES + C::B_BYTES) / 4; e += SPLIT_THREADS) {
-                    const uint32_t bits = raw[e];
-                    lo[e] = __uint_as_float(bits) - __uint_as_float(bits & 0xffffe000u);
+                for (int e = t; e < C::A_BYTES / 16; e += SPLIT_THREADS) {
+                    const uint4 v = raw[e];
+                    lo[e] = make_float4(low_part(v.x), low_part(v.y), low_part(v.z), low_part(v.w));
                 }
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                 mbar_arrive(&split_bar[s]);
@@ -281,8 +300,9 @@ __global__ void __launch_bounds__(ProjCfg<MODE>::THREADS, 1)
 }
 
 template <int MODE>
-cudaError_t launch_tc(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUtensorMap &tmP,
-                      int64_t rows, int d_in, int n_out, cudaStream_t stream) {
+cudaError_t launch_tc(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUtensorMap &tmBlo,
+                      const CUtensorMap &tmP, int64_t rows, int d_in, int n_out,
+                      cudaStream_t stream) {
     using C = ProjCfg<MODE>;
     static std::atomic<unsigned long long> configured{0};
     static int sms_of[64];   // SMs per device: one persistent CTA each
@@ -307,7 +327,7 @@ cudaError_t launch_tc(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUte
     const int64_t n_tiles = ((rows + C::BM - 1) / C::BM) * ((n_out + C::BN - 1) / C::BN);
     const int64_t grid = n_tiles < sms_of[dev] ? n_tiles : sms_of[dev];
     k_projection_tc<MODE><<<static_cast<unsigned>(grid), C::THREADS, smem, stream>>>(
-        tmA, tmB, tmP, rows, d_in, n_out);
+        tmA, tmB, tmBlo, tmP, rows, d_in, n_out);
     return cudaGetLastError();
 }
 
@@ -316,16 +336,24 @@ cudaError_t launch_tc(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUte
 cudaError_t launch_projection_tc(const CUtensorMap &tmA, const CUtensorMap &tmB,
                                  const CUtensorMap &tmP, int64_t rows, int d_in, int n_out,
                                  cudaStream_t stream) {
-    return launch_tc<0>(tmA, tmB, tmP, rows, d_in, n_out, stream);
+    return launch_tc<0>(tmA, tmB, tmB, tmP, rows, d_in, n_out, stream);
 }
 
 int projection_tf32x3_bn(int n_out) { return n_out >= 512 ? 256 : 128; }
 
 cudaError_t launch_projection_tf32x3(const CUtensorMap &tmA, const CUtensorMap &tmB,
-                                     const CUtensorMap &tmP, int64_t rows, int d_in, int n_out,
-                                     cudaStream_t stream) {
-    if (projection_tf32x3_bn(n_out) == 256) return launch_tc<2>(tmA, tmB, tmP, rows, d_in, n_out, stream);
-    return launch_tc<1>(tmA, tmB, tmP, rows, d_in, n_out, stream);
+                                     const CUtensorMap &tmBlo, const CUtensorMap &tmP,
+                                     int64_t rows, int d_in, int n_out, cudaStream_t stream) {
+    if (projection_tf32x3_bn(n_out) == 256)
+        return launch_tc<2>(tmA, tmB, tmBlo, tmP, rows, d_in, n_out, stream);
+    return launch_tc<1>(tmA, tmB, tmBlo, tmP, rows, d_in, n_out, stream);
+}
+
+cudaError_t launch_split_low(const void *w, void *lo, int64_t n, cudaStream_t stream) {
+    const int64_t blocks = (n + 255) / 256;
+    k_split_low<<<static_cast<unsigned>(blocks < 1216 ? blocks : 1216), 256, 0, stream>>>(
+        static_cast<const uint32_t *>(w), static_cast<float *>(lo), n);
+    return cudaGetLastError();
 }
 
 }  // namespace nrnn

@@ -111,3 +111,23 @@ def test_decode_overlap_check_uses_each_buffer_size():
     st = lib.nrnn_decode_step(ctypes.c_void_p(pre), 0, ctypes.c_void_p(256), slots, d_h, None,
                               ctypes.c_void_p(pre + 64), None)
     assert st == -1
+
+
+def test_projection_workspace_size_and_checks():
+    """fp32 takes the low part of W_x (3 d_h x d_in fp32) in the caller's
+    workspace; bf16 needs none.  Checks run before any launch."""
+    lib = nr.load()
+    assert lib.nrnn_input_projection_workspace_bytes(0, 512, 512) == 3 * 512 * 512 * 4
+    assert lib.nrnn_input_projection_workspace_bytes(1, 512, 512) == 0
+    assert lib.nrnn_input_projection_workspace_bytes(5, 512, 512) == 0
+    fake = ctypes.c_void_p(256)
+    need = 3 * 16 * 64 * 4
+
+    def call(ws, wsb, dtype=0, rows=100):
+        return lib.nrnn_input_projection(fake, fake, dtype, rows, 64, 16, ctypes.c_void_p(1 << 24),
+                                         ws, wsb, None)
+    assert call(None, 0) == -7                            # fp32 without a workspace
+    assert call(ctypes.c_void_p(4096), need - 4) == -7    # too small
+    assert call(ctypes.c_void_p(4096 + 16), need) == -7   # not 256-byte aligned
+    assert call(None, 0, rows=0) == 0                     # nothing to do
+    assert lib.nrnn_input_projection(fake, fake, 0, 100, 60, 16, fake, None, 0, None) == -3
