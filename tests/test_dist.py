@@ -50,7 +50,7 @@ def test_two_rank_max_timing_and_token_total():
 def test_traffic_record_is_tied_to_the_kernel_sources(monkeypatch):
     import bench
     import synthetic as syn
-    w = syn.WORKLOADS[1]
+    w = syn.WORKLOADS[bench.DEFAULT_WORKLOAD]   # the headline workload is always recorded
     with open(os.path.join(bench.ROOT, "profiles", "traffic.json")) as fh:
         rec = __import__("json").load(fh)
     if rec.get("_kernel_sources_sha256") == bench.kernel_sources_digest():
