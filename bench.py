@@ -198,7 +198,7 @@ def time_workload(torch, nr, w, args, dev, flush, stream, xu_rates, props, mhz):
         else:
             step = call
         for _ in range(args.warmup):
-            flush.fill_(1.0)
+            flush()
             step()
         ms_l, _ = time_steps(torch, step, max(3, min(args.steps, 10)), flush, stream, nvtx=False)
         ms = sum(ms_l) / len(ms_l)
@@ -229,7 +229,7 @@ def time_graph(torch, fn, args, flush, stream):
             fn()
         step = g.replay
     for _ in range(args.warmup):
-        flush.fill_(1.0)
+        flush()
         step()
     ms, _ = time_steps(torch, step, max(3, min(args.steps, 10)), flush, stream, nvtx=False)
     return statistics.median(ms)
@@ -254,7 +254,25 @@ def bench_config(w, args, world):
             "K": w.K, "segments": w.segments, "algo": args.algo,
             "parallelism": f"replica x{world}",
             "launch": "CUDA graph replay of one forward" if args.graph else "eager launches",
-            "l2": f"flushed between steps ({L2_FLUSH_BYTES >> 20} MiB write, untimed)"}
+            "l2": f"flushed between steps ({L2_FLUSH_BYTES >> 20} MiB write, then "
+                  f"{L2_FLUSH_BYTES >> 20} MiB read; untimed)"}
+
+
+class L2Flush:
+    """Empties L2 between timed steps, outside the timed region: writes a buffer
+    larger than L2, then reads another one, so that the step starts with a
+    cold L2 holding clean lines only (dirty lines of the write alone would be
+    written back during the timed step)."""
+
+    def __init__(self, torch, dev):
+        self.torch = torch
+        self.w = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+        self.r = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+        self.out = torch.empty((), dtype=torch.float32, device=dev)
+
+    def __call__(self):
+        self.w.fill_(1.0)
+        self.torch.sum(self.r, 0, out=self.out)
 
 
 def time_steps(torch, fn, steps, flush, stream, nvtx=True):
@@ -263,7 +281,7 @@ def time_steps(torch, fn, steps, flush, stream, nvtx=True):
           for _ in range(steps)]
     out = None
     for i in range(steps):
-        flush.fill_(1.0)
+        flush()
         if nvtx:
             torch.cuda.nvtx.range_push("nrnn_step")
         ev[i][0].record(stream)
@@ -293,7 +311,7 @@ def run_ours(args, w, rank, world, local):
     algo = args.algo
     ws = torch.empty(max(nr.workspace_bytes(w.B, w.T, w.d_h, tdt, w.K, a) for a in ("fused", "per_iter")),
                      dtype=torch.uint8, device=dev)
-    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    flush = L2Flush(torch, dev)
     stream = torch.cuda.current_stream(dev)
 
     def newton_call(a=algo):
@@ -326,7 +344,7 @@ def run_ours(args, w, rank, world, local):
     xu_rates = nr.probe_xu_rates(dev)   # live denominator of the fused kernel's ALU roof
 
     for _ in range(args.warmup):
-        flush.fill_(1.0)
+        flush()
         newton()
     torch.cuda.synchronize()
 
@@ -336,7 +354,7 @@ def run_ours(args, w, rank, world, local):
         t_pre = time.perf_counter()
         while time.perf_counter() - t_pre < args.preroll_s:
             for _ in range(20):
-                flush.fill_(1.0)
+                flush()
                 newton()
             torch.cuda.synchronize()
         if world > 1:
@@ -472,6 +490,10 @@ def run_ours(args, w, rank, world, local):
                          "achieved_gbs": nbytes / (dm * 1e-3) / 1e9,
                          "frac": nbytes / (dm * 1e-3) / 1e9 / pk["hbm_gbs"]}
 
+        # a step for every token of the workload as a slot (P and h far larger
+        # than L2: the kernel's bandwidth), then the batch sizes of serving;
+        # small steps sit near the event-timing floor of a few microseconds
+        decode_leg("decode_all_tokens", tokens, False)
         big = min(8192, tokens)
         decode_leg("decode", big, False)
         decode_leg("decode_x", big, True)                       # projection, then the step

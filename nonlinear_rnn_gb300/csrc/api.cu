@@ -538,6 +538,18 @@ int nrnn_decode_step_x(const void *x, const void *W_x, int dtype, const float *p
     if (slots > 8 * 65535 || d_h > INT32_MAX / 3 || d_in > INT32_MAX || d_in % 8 != 0)
         return NRNN_ERR_UNSUPPORTED;
     if (!aligned16(x) || !aligned16(W_x)) return NRNN_ERR_INVALID_ARG;
+    if (dtype == NRNN_BF16) {
+        // the projection on the tensor cores, the step in the epilogue
+        CUtensorMap tmX, tmW;
+        const int units = decode_xtc_units(static_cast<int>(slots), static_cast<int>(d_h));
+        if (!make_map_2d_sw128(&tmX, x, d_in, slots, 64, 64) ||
+            !make_map_2d_sw128(&tmW, W_x, d_in, 3 * d_h, 64, static_cast<uint32_t>(units)))
+            return NRNN_ERR_CUDA;
+        return cuda_status(launch_decode_step_xtc(tmX, tmW, params, h_in, h_out,
+                                                  static_cast<int>(slots), static_cast<int>(d_in),
+                                                  static_cast<int>(d_h),
+                                                  static_cast<cudaStream_t>(stream)));
+    }
     return cuda_status(launch_decode_step_x(dtype, x, W_x, params, h_in, h_out,
                                             static_cast<int>(slots), static_cast<int>(d_in),
                                             static_cast<int>(d_h),

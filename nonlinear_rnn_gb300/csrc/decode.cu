@@ -8,8 +8,10 @@
 // allow).
 // k_decode_step_x: the same step with the input projection fused in, for
 // small slot counts (a batched matrix-vector product per step; see below).
+// k_decode_step_xtc: the same for bf16 on the tensor cores (see below).
 #include "nrnn_device.cuh"
 #include "nrnn_internal.h"
+#include "tcgen05.cuh"
 
 namespace nrnn {
 
@@ -168,7 +170,171 @@ __global__ void __launch_bounds__(DX_UNITS * 32)
     }
 }
 
+// k_decode_step_xtc (bf16): the projection of a small batch of slots on the
+// tensor cores, the step in the epilogue.  A CTA takes UNITS units (32, or 8
+// when that leaves too few CTAs to keep W_x streaming from HBM) and 64 slots:
+// D = W_tile x_tile^T with M = 128 TMEM lanes (gate g's UNITS rows of W_x at
+// rows 32 g ..; the other rows unused), N = 64 slots, K = d_in in 64-wide
+// slices through a ring of TMA stages (128-byte swizzle; rows past the slots
+// or units and columns past d_in are zero-filled).  Warps 0..2 then read their
+// gate's lanes (lane = unit, registers = slots), round them to bf16 as a
+// stored preactivation would be, and pass them through shared memory; every
+// thread applies the cell to (slot, unit) pairs, adjacent units of a slot on
+// adjacent lanes.  A wait that gives up writes NaN.
+constexpr int XT_SLOTS = 64;
+constexpr int XT_BK = 64;
+constexpr int XT_STAGES = 8;
+constexpr int XT_A_BYTES = 128 * XT_BK * 2;                 // M = 128 rows
+constexpr int XT_B_BYTES = XT_SLOTS * XT_BK * 2;
+constexpr int XT_STAGE_BYTES = XT_A_BYTES + XT_B_BYTES;     // 24 KiB
+constexpr uint32_t XT_TMEM_COLS = XT_SLOTS;
+constexpr uint32_t XT_IDESC = idesc_kmajor<false>(128, XT_SLOTS);
+constexpr uint64_t XT_WAIT_NS = 2000000000ull;
+static_assert(XT_STAGES * XT_STAGE_BYTES >= 3 * XT_SLOTS * 32 * 4,
+              "the gate values must fit in the stage ring");
+
+template <int UNITS>
+__global__ void __launch_bounds__(128)
+    k_decode_step_xtc(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
+                      const float *__restrict__ params, const __nv_bfloat16 *__restrict__ h_in,
+                      __nv_bfloat16 *__restrict__ h_out, int slots, int d_in, int d_h) {
+    constexpr int W_BOX_BYTES = UNITS * XT_BK * 2;   // one gate's UNITS rows of W_x
+    extern __shared__ unsigned char xt_raw[];
+    unsigned char *smem = reinterpret_cast<unsigned char *>(
+        (reinterpret_cast<uintptr_t>(xt_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    __shared__ __align__(8) uint64_t full_bar[XT_STAGES], empty_bar[XT_STAGES], acc_bar;
+    __shared__ uint32_t s_tmem, s_err;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int u0 = blockIdx.x * UNITS, s0 = blockIdx.y * XT_SLOTS;
+    const int kt_count = (d_in + XT_BK - 1) / XT_BK;
+    if (tid == 0) {
+        for (int i = 0; i < XT_STAGES; ++i) {
+            mbar_init(&full_bar[i], 1);
+            mbar_init(&empty_bar[i], 1);
+        }
+        mbar_init(&acc_bar, 1);
+        s_err = 0u;
+        fence_mbar_init();
+        prefetch_tensormap(&tmX);
+        prefetch_tensormap(&tmW);
+    }
+    if (warp == 2) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_u32(&s_tmem)),
+                     "r"(XT_TMEM_COLS)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    __syncthreads();
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    const uint32_t tmem = s_tmem;
+    if (warp == 0 && lane == 0) {
+        // TMA producer: the three gates' W_x rows of this unit tile, x rows of these slots
+        for (int kt = 0; kt < kt_count; ++kt) {
+            const int st = kt % XT_STAGES;
+            if (kt >= XT_STAGES)
+                mbar_wait_bounded(&empty_bar[st], ((kt / XT_STAGES) - 1) & 1, XT_WAIT_NS, &s_err);
+            unsigned char *A = smem + st * XT_STAGE_BYTES;
+            mbar_arrive_expect_tx(&full_bar[st], 3 * W_BOX_BYTES + XT_B_BYTES);
+#pragma unroll
+            for (int g = 0; g < 3; ++g)   // gate g at rows 32 g (32 rows x 128 bytes apart)
+                tma_load_2d(A + g * 32 * XT_BK * 2, &tmW, &full_bar[st], kt * XT_BK, g * d_h + u0);
+            tma_load_2d(A + XT_A_BYTES, &tmX, &full_bar[st], kt * XT_BK, s0);
+        }
+    } else if (warp == 1 && lane == 0) {
+        // MMA issuer
+        for (int kt = 0; kt < kt_count; ++kt) {
+            const int st = kt % XT_STAGES;
+            mbar_wait_bounded(&full_bar[st], (kt / XT_STAGES) & 1, XT_WAIT_NS, &s_err);
+            asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+            const uint32_t A = smem_u32(smem + st * XT_STAGE_BYTES);
+#pragma unroll
+            for (int kk = 0; kk < XT_BK / 16; ++kk)
+                mma<false, XT_IDESC>(tmem, sw128_desc(A + kk * 32), sw128_desc(A + XT_A_BYTES + kk * 32),
+                                     (kt > 0 || kk > 0) ? 1u : 0u);
+            mma_commit(&empty_bar[st]);
+        }
+        mma_commit(&acc_bar);
+    }
+    __syncwarp();
+    const bool ok = mbar_wait_bounded(&acc_bar, 0, XT_WAIT_NS, &s_err);
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    fence_proxy_async_smem();   // the gate values overwrite the stages
+    float *Pg = reinterpret_cast<float *>(smem);   // [3 gates][64 slots][UNITS units]
+    if (warp < 3) {
+#pragma unroll 1
+        for (int cc = 0; cc < XT_SLOTS / 32; ++cc) {
+            uint32_t v[32];
+            tmem_ld_cols<32>(tmem + (static_cast<uint32_t>(warp * 32) << 16) + cc * 32, v);
+            if (lane < UNITS) {
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                    Pg[(warp * XT_SLOTS + cc * 32 + i) * UNITS + lane] =
+                        ok ? round_to<__nv_bfloat16>(__uint_as_float(v[i])) : __int_as_float(0x7fffffff);
+            }
+        }
+    }
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    __syncthreads();
+    if (warp == 2) {
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                     "r"(XT_TMEM_COLS)
+                     : "memory");
+    }
+    // the step: thread t takes unit u0 + t % UNITS of slots t / UNITS, + 128 / UNITS, ...
+    const int ul = tid % UNITS, u = u0 + ul;
+    if (u >= d_h) return;
+    const UnitParams prm = load_unit_params(params, d_h, u, true);
+#pragma unroll 4
+    for (int s = tid / UNITS; s < XT_SLOTS; s += 128 / UNITS) {
+        const int slot = s0 + s;
+        if (slot >= slots) break;
+        const int64_t i = static_cast<int64_t>(slot) * d_h + u;
+        const float h = (h_in != nullptr) ? to_f32(h_in[i]) : 0.f;
+        h_out[i] = from_f32<__nv_bfloat16>(cell_f(h, Pg[(0 * XT_SLOTS + s) * UNITS + ul],
+                                                  Pg[(1 * XT_SLOTS + s) * UNITS + ul],
+                                                  Pg[(2 * XT_SLOTS + s) * UNITS + ul], prm));
+    }
+}
+
 }  // namespace
+
+int decode_xtc_units(int slots, int d_h) {
+    // 32-unit tiles when they alone give about one CTA per SM, else 8-unit
+    // tiles (four times the CTAs streaming W_x)
+    const int64_t ctas32 = static_cast<int64_t>((d_h + 31) / 32) * ((slots + XT_SLOTS - 1) / XT_SLOTS);
+    return ctas32 >= 128 ? 32 : 8;
+}
+
+template <int UNITS>
+cudaError_t launch_xtc(const CUtensorMap &tmX, const CUtensorMap &tmW, const float *params,
+                       const void *h_in, void *h_out, int slots, int d_in, int d_h,
+                       cudaStream_t stream) {
+    static std::atomic<unsigned long long> configured{0};
+    constexpr size_t smem = static_cast<size_t>(XT_STAGES) * XT_STAGE_BYTES + 1024;
+    cudaError_t e = once_per_device(configured, [](int) {
+        return cudaFuncSetAttribute(k_decode_step_xtc<UNITS>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    static_cast<int>(smem));
+    });
+    if (e != cudaSuccess) return e;
+    const dim3 grid((d_h + UNITS - 1) / UNITS, (slots + XT_SLOTS - 1) / XT_SLOTS);
+    k_decode_step_xtc<UNITS><<<grid, 128, smem, stream>>>(
+        tmX, tmW, params, static_cast<const __nv_bfloat16 *>(h_in),
+        static_cast<__nv_bfloat16 *>(h_out), slots, d_in, d_h);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_decode_step_xtc(const CUtensorMap &tmX, const CUtensorMap &tmW,
+                                   const float *params, const void *h_in, void *h_out, int slots,
+                                   int d_in, int d_h, cudaStream_t stream) {
+    if (slots == 0) return cudaSuccess;
+    if (decode_xtc_units(slots, d_h) == 32)
+        return launch_xtc<32>(tmX, tmW, params, h_in, h_out, slots, d_in, d_h, stream);
+    return launch_xtc<8>(tmX, tmW, params, h_in, h_out, slots, d_in, d_h, stream);
+}
 
 cudaError_t launch_decode_step(int dtype, const void *P, const float *params, const void *h_in,
                                void *h_out, int slots, int d_h, cudaStream_t stream) {

@@ -133,6 +133,13 @@ cudaError_t launch_decode_step(int dtype, const void *P, const float *params, co
 cudaError_t launch_decode_step_x(int dtype, const void *x, const void *W, const float *params,
                                  const void *h_in, void *h_out, int slots, int d_in, int d_h,
                                  cudaStream_t stream);
+// bf16 decode step with the projection on the tensor cores: tmX over x (d_in,
+// slots) with a 64 x 64 box, tmW over W_x (d_in, 3 d_h) with a 64 x
+// decode_xtc_units(slots, d_h) box, both with the 128-byte swizzle
+int decode_xtc_units(int slots, int d_h);
+cudaError_t launch_decode_step_xtc(const CUtensorMap &tmX, const CUtensorMap &tmW,
+                                   const float *params, const void *h_in, void *h_out, int slots,
+                                   int d_in, int d_h, cudaStream_t stream);
 
 cudaError_t launch_sequential(int dtype, const void *P, const float *params, int B, int T,
                               int d_h, const int32_t *cu, int S, void *H, cudaStream_t stream);
