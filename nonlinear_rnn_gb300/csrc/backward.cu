@@ -20,7 +20,10 @@
 // chunk waited for has started); the carry nu at the chunk end is then applied,
 // dL/dP staged in the P tile and stored by TMA.  Parameter gradients are reduced
 // over the CTA and added with one atomicAdd per (gate, unit).  Every wait is
-// bounded.
+// bounded.  When few chunks of each column are resident at once, the next
+// chunk in time (processed earlier) has usually finished: warp 0 then reads
+// the look-back slots of chunks c + 1 and c + 2 as soon as the tile is known,
+// and the look-back starts from what they held (EARLY).
 #include "nrnn_device.cuh"
 #include "nrnn_internal.h"
 #include "tcgen05.cuh"
@@ -109,7 +112,7 @@ __device__ __forceinline__ Derivs2 derivs2(float2 hs, float2 pz, float2 pr, floa
     return d;
 }
 
-template <typename TS>
+template <typename TS, bool EARLY>
 __global__ void __launch_bounds__(NW * 32, 4)
     k_backward(const __grid_constant__ CUtensorMap tmP, const __grid_constant__ CUtensorMap tmH,
                const __grid_constant__ CUtensorMap tmG, const __grid_constant__ CUtensorMap tmGP,
@@ -139,6 +142,13 @@ __global__ void __launch_bounds__(NW * 32, 4)
 
     const int c = s_tile[0], b = s_tile[1], ut = s_tile[2];
     const int t0 = c * L, u0 = ut * U;
+    const int tile = (b * a.n_ut + ut) * a.n_chunks + c;
+    unsigned long long *slot = a.slots + static_cast<size_t>(tile) * 32 + lane;
+    unsigned long long pre1 = SLOT_EMPTY, pre2 = SLOT_EMPTY;
+    if (EARLY && warp == 0) {
+        if (c + 1 < a.n_chunks) pre1 = ld_relaxed_u64(slot + 32);
+        if (c + 2 < a.n_chunks) pre2 = ld_relaxed_u64(slot + 64);
+    }
 
     if (tid == 0) {
         mbar_init(&s_bar, 1);
@@ -217,14 +227,12 @@ __global__ void __launch_bounds__(NW * 32, 4)
             tB = fmaf(s_aggA[w][lane], tB, s_aggB[w][lane]);
             tA *= s_aggA[w][lane];
         }
-        const int tile = (b * a.n_ut + ut) * a.n_chunks + c;
-        unsigned long long *slot = a.slots + static_cast<size_t>(tile) * 32 + lane;
         float C = 0.f;   // nu at the first step after the chunk
         if (c == a.n_chunks - 1) {
             publish(slot, 0.f, tB);
         } else {
             publish(slot, tA, tB);
-            C = lookback_lane<4>(slot, c, +1, a.n_chunks, a.wait_ns, a.error);
+            C = lookback_lane<4>(slot, c, +1, a.n_chunks, a.wait_ns, a.error, pre1, pre2);
             publish(slot, 0.f, fmaf(tA, C, tB));
         }
         s_C[lane] = C;
@@ -285,19 +293,38 @@ __global__ void __launch_bounds__(NW * 32, 4)
     if (tid == 0) bulk_wait_read<0>();   // the tile outlives the store's reads
 }
 
-template <typename TS>
+template <typename TS, bool EARLY>
 cudaError_t launch_bw(const CUtensorMap &tmP, const CUtensorMap &tmH, const CUtensorMap &tmG,
                       const CUtensorMap &tmGP, const BackwardArgs &a, int64_t n_ctas,
                       cudaStream_t stream) {
     static std::atomic<unsigned long long> configured{0};
     constexpr size_t smem = static_cast<size_t>(5) * L * U * sizeof(TS);
     cudaError_t e = once_per_device(configured, [](int) {
-        return cudaFuncSetAttribute(k_backward<TS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        return cudaFuncSetAttribute(k_backward<TS, EARLY>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     static_cast<int>(smem));
     });
     if (e != cudaSuccess) return e;
-    k_backward<TS><<<static_cast<unsigned>(n_ctas), NW * 32, smem, stream>>>(tmP, tmH, tmG, tmGP, a);
+    k_backward<TS, EARLY><<<static_cast<unsigned>(n_ctas), NW * 32, smem, stream>>>(tmP, tmH, tmG,
+                                                                                 tmGP, a);
     return cudaGetLastError();
+}
+
+// the early reads pay when at most 4 chunks per column are resident at once
+// (4 CTAs per SM)
+bool bw_early(const BackwardArgs &a) {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return false;
+    return static_cast<int64_t>(sms) * 4 <= 4 * static_cast<int64_t>(a.B) * a.n_ut;
+}
+
+template <typename TS>
+cudaError_t launch_bw(const CUtensorMap &tmP, const CUtensorMap &tmH, const CUtensorMap &tmG,
+                      const CUtensorMap &tmGP, const BackwardArgs &a, int64_t n_ctas,
+                      cudaStream_t stream) {
+    return bw_early(a) ? launch_bw<TS, true>(tmP, tmH, tmG, tmGP, a, n_ctas, stream)
+                       : launch_bw<TS, false>(tmP, tmH, tmG, tmGP, a, n_ctas, stream);
 }
 
 }  // namespace
