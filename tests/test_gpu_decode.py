@@ -102,3 +102,35 @@ def test_decode_step_with_projection_at_other_sizes(dtype, slots, d_in, d_h):
     ref = oracle.decode_step(P, prm, h0)
     h = nr.decode_step(prm, h=dev(h0, tdt), x=dev(x, tdt), W_x=dev(W, tdt))
     assert np.max(np.abs(host(h) - ref)) <= (1e-5 if dtype == "f32" else 1.6e-2)
+
+
+@pytest.mark.parametrize("slots,d_in,d_h,zero_h", [(200, 200, 96, False), (512, 136, 512, False),
+                                                   (70, 64, 40, True)])
+def test_decode_step_x_bf16_tensor_core_path_through_the_c_abi(slots, d_in, d_h, zero_h):
+    """nrnn_decode_step_x for bf16 runs the projection on the tensor cores for
+    any slot count: 8-unit tiles (200 x 96; 70 x 40 from the zero state, with a
+    ragged unit tile) and 32-unit tiles (512 x 512, 128 CTAs); ragged slot
+    tiles and a K tail (d_in not a multiple of 64) are zero-filled by TMA."""
+    import ctypes
+    import nonlinear_rnn_gb300 as nr
+    lib = nr.load()
+    rng = np.random.default_rng(slots * 7 + d_h)
+    x = syn.round_bf16(rng.normal(size=(slots, d_in)).astype(np.float32))
+    W = syn.round_bf16((rng.uniform(-1, 1, size=(3 * d_h, d_in)) / math.sqrt(d_in)).astype(np.float32))
+    h0 = np.zeros((slots, d_h), np.float32) if zero_h else \
+        syn.round_bf16(rng.uniform(-0.5, 0.5, size=(slots, d_h)).astype(np.float32))
+    prm = syn.make_params(syn.small_workload(d_h=d_h, seed=65))
+    P = syn.round_bf16(oracle.input_projection(x, W).astype(np.float32))
+    ref = oracle.decode_step(P, prm, None if zero_h else h0)
+    xd, Wd = dev(x, torch.bfloat16), dev(W, torch.bfloat16)
+    hd = dev(h0, torch.bfloat16)
+    out = torch.full((slots, d_h), float("nan"), dtype=torch.bfloat16, device="cuda")
+    pd = nr.params_tensor(prm, d_h, "cuda")
+    p = lambda t: ctypes.c_void_p(t.data_ptr())   # noqa: E731
+    st = lib.nrnn_decode_step_x(p(xd), p(Wd), 1, p(pd), slots, d_in, d_h,
+                                None if zero_h else p(hd), p(out),
+                                ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert st == 0
+    torch.cuda.synchronize()
+    assert not torch.isnan(out).any()
+    assert np.max(np.abs(host(out) - ref)) <= 1.6e-2
