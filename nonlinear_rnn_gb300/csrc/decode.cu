@@ -9,6 +9,8 @@
 // k_decode_step_x: the same step with the input projection fused in, for
 // small slot counts (a batched matrix-vector product per step; see below).
 // k_decode_step_xtc: the same for bf16 on the tensor cores (see below).
+// Every decode kernel evaluates the cell in the storage type's formulation,
+// as the Newton kernels do: ex2/rcp for fp32, tanh.approx for bf16.
 #include "nrnn_device.cuh"
 #include "nrnn_internal.h"
 #include "tcgen05.cuh"
@@ -27,7 +29,7 @@ __global__ void __launch_bounds__(256)
     const UnitParams prm = load_unit_params(params, d_h, j, true);
     const TS *p = P + static_cast<int64_t>(s) * 3 * d_h + j;
     const float h = (h_in != nullptr) ? to_f32(h_in[i]) : 0.f;
-    h_out[i] = from_f32<TS>(cell_f(h, to_f32(p[0]), to_f32(p[d_h]), to_f32(p[2 * d_h]), prm));
+    h_out[i] = from_f32<TS>(cell_f_storage<TS>(h, to_f32(p[0]), to_f32(p[d_h]), to_f32(p[2 * d_h]), prm));
 }
 
 __device__ __forceinline__ void unpack16(const uint4 &v, float (&o)[4]) {
@@ -87,7 +89,7 @@ __global__ void __launch_bounds__(256)
 #pragma unroll
     for (int e = 0; e < VEC; ++e) {
         const UnitParams up{prm[0][e], prm[1][e], prm[2][e], prm[3][e], prm[4][e], prm[5][e]};
-        o[e] = from_f32<TS>(cell_f(h[e], z[e], r[e], c[e], up));
+        o[e] = from_f32<TS>(cell_f_storage<TS>(h[e], z[e], r[e], c[e], up));
     }
     *reinterpret_cast<uint4 *>(h_out + i0) = *reinterpret_cast<const uint4 *>(o);
 }
@@ -165,7 +167,7 @@ __global__ void __launch_bounds__(DX_UNITS * 32)
     if (lane < ns) {
         const int64_t i = static_cast<int64_t>(s0 + lane) * d_h + j;
         const float h = (h_in != nullptr) ? to_f32(h_in[i]) : 0.f;
-        h_out[i] = from_f32<TS>(cell_f(h, round_to<TS>(pz), round_to<TS>(pr), round_to<TS>(pc),
+        h_out[i] = from_f32<TS>(cell_f_storage<TS>(h, round_to<TS>(pz), round_to<TS>(pr), round_to<TS>(pc),
                                        load_unit_params(params, d_h, j, true)));
     }
 }
@@ -293,7 +295,7 @@ __global__ void __launch_bounds__(128)
         if (slot >= slots) break;
         const int64_t i = static_cast<int64_t>(slot) * d_h + u;
         const float h = (h_in != nullptr) ? to_f32(h_in[i]) : 0.f;
-        h_out[i] = from_f32<__nv_bfloat16>(cell_f(h, Pg[(0 * XT_SLOTS + s) * UNITS + ul],
+        h_out[i] = from_f32<__nv_bfloat16>(cell_f_storage<__nv_bfloat16>(h, Pg[(0 * XT_SLOTS + s) * UNITS + ul],
                                                   Pg[(1 * XT_SLOTS + s) * UNITS + ul],
                                                   Pg[(2 * XT_SLOTS + s) * UNITS + ul], prm));
     }
