@@ -277,6 +277,33 @@ def test_lookback_timeout_is_reported_and_context_survives(nr, algo):
     assert np.max(np.abs(host(H) - Href)) <= 2e-5
 
 
+@pytest.mark.parametrize("algo", ["fused", "per_iter"])
+def test_lookback_timeout_in_the_early_form(nr, algo):
+    """320 columns (10 rows x 32 unit tiles) leave at most 4 chunks of a column
+    resident, so the launcher takes the early look-back form, which reads the
+    nearest predecessors' slots before the CTA barrier: a tile that withholds
+    its publish still makes its successors' bounded waits run out, the call
+    reports NRNN_ERR_TIMEOUT, and the next call is correct."""
+    w = syn.small_workload(B=10, T=256, d_h=1024, seed=91)   # 4 chunks per column
+    P = syn.direct_preact(w)
+    prm = syn.make_params(w)
+    n_ut, n_chunks = 1024 // 32, 4
+    old_limit = nr.set_wait_limit_ns(2_000_000)               # 2 ms
+    try:
+        nr.debug_withhold_publish((3 * n_ut + 5) * n_chunks + 1)   # row 3, unit tile 5, chunk 1
+        with pytest.raises(nr.NrnnError) as ei:
+            nr.newton_forward(dev(P), prm, K=2, algo=algo)
+        assert ei.value.status == -6
+    finally:
+        nr.debug_withhold_publish(-1)
+        nr.set_wait_limit_ns(old_limit)
+    units = np.array([0, 5 * 32 + 7, 1023])
+    Pc, pc = oracle.columns(P, prm, units)
+    Href, _ = oracle.newton(Pc, pc, 2)
+    H, _ = nr.newton_forward(dev(P), prm, K=2, algo=algo)
+    assert np.max(np.abs(host(H)[:, :, units] - Href)) <= 2e-5
+
+
 def test_probe_xu_rates(nr):
     # special-function throughput per SM clock: a power-of-two rate on every
     # NVIDIA part so far; ex2 at least as fast as rcp
