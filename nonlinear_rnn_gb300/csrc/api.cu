@@ -236,7 +236,7 @@ const char *nrnn_status_string(int status) {
     }
 }
 
-int nrnn_version(void) { return 100; }
+int nrnn_version(void) { return 200; }   // 0.2.0: nrnn_input_projection takes a workspace
 
 uint64_t nrnn_set_wait_limit_ns(uint64_t ns) { return g_wait_ns.exchange(ns); }
 
