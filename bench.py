@@ -431,20 +431,31 @@ def run_ours(args, w, rank, world, local):
     seq_ms, _ = time_steps(torch, replay_of(lambda: nr.sequential_forward(P, prm, cu_seqlens=cu, out=H)), 3,
                            flush, stream, nvtx=False)
 
-    # end to end through the C-ABI call on host buffers (nrnn_newton_forward_host:
-    # blocks of rows or segments, copies overlapped with the kernels)
+    # end to end through the C-ABI calls on host buffers, copies overlapped
+    # block by block (blocks of rows or segments) with the kernels:
+    # nrnn_newton_forward_x_host takes x (W_x resident on the device, each
+    # block projected there), nrnn_newton_forward_host the preactivations
+    x_host = x.cpu().pin_memory()
     P_host = P.cpu().pin_memory()
     H_host = torch.empty(H.shape, dtype=H.dtype).pin_memory()
     cu_host = None if inp["cu_seqlens"] is None else inp["cu_seqlens"]
-    staging = torch.empty(nr.host_staging_bytes(w.B, w.T, w.d_h, tdt, w.K, cu_seqlens=cu_host),
+    staging = torch.empty(max(nr.x_host_staging_bytes(w.B, w.T, w.d_in, w.d_h, tdt, w.K, cu_seqlens=cu_host),
+                              nr.host_staging_bytes(w.B, w.T, w.d_h, tdt, w.K, cu_seqlens=cu_host)),
                           dtype=torch.uint8, device=dev)
 
-    def e2e_step():
+    def e2e_x_step():
+        nr.newton_forward_x_host(x_host, W, prm, cu_seqlens=cu_host, K=w.K, out=H_host,
+                                 staging=staging, check=False)
+
+    def e2e_p_step():
         nr.newton_forward_host(P_host, prm, cu_seqlens=cu_host, K=w.K, out=H_host,
                                staging=staging, device=dev, check=False)
-    e2e_step()
-    e2e, _ = time_steps(torch, e2e_step, max(3, min(args.steps, 10)), flush, stream, nvtx=False)
-    e2e_ms = statistics.median(e2e)
+    e2e_ms = {}
+    for name, fn in (("x", e2e_x_step), ("preact", e2e_p_step)):
+        fn()
+        t_e2e, _ = time_steps(torch, fn, max(3, min(args.steps, 10)), flush, stream, nvtx=False)
+        e2e_ms[name] = statistics.median(t_e2e)
+    del P_host, x_host
 
     proj = statistics.median(proj_ms)
 
@@ -548,9 +559,17 @@ def run_ours(args, w, rank, world, local):
         "config": bench_config(w, args, world),
         "roofline": roof,
         "per_iter_roofline": per_iter,
-        "e2e": {"value": tokens * world / (e2e_ms * 1e-3), "unit": "tokens/s",
-                "h2d_bytes_per_step": P.numel() * P.element_size(),
-                "d2h_bytes_per_step": H.numel() * H.element_size() + 4},
+        "e2e": {"value": tokens * world / (e2e_ms["x"] * 1e-3), "unit": "tokens/s",
+                "h2d_bytes_per_step": x.numel() * x.element_size(),
+                "d2h_bytes_per_step": H.numel() * H.element_size() + 4,
+                "ms_per_step": e2e_ms["x"],
+                "call": "nrnn_newton_forward_x_host (x on the host, W_x on the device, "
+                        "projection and forward per block)",
+                "from_preactivations": {
+                    "value": tokens * world / (e2e_ms["preact"] * 1e-3), "unit": "tokens/s",
+                    "h2d_bytes_per_step": P.numel() * P.element_size(),
+                    "d2h_bytes_per_step": H.numel() * H.element_size() + 4,
+                    "ms_per_step": e2e_ms["preact"], "call": "nrnn_newton_forward_host"}},
         # per step: the clear kernel of the call's workspace, then the Newton launch(es)
         "gpu_launches": (launches + 1) * args.steps,
         "with_projection": {"projection_ms": proj,

@@ -340,6 +340,34 @@ int nrnn_newton_forward_host(const void *preact_host, int dtype, const float *pa
                              int64_t tokens_per_block, void *stream);
 
 /*
+ * The same host-buffer forward from the input sequence x instead of its
+ * preactivations: the cell's input weights W_x stay on the device, each
+ * block's rows of x are copied in, projected by nrnn_input_projection into
+ * the block's preactivations on `stream`, and run through the forward as
+ * above.  d_in values per token cross the host link instead of 3 d_h.
+ *   x_host     host, (B, T, d_in) of dtype (page-locked for asynchronous copies)
+ *   W_x        device, (3 d_h, d_in) of dtype, 16-byte aligned
+ *   d_in       > 0 and a multiple of 8 (else NRNN_ERR_INVALID_ARG /
+ *              NRNN_ERR_UNSUPPORTED)
+ *   staging    device, staging_bytes >= nrnn_newton_x_host_staging_bytes(same
+ *              shape, cu_seqlens_host, tokens_per_block); 256-byte aligned;
+ *              it also holds the projection's workspace
+ * Other arguments, synchronisation and return codes as for
+ * nrnn_newton_forward_host.  Results equal nrnn_input_projection followed by
+ * nrnn_newton_forward up to the look-back's composition order.
+ * nrnn_newton_x_host_staging_bytes returns 0 for an invalid shape.
+ */
+size_t nrnn_newton_x_host_staging_bytes(int64_t B, int64_t T, int64_t d_in, int64_t d_h, int dtype,
+                                        int K, const int32_t *cu_seqlens_host,
+                                        int64_t num_segments, int64_t tokens_per_block);
+int nrnn_newton_forward_x_host(const void *x_host, const void *W_x, int dtype, const float *params,
+                               int64_t B, int64_t T, int64_t d_in, int64_t d_h,
+                               const int32_t *cu_seqlens_host, int64_t num_segments, int K,
+                               float residual_fail, void *H_host, float *residual_host,
+                               void *staging, size_t staging_bytes, int64_t tokens_per_block,
+                               void *stream);
+
+/*
  * Size of the device scratch array that nrnn_newton_forward_noalloc uses
  * (64 MiB on every GPU where the library is used, held until process exit).
  */

@@ -25,6 +25,7 @@ from ._binding import (  # noqa: F401
     newton_forward,
     newton_forward_host,
     newton_forward_x,
+    newton_forward_x_host,
     params_tensor,
     picard,
     probe_xu_rates,
@@ -35,6 +36,7 @@ from ._binding import (  # noqa: F401
     validate_cu_seqlens,
     verify_agreement,
     workspace_bytes,
+    x_host_staging_bytes,
 )
 
 load()

@@ -56,6 +56,9 @@ _SIGNATURES = {
     "nrnn_newton_host_staging_bytes": ([_i64, _i64, _i64, _int, _int, _vp, _i64, _i64], _sz),
     "nrnn_newton_forward_host": ([_vp, _int, _vp, _i64, _i64, _i64, _vp, _i64, _int, _f, _vp, _vp,
                                   _vp, _sz, _i64, _vp], _int),
+    "nrnn_newton_x_host_staging_bytes": ([_i64, _i64, _i64, _i64, _int, _int, _vp, _i64, _i64], _sz),
+    "nrnn_newton_forward_x_host": ([_vp, _vp, _int, _vp, _i64, _i64, _i64, _i64, _vp, _i64, _int, _f,
+                                    _vp, _vp, _vp, _sz, _i64, _vp], _int),
     "nrnn_newton_forward_noalloc": ([_vp, _int, _vp, _i64, _i64, _i64, _vp, _i64, _int, _f, _vp,
                                      _vp, _vp, _vp], _int),
 }
@@ -293,6 +296,70 @@ def newton_forward_host(preact: torch.Tensor, params, cu_seqlens=None, K: int = 
     if st == -5 and not check:
         return H, float(rho.value)
     _raise(st, "newton_forward_host", H=H, residual=float(rho.value))
+    return H, float(rho.value)
+
+
+def x_host_staging_bytes(B, T, d_in, d_h, dtype=torch.float32, K=3, cu_seqlens=None,
+                         tokens_per_block: int = 0) -> int:
+    code = F32 if dtype == torch.float32 else BF16
+    cu32 = None if cu_seqlens is None else validate_cu_seqlens(cu_seqlens, T)
+    return int(load().nrnn_newton_x_host_staging_bytes(
+        B, T, d_in, d_h, code, int(K),
+        None if cu32 is None else cu32.ctypes.data_as(ctypes.c_void_p),
+        0 if cu32 is None else cu32.size - 1, int(tokens_per_block)))
+
+
+def newton_forward_x_host(x: torch.Tensor, W_x: torch.Tensor, params, cu_seqlens=None, K: int = 3,
+                          residual_fail: float = 1.0, out: torch.Tensor | None = None,
+                          staging: torch.Tensor | None = None, tokens_per_block: int = 0,
+                          check: bool = True):
+    """Newton forward from x on the host (nrnn_newton_forward_x_host): x (B, T,
+    d_in) float32/bfloat16 CPU tensor, ideally pinned; W_x (3 d_h, d_in) a
+    device tensor of x's dtype, which names the device.  Each block of x is
+    copied in, projected on the device and run through the forward, the
+    copies overlapped with the kernels.  Returns (H, residual) as
+    newton_forward_host does."""
+    lib = load()
+    if x.device.type != "cpu":
+        raise ValueError("x must be a host tensor; use newton_forward_x for device tensors")
+    W_x = _device_tensor(W_x, "W_x")
+    if x.dtype != W_x.dtype:
+        raise TypeError("x and W_x must share a dtype")
+    if not x.is_contiguous():
+        x = x.contiguous()
+    if x.dim() != 3 or W_x.dim() != 2 or W_x.shape[1] != x.shape[2] or W_x.shape[0] % 3:
+        raise ValueError("x must have shape (B, T, d_in) and W_x (3 d_h, d_in)")
+    B, T, d_in = x.shape
+    d_h = W_x.shape[0] // 3
+    code = _dtype_code(x)
+    dev = W_x.device
+    prm = params_tensor(params, d_h, dev)
+    cu32 = None
+    if cu_seqlens is not None:
+        if B != 1:
+            raise ValueError("cu_seqlens requires batch 1 (x of shape (1, N, d))")
+        cu32 = validate_cu_seqlens(cu_seqlens, T)
+    H = out if out is not None else torch.empty((B, T, d_h), dtype=x.dtype).pin_memory()
+    if tuple(H.shape) != (B, T, d_h) or H.dtype != x.dtype or not H.is_contiguous() \
+            or H.device.type != "cpu":
+        raise ValueError("out must be a contiguous host tensor of shape (B, T, d_h) and x's dtype")
+    cu_ptr = None if cu32 is None else cu32.ctypes.data_as(ctypes.c_void_p)
+    S = 0 if cu32 is None else cu32.size - 1
+    nbytes = lib.nrnn_newton_x_host_staging_bytes(B, T, d_in, d_h, code, int(K), cu_ptr, S,
+                                                  int(tokens_per_block))
+    if nbytes == 0:
+        raise ValueError("invalid shape or K")
+    if staging is None or staging.numel() < nbytes:
+        staging = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    rho = ctypes.c_float(0.0)
+    with torch.cuda.device(dev):
+        st = lib.nrnn_newton_forward_x_host(_ptr(x), _ptr(W_x), code, _ptr(prm), B, T, d_in, d_h,
+                                            cu_ptr, S, int(K), float(residual_fail), _ptr(H),
+                                            ctypes.byref(rho), _ptr(staging), staging.numel(),
+                                            int(tokens_per_block), _stream(dev))
+    if st == -5 and not check:
+        return H, float(rho.value)
+    _raise(st, "newton_forward_x_host", H=H, residual=float(rho.value))
     return H, float(rho.value)
 
 

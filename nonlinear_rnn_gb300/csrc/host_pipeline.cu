@@ -6,7 +6,11 @@
 // stream, ordered by events, so the copies of one block overlap the kernels
 // and the copies of its neighbours.  Results equal nrnn_newton_forward on the
 // whole problem up to the look-back's composition order (a pack's blocks
-// start their time chunks at their own first token).
+// start their time chunks at their own first token).  The input of a block is
+// either its preactivations (nrnn_newton_forward_host) or its rows of x, which
+// nrnn_input_projection turns into preactivations on the device before the
+// forward (nrnn_newton_forward_x_host: d_in instead of 3 d_h values per token
+// cross the host link).
 #include <algorithm>
 #include <cmath>
 #include <cstring>
@@ -34,15 +38,18 @@ struct Block {
 
 struct Plan {
     std::vector<Block> blocks;
-    size_t p_bytes = 0, h_bytes = 0, ws_bytes = 0;   // per slot
+    size_t x_bytes = 0, p_bytes = 0, h_bytes = 0, ws_bytes = 0;   // per slot
     size_t slots_off[NSLOT] = {}, res_off = 0, err_off = 0, cu_off = 0, total = 0;
+    size_t proj_off = 0, proj_bytes = 0;   // x input: the projection's workspace (one)
     int64_t cu_ints = 0;
 };
 
 // Splits the problem into blocks of about tokens_per_block tokens (0: about
-// six blocks) and lays out the staging area.  Returns false on a bad shape.
-bool make_plan(int64_t B, int64_t T, int64_t d_h, int dtype, int K, const int32_t *cu,
-               int64_t S, int64_t tokens_per_block, Plan &pl) {
+// six blocks) and lays out the staging area: per slot [x rows (d_in > 0)] [P]
+// [H] [forward workspace], then the projection's workspace, residuals, error
+// words and rebased segment bounds.  Returns false on a bad shape.
+bool make_plan(int64_t B, int64_t T, int64_t d_in, int64_t d_h, int dtype, int K,
+               const int32_t *cu, int64_t S, int64_t tokens_per_block, Plan &pl) {
     const int64_t total = B * T;
     if (total == 0) return true;
     if (tokens_per_block <= 0) tokens_per_block = (total + 5) / 6;
@@ -66,6 +73,7 @@ bool make_plan(int64_t B, int64_t T, int64_t d_h, int dtype, int K, const int32_
     const size_t es = esize(dtype);
     for (const Block &bk : pl.blocks) {
         const size_t n = static_cast<size_t>(bk.nb * bk.nt);
+        if (d_in > 0) pl.x_bytes = std::max(pl.x_bytes, align_up(n * d_in * es));
         pl.p_bytes = std::max(pl.p_bytes, align_up(n * 3 * d_h * es));
         pl.h_bytes = std::max(pl.h_bytes, align_up(n * d_h * es));
         const size_t ws = nrnn_newton_workspace_bytes(bk.nb, bk.nt, d_h, dtype, K, NRNN_ALGO_FUSED);
@@ -75,7 +83,12 @@ bool make_plan(int64_t B, int64_t T, int64_t d_h, int dtype, int K, const int32_
     size_t off = 0;
     for (int i = 0; i < NSLOT; ++i) {
         pl.slots_off[i] = off;
-        off += pl.p_bytes + pl.h_bytes + pl.ws_bytes;
+        off += pl.x_bytes + pl.p_bytes + pl.h_bytes + pl.ws_bytes;
+    }
+    if (d_in > 0) {
+        pl.proj_off = off;
+        pl.proj_bytes = align_up(nrnn_input_projection_workspace_bytes(dtype, d_in, d_h));
+        off += pl.proj_bytes;
     }
     const size_t nblk = pl.blocks.size();
     pl.res_off = off;                                   // residuals, then error words:
@@ -117,13 +130,19 @@ Lanes *lanes_for_current_device() {
 
 int validate(const void *preact_host, int dtype, const float *params, int64_t B, int64_t T,
              int64_t d_h, const int32_t *cu, int64_t S, int K, const void *H_host,
-             const float *residual_host) {
+             const float *residual_host, int64_t d_in = 0, const void *W_x = nullptr) {
     if (dtype != NRNN_F32 && dtype != NRNN_BF16) return NRNN_ERR_INVALID_ARG;
     if (B < 0 || T < 0 || d_h <= 0 || K < 0 || residual_host == nullptr) return NRNN_ERR_INVALID_ARG;
     if (B > INT32_MAX || T > INT32_MAX || d_h > (1 << 24)) return NRNN_ERR_UNSUPPORTED;
     if (d_h % 8 != 0) return NRNN_ERR_UNSUPPORTED;
     if (B * T > 0 && (preact_host == nullptr || H_host == nullptr || params == nullptr))
         return NRNN_ERR_INVALID_ARG;
+    if (d_in != 0) {
+        if (d_in < 0) return NRNN_ERR_INVALID_ARG;
+        if (d_in % 8 != 0 || d_in > INT32_MAX) return NRNN_ERR_UNSUPPORTED;
+        if (B * T > 0 && (W_x == nullptr || (reinterpret_cast<uintptr_t>(W_x) & 15u) != 0))
+            return NRNN_ERR_INVALID_ARG;
+    }
     if (cu != nullptr) {
         if (B != 1) return NRNN_ERR_CU_SEQLENS;
         const int st = nrnn_validate_cu_seqlens(cu, S, T);
@@ -132,33 +151,33 @@ int validate(const void *preact_host, int dtype, const float *params, int64_t B,
     return NRNN_OK;
 }
 
-}  // namespace
-
-extern "C" {
-
-size_t nrnn_newton_host_staging_bytes(int64_t B, int64_t T, int64_t d_h, int dtype, int K,
-                                      const int32_t *cu_seqlens_host, int64_t num_segments,
-                                      int64_t tokens_per_block) {
+size_t staging_bytes(int64_t B, int64_t T, int64_t d_in, int64_t d_h, int dtype, int K,
+                     const int32_t *cu_seqlens_host, int64_t num_segments,
+                     int64_t tokens_per_block) {
     if (dtype != NRNN_F32 && dtype != NRNN_BF16) return 0;
-    if (B < 0 || T < 0 || d_h <= 0 || d_h % 8 != 0 || K < 0) return 0;
+    if (B < 0 || T < 0 || d_h <= 0 || d_h % 8 != 0 || K < 0 || d_in < 0) return 0;
     if (cu_seqlens_host != nullptr &&
         (B != 1 || nrnn_validate_cu_seqlens(cu_seqlens_host, num_segments, T) != NRNN_OK))
         return 0;
     Plan pl;
-    if (!make_plan(B, T, d_h, dtype, K, cu_seqlens_host, num_segments, tokens_per_block, pl)) return 0;
+    if (!make_plan(B, T, d_in, d_h, dtype, K, cu_seqlens_host, num_segments, tokens_per_block, pl))
+        return 0;
     return std::max<size_t>(pl.total, ALIGN);
 }
 
-int nrnn_newton_forward_host(const void *preact_host, int dtype, const float *params, int64_t B,
-                             int64_t T, int64_t d_h, const int32_t *cu_seqlens_host,
-                             int64_t num_segments, int K, float residual_fail, void *H_host,
-                             float *residual_host, void *staging, size_t staging_bytes,
-                             int64_t tokens_per_block, void *stream_) {
-    int st = validate(preact_host, dtype, params, B, T, d_h, cu_seqlens_host, num_segments, K,
-                      H_host, residual_host);
+// The pipeline behind both entry points; in_host holds the blocks' inputs:
+// x rows (d_in values per token, then projected with W_x) when d_in > 0,
+// else preactivations (3 d_h values per token).
+int forward_host(const void *in_host, int64_t d_in, const void *W_x, int dtype,
+                 const float *params, int64_t B, int64_t T, int64_t d_h,
+                 const int32_t *cu_seqlens_host, int64_t num_segments, int K,
+                 float residual_fail, void *H_host, float *residual_host, void *staging,
+                 size_t staging_bytes, int64_t tokens_per_block, void *stream_) {
+    int st = validate(in_host, dtype, params, B, T, d_h, cu_seqlens_host, num_segments, K,
+                      H_host, residual_host, d_in, W_x);
     if (st != NRNN_OK) return st;
     Plan pl;
-    if (!make_plan(B, T, d_h, dtype, K, cu_seqlens_host, num_segments, tokens_per_block, pl))
+    if (!make_plan(B, T, d_in, d_h, dtype, K, cu_seqlens_host, num_segments, tokens_per_block, pl))
         return NRNN_ERR_INVALID_ARG;
     if (B * T == 0) {
         *residual_host = 0.f;
@@ -199,21 +218,29 @@ int nrnn_newton_forward_host(const void *preact_host, int dtype, const float *pa
     for (size_t i = 0; i < nblk && e == cudaSuccess && call_status == NRNN_OK; ++i) {
         const int s = static_cast<int>(i % NSLOT);
         const Block &bk = pl.blocks[i];
-        unsigned char *P = base + pl.slots_off[s];
+        unsigned char *X = base + pl.slots_off[s];
+        unsigned char *P = X + pl.x_bytes;
         unsigned char *H = P + pl.p_bytes;
         unsigned char *ws = H + pl.h_bytes;
         // host offsets of the block: rows b0.. (full T) or tokens t0.. of row 0
         const size_t first = static_cast<size_t>(bk.b0 * T + bk.t0);
         const size_t n = static_cast<size_t>(bk.nb * bk.nt);
-        const unsigned char *src = static_cast<const unsigned char *>(preact_host) + first * 3 * d_h * es;
+        const size_t in_row = static_cast<size_t>(d_in > 0 ? d_in : 3 * d_h) * es;   // per token
+        const unsigned char *src = static_cast<const unsigned char *>(in_host) + first * in_row;
         unsigned char *dst = static_cast<unsigned char *>(H_host) + first * d_h * es;
 
-        if (i >= NSLOT) e = cudaStreamWaitEvent(s_in, ln->computed[s], 0);   // P slot read
-        if (e == cudaSuccess) e = cudaMemcpyAsync(P, src, n * 3 * d_h * es, cudaMemcpyHostToDevice, s_in);
+        if (i >= NSLOT) e = cudaStreamWaitEvent(s_in, ln->computed[s], 0);   // input slot read
+        if (e == cudaSuccess)
+            e = cudaMemcpyAsync(d_in > 0 ? X : P, src, n * in_row, cudaMemcpyHostToDevice, s_in);
         if (e == cudaSuccess && !single) e = cudaEventRecord(ln->loaded[s], s_in);
         if (e == cudaSuccess && !single) e = cudaStreamWaitEvent(stream, ln->loaded[s], 0);
         if (e == cudaSuccess && i >= NSLOT) e = cudaStreamWaitEvent(stream, ln->drained[s], 0);
         if (e != cudaSuccess) break;
+        if (d_in > 0) {
+            call_status = nrnn_input_projection(X, W_x, dtype, static_cast<int64_t>(n), d_in, d_h, P,
+                                                base + pl.proj_off, pl.proj_bytes, stream_);
+            if (call_status != NRNN_OK) break;
+        }
         call_status = nrnn_newton_forward(P, dtype, params, bk.nb, bk.nt, d_h,
                                           cu_seqlens_host ? cu_dev + bk.cu_off : nullptr,
                                           cu_seqlens_host ? bk.ns : 0, K, residual_fail,
@@ -254,6 +281,45 @@ int nrnn_newton_forward_host(const void *preact_host, int dtype, const float *pa
     if (timeout) return NRNN_ERR_TIMEOUT;
     if (!std::isfinite(rho) || rho > residual_fail) return NRNN_ERR_DIVERGED;
     return NRNN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t nrnn_newton_host_staging_bytes(int64_t B, int64_t T, int64_t d_h, int dtype, int K,
+                                      const int32_t *cu_seqlens_host, int64_t num_segments,
+                                      int64_t tokens_per_block) {
+    return staging_bytes(B, T, 0, d_h, dtype, K, cu_seqlens_host, num_segments, tokens_per_block);
+}
+
+size_t nrnn_newton_x_host_staging_bytes(int64_t B, int64_t T, int64_t d_in, int64_t d_h, int dtype,
+                                        int K, const int32_t *cu_seqlens_host,
+                                        int64_t num_segments, int64_t tokens_per_block) {
+    if (d_in <= 0 || d_in % 8 != 0) return 0;
+    return staging_bytes(B, T, d_in, d_h, dtype, K, cu_seqlens_host, num_segments, tokens_per_block);
+}
+
+int nrnn_newton_forward_host(const void *preact_host, int dtype, const float *params, int64_t B,
+                             int64_t T, int64_t d_h, const int32_t *cu_seqlens_host,
+                             int64_t num_segments, int K, float residual_fail, void *H_host,
+                             float *residual_host, void *staging, size_t staging_bytes,
+                             int64_t tokens_per_block, void *stream) {
+    return forward_host(preact_host, 0, nullptr, dtype, params, B, T, d_h, cu_seqlens_host,
+                        num_segments, K, residual_fail, H_host, residual_host, staging,
+                        staging_bytes, tokens_per_block, stream);
+}
+
+int nrnn_newton_forward_x_host(const void *x_host, const void *W_x, int dtype, const float *params,
+                               int64_t B, int64_t T, int64_t d_in, int64_t d_h,
+                               const int32_t *cu_seqlens_host, int64_t num_segments, int K,
+                               float residual_fail, void *H_host, float *residual_host,
+                               void *staging, size_t staging_bytes, int64_t tokens_per_block,
+                               void *stream) {
+    if (d_in <= 0) return NRNN_ERR_INVALID_ARG;
+    return forward_host(x_host, d_in, W_x, dtype, params, B, T, d_h, cu_seqlens_host,
+                        num_segments, K, residual_fail, H_host, residual_host, staging,
+                        staging_bytes, tokens_per_block, stream);
 }
 
 }  // extern "C"

@@ -131,3 +131,26 @@ def test_projection_workspace_size_and_checks():
     assert call(ctypes.c_void_p(4096 + 16), need) == -7   # not 256-byte aligned
     assert call(None, 0, rows=0) == 0                     # nothing to do
     assert lib.nrnn_input_projection(fake, fake, 0, 100, 60, 16, fake, None, 0, None) == -3
+
+
+def test_host_staging_sizes():
+    """The x-input host forward stages each slot's x rows besides what the
+    preactivation form stages, plus the projection's workspace (fp32)."""
+    f32, bf16 = torch.float32, torch.bfloat16
+    base = nr.host_staging_bytes(4, 1000, 64, f32, 3, tokens_per_block=1000)
+    xs = nr.x_host_staging_bytes(4, 1000, 32, 64, f32, 3, tokens_per_block=1000)
+    # three slots of 1000 x 32 fp32 rows, the low part of W_x (192 x 32 fp32)
+    assert xs - base >= 3 * 1000 * 32 * 4 + 192 * 32 * 4
+    xb = nr.x_host_staging_bytes(4, 1000, 32, 64, bf16, 3, tokens_per_block=1000)
+    assert xb - nr.host_staging_bytes(4, 1000, 64, bf16, 3, tokens_per_block=1000) >= 3 * 1000 * 32 * 2
+    assert nr.x_host_staging_bytes(4, 1000, 30, 64, f32, 3) == 0      # d_in % 8
+    assert nr.x_host_staging_bytes(4, 1000, 0, 64, f32, 3) == 0
+    assert nr.x_host_staging_bytes(4, 1000, 32, 60, f32, 3) == 0      # d_h % 8
+    assert nr.x_host_staging_bytes(1, 10, 32, 64, f32, 3, cu_seqlens=[0, 4, 10]) > 0
+    lib = nr.load()
+    fake = ctypes.c_void_p(256)
+    # d_in not positive / not a multiple of 8, before anything touches a pointer
+    assert lib.nrnn_newton_forward_x_host(fake, fake, 0, fake, 1, 8, 0, 16, None, 0, 3, 1.0,
+                                          fake, fake, fake, 1 << 20, 0, None) == -1
+    assert lib.nrnn_newton_forward_x_host(fake, fake, 0, fake, 1, 8, 12, 16, None, 0, 3, 1.0,
+                                          fake, fake, fake, 1 << 20, 0, None) == -3

@@ -100,3 +100,83 @@ def test_divergence_and_staging_errors(nr):
                                           small.numel(), 100, None)
         nr._binding._raise(st, "newton_forward_host")
     assert ei2.value.status == -7
+
+
+def _x_case(dtype, B, T, d_in, d_h, seed, cu=None):
+    w = syn.small_workload(B=B, T=T, d_in=d_in, d_h=d_h, dtype=dtype, seed=seed)
+    inp = syn.make_inputs(w)
+    P = oracle.input_projection(inp["x"], inp["W_x"])
+    if dtype == "bf16":
+        P = syn.round_bf16(P.astype(np.float32))    # the projection stores bf16
+    return inp, P
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("rows_per_block", [1, 3, 0])
+def test_x_input_row_blocks_match_oracle_and_device_calls(nr, dtype, rows_per_block):
+    B, T, d_in, d_h = 5, 260, 64, 72
+    inp, Pref = _x_case(dtype, B, T, d_in, d_h, seed=65)
+    prm = inp["params"]
+    xh = host_tensor(inp["x"], TDT[dtype])
+    Wd = torch.from_numpy(inp["W_x"]).to(TDT[dtype]).cuda()
+    H, rho = nr.newton_forward_x_host(xh, Wd, prm, K=3, tokens_per_block=rows_per_block * T)
+    assert H.device.type == "cpu" and H.dtype == TDT[dtype] and H.shape == (B, T, d_h)
+    Href, rho_ref = oracle.newton(Pref, prm, 3)
+    assert np.max(np.abs(as_f64(H) - Href)) <= TOL[dtype]
+    assert abs(rho - rho_ref) <= TOL[dtype]
+    # the device entry points on the same values: projection, then the forward
+    Pd = nr.input_projection(xh.cuda(), Wd)
+    Hd, rd = nr.newton_forward(Pd, prm, K=3)
+    assert np.max(np.abs(as_f64(H) - Hd.float().cpu().numpy())) <= (1e-5 if dtype == "f32" else 2e-2)
+    assert abs(rho - rd.item()) <= (1e-5 if dtype == "f32" else 2e-2)
+
+
+@pytest.mark.parametrize("tokens_per_block", [1, 400, 0])
+def test_x_input_segment_blocks_of_a_pack(nr, tokens_per_block):
+    cu = syn.cu_from_lengths([100, 1, 0, 250, 129, 64, 0, 300, 7])
+    inp, Pref = _x_case("f32", 1, int(cu[-1]), 24, 40, seed=66)
+    H, rho = nr.newton_forward_x_host(host_tensor(inp["x"], torch.float32),
+                                      torch.from_numpy(inp["W_x"]).cuda(), inp["params"],
+                                      cu_seqlens=cu, K=3, tokens_per_block=tokens_per_block)
+    Href, rho_ref = oracle.newton(Pref, inp["params"], 3, cu_seqlens=cu)
+    assert np.max(np.abs(as_f64(H) - Href)) <= TOL["f32"]
+    assert abs(rho - rho_ref) <= TOL["f32"]
+
+
+def test_x_input_pageable_empty_and_errors(nr):
+    inp, Pref = _x_case("f32", 2, 150, 16, 24, seed=67)
+    Wd = torch.from_numpy(inp["W_x"]).cuda()
+    H, rho = nr.newton_forward_x_host(host_tensor(inp["x"], torch.float32, pinned=False), Wd,
+                                      inp["params"], K=2, out=torch.empty((2, 150, 24)),
+                                      tokens_per_block=150)
+    Href, _ = oracle.newton(Pref, inp["params"], 2)
+    assert np.max(np.abs(as_f64(H) - Href)) <= TOL["f32"]
+    He, re = nr.newton_forward_x_host(torch.empty((3, 0, 16)), Wd, inp["params"], K=3)
+    assert He.shape == (3, 0, 24) and re == 0.0
+    # a NaN in x reaches the residual gate of its block
+    x2 = inp["x"].copy()
+    x2[1, 70, 5] = np.nan
+    with pytest.raises(nr.NewtonDivergenceError) as ei:
+        nr.newton_forward_x_host(host_tensor(x2, torch.float32), Wd, inp["params"], K=3,
+                                 tokens_per_block=150)
+    assert math.isinf(ei.value.residual)
+    # W_x misaligned on the device: rejected before any work
+    lib = nr.load()
+    need = nr.x_host_staging_bytes(2, 150, 16, 24, torch.float32, 3)
+    stg = torch.empty(need, dtype=torch.uint8, device="cuda")
+    Wbuf = torch.empty(Wd.numel() + 1, device="cuda")
+    Wbuf[1:].copy_(Wd.reshape(-1))
+    prm_d = nr.params_tensor(inp["params"], 24, "cuda")
+    xh = host_tensor(inp["x"], torch.float32)
+    Hh = torch.empty((2, 150, 24)).pin_memory()
+    rho_c = ctypes.c_float(0)
+    vp = ctypes.c_void_p
+
+    def call(W_ptr, nbytes):
+        return lib.nrnn_newton_forward_x_host(vp(xh.data_ptr()), vp(W_ptr), 0, vp(prm_d.data_ptr()),
+                                              2, 150, 16, 24, None, 0, 3, 1.0, vp(Hh.data_ptr()),
+                                              ctypes.byref(rho_c), vp(stg.data_ptr()), nbytes, 0, None)
+    assert call(Wbuf.data_ptr() + 4, need) == -1          # NRNN_ERR_INVALID_ARG
+    assert call(Wd.data_ptr(), need - 256) == -7          # NRNN_ERR_WORKSPACE
+    assert call(Wd.data_ptr(), need) == 0
+    assert np.max(np.abs(as_f64(Hh) - oracle.newton(Pref, inp["params"], 3)[0])) <= TOL["f32"]
