@@ -414,6 +414,17 @@ int nrnn_newton_forward_noalloc(const void *preact, int dtype, const float *para
 int64_t nrnn_debug_withhold_publish(int64_t tile);
 
 /*
+ * Debug: the look-back form nrnn_newton_forward's kernels take on the current
+ * device for a problem of this shape (algo as for nrnn_newton_forward):
+ *   0  plain: after the CTA barrier warp 0 reads up to 4 predecessor slots
+ *      per round
+ *   1  early: warp 0 reads the two nearest predecessor slots before the CTA
+ *      barrier (at most 4 chunks of each column resident at once)
+ * or NRNN_ERR_INVALID_ARG.  Host only; launches nothing.
+ */
+int nrnn_debug_lookback_form(int64_t B, int64_t T, int64_t d_h, int dtype, int algo);
+
+/*
  * Upper limit, in nanoseconds, of every bounded device wait that later calls
  * launch (default 2e9 = 2 s).  Process-wide; returns the previous value.
  */

@@ -21,6 +21,7 @@ from ._binding import (  # noqa: F401
     input_projection,
     lib_path,
     load,
+    lookback_form,
     newton_backward,
     newton_forward,
     newton_forward_host,

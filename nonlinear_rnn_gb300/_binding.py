@@ -52,6 +52,7 @@ _SIGNATURES = {
     "nrnn_debug_bounded_wait": ([_vp, _u64, _vp, _vp], _int),
     "nrnn_set_wait_limit_ns": ([_u64], _u64),
     "nrnn_debug_withhold_publish": ([_i64], _i64),
+    "nrnn_debug_lookback_form": ([_i64, _i64, _i64, _int, _int], _int),
     "nrnn_probe_xu_rates": ([ctypes.POINTER(ctypes.c_float)] * 3 + [_vp], _int),
     "nrnn_newton_host_staging_bytes": ([_i64, _i64, _i64, _int, _int, _vp, _i64, _i64], _sz),
     "nrnn_newton_forward_host": ([_vp, _int, _vp, _i64, _i64, _i64, _vp, _i64, _int, _f, _vp, _vp,
@@ -585,6 +586,18 @@ def set_wait_limit_ns(ns: int) -> int:
 def debug_withhold_publish(tile: int) -> int:
     """Debug: the given Newton tile stops publishing its look-back slot (-1: off)."""
     return int(load().nrnn_debug_withhold_publish(int(tile)))
+
+
+LOOKBACK_FORMS = {0: "plain", 1: "early"}
+
+
+def lookback_form(B: int, T: int, d_h: int, dtype=torch.float32, algo: str = "fused") -> str:
+    """The look-back form the Newton kernels take for this shape on the current
+    device: "plain" or "early" (nrnn_debug_lookback_form)."""
+    code = F32 if dtype == torch.float32 else BF16
+    st = load().nrnn_debug_lookback_form(int(B), int(T), int(d_h), code, ALGOS[algo])
+    _raise(st if st < 0 else 0, "lookback_form")
+    return LOOKBACK_FORMS[st]
 
 
 @dataclass

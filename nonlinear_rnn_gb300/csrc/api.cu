@@ -240,6 +240,20 @@ int nrnn_version(void) { return 200; }   // 0.2.0: nrnn_input_projection takes a
 
 uint64_t nrnn_set_wait_limit_ns(uint64_t ns) { return g_wait_ns.exchange(ns); }
 
+int nrnn_debug_lookback_form(int64_t B, int64_t T, int64_t d_h, int dtype, int algo) {
+    if ((dtype != NRNN_F32 && dtype != NRNN_BF16) || B < 1 || T < 1 || d_h < 1 ||
+        (algo != NRNN_ALGO_AUTO && algo != NRNN_ALGO_FUSED && algo != NRNN_ALGO_PER_ITER) ||
+        B * ((d_h + TILE_U - 1) / TILE_U) * ((T + NEWTON_L - 1) / NEWTON_L) > INT32_MAX)
+        return NRNN_ERR_INVALID_ARG;
+    NewtonArgs a{};
+    a.B = static_cast<int>(B);
+    a.T = static_cast<int>(T);
+    a.d_h = static_cast<int>(d_h);
+    a.n_ut = static_cast<int>((d_h + TILE_U - 1) / TILE_U);
+    a.n_chunks = static_cast<int>((T + NEWTON_L - 1) / NEWTON_L);
+    return newton_lookback_form(dtype, algo != NRNN_ALGO_PER_ITER, a);
+}
+
 int64_t nrnn_debug_withhold_publish(int64_t tile) {
     return g_withhold_tile.exchange(tile < 0 || tile > INT32_MAX ? -1 : tile);
 }

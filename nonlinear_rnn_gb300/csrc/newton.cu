@@ -656,6 +656,14 @@ size_t newton_smem_bytes(int dtype, bool fused) {
     return fused ? smem_bytes_for<float, true>(true) : smem_bytes_for<float, false>(true);
 }
 
+int newton_lookback_form(int dtype, bool fused, const NewtonArgs &a) {
+    const int per_sm = dtype == 1 ? (fused ? newton_min_blocks<__nv_bfloat16, true>()
+                                           : newton_min_blocks<__nv_bfloat16, false>())
+                                  : (fused ? newton_min_blocks<float, true>()
+                                           : newton_min_blocks<float, false>());
+    return early_lookback(a, per_sm) ? 1 : 0;
+}
+
 cudaError_t launch_newton(int dtype, bool fused, const CUtensorMap &tmP, const CUtensorMap &tmH,
                           const CUtensorMap &tmO, const NewtonArgs &a, int64_t n_ctas,
                           cudaStream_t stream) {

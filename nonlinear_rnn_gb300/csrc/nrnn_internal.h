@@ -110,6 +110,9 @@ size_t newton_error_offset(int K);
 
 // tmP over P (3 d_h, T, B), tmH over the H^(k-1) or H^(0) input, tmO over the
 // H output, all with a TILE_U x NEWTON_L x 1 box
+// Which look-back form launch_newton takes for these arguments (B, n_ut are
+// read): 0 plain, 1 early reads.
+int newton_lookback_form(int dtype, bool fused, const NewtonArgs &a);
 cudaError_t launch_newton(int dtype, bool fused, const CUtensorMap &tmP, const CUtensorMap &tmH,
                           const CUtensorMap &tmO, const NewtonArgs &a, int64_t n_ctas,
                           cudaStream_t stream);

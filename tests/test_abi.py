@@ -154,3 +154,11 @@ def test_host_staging_sizes():
                                           fake, fake, fake, 1 << 20, 0, None) == -1
     assert lib.nrnn_newton_forward_x_host(fake, fake, 0, fake, 1, 8, 12, 16, None, 0, 3, 1.0,
                                           fake, fake, fake, 1 << 20, 0, None) == -3
+
+
+def test_lookback_form_query_checks_its_arguments():
+    lib = nr.load()
+    assert lib.nrnn_debug_lookback_form(0, 10, 16, 0, 0) == -1      # B < 1
+    assert lib.nrnn_debug_lookback_form(1, 10, 16, 5, 0) == -1      # dtype
+    assert lib.nrnn_debug_lookback_form(1, 10, 16, 0, 7) == -1      # algo
+    assert lib.nrnn_debug_lookback_form(1, 10, 16, 0, 2) in (0, 1)

@@ -261,6 +261,7 @@ def test_lookback_timeout_is_reported_and_context_survives(nr, algo):
     """A tile that never publishes makes its successors' bounded waits run out:
     the call terminates, reports NRNN_ERR_TIMEOUT, and the next call is correct."""
     w = syn.small_workload(B=1, T=1000, d_h=16, seed=90)    # one column of chunks
+    assert nr.lookback_form(1, 1000, 16, torch.float32, algo) == "plain"
     P = syn.direct_preact(w)
     prm = syn.make_params(w)
     old_limit = nr.set_wait_limit_ns(2_000_000)               # 2 ms
@@ -285,6 +286,7 @@ def test_lookback_timeout_in_the_early_form(nr, algo):
     its publish still makes its successors' bounded waits run out, the call
     reports NRNN_ERR_TIMEOUT, and the next call is correct."""
     w = syn.small_workload(B=10, T=256, d_h=1024, seed=91)   # 4 chunks per column
+    assert nr.lookback_form(10, 256, 1024, torch.float32, algo) == "early"
     P = syn.direct_preact(w)
     prm = syn.make_params(w)
     n_ut, n_chunks = 1024 // 32, 4
