@@ -221,10 +221,17 @@ __global__ void __launch_bounds__(NW * 32, newton_min_blocks<TS, FUSED>())
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     constexpr bool REG_H = !FUSED && sizeof(TS) == 4;   // H^(k-1) in registers, not a tile
     // launched as a dependent of the kernel before it on the stream (the
-    // workspace clear, or the previous iteration): every access to memory lies
-    // behind the wait; the next iteration's CTAs may be scheduled as soon as
-    // all of this grid's have started, and wait for its completion in turn
-    asm volatile("griddepcontrol.wait;" ::: "memory");
+    // workspace clear, or the previous iteration); the next iteration's CTAs
+    // may be scheduled as soon as all of this grid's have started.  Every
+    // access to memory lies behind griddepcontrol.wait, except in iterations
+    // 2..K of the per-iteration forward: these CTAs start only once the
+    // previous iteration's have all started, so that the workspace clear
+    // before iteration 1 has completed; they take their ticket (cleared
+    // there) and load their tile of P (read-only) while the previous
+    // iteration finishes, and wait only before they touch H^(k-1) and the
+    // look-back slots
+    const bool early_p = !FUSED && !XPROJ && a.k_first > 1;
+    if (!early_p) asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;");
     if (tid == 0) {
         // tickets run chunk-major: every chunk this tile's look-back waits for
@@ -261,10 +268,12 @@ __global__ void __launch_bounds__(NW * 32, newton_min_blocks<TS, FUSED>())
 #pragma unroll
             for (int g = 0; g < 3; ++g)
                 tma_load_3d(Pt + g * L * U, &tmP, &s_bar, g * a.d_h + u0, t0, b);
+            if (early_p) asm volatile("griddepcontrol.wait;" ::: "memory");
             if (tile_h) tma_load_3d(Hs, &tmH, &s_bar, u0, t0, b);
         }
         mark_heads(a.cu, a.S, t0, L, s_heads);
     }
+    if (early_p && tid != 0) asm volatile("griddepcontrol.wait;" ::: "memory");
     if constexpr (XPROJ) {
         if (warp == 2) {
             asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
