@@ -305,7 +305,7 @@ int nrnn_debug_bounded_wait(const uint32_t *flag_dev, uint64_t wait_ns, uint32_t
  * this is the library's end-to-end entry point for data that lives on the
  * host).  The problem is cut into blocks that need nothing from one another
  * -- groups of batch rows, or for a pack groups of whole segments -- of about
- * tokens_per_block tokens each (0: about six blocks).  Each block is copied
+ * tokens_per_block tokens each (0: about 16 blocks).  Each block is copied
  * in on a library stream, run through nrnn_newton_forward (fused algorithm)
  * on `stream`, and copied out on a second library stream, on one of three
  * slots of `staging`, so that one block's copies overlap another's kernels.

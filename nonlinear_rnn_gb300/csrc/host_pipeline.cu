@@ -45,14 +45,14 @@ struct Plan {
 };
 
 // Splits the problem into blocks of about tokens_per_block tokens (0: about
-// six blocks) and lays out the staging area: per slot [x rows (d_in > 0)] [P]
+// 16 blocks) and lays out the staging area: per slot [x rows (d_in > 0)] [P]
 // [H] [forward workspace], then the projection's workspace, residuals, error
 // words and rebased segment bounds.  Returns false on a bad shape.
 bool make_plan(int64_t B, int64_t T, int64_t d_in, int64_t d_h, int dtype, int K,
                const int32_t *cu, int64_t S, int64_t tokens_per_block, Plan &pl) {
     const int64_t total = B * T;
     if (total == 0) return true;
-    if (tokens_per_block <= 0) tokens_per_block = (total + 5) / 6;
+    if (tokens_per_block <= 0) tokens_per_block = (total + 15) / 16;
     if (cu == nullptr) {
         const int64_t rows = std::max<int64_t>(1, std::min<int64_t>(B, tokens_per_block / std::max<int64_t>(T, 1)));
         for (int64_t b = 0; b < B; b += rows)
