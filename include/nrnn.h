@@ -102,6 +102,20 @@ size_t nrnn_newton_workspace_bytes(int64_t B, int64_t T, int64_t d_h, int dtype,
                                    int algo);
 
 /*
+ * Workspace bytes for a forward over a cu_seqlens pack (x of shape (1, N, d))
+ * of num_segments segments (shapes_layout, "cu_seqlens").  With a workspace of
+ * at least this size nrnn_newton_forward cuts each segment into chunks of its
+ * own instead of cutting the pack's time axis, which keeps many more
+ * look-back chains in flight (one per segment): for packs of 2 to 4096
+ * segments, N <= 524288 and num_segments <= ceil(N / 64) / 8; other packs,
+ * and a workspace sized by nrnn_newton_workspace_bytes, take the time-axis
+ * chunks.  Results agree to rounding either way (the look-back composes in
+ * another grouping).  Returns 0 for invalid arguments.
+ */
+size_t nrnn_newton_workspace_bytes_pack(int64_t N, int64_t d_h, int dtype, int K, int algo,
+                                        int64_t num_segments);
+
+/*
  * Parallel Newton forward (numerics contract, "Invariant"; FAQs "How many
  * Newton iterations should I use?": a fixed K).
  *
@@ -423,6 +437,19 @@ int64_t nrnn_debug_withhold_publish(int64_t tile);
  * or NRNN_ERR_INVALID_ARG.  Host only; launches nothing.
  */
 int nrnn_debug_lookback_form(int64_t B, int64_t T, int64_t d_h, int dtype, int algo);
+
+/*
+ * Debug: writes the segment-aligned chunk plan that nrnn_newton_forward uses
+ * for a pack (see nrnn_newton_workspace_bytes_pack) into plan, device, at
+ * least (2 + ceil(N / 64) + num_segments) x 4 int32, 16-byte aligned:
+ * plan[0] = number of chunks n, then n entries {first row, end row of the
+ * segment, chunk index j within the segment, index of the chunk in segment
+ * order}, in the order the Newton kernels take them (by j; within one j by
+ * the segment's number of chunks, most first).  cu_seqlens: device, validated.  Returns
+ * NRNN_ERR_INVALID_ARG for packs that take the time-axis chunks.
+ */
+int nrnn_debug_pack_plan(const int32_t *cu_seqlens, int64_t num_segments, int64_t N, void *plan,
+                         void *stream);
 
 /*
  * Upper limit, in nanoseconds, of every bounded device wait that later calls

@@ -27,6 +27,7 @@ from ._binding import (  # noqa: F401
     newton_forward_host,
     newton_forward_x,
     newton_forward_x_host,
+    pack_plan,
     params_tensor,
     picard,
     probe_xu_rates,

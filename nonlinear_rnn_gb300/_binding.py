@@ -33,6 +33,7 @@ _SIGNATURES = {
     "nrnn_version": ([], _int),
     "nrnn_validate_cu_seqlens": ([_vp, _i64, _i64], _int),
     "nrnn_newton_workspace_bytes": ([_i64, _i64, _i64, _int, _int, _int], _sz),
+    "nrnn_newton_workspace_bytes_pack": ([_i64, _i64, _int, _int, _int, _i64], _sz),
     "nrnn_newton_forward": ([_vp, _int, _vp, _i64, _i64, _i64, _vp, _i64, _int, _f, _int, _vp,
                              _vp, _vp, _vp, _sz, _vp], _int),
     "nrnn_newton_forward_init": ([_vp, _int, _vp, _i64, _i64, _i64, _vp, _i64, _vp, _int, _f,
@@ -53,6 +54,7 @@ _SIGNATURES = {
     "nrnn_set_wait_limit_ns": ([_u64], _u64),
     "nrnn_debug_withhold_publish": ([_i64], _i64),
     "nrnn_debug_lookback_form": ([_i64, _i64, _i64, _int, _int], _int),
+    "nrnn_debug_pack_plan": ([_vp, _i64, _i64, _vp, _vp], _int),
     "nrnn_probe_xu_rates": ([ctypes.POINTER(ctypes.c_float)] * 3 + [_vp], _int),
     "nrnn_newton_host_staging_bytes": ([_i64, _i64, _i64, _int, _int, _vp, _i64, _i64], _sz),
     "nrnn_newton_forward_host": ([_vp, _int, _vp, _i64, _i64, _i64, _vp, _i64, _int, _f, _vp, _vp,
@@ -188,8 +190,15 @@ def _cu_device(cu_seqlens, B, T, device):
     return torch.from_numpy(cu32).to(device), cu32.size - 1
 
 
-def workspace_bytes(B, T, d_h, dtype=torch.float32, K=3, algo="auto") -> int:
+def workspace_bytes(B, T, d_h, dtype=torch.float32, K=3, algo="auto", num_segments: int = 0) -> int:
+    """Workspace of nrnn_newton_forward; num_segments > 0: for a cu_seqlens pack
+    of that many segments (B = 1), with room for segment-aligned chunks."""
     code = F32 if dtype == torch.float32 else BF16
+    if num_segments > 0:
+        if B != 1:
+            raise ValueError("a cu_seqlens pack has batch 1")
+        return int(load().nrnn_newton_workspace_bytes_pack(T, d_h, code, K, ALGOS[algo],
+                                                           int(num_segments)))
     return int(load().nrnn_newton_workspace_bytes(B, T, d_h, code, K, ALGOS[algo]))
 
 
@@ -222,7 +231,8 @@ def newton_forward(preact: torch.Tensor, params, cu_seqlens=None, K: int = 3,
     if tuple(H.shape) != (B, T, d_h) or H.dtype != preact.dtype or not H.is_contiguous():
         raise ValueError("out has the wrong shape, dtype or layout")
     rho = torch.empty((), dtype=torch.float32, device=dev)
-    nbytes = lib.nrnn_newton_workspace_bytes(B, T, d_h, code, int(K), ALGOS[algo])
+    nbytes = (lib.nrnn_newton_workspace_bytes_pack(T, d_h, code, int(K), ALGOS[algo], S) if S > 0
+              else lib.nrnn_newton_workspace_bytes(B, T, d_h, code, int(K), ALGOS[algo]))
     if nbytes == 0:
         raise ValueError("invalid shape, K or algo")
     if workspace is None or workspace.numel() < nbytes:
@@ -586,6 +596,21 @@ def set_wait_limit_ns(ns: int) -> int:
 def debug_withhold_publish(tile: int) -> int:
     """Debug: the given Newton tile stops publishing its look-back slot (-1: off)."""
     return int(load().nrnn_debug_withhold_publish(int(tile)))
+
+
+def pack_plan(cu_seqlens, N: int, device="cuda") -> torch.Tensor:
+    """The segment-aligned chunk plan of a pack as the Newton kernels take it
+    (nrnn_debug_pack_plan): an (n, 4) int32 tensor of {first row, segment end,
+    chunk index within the segment, chunk index in segment order}."""
+    lib = load()
+    cu32 = validate_cu_seqlens(cu_seqlens, N)
+    cu = torch.from_numpy(cu32).to(device)
+    S = cu32.size - 1
+    plan = torch.zeros((2 + (N + 63) // 64 + S, 4), dtype=torch.int32, device=device)
+    st = lib.nrnn_debug_pack_plan(_ptr(cu), S, N, _ptr(plan), _stream(torch.device(device)))
+    _raise(st, "pack_plan")
+    n = int(plan[0, 0].item())
+    return plan[1:1 + n].cpu()
 
 
 LOOKBACK_FORMS = {0: "plain", 1: "early"}

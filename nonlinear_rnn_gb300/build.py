@@ -15,7 +15,7 @@ CSRC = os.path.join(HERE, "csrc")
 OUT = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT, "libnrnn.so")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
-SOURCES = ["api.cu", "newton.cu", "picard.cu", "sequential.cu", "projection_tc.cu", "decode.cu", "backward.cu", "noalloc.cu", "probe.cu", "host_pipeline.cu"]
+SOURCES = ["api.cu", "newton.cu", "picard.cu", "sequential.cu", "projection_tc.cu", "decode.cu", "backward.cu", "noalloc.cu", "probe.cu", "host_pipeline.cu", "pack_plan.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

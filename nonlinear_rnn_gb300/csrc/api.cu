@@ -33,13 +33,16 @@ bool overlaps(const void *a, const void *b, size_t bytes) { return ranges_overla
 
 // Workspace: [counters (K+1) u32 | error u32], then [slots K x n_tiles x 32
 // u64], both cleared by one kernel per call, then (per-iteration, K > 1) one
-// H buffer.
-SyncLayout layout(int64_t B, int64_t T, int64_t d_h, int dtype, int K, bool fused) {
+// H buffer, then (a pack cut into segment-aligned chunks) the chunk plan.
+// S > 0: the call carries a pack of S segments.
+SyncLayout layout(int64_t B, int64_t T, int64_t d_h, int dtype, int K, bool fused, int64_t S = 0) {
     SyncLayout s{};
     const int64_t n_ut = (d_h + TILE_U - 1) / TILE_U;
     const int64_t n_chunks = (T + NEWTON_L - 1) / NEWTON_L;
     const int64_t kk = K > 0 ? K : 1;
-    s.n_tiles = B * n_ut * n_chunks;
+    s.plan = S > 0 && pack_plan_applies(B, T, S);
+    s.chain_stride = n_chunks + (s.plan ? S : 0);   // a segment adds at most one chunk
+    s.n_tiles = B * n_ut * s.chain_stride;
     s.counters_off = 0;
     s.error_off = sizeof(uint32_t) * (kk + 1);
     s.slots_off = align_up(s.error_off + sizeof(uint32_t), 256);
@@ -48,6 +51,8 @@ SyncLayout layout(int64_t B, int64_t T, int64_t d_h, int dtype, int K, bool fuse
     size_t end = s.zero_bytes;
     s.hbuf_off = align_up(end, 256);
     if (!fused && K > 1) end = s.hbuf_off + elem_size(dtype) * B * T * d_h;
+    s.plan_off = align_up(end, 256);
+    if (s.plan) end = s.plan_off + pack_plan_bytes(T, S);
     s.total = align_up(end, 256);
     return s;
 }
@@ -251,7 +256,19 @@ int nrnn_debug_lookback_form(int64_t B, int64_t T, int64_t d_h, int dtype, int a
     a.d_h = static_cast<int>(d_h);
     a.n_ut = static_cast<int>((d_h + TILE_U - 1) / TILE_U);
     a.n_chunks = static_cast<int>((T + NEWTON_L - 1) / NEWTON_L);
+    a.chain_stride = a.n_chunks;
     return newton_lookback_form(dtype, algo != NRNN_ALGO_PER_ITER, a);
+}
+
+int nrnn_debug_pack_plan(const int32_t *cu_seqlens, int64_t num_segments, int64_t N, void *plan,
+                         void *stream) {
+    if (cu_seqlens == nullptr || plan == nullptr || N < 1 || !pack_plan_applies(1, N, num_segments))
+        return NRNN_ERR_INVALID_ARG;
+    return launch_pack_plan(cu_seqlens, static_cast<int>(num_segments),
+                            static_cast<int>((N + NEWTON_L - 1) / NEWTON_L), static_cast<int4 *>(plan),
+                            static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? NRNN_OK
+               : NRNN_ERR_CUDA;
 }
 
 int64_t nrnn_debug_withhold_publish(int64_t tile) {
@@ -274,6 +291,13 @@ size_t nrnn_newton_workspace_bytes(int64_t B, int64_t T, int64_t d_h, int dtype,
     if (dtype != NRNN_F32 && dtype != NRNN_BF16) return 0;
     if (algo < NRNN_ALGO_AUTO || algo > NRNN_ALGO_FUSED) return 0;
     return layout(B, T, d_h, dtype, K, algo != NRNN_ALGO_PER_ITER).total;
+}
+
+size_t nrnn_newton_workspace_bytes_pack(int64_t N, int64_t d_h, int dtype, int K, int algo,
+                                        int64_t num_segments) {
+    if (num_segments < 1) return 0;
+    if (nrnn_newton_workspace_bytes(1, N, d_h, dtype, K, algo) == 0) return 0;
+    return layout(1, N, d_h, dtype, K, algo != NRNN_ALGO_PER_ITER, num_segments).total;
 }
 
 int nrnn_newton_forward(const void *preact, int dtype, const float *params, int64_t B,
@@ -306,7 +330,10 @@ int nrnn_newton_forward_init(const void *preact, int dtype, const float *params,
         if (ranges_overlap(preact, 3 * hb, H_out, hb)) return NRNN_ERR_INVALID_ARG;
     }
     const bool fused = algo != NRNN_ALGO_PER_ITER;
-    const SyncLayout ly = layout(B, T, d_h, dtype, K, fused);
+    // a pack is cut into segment-aligned chunks when the workspace was sized
+    // for it (nrnn_newton_workspace_bytes_pack), else into chunks of the time axis
+    SyncLayout ly = layout(B, T, d_h, dtype, K, fused, cu_seqlens ? num_segments : 0);
+    if (ly.plan && ws_bytes < ly.total) ly = layout(B, T, d_h, dtype, K, fused);
     if (workspace == nullptr || ws_bytes < ly.total ||
         (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
         return NRNN_ERR_WORKSPACE;
@@ -316,6 +343,12 @@ int nrnn_newton_forward_init(const void *preact, int dtype, const float *params,
     uint32_t *err = reinterpret_cast<uint32_t *>(ws + ly.error_off);
     const int S = static_cast<int>(cu_seqlens ? num_segments : 0);
 
+    // the chunk plan of a segment-aligned pack, before the clear kernel (whose
+    // dependents, the Newton launches, read it)
+    if (ly.plan && K > 0 && B * T > 0 &&
+        launch_pack_plan(cu_seqlens, S, static_cast<int>((T + NEWTON_L - 1) / NEWTON_L),
+                         reinterpret_cast<int4 *>(ws + ly.plan_off), stream) != cudaSuccess)
+        return NRNN_ERR_CUDA;
     // one kernel clears counters, error word, slots and rho; rho accumulates by
     // atomicMax into residual_dev
     cudaError_t e = clear_for_call(ws, ly.zero_bytes, residual_dev, sizeof(float), stream);
@@ -348,6 +381,8 @@ int nrnn_newton_forward_init(const void *preact, int dtype, const float *params,
             a.error = err;
             a.wait_ns = g_wait_ns.load();
             a.withhold_tile = static_cast<int>(g_withhold_tile.load());
+            a.chain_stride = static_cast<int>(ly.chain_stride);
+            if (ly.plan) a.plan = reinterpret_cast<const int4 *>(ws + ly.plan_off);
             uint32_t *counters = reinterpret_cast<uint32_t *>(ws + ly.counters_off);
             if (fused) {
                 CUtensorMap tmH = tmP;
@@ -424,6 +459,7 @@ int nrnn_newton_forward_x(const void *x, const void *W_x, int dtype, const float
         a.d_in = static_cast<int>(d_in);
         a.n_ut = static_cast<int>((d_h + TILE_U - 1) / TILE_U);
         a.n_chunks = static_cast<int>((T + NEWTON_L - 1) / NEWTON_L);
+        a.chain_stride = a.n_chunks;
         a.slots = reinterpret_cast<unsigned long long *>(ws + ly.slots_off);
         a.residual_bits = reinterpret_cast<uint32_t *>(residual_dev);
         a.error = err;

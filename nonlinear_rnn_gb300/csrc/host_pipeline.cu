@@ -76,7 +76,10 @@ bool make_plan(int64_t B, int64_t T, int64_t d_in, int64_t d_h, int dtype, int K
         if (d_in > 0) pl.x_bytes = std::max(pl.x_bytes, align_up(n * d_in * es));
         pl.p_bytes = std::max(pl.p_bytes, align_up(n * 3 * d_h * es));
         pl.h_bytes = std::max(pl.h_bytes, align_up(n * d_h * es));
-        const size_t ws = nrnn_newton_workspace_bytes(bk.nb, bk.nt, d_h, dtype, K, NRNN_ALGO_FUSED);
+        const size_t ws = cu == nullptr
+                              ? nrnn_newton_workspace_bytes(bk.nb, bk.nt, d_h, dtype, K, NRNN_ALGO_FUSED)
+                              : nrnn_newton_workspace_bytes_pack(bk.nt, d_h, dtype, K, NRNN_ALGO_FUSED,
+                                                                 bk.ns);
         if (ws == 0 && bk.nb * bk.nt > 0) return false;
         pl.ws_bytes = std::max(pl.ws_bytes, align_up(ws));
     }

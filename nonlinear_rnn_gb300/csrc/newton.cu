@@ -215,7 +215,10 @@ __global__ void __launch_bounds__(NW * 32, newton_min_blocks<TS, FUSED>())
     __shared__ __align__(8) uint64_t s_bar;
     __shared__ __align__(8) uint64_t s_xfull[2], s_xempty[2], s_xacc;   // XPROJ only
     __shared__ uint32_t s_tmem;                                         // XPROJ only
-    __shared__ int s_tile[3];   // chunk, batch row, unit tile of this CTA's ticket
+    // this CTA's ticket: chunk (position in its look-back chain), batch row,
+    // unit tile, first row, end of the rows it may write, chain index of the
+    // look-back slots
+    __shared__ int s_tile[6];
     __shared__ uint32_t s_red[NW];
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -237,17 +240,38 @@ __global__ void __launch_bounds__(NW * 32, newton_min_blocks<TS, FUSED>())
         // tickets run chunk-major: every chunk this tile's look-back waits for
         // belongs to a CTA that has already started
         const uint32_t ticket = atomicAdd(a.ticket, 1u);
-        const uint32_t per_chunk = static_cast<uint32_t>(a.B) * a.n_ut;
-        const uint32_t cc = ticket / per_chunk, rem = ticket - cc * per_chunk;
-        s_tile[0] = static_cast<int>(cc);
-        s_tile[1] = static_cast<int>(rem / a.n_ut);
-        s_tile[2] = static_cast<int>(rem % a.n_ut);
+        if (a.plan != nullptr) {
+            // segment-aligned chunks of a pack, level by level; the grid is
+            // sized for an upper bound of their number
+            const uint32_t item = ticket / a.n_ut;
+            const int n_items = a.plan[0].x;
+            const int4 e = a.plan[1 + item];
+            s_tile[0] = e.z;
+            s_tile[1] = 0;
+            s_tile[2] = static_cast<int>(ticket - item * a.n_ut);
+            s_tile[3] = item < static_cast<uint32_t>(n_items) ? e.x : -1;
+            s_tile[4] = e.y;
+            s_tile[5] = e.w;
+        } else {
+            const uint32_t per_chunk = static_cast<uint32_t>(a.B) * a.n_ut;
+            const uint32_t cc = ticket / per_chunk, rem = ticket - cc * per_chunk;
+            s_tile[0] = static_cast<int>(cc);
+            s_tile[1] = static_cast<int>(rem / a.n_ut);
+            s_tile[2] = static_cast<int>(rem % a.n_ut);
+            s_tile[3] = static_cast<int>(cc) * L;
+            s_tile[4] = a.T;
+            s_tile[5] = static_cast<int>(cc);
+        }
     }
     if (tid < L / 32) s_heads[tid] = 0u;
     __syncthreads();
+    if (s_tile[3] < 0) return;   // a ticket past the plan's last chunk
 
     const int c = s_tile[0], b = s_tile[1], ut = s_tile[2];
-    const int t0 = c * L, u0 = ut * U;
+    // t_end: rows at or past it are outside this tile's sequence (the end of
+    // the row, or of the tile's segment in a segment-aligned pack)
+    const int t0 = s_tile[3], t_end = s_tile[4], chain = s_tile[5];
+    const int u0 = ut * U;
     const bool load_h = a.H_prev != nullptr;   // H^(k-1) (per-iteration) or H^(0) (fused)
 
     if (tid == 0) {
@@ -271,7 +295,11 @@ __global__ void __launch_bounds__(NW * 32, newton_min_blocks<TS, FUSED>())
             if (early_p) asm volatile("griddepcontrol.wait;" ::: "memory");
             if (tile_h) tma_load_3d(Hs, &tmH, &s_bar, u0, t0, b);
         }
-        mark_heads(a.cu, a.S, t0, L, s_heads);
+        if (a.plan != nullptr) {
+            if (c == 0) s_heads[0] = 1u;   // a segment's first chunk starts at its head
+        } else {
+            mark_heads(a.cu, a.S, t0, L, s_heads);
+        }
     }
     if (early_p && tid != 0) asm volatile("griddepcontrol.wait;" ::: "memory");
     if constexpr (XPROJ) {
@@ -307,7 +335,7 @@ __global__ void __launch_bounds__(NW * 32, newton_min_blocks<TS, FUSED>())
         if (load_h && uok) {
             const TS *Hp = reinterpret_cast<const TS *>(a.H_prev) +
                            (static_cast<size_t>(b) * a.T + t0) * a.d_h + u;
-            const int rows = a.T - t0;   // rows of this chunk inside the sequence
+            const int rows = t_end - t0;   // rows of this chunk inside the sequence
 #pragma unroll
             for (int j = 0; j < HALF; ++j) {
                 if (r0 + j < rows) Hreg[j].x = to_f32(Hp[static_cast<size_t>(r0 + j) * a.d_h]);
@@ -422,12 +450,12 @@ __global__ void __launch_bounds__(NW * 32, newton_min_blocks<TS, FUSED>())
                         : splat2(0.f);
     if (!REG_H && load_h && warp > 0) hb = to_f32(Hs[(r0 - 1) * U + lane]);
     const uint32_t hm = (s_heads[r0 >> 5] >> (r0 & 31)) & ((1u << SEG) - 1u);
-    const int nvalid = min(SEG, a.T - (t0 + r0));
+    const int nvalid = min(SEG, t_end - (t0 + r0));
     const bool general = (hm != 0u) || (nvalid < SEG);
     const void *Pv = FUSED ? static_cast<const void *>(Pf) : static_cast<const void *>(Pt);
 
-    const int n_tiles = a.B * a.n_ut * a.n_chunks;
-    const int tile = (b * a.n_ut + ut) * a.n_chunks + c;
+    const int n_tiles = a.B * a.n_ut * a.chain_stride;
+    const int tile = (b * a.n_ut + ut) * a.chain_stride + chain;
 
     for (int k = a.k_first; k <= a.k_last; ++k) {
         float2 J2[HALF];
@@ -516,6 +544,21 @@ __global__ void __launch_bounds__(NW * 32, newton_min_blocks<TS, FUSED>())
         }
     }
 
+    if (t_end - t0 < L && a.plan != nullptr) {
+        // the last chunk of a segment in a segment-aligned pack: the rows after
+        // it belong to the next segment, so the rows are stored one by one
+        if (uok) {
+            TS *Ho = static_cast<TS *>(a.H_next) + static_cast<size_t>(t0) * a.d_h + u;
+            const int rows = t_end - t0;
+#pragma unroll
+            for (int j = 0; j < HALF; ++j) {
+                if (r0 + j < rows) Ho[static_cast<size_t>(r0 + j) * a.d_h] = from_f32<TS>(G[j].x);
+                if (r0 + HALF + j < rows)
+                    Ho[static_cast<size_t>(r0 + HALF + j) * a.d_h] = from_f32<TS>(G[j].y);
+            }
+        }
+        return;
+    }
     // H^(K) of the tile -> shared memory (the P tile's space: every read of it
     // lies behind the last barrier) -> one TMA store, which clips rows past T
     // and units past d_h
@@ -616,7 +659,8 @@ bool early_lookback(const NewtonArgs &a, int ctas_per_sm) {
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
         return false;
     const int64_t resident = static_cast<int64_t>(sms) * ctas_per_sm;
-    const int64_t columns = static_cast<int64_t>(a.B) * a.n_ut;
+    // a segment-aligned pack has one look-back chain per segment and unit tile
+    const int64_t columns = static_cast<int64_t>(a.plan != nullptr ? a.S : a.B) * a.n_ut;
     return resident <= EARLY_LOOKBACK_CHUNKS * columns;
 }
 

@@ -71,6 +71,9 @@ struct NewtonArgs {
     unsigned long long wait_ns;   // limit of every bounded wait
     int withhold_tile;            // debug: this tile never publishes its look-back slot (-1: none)
     int d_in;                     // fused projection only: input width
+    const int4 *plan;             // segment-aligned chunks of a pack (k_pack_plan) or null:
+                                  // chunks of 64 steps of the whole time axis
+    int chain_stride;             // look-back slots per unit tile and iteration
 };
 
 struct BackwardArgs {
@@ -99,20 +102,40 @@ cudaError_t launch_backward(int dtype, const CUtensorMap &tmP, const CUtensorMap
 // variant, K > 1) one H buffer.
 struct SyncLayout {
     size_t counters_off, error_off, zero_bytes;
-    size_t slots_off, slots_bytes, hbuf_off, total;
-    int64_t n_tiles;
+    size_t slots_off, slots_bytes, hbuf_off, plan_off, total;
+    int64_t n_tiles;        // CTAs of a Newton launch (an upper bound with a plan)
+    int64_t chain_stride;   // look-back slots per (row, unit tile) and iteration
+    bool plan;              // segment-aligned chunks of a pack
 };
+
+// Segment-aligned chunks of a cu_seqlens pack: chunk j of segment s covers
+// rows [cu[s] + 64 j, min(cu[s] + 64 (j + 1), cu[s + 1])), so that every
+// segment is a chain of its own and a pack of S segments has about S times
+// as many independent chains as the time axis cut into 64-step chunks.
+// plan[0].x = number of chunks; plan[1 + i] = {first row, end row of the
+// segment, j, index of the chunk in segment order}; chunks in the order
+// the tickets hand them out: by j, and within one j by the segment's
+// number of chunks, most first (every chunk's predecessor comes earlier).  Used for packs
+// of 2..PACK_PLAN_MAX_S segments, at most PACK_PLAN_MAX_CHUNKS 64-step
+// chunks, and S <= n_chunks / 8 (so that at most 1/8 more chunks than the
+// plain cut).
+constexpr int PACK_PLAN_MAX_S = 4096;
+constexpr int PACK_PLAN_MAX_CHUNKS = 8192;
+bool pack_plan_applies(int64_t B, int64_t T, int64_t S);
+size_t pack_plan_bytes(int64_t T, int64_t S);
+cudaError_t launch_pack_plan(const int32_t *cu, int S, int n_chunks, int4 *plan,
+                             cudaStream_t stream);
 
 size_t newton_smem_bytes(int dtype, bool fused);
 
 // byte offset of the error word in a Newton forward's workspace
 size_t newton_error_offset(int K);
 
+// Which look-back form launch_newton takes for these arguments (B, n_ut,
+// plan are read): 0 plain, 1 early reads.
+int newton_lookback_form(int dtype, bool fused, const NewtonArgs &a);
 // tmP over P (3 d_h, T, B), tmH over the H^(k-1) or H^(0) input, tmO over the
 // H output, all with a TILE_U x NEWTON_L x 1 box
-// Which look-back form launch_newton takes for these arguments (B, n_ut are
-// read): 0 plain, 1 early reads.
-int newton_lookback_form(int dtype, bool fused, const NewtonArgs &a);
 cudaError_t launch_newton(int dtype, bool fused, const CUtensorMap &tmP, const CUtensorMap &tmH,
                           const CUtensorMap &tmO, const NewtonArgs &a, int64_t n_ctas,
                           cudaStream_t stream);

@@ -162,3 +162,24 @@ def test_lookback_form_query_checks_its_arguments():
     assert lib.nrnn_debug_lookback_form(1, 10, 16, 5, 0) == -1      # dtype
     assert lib.nrnn_debug_lookback_form(1, 10, 16, 0, 7) == -1      # algo
     assert lib.nrnn_debug_lookback_form(1, 10, 16, 0, 2) in (0, 1)
+
+
+def test_pack_workspace_and_plan_checks():
+    """A pack of 2..4096 segments with num_segments <= chunks / 8 gets room for
+    segment-aligned chunks (more look-back slots and the chunk plan); other
+    packs need what the time-axis chunks need."""
+    lib = nr.load()
+    plain = lib.nrnn_newton_workspace_bytes(1, 4096, 64, 0, 3, 2)
+    pack = lib.nrnn_newton_workspace_bytes_pack(4096, 64, 0, 3, 2, 8)      # 64 chunks, 8 segments
+    # 8 more chunks per unit tile in the slots (3 iterations x 2 unit tiles x
+    # 8 x 32 words) and the plan (1 + 64 + 8 entries of 16 bytes)
+    assert pack >= plain + 3 * 2 * 8 * 32 * 8 + 73 * 16
+    assert lib.nrnn_newton_workspace_bytes_pack(4096, 64, 0, 3, 2, 1) == plain   # one segment
+    assert lib.nrnn_newton_workspace_bytes_pack(4096, 64, 0, 3, 2, 9) == plain   # 9 > 64 / 8
+    assert lib.nrnn_newton_workspace_bytes_pack(4096, 64, 0, 3, 2, 0) == 0
+    assert lib.nrnn_newton_workspace_bytes_pack(4096, 64, 0, 99, 2, 8) == 0      # K
+    assert nr.workspace_bytes(1, 4096, 64, torch.float32, 3, "fused", num_segments=8) == pack
+    fake = ctypes.c_void_p(256)
+    assert lib.nrnn_debug_pack_plan(fake, 1, 4096, fake, None) == -1
+    assert lib.nrnn_debug_pack_plan(fake, 9, 4096, fake, None) == -1
+    assert lib.nrnn_debug_pack_plan(None, 8, 4096, fake, None) == -1
