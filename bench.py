@@ -168,6 +168,12 @@ def xu_work(w, rates):
     return per_eval * (w.K + 1) * w.B * w.T * w.d_h
 
 
+def segments_of(inp):
+    """Segments of a workload's cu_seqlens pack (0: no pack): the workspace then
+    has room for segment-aligned chunks."""
+    return 0 if inp["cu_seqlens"] is None else len(inp["cu_seqlens"]) - 1
+
+
 def time_workload(torch, nr, w, args, dev, flush, stream, xu_rates, props, mhz):
     """Fused and per-iteration forward of workload w (CUDA-graph replays, L2
     flushed between steps): ms, tokens/s, the fused kernel's MUFU fraction and
@@ -178,7 +184,8 @@ def time_workload(torch, nr, w, args, dev, flush, stream, xu_rates, props, mhz):
     cu = None if inp["cu_seqlens"] is None else nr.DeviceCuSeqlens(inp["cu_seqlens"], w.T, dev)
     tdt = P.dtype
     H = torch.empty((w.B, w.T, w.d_h), dtype=tdt, device=dev)
-    ws = torch.empty(max(nr.workspace_bytes(w.B, w.T, w.d_h, tdt, w.K, a) for a in ("fused", "per_iter")),
+    ws = torch.empty(max(nr.workspace_bytes(w.B, w.T, w.d_h, tdt, w.K, a, num_segments=segments_of(inp))
+                         for a in ("fused", "per_iter")),
                      dtype=torch.uint8, device=dev)
     res = {"B": w.B, "T": w.T, "d_h": w.d_h, "K": w.K, "dtype": w.dtype,
            "input": "preact drawn directly, U(-1, 1)"}
@@ -309,7 +316,8 @@ def run_ours(args, w, rank, world, local):
     P = nr.input_projection(x, W)
     H = torch.empty((w.B, w.T, w.d_h), dtype=tdt, device=dev)
     algo = args.algo
-    ws = torch.empty(max(nr.workspace_bytes(w.B, w.T, w.d_h, tdt, w.K, a) for a in ("fused", "per_iter")),
+    ws = torch.empty(max(nr.workspace_bytes(w.B, w.T, w.d_h, tdt, w.K, a, num_segments=segments_of(inp))
+                         for a in ("fused", "per_iter")),
                      dtype=torch.uint8, device=dev)
     flush = L2Flush(torch, dev)
     stream = torch.cuda.current_stream(dev)
