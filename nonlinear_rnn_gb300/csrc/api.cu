@@ -256,7 +256,6 @@ int nrnn_debug_lookback_form(int64_t B, int64_t T, int64_t d_h, int dtype, int a
     a.d_h = static_cast<int>(d_h);
     a.n_ut = static_cast<int>((d_h + TILE_U - 1) / TILE_U);
     a.n_chunks = static_cast<int>((T + NEWTON_L - 1) / NEWTON_L);
-    a.chain_stride = a.n_chunks;
     return newton_lookback_form(dtype, algo != NRNN_ALGO_PER_ITER, a);
 }
 
@@ -381,8 +380,10 @@ int nrnn_newton_forward_init(const void *preact, int dtype, const float *params,
             a.error = err;
             a.wait_ns = g_wait_ns.load();
             a.withhold_tile = static_cast<int>(g_withhold_tile.load());
-            a.chain_stride = static_cast<int>(ly.chain_stride);
-            if (ly.plan) a.plan = reinterpret_cast<const int4 *>(ws + ly.plan_off);
+            if (ly.plan) {   // the kernels read the plan, not the segment bounds
+                a.plan = reinterpret_cast<const int4 *>(ws + ly.plan_off);
+                a.chain_stride = static_cast<int>(ly.chain_stride);
+            }
             uint32_t *counters = reinterpret_cast<uint32_t *>(ws + ly.counters_off);
             if (fused) {
                 CUtensorMap tmH = tmP;
@@ -396,7 +397,7 @@ int nrnn_newton_forward_init(const void *preact, int dtype, const float *params,
                 a.ticket = counters;
                 CUtensorMap tmO;
                 if (!make_map(&tmO, H_out, dtype, d_h, T, B)) return NRNN_ERR_CUDA;
-                e = launch_newton(dtype, true, tmP, tmH, tmO, a, ly.n_tiles, stream);
+                e = launch_newton(dtype, true, tmP, tmH, tmO, a, ly.n_tiles, stream, ly.plan);
                 if (e != cudaSuccess) return NRNN_ERR_CUDA;
             } else {
                 void *hbuf = ws + ly.hbuf_off;
@@ -413,7 +414,7 @@ int nrnn_newton_forward_init(const void *preact, int dtype, const float *params,
                     a.k_first = a.k_last = k;
                     a.last = (k == K) ? 1 : 0;
                     a.ticket = counters + k;
-                    e = launch_newton(dtype, false, tmP, tmH, tmO, a, ly.n_tiles, stream);
+                    e = launch_newton(dtype, false, tmP, tmH, tmO, a, ly.n_tiles, stream, ly.plan);
                     if (e != cudaSuccess) return NRNN_ERR_CUDA;
                     prev = dst;
                 }
@@ -459,7 +460,6 @@ int nrnn_newton_forward_x(const void *x, const void *W_x, int dtype, const float
         a.d_in = static_cast<int>(d_in);
         a.n_ut = static_cast<int>((d_h + TILE_U - 1) / TILE_U);
         a.n_chunks = static_cast<int>((T + NEWTON_L - 1) / NEWTON_L);
-        a.chain_stride = a.n_chunks;
         a.slots = reinterpret_cast<unsigned long long *>(ws + ly.slots_off);
         a.residual_bits = reinterpret_cast<uint32_t *>(residual_dev);
         a.error = err;

@@ -189,7 +189,8 @@ constexpr int newton_min_blocks() { return (!FUSED && sizeof(TS) == 2) ? 9 : 8; 
 
 // EARLY: warp 0 reads the nearest predecessors' look-back slots before the
 // CTA barrier (see with_lookback_mode)
-template <typename TS, bool FUSED, bool XPROJ = false, bool EARLY = false>
+// PLAN: the chunks of a pack are segment-aligned, taken from a.plan.
+template <typename TS, bool FUSED, bool XPROJ = false, bool EARLY = false, bool PLAN = false>
 __global__ void __launch_bounds__(NW * 32, newton_min_blocks<TS, FUSED>())
     k_newton(const __grid_constant__ CUtensorMap tmP, const __grid_constant__ CUtensorMap tmH,
              const __grid_constant__ CUtensorMap tmO, const __grid_constant__ CUtensorMap tmX,
@@ -240,7 +241,7 @@ __global__ void __launch_bounds__(NW * 32, newton_min_blocks<TS, FUSED>())
         // tickets run chunk-major: every chunk this tile's look-back waits for
         // belongs to a CTA that has already started
         const uint32_t ticket = atomicAdd(a.ticket, 1u);
-        if (a.plan != nullptr) {
+        if constexpr (PLAN) {
             // segment-aligned chunks of a pack, level by level; the grid is
             // sized for an upper bound of their number
             const uint32_t item = ticket / a.n_ut;
@@ -258,19 +259,19 @@ __global__ void __launch_bounds__(NW * 32, newton_min_blocks<TS, FUSED>())
             s_tile[0] = static_cast<int>(cc);
             s_tile[1] = static_cast<int>(rem / a.n_ut);
             s_tile[2] = static_cast<int>(rem % a.n_ut);
-            s_tile[3] = static_cast<int>(cc) * L;
-            s_tile[4] = a.T;
-            s_tile[5] = static_cast<int>(cc);
         }
     }
     if (tid < L / 32) s_heads[tid] = 0u;
     __syncthreads();
-    if (s_tile[3] < 0) return;   // a ticket past the plan's last chunk
+    if constexpr (PLAN) {
+        if (s_tile[3] < 0) return;   // a ticket past the plan's last chunk
+    }
 
     const int c = s_tile[0], b = s_tile[1], ut = s_tile[2];
     // t_end: rows at or past it are outside this tile's sequence (the end of
     // the row, or of the tile's segment in a segment-aligned pack)
-    const int t0 = s_tile[3], t_end = s_tile[4], chain = s_tile[5];
+    const int t0 = PLAN ? s_tile[3] : c * L, t_end = PLAN ? s_tile[4] : a.T;
+    const int chain = PLAN ? s_tile[5] : c;
     const int u0 = ut * U;
     const bool load_h = a.H_prev != nullptr;   // H^(k-1) (per-iteration) or H^(0) (fused)
 
@@ -295,7 +296,7 @@ __global__ void __launch_bounds__(NW * 32, newton_min_blocks<TS, FUSED>())
             if (early_p) asm volatile("griddepcontrol.wait;" ::: "memory");
             if (tile_h) tma_load_3d(Hs, &tmH, &s_bar, u0, t0, b);
         }
-        if (a.plan != nullptr) {
+        if constexpr (PLAN) {
             if (c == 0) s_heads[0] = 1u;   // a segment's first chunk starts at its head
         } else {
             mark_heads(a.cu, a.S, t0, L, s_heads);
@@ -454,8 +455,9 @@ __global__ void __launch_bounds__(NW * 32, newton_min_blocks<TS, FUSED>())
     const bool general = (hm != 0u) || (nvalid < SEG);
     const void *Pv = FUSED ? static_cast<const void *>(Pf) : static_cast<const void *>(Pt);
 
-    const int n_tiles = a.B * a.n_ut * a.chain_stride;
-    const int tile = (b * a.n_ut + ut) * a.chain_stride + chain;
+    const int stride = PLAN ? a.chain_stride : a.n_chunks;   // look-back slots per column
+    const int n_tiles = a.B * a.n_ut * stride;
+    const int tile = (b * a.n_ut + ut) * stride + chain;
 
     for (int k = a.k_first; k <= a.k_last; ++k) {
         float2 J2[HALF];
@@ -544,20 +546,22 @@ __global__ void __launch_bounds__(NW * 32, newton_min_blocks<TS, FUSED>())
         }
     }
 
-    if (t_end - t0 < L && a.plan != nullptr) {
-        // the last chunk of a segment in a segment-aligned pack: the rows after
-        // it belong to the next segment, so the rows are stored one by one
-        if (uok) {
-            TS *Ho = static_cast<TS *>(a.H_next) + static_cast<size_t>(t0) * a.d_h + u;
-            const int rows = t_end - t0;
+    if constexpr (PLAN) {
+        if (t_end - t0 < L) {
+            // the last chunk of a segment in a segment-aligned pack: the rows
+            // after it belong to the next segment, so the rows are stored one by one
+            if (uok) {
+                TS *Ho = static_cast<TS *>(a.H_next) + static_cast<size_t>(t0) * a.d_h + u;
+                const int rows = t_end - t0;
 #pragma unroll
-            for (int j = 0; j < HALF; ++j) {
-                if (r0 + j < rows) Ho[static_cast<size_t>(r0 + j) * a.d_h] = from_f32<TS>(G[j].x);
-                if (r0 + HALF + j < rows)
-                    Ho[static_cast<size_t>(r0 + HALF + j) * a.d_h] = from_f32<TS>(G[j].y);
+                for (int j = 0; j < HALF; ++j) {
+                    if (r0 + j < rows) Ho[static_cast<size_t>(r0 + j) * a.d_h] = from_f32<TS>(G[j].x);
+                    if (r0 + HALF + j < rows)
+                        Ho[static_cast<size_t>(r0 + HALF + j) * a.d_h] = from_f32<TS>(G[j].y);
+                }
             }
+            return;
         }
-        return;
     }
     // H^(K) of the tile -> shared memory (the P tile's space: every read of it
     // lies behind the last barrier) -> one TMA store, which clips rows past T
@@ -653,38 +657,41 @@ size_t smem_bytes_for(bool with_h) {
 // published its inclusive prefix by the time a tile has its own aggregate.
 // With many resident chunks per column (long sequences of few columns) the
 // early read mostly finds a predecessor still at work.
-bool early_lookback(const NewtonArgs &a, int ctas_per_sm) {
+bool early_lookback(const NewtonArgs &a, int ctas_per_sm, bool plan) {
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
         return false;
     const int64_t resident = static_cast<int64_t>(sms) * ctas_per_sm;
     // a segment-aligned pack has one look-back chain per segment and unit tile
-    const int64_t columns = static_cast<int64_t>(a.plan != nullptr ? a.S : a.B) * a.n_ut;
+    const int64_t columns = static_cast<int64_t>(plan ? a.S : a.B) * a.n_ut;
     return resident <= EARLY_LOOKBACK_CHUNKS * columns;
 }
 
-template <typename TS, bool FUSED, bool EARLY>
+template <typename TS, bool FUSED, bool EARLY, bool PLAN>
 cudaError_t launch_one(const CUtensorMap &tmP, const CUtensorMap &tmH, const CUtensorMap &tmO,
                        const NewtonArgs &a, int64_t n_ctas, cudaStream_t stream) {
     static std::atomic<unsigned long long> configured{0};
     const size_t smem = smem_bytes_for<TS, FUSED>(a.H_prev != nullptr);
     cudaError_t e = once_per_device(configured, [](int) {
-        return cudaFuncSetAttribute(k_newton<TS, FUSED, false, EARLY>,
+        return cudaFuncSetAttribute(k_newton<TS, FUSED, false, EARLY, PLAN>,
                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     static_cast<int>(smem_bytes_for<TS, FUSED>(true)));
     });
     if (e != cudaSuccess) return e;
-    return launch_dependent(k_newton<TS, FUSED, false, EARLY>, static_cast<unsigned>(n_ctas),
+    return launch_dependent(k_newton<TS, FUSED, false, EARLY, PLAN>, static_cast<unsigned>(n_ctas),
                             NW * 32, smem, stream, tmP, tmH, tmO, tmP, tmP, a);
 }
 
 template <typename TS, bool FUSED>
 cudaError_t launch_one(const CUtensorMap &tmP, const CUtensorMap &tmH, const CUtensorMap &tmO,
-                       const NewtonArgs &a, int64_t n_ctas, cudaStream_t stream) {
-    return early_lookback(a, newton_min_blocks<TS, FUSED>())
-               ? launch_one<TS, FUSED, true>(tmP, tmH, tmO, a, n_ctas, stream)
-               : launch_one<TS, FUSED, false>(tmP, tmH, tmO, a, n_ctas, stream);
+                       const NewtonArgs &a, int64_t n_ctas, cudaStream_t stream, bool plan) {
+    const bool early = early_lookback(a, newton_min_blocks<TS, FUSED>(), plan);
+    if (plan)
+        return early ? launch_one<TS, FUSED, true, true>(tmP, tmH, tmO, a, n_ctas, stream)
+                     : launch_one<TS, FUSED, false, true>(tmP, tmH, tmO, a, n_ctas, stream);
+    return early ? launch_one<TS, FUSED, true, false>(tmP, tmH, tmO, a, n_ctas, stream)
+                 : launch_one<TS, FUSED, false, false>(tmP, tmH, tmO, a, n_ctas, stream);
 }
 
 cudaError_t launch_x(const CUtensorMap &tmX, const CUtensorMap &tmW, const CUtensorMap &tmO,
@@ -709,22 +716,22 @@ size_t newton_smem_bytes(int dtype, bool fused) {
     return fused ? smem_bytes_for<float, true>(true) : smem_bytes_for<float, false>(true);
 }
 
-int newton_lookback_form(int dtype, bool fused, const NewtonArgs &a) {
+int newton_lookback_form(int dtype, bool fused, const NewtonArgs &a, bool plan) {
     const int per_sm = dtype == 1 ? (fused ? newton_min_blocks<__nv_bfloat16, true>()
                                            : newton_min_blocks<__nv_bfloat16, false>())
                                   : (fused ? newton_min_blocks<float, true>()
                                            : newton_min_blocks<float, false>());
-    return early_lookback(a, per_sm) ? 1 : 0;
+    return early_lookback(a, per_sm, plan) ? 1 : 0;
 }
 
 cudaError_t launch_newton(int dtype, bool fused, const CUtensorMap &tmP, const CUtensorMap &tmH,
                           const CUtensorMap &tmO, const NewtonArgs &a, int64_t n_ctas,
-                          cudaStream_t stream) {
+                          cudaStream_t stream, bool plan) {
     if (dtype == 1)
-        return fused ? launch_one<__nv_bfloat16, true>(tmP, tmH, tmO, a, n_ctas, stream)
-                     : launch_one<__nv_bfloat16, false>(tmP, tmH, tmO, a, n_ctas, stream);
-    return fused ? launch_one<float, true>(tmP, tmH, tmO, a, n_ctas, stream)
-                 : launch_one<float, false>(tmP, tmH, tmO, a, n_ctas, stream);
+        return fused ? launch_one<__nv_bfloat16, true>(tmP, tmH, tmO, a, n_ctas, stream, plan)
+                     : launch_one<__nv_bfloat16, false>(tmP, tmH, tmO, a, n_ctas, stream, plan);
+    return fused ? launch_one<float, true>(tmP, tmH, tmO, a, n_ctas, stream, plan)
+                 : launch_one<float, false>(tmP, tmH, tmO, a, n_ctas, stream, plan);
 }
 
 cudaError_t launch_newton_x(const CUtensorMap &tmX, const CUtensorMap &tmW, const CUtensorMap &tmO,

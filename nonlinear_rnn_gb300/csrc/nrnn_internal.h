@@ -58,7 +58,13 @@ struct NewtonArgs {
                                   // initial iterate H^(0) (fused); null = zero
     void *H_next;                 // (B, T, d_h) storage type
     const float *params;          // (6, d_h)
-    const int32_t *cu;            // null or (S + 1)
+    // the kernels that take a pack's segment-aligned chunks (k_pack_plan)
+    // read the plan instead of the segment bounds; the layout of the struct
+    // stays that of the other kernels (register allocation follows it)
+    union {
+        const int32_t *cu;        // null or (S + 1)
+        const int4 *plan;         // segment-aligned chunks of the pack
+    };
     int S;
     int B, T, d_h;
     int n_ut, n_chunks;           // unit tiles, time chunks
@@ -70,10 +76,11 @@ struct NewtonArgs {
     uint32_t *error;              // error word (bit 0: look-back timeout, bit 1: TMA timeout)
     unsigned long long wait_ns;   // limit of every bounded wait
     int withhold_tile;            // debug: this tile never publishes its look-back slot (-1: none)
-    int d_in;                     // fused projection only: input width
-    const int4 *plan;             // segment-aligned chunks of a pack (k_pack_plan) or null:
-                                  // chunks of 64 steps of the whole time axis
-    int chain_stride;             // look-back slots per unit tile and iteration
+    union {
+        int d_in;                 // fused projection only: input width
+        int chain_stride;         // segment-aligned chunks: look-back slots per unit tile
+                                  // and iteration
+    };
 };
 
 struct BackwardArgs {
@@ -133,12 +140,13 @@ size_t newton_error_offset(int K);
 
 // Which look-back form launch_newton takes for these arguments (B, n_ut,
 // plan are read): 0 plain, 1 early reads.
-int newton_lookback_form(int dtype, bool fused, const NewtonArgs &a);
+int newton_lookback_form(int dtype, bool fused, const NewtonArgs &a, bool plan = false);
 // tmP over P (3 d_h, T, B), tmH over the H^(k-1) or H^(0) input, tmO over the
 // H output, all with a TILE_U x NEWTON_L x 1 box
+// plan: a.plan holds a pack's segment-aligned chunks (n_ctas an upper bound)
 cudaError_t launch_newton(int dtype, bool fused, const CUtensorMap &tmP, const CUtensorMap &tmH,
                           const CUtensorMap &tmO, const NewtonArgs &a, int64_t n_ctas,
-                          cudaStream_t stream);
+                          cudaStream_t stream, bool plan = false);
 
 // fused algorithm with the input projection computed in-kernel (bf16): tmX over
 // x (d_in, T, B) with a 64 x NEWTON_L x 1 box, tmW over W_x (d_in, 3 d_h) with
