@@ -696,11 +696,19 @@ def main():
                     help="launch each forward eagerly instead of replaying a CUDA graph")
     ap.add_argument("--batch", type=int, default=0,
                     help="override the workload's batch rows (smaller profiling captures)")
+    ap.add_argument("--segments", type=int, default=0,
+                    help="pack workloads: that many segments over proportionally fewer tokens "
+                         "(smaller profiling captures)")
     args = ap.parse_args()
     w = syn.WORKLOADS[args.workload]
     if args.batch > 0:
         import dataclasses
         w = dataclasses.replace(w, B=args.batch, name=w.name.replace(f"B{w.B} ", f"B{args.batch} "))
+    if args.segments > 0 and w.segments > 0:
+        import dataclasses
+        T = w.T * args.segments // w.segments
+        w = dataclasses.replace(w, T=T, segments=args.segments,
+                                name=w.name.replace(f"N{w.T} S{w.segments} ", f"N{T} S{args.segments} "))
     rank, world, local = dist_env()
 
     if args.impl == "reference":
