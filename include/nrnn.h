@@ -194,7 +194,10 @@ int nrnn_newton_forward_x(const void *x, const void *W_x, int dtype, const float
  *   gP        device, (B, T, 3 d_h) of dtype, 16-byte aligned (out; written by
  *             TMA stores of whole gate blocks)
  *   gparams   device, fp32 (6, d_h) (out; overwritten)
- *   workspace >= nrnn_newton_workspace_bytes(B, T, d_h, dtype, 1, NRNN_ALGO_FUSED)
+ *   workspace >= nrnn_newton_workspace_bytes(B, T, d_h, dtype, 1, NRNN_ALGO_FUSED); for a
+ *              pack, one of nrnn_newton_workspace_bytes_pack(T, d_h, dtype, 1,
+ *              NRNN_ALGO_FUSED, num_segments) bytes runs on segment-aligned
+ *              chunks as the forward does (in reverse order)
  * Results are accumulated with atomics: within float rounding, not bitwise
  * reproducible.
  */
@@ -439,17 +442,19 @@ int64_t nrnn_debug_withhold_publish(int64_t tile);
 int nrnn_debug_lookback_form(int64_t B, int64_t T, int64_t d_h, int dtype, int algo);
 
 /*
- * Debug: writes the segment-aligned chunk plan that nrnn_newton_forward uses
- * for a pack (see nrnn_newton_workspace_bytes_pack) into plan, device, at
- * least (2 + ceil(N / 64) + num_segments) x 4 int32, 16-byte aligned:
- * plan[0] = number of chunks n, then n entries {first row, end row of the
- * segment, chunk index j within the segment, index of the chunk in segment
- * order}, in the order the Newton kernels take them (by j; within one j by
- * the segment's number of chunks, most first).  cu_seqlens: device, validated.  Returns
+ * Debug: writes the segment-aligned chunk plan that nrnn_newton_forward
+ * (reverse = 0) or nrnn_newton_backward (reverse != 0) uses for a pack (see
+ * nrnn_newton_workspace_bytes_pack) into plan, device, at least
+ * (2 + ceil(N / 64) + num_segments) x 4 int32, 16-byte aligned: plan[0] =
+ * number of chunks n, then n entries {first row, end row of the segment,
+ * chunk index j within the segment, index of the chunk in segment order}, in
+ * the order the kernels take them (by j, or for reverse by the number of
+ * chunks of the segment after j; within one level by the segment's number of
+ * chunks, most first).  cu_seqlens: device, validated.  Returns
  * NRNN_ERR_INVALID_ARG for packs that take the time-axis chunks.
  */
-int nrnn_debug_pack_plan(const int32_t *cu_seqlens, int64_t num_segments, int64_t N, void *plan,
-                         void *stream);
+int nrnn_debug_pack_plan(const int32_t *cu_seqlens, int64_t num_segments, int64_t N, int reverse,
+                         void *plan, void *stream);
 
 /*
  * Upper limit, in nanoseconds, of every bounded device wait that later calls

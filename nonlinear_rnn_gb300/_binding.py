@@ -54,7 +54,7 @@ _SIGNATURES = {
     "nrnn_set_wait_limit_ns": ([_u64], _u64),
     "nrnn_debug_withhold_publish": ([_i64], _i64),
     "nrnn_debug_lookback_form": ([_i64, _i64, _i64, _int, _int], _int),
-    "nrnn_debug_pack_plan": ([_vp, _i64, _i64, _vp, _vp], _int),
+    "nrnn_debug_pack_plan": ([_vp, _i64, _i64, _int, _vp, _vp], _int),
     "nrnn_probe_xu_rates": ([ctypes.POINTER(ctypes.c_float)] * 3 + [_vp], _int),
     "nrnn_newton_host_staging_bytes": ([_i64, _i64, _i64, _int, _int, _vp, _i64, _i64], _sz),
     "nrnn_newton_forward_host": ([_vp, _int, _vp, _i64, _i64, _i64, _vp, _i64, _int, _f, _vp, _vp,
@@ -408,9 +408,11 @@ def newton_forward_x(x: torch.Tensor, W_x: torch.Tensor, params, cu_seqlens=None
 
 
 def newton_backward(preact: torch.Tensor, params, H: torch.Tensor, gH: torch.Tensor,
-                    cu_seqlens=None):
+                    cu_seqlens=None, workspace: torch.Tensor | None = None):
     """Adjoint of the recurrence at trajectory H for upstream gradient gH = dL/dH.
-    Returns (gP (B, T, 3 d_h) in preact's dtype, gparams (6, d_h) fp32)."""
+    Returns (gP (B, T, 3 d_h) in preact's dtype, gparams (6, d_h) fp32).  The
+    workspace is allocated here unless given (a uint8 CUDA tensor; for a pack
+    its size decides between segment-aligned and time-axis chunks)."""
     lib = load()
     preact = _device_tensor(preact, "preact")
     H = _device_tensor(H, "H")
@@ -426,8 +428,10 @@ def newton_backward(preact: torch.Tensor, params, H: torch.Tensor, gH: torch.Ten
     code = _dtype_code(preact)
     gP = torch.empty_like(preact)
     gprm = torch.empty((6, d_h), dtype=torch.float32, device=dev)
-    nbytes = lib.nrnn_newton_workspace_bytes(B, T, d_h, code, 1, ALGOS["fused"])
-    ws = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=dev)
+    nbytes = (lib.nrnn_newton_workspace_bytes_pack(T, d_h, code, 1, ALGOS["fused"], S) if S > 0
+              else lib.nrnn_newton_workspace_bytes(B, T, d_h, code, 1, ALGOS["fused"]))
+    ws = workspace if workspace is not None else torch.empty(max(nbytes, 256), dtype=torch.uint8,
+                                                             device=dev)
     with torch.cuda.device(dev):
         st = lib.nrnn_newton_backward(_ptr(preact), code, _ptr(prm), B, T, d_h, _ptr(cu), S,
                                       _ptr(H), _ptr(gH), _ptr(gP), _ptr(gprm), _ptr(ws),
@@ -598,16 +602,18 @@ def debug_withhold_publish(tile: int) -> int:
     return int(load().nrnn_debug_withhold_publish(int(tile)))
 
 
-def pack_plan(cu_seqlens, N: int, device="cuda") -> torch.Tensor:
-    """The segment-aligned chunk plan of a pack as the Newton kernels take it
-    (nrnn_debug_pack_plan): an (n, 4) int32 tensor of {first row, segment end,
-    chunk index within the segment, chunk index in segment order}."""
+def pack_plan(cu_seqlens, N: int, device="cuda", reverse: bool = False) -> torch.Tensor:
+    """The segment-aligned chunk plan of a pack as the Newton kernels (or, with
+    reverse, the backward kernel) take it (nrnn_debug_pack_plan): an (n, 4)
+    int32 tensor of {first row, segment end, chunk index within the segment,
+    chunk index in segment order}."""
     lib = load()
     cu32 = validate_cu_seqlens(cu_seqlens, N)
     cu = torch.from_numpy(cu32).to(device)
     S = cu32.size - 1
     plan = torch.zeros((2 + (N + 63) // 64 + S, 4), dtype=torch.int32, device=device)
-    st = lib.nrnn_debug_pack_plan(_ptr(cu), S, N, _ptr(plan), _stream(torch.device(device)))
+    st = lib.nrnn_debug_pack_plan(_ptr(cu), S, N, int(bool(reverse)), _ptr(plan),
+                                  _stream(torch.device(device)))
     _raise(st, "pack_plan")
     n = int(plan[0, 0].item())
     return plan[1:1 + n].cpu()

@@ -259,13 +259,13 @@ int nrnn_debug_lookback_form(int64_t B, int64_t T, int64_t d_h, int dtype, int a
     return newton_lookback_form(dtype, algo != NRNN_ALGO_PER_ITER, a);
 }
 
-int nrnn_debug_pack_plan(const int32_t *cu_seqlens, int64_t num_segments, int64_t N, void *plan,
-                         void *stream) {
+int nrnn_debug_pack_plan(const int32_t *cu_seqlens, int64_t num_segments, int64_t N, int reverse,
+                         void *plan, void *stream) {
     if (cu_seqlens == nullptr || plan == nullptr || N < 1 || !pack_plan_applies(1, N, num_segments))
         return NRNN_ERR_INVALID_ARG;
     return launch_pack_plan(cu_seqlens, static_cast<int>(num_segments),
                             static_cast<int>((N + NEWTON_L - 1) / NEWTON_L), static_cast<int4 *>(plan),
-                            static_cast<cudaStream_t>(stream)) == cudaSuccess
+                            reverse != 0, static_cast<cudaStream_t>(stream)) == cudaSuccess
                ? NRNN_OK
                : NRNN_ERR_CUDA;
 }
@@ -346,7 +346,7 @@ int nrnn_newton_forward_init(const void *preact, int dtype, const float *params,
     // dependents, the Newton launches, read it)
     if (ly.plan && K > 0 && B * T > 0 &&
         launch_pack_plan(cu_seqlens, S, static_cast<int>((T + NEWTON_L - 1) / NEWTON_L),
-                         reinterpret_cast<int4 *>(ws + ly.plan_off), stream) != cudaSuccess)
+                         reinterpret_cast<int4 *>(ws + ly.plan_off), false, stream) != cudaSuccess)
         return NRNN_ERR_CUDA;
     // one kernel clears counters, error word, slots and rho; rho accumulates by
     // atomicMax into residual_dev
@@ -488,7 +488,10 @@ int nrnn_newton_backward(const void *preact, int dtype, const float *params, int
     if (B * T > 0 && (H == nullptr || gH == nullptr || gP == nullptr || !aligned16(H) ||
                       !aligned16(gH) || !aligned16(gP)))
         return NRNN_ERR_INVALID_ARG;
-    const SyncLayout ly = layout(B, T, d_h, dtype, 1, true);
+    // segment-aligned chunks of a pack when the workspace has room for them
+    // (nrnn_newton_workspace_bytes_pack with K = 1)
+    SyncLayout ly = layout(B, T, d_h, dtype, 1, true, cu_seqlens ? num_segments : 0);
+    if (ly.plan && ws_bytes < ly.total) ly = layout(B, T, d_h, dtype, 1, true);
     if (workspace == nullptr || ws_bytes < ly.total ||
         (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
         return NRNN_ERR_WORKSPACE;
@@ -496,6 +499,11 @@ int nrnn_newton_backward(const void *preact, int dtype, const float *params, int
     unsigned char *ws = static_cast<unsigned char *>(workspace);
     if (B * T == 0)
         return cuda_status(cudaMemsetAsync(gparams, 0, sizeof(float) * 6 * d_h, stream));
+    if (ly.plan && launch_pack_plan(cu_seqlens, static_cast<int>(num_segments),
+                                    static_cast<int>((T + NEWTON_L - 1) / NEWTON_L),
+                                    reinterpret_cast<int4 *>(ws + ly.plan_off), true,
+                                    stream) != cudaSuccess)
+        return NRNN_ERR_CUDA;
     cudaError_t e = clear_for_call(ws, ly.zero_bytes, gparams, sizeof(float) * 6 * d_h, stream);
     if (e != cudaSuccess) return NRNN_ERR_CUDA;
     CUtensorMap tmP, tmH, tmG, tmGP;
@@ -514,11 +522,16 @@ int nrnn_newton_backward(const void *preact, int dtype, const float *params, int
     a.d_h = static_cast<int>(d_h);
     a.n_ut = static_cast<int>((d_h + TILE_U - 1) / TILE_U);
     a.n_chunks = static_cast<int>((T + NEWTON_L - 1) / NEWTON_L);
+    if (ly.plan) {   // the kernel reads the plan, not the segment bounds
+        a.plan = reinterpret_cast<const int4 *>(ws + ly.plan_off);
+        a.n_chunks = static_cast<int>(ly.chain_stride);
+    }
     a.slots = reinterpret_cast<unsigned long long *>(ws + ly.slots_off);
     a.ticket = reinterpret_cast<uint32_t *>(ws + ly.counters_off);
     a.error = reinterpret_cast<uint32_t *>(ws + ly.error_off);
     a.wait_ns = g_wait_ns.load();
-    return cuda_status(launch_backward(dtype, tmP, tmH, tmG, tmGP, a, ly.n_tiles, stream));
+    a.gP = gP;
+    return cuda_status(launch_backward(dtype, tmP, tmH, tmG, tmGP, a, ly.n_tiles, stream, ly.plan));
 }
 
 int nrnn_picard(const void *preact, int dtype, const float *params, int64_t B, int64_t T,

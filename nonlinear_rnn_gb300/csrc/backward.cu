@@ -112,7 +112,9 @@ __device__ __forceinline__ Derivs2 derivs2(float2 hs, float2 pz, float2 pr, floa
     return d;
 }
 
-template <typename TS, bool EARLY>
+// PLAN: the chunks of a pack are segment-aligned, taken from a.plan (last
+// chunks of the segments first).
+template <typename TS, bool EARLY, bool PLAN>
 __global__ void __launch_bounds__(NW * 32, 4)
     k_backward(const __grid_constant__ CUtensorMap tmP, const __grid_constant__ CUtensorMap tmH,
                const __grid_constant__ CUtensorMap tmG, const __grid_constant__ CUtensorMap tmGP,
@@ -126,28 +128,52 @@ __global__ void __launch_bounds__(NW * 32, 4)
     __shared__ float s_red[6][NW][32];
     __shared__ uint32_t s_heads[L / 32];
     __shared__ __align__(8) uint64_t s_bar;
-    __shared__ int s_tile[3];   // chunk, batch row, unit tile of this CTA's ticket
+    // this CTA's ticket: chunk (position in its look-back chain), batch row,
+    // unit tile, first row, end of the rows it may write, chain index of the
+    // look-back slots
+    __shared__ int s_tile[PLAN ? 6 : 3];
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     if (tid == 0) {
         const uint32_t ticket = atomicAdd(a.ticket, 1u);
-        const uint32_t per_chunk = static_cast<uint32_t>(a.B) * a.n_ut;
-        const uint32_t rem = ticket % per_chunk;
-        s_tile[0] = a.n_chunks - 1 - static_cast<int>(ticket / per_chunk);   // last chunk first
-        s_tile[1] = static_cast<int>(rem / a.n_ut);
-        s_tile[2] = static_cast<int>(rem % a.n_ut);
+        if constexpr (PLAN) {
+            // segment-aligned chunks, the last ones of the segments first; the
+            // grid is sized for an upper bound of their number
+            const uint32_t item = ticket / a.n_ut;
+            const int n_items = a.plan[0].x;
+            const int4 e = a.plan[1 + item];
+            s_tile[0] = e.z;
+            s_tile[1] = 0;
+            s_tile[2] = static_cast<int>(ticket - item * a.n_ut);
+            s_tile[3] = item < static_cast<uint32_t>(n_items) ? e.x : -1;
+            s_tile[4] = e.y;
+            s_tile[5] = e.w;
+        } else {
+            const uint32_t per_chunk = static_cast<uint32_t>(a.B) * a.n_ut;
+            const uint32_t rem = ticket % per_chunk;
+            s_tile[0] = a.n_chunks - 1 - static_cast<int>(ticket / per_chunk);   // last chunk first
+            s_tile[1] = static_cast<int>(rem / a.n_ut);
+            s_tile[2] = static_cast<int>(rem % a.n_ut);
+        }
     }
     if (tid < L / 32) s_heads[tid] = 0u;
     __syncthreads();
+    if constexpr (PLAN) {
+        if (s_tile[3] < 0) return;   // a ticket past the plan's last chunk
+    }
 
     const int c = s_tile[0], b = s_tile[1], ut = s_tile[2];
-    const int t0 = c * L, u0 = ut * U;
-    const int tile = (b * a.n_ut + ut) * a.n_chunks + c;
+    // t_end: rows at or past it are outside this tile's sequence; the chain
+    // holds chunks 0 .. n_chain - 1, the slot of chunk c + d lies d slots on
+    const int t0 = PLAN ? s_tile[3] : c * L, t_end = PLAN ? s_tile[4] : a.T;
+    const int n_chain = PLAN ? c + (t_end - t0 + L - 1) / L : a.n_chunks;
+    const int u0 = ut * U;
+    const int tile = (b * a.n_ut + ut) * a.n_chunks + (PLAN ? s_tile[5] : c);
     unsigned long long *slot = a.slots + static_cast<size_t>(tile) * 32 + lane;
     unsigned long long pre1 = SLOT_EMPTY, pre2 = SLOT_EMPTY;
     if (EARLY && warp == 0) {
-        if (c + 1 < a.n_chunks) pre1 = ld_relaxed_u64(slot + 32);
-        if (c + 2 < a.n_chunks) pre2 = ld_relaxed_u64(slot + 64);
+        if (c + 1 < n_chain) pre1 = ld_relaxed_u64(slot + 32);
+        if (c + 2 < n_chain) pre2 = ld_relaxed_u64(slot + 64);
     }
 
     if (tid == 0) {
@@ -158,7 +184,11 @@ __global__ void __launch_bounds__(NW * 32, 4)
         for (int g = 0; g < 3; ++g) tma_load_3d(Ps + g * L * U, &tmP, &s_bar, g * a.d_h + u0, t0, b);
         tma_load_3d(Hs, &tmH, &s_bar, u0, t0, b);
         tma_load_3d(Gs, &tmG, &s_bar, u0, t0, b);
-        mark_heads(a.cu, a.S, t0, L, s_heads);
+        if constexpr (PLAN) {
+            if (c == 0) s_heads[0] = 1u;   // a segment's first chunk starts at its head
+        } else {
+            mark_heads(a.cu, a.S, t0, L, s_heads);
+        }
     }
     const int u = u0 + lane;
     const bool uok = u < a.d_h;
@@ -173,7 +203,7 @@ __global__ void __launch_bounds__(NW * 32, 4)
     mbar_wait_bounded(&s_bar, 0, a.wait_ns, a.error);
     if (warp > 0) hb = to_f32(Hs[(r0 - 1) * U + lane]);
     const uint32_t hm = (s_heads[r0 >> 5] >> (r0 & 31)) & ((1u << SEG) - 1u);
-    const int nvalid = min(SEG, a.T - (t0 + r0));
+    const int nvalid = min(SEG, t_end - (t0 + r0));
 
     // Each thread takes its 16 rows as 8 pairs (i, i + 8) on packed f32x2
     // arithmetic: .x the lower half of the warp's rows, .y the upper half.
@@ -228,11 +258,11 @@ __global__ void __launch_bounds__(NW * 32, 4)
             tA *= s_aggA[w][lane];
         }
         float C = 0.f;   // nu at the first step after the chunk
-        if (c == a.n_chunks - 1) {
+        if (c == n_chain - 1) {
             publish(slot, 0.f, tB);
         } else {
             publish(slot, tA, tB);
-            C = lookback_lane<4>(slot, c, +1, a.n_chunks, a.wait_ns, a.error, pre1, pre2);
+            C = lookback_lane<4>(slot, c, +1, n_chain, a.wait_ns, a.error, pre1, pre2);
             publish(slot, 0.f, fmaf(tA, C, tB));
         }
         s_C[lane] = C;
@@ -277,7 +307,18 @@ __global__ void __launch_bounds__(NW * 32, 4)
     s_red[5][warp][lane] = g_bc.x + g_bc.y;
     fence_proxy_async_smem();   // the staged dL/dP is visible to the TMA store
     __syncthreads();
-    if (tid == 0) {
+    // a segment's short last chunk: the rows after it belong to the next
+    // segment, so its rows of dL/dP are stored one by one
+    const bool rowwise = PLAN && t_end - t0 < L;
+    if (rowwise) {
+        if (uok) {
+            TS *o = static_cast<TS *>(a.gP) + static_cast<size_t>(t0) * 3 * a.d_h + u;
+            for (int r = warp; r < t_end - t0; r += NW)
+#pragma unroll
+                for (int g = 0; g < 3; ++g)
+                    o[static_cast<size_t>(r) * 3 * a.d_h + g * a.d_h] = Ps[(g * L + r) * U + lane];
+        }
+    } else if (tid == 0) {
 #pragma unroll
         for (int g = 0; g < 3; ++g) tma_store_4d(&tmGP, Ps + g * L * U, u0, g, t0, b);
         bulk_commit();
@@ -290,50 +331,55 @@ __global__ void __launch_bounds__(NW * 32, 4)
             atomicAdd(a.gparams + g * a.d_h + u, s);
         }
     }
-    if (tid == 0) bulk_wait_read<0>();   // the tile outlives the store's reads
+    if (tid == 0 && !rowwise) bulk_wait_read<0>();   // the tile outlives the store's reads
 }
 
-template <typename TS, bool EARLY>
+template <typename TS, bool EARLY, bool PLAN>
 cudaError_t launch_bw(const CUtensorMap &tmP, const CUtensorMap &tmH, const CUtensorMap &tmG,
                       const CUtensorMap &tmGP, const BackwardArgs &a, int64_t n_ctas,
                       cudaStream_t stream) {
     static std::atomic<unsigned long long> configured{0};
     constexpr size_t smem = static_cast<size_t>(5) * L * U * sizeof(TS);
     cudaError_t e = once_per_device(configured, [](int) {
-        return cudaFuncSetAttribute(k_backward<TS, EARLY>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    static_cast<int>(smem));
+        return cudaFuncSetAttribute(k_backward<TS, EARLY, PLAN>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     });
     if (e != cudaSuccess) return e;
-    k_backward<TS, EARLY><<<static_cast<unsigned>(n_ctas), NW * 32, smem, stream>>>(tmP, tmH, tmG,
-                                                                                 tmGP, a);
+    k_backward<TS, EARLY, PLAN><<<static_cast<unsigned>(n_ctas), NW * 32, smem, stream>>>(
+        tmP, tmH, tmG, tmGP, a);
     return cudaGetLastError();
 }
 
 // the early reads pay when at most 4 chunks per column are resident at once
-// (4 CTAs per SM)
-bool bw_early(const BackwardArgs &a) {
+// (4 CTAs per SM); a segment-aligned pack has one column per segment and unit
+// tile
+bool bw_early(const BackwardArgs &a, bool plan) {
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
         return false;
-    return static_cast<int64_t>(sms) * 4 <= 4 * static_cast<int64_t>(a.B) * a.n_ut;
+    return static_cast<int64_t>(sms) * 4 <= 4 * static_cast<int64_t>(plan ? a.S : a.B) * a.n_ut;
 }
 
 template <typename TS>
 cudaError_t launch_bw(const CUtensorMap &tmP, const CUtensorMap &tmH, const CUtensorMap &tmG,
                       const CUtensorMap &tmGP, const BackwardArgs &a, int64_t n_ctas,
-                      cudaStream_t stream) {
-    return bw_early(a) ? launch_bw<TS, true>(tmP, tmH, tmG, tmGP, a, n_ctas, stream)
-                       : launch_bw<TS, false>(tmP, tmH, tmG, tmGP, a, n_ctas, stream);
+                      cudaStream_t stream, bool plan) {
+    const bool early = bw_early(a, plan);
+    if (plan)
+        return early ? launch_bw<TS, true, true>(tmP, tmH, tmG, tmGP, a, n_ctas, stream)
+                     : launch_bw<TS, false, true>(tmP, tmH, tmG, tmGP, a, n_ctas, stream);
+    return early ? launch_bw<TS, true, false>(tmP, tmH, tmG, tmGP, a, n_ctas, stream)
+                 : launch_bw<TS, false, false>(tmP, tmH, tmG, tmGP, a, n_ctas, stream);
 }
 
 }  // namespace
 
 cudaError_t launch_backward(int dtype, const CUtensorMap &tmP, const CUtensorMap &tmH,
                             const CUtensorMap &tmG, const CUtensorMap &tmGP, const BackwardArgs &a,
-                            int64_t n_ctas, cudaStream_t stream) {
-    if (dtype == 1) return launch_bw<__nv_bfloat16>(tmP, tmH, tmG, tmGP, a, n_ctas, stream);
-    return launch_bw<float>(tmP, tmH, tmG, tmGP, a, n_ctas, stream);
+                            int64_t n_ctas, cudaStream_t stream, bool plan) {
+    if (dtype == 1) return launch_bw<__nv_bfloat16>(tmP, tmH, tmG, tmGP, a, n_ctas, stream, plan);
+    return launch_bw<float>(tmP, tmH, tmG, tmGP, a, n_ctas, stream, plan);
 }
 
 }  // namespace nrnn

@@ -88,21 +88,29 @@ struct BackwardArgs {
     const void *gH;               // (B, T, d_h) dL/dH
     float *gparams;               // (6, d_h) dL/d(params), accumulated (zeroed by the caller)
     const float *params;
-    const int32_t *cu;
+    union {
+        const int32_t *cu;        // null or (S + 1)
+        const int4 *plan;         // segment-aligned chunks of the pack, last chunks first
+    };
     int S;
     int B, T, d_h;
-    int n_ut, n_chunks;
+    int n_ut, n_chunks;           // unit tiles; time chunks (segment-aligned: look-back
+                                  // slots per unit tile)
     unsigned long long *slots;    // [n_tiles][32]
     uint32_t *ticket;
     uint32_t *error;
     unsigned long long wait_ns;
+    void *gP;                     // (B, T, 3 d_h) dL/dP: a segment's short last chunk
+                                  // stores its rows one by one
 };
 
 // tmP, tmH, tmG: load maps as for the Newton kernel (tile boxes of P, H, dL/dH);
 // tmGP: 4-D store map over dL/dP as (d_h, 3, T, B) with a (32, 1, 64, 1) box.
+// plan: a.plan holds a pack's segment-aligned chunks in reverse order (n_ctas
+// an upper bound)
 cudaError_t launch_backward(int dtype, const CUtensorMap &tmP, const CUtensorMap &tmH,
                             const CUtensorMap &tmG, const CUtensorMap &tmGP, const BackwardArgs &a,
-                            int64_t n_ctas, cudaStream_t stream);
+                            int64_t n_ctas, cudaStream_t stream, bool plan = false);
 
 // Workspace of one call: [counters | error] and [slots], cleared together at
 // the start of every call (zero_bytes from the start), then (per-iteration
@@ -122,7 +130,9 @@ struct SyncLayout {
 // plan[0].x = number of chunks; plan[1 + i] = {first row, end row of the
 // segment, j, index of the chunk in segment order}; chunks in the order
 // the tickets hand them out: by j, and within one j by the segment's
-// number of chunks, most first (every chunk's predecessor comes earlier).  Used for packs
+// number of chunks, most first (every chunk's predecessor comes earlier).
+// reverse (the backward scan, whose chains run from a segment's end): by the
+// number of chunks after j instead of j.  Used for packs
 // of 2..PACK_PLAN_MAX_S segments, at most PACK_PLAN_MAX_CHUNKS 64-step
 // chunks, and S <= n_chunks / 8 (so that at most 1/8 more chunks than the
 // plain cut).
@@ -130,7 +140,7 @@ constexpr int PACK_PLAN_MAX_S = 4096;
 constexpr int PACK_PLAN_MAX_CHUNKS = 8192;
 bool pack_plan_applies(int64_t B, int64_t T, int64_t S);
 size_t pack_plan_bytes(int64_t T, int64_t S);
-cudaError_t launch_pack_plan(const int32_t *cu, int S, int n_chunks, int4 *plan,
+cudaError_t launch_pack_plan(const int32_t *cu, int S, int n_chunks, int4 *plan, bool reverse,
                              cudaStream_t stream);
 
 size_t newton_smem_bytes(int dtype, bool fused);

@@ -10,7 +10,9 @@
 // gives one chain per segment; handing the chunks out level by level (chunk j
 // of every segment before chunk j + 1 of any) spreads the chunks in flight
 // over all segments, so that a chunk's predecessor has usually finished the
-// iteration it waits for.  The last chunk of a segment may be short.
+// iteration it waits for.  The last chunk of a segment may be short.  The
+// backward scan runs each chain from the segment's end: its plan orders the
+// chunks by how many chunks of the segment follow them.
 #include "nrnn_device.cuh"
 #include "nrnn_internal.h"
 
@@ -62,7 +64,7 @@ __device__ int cta_exclusive_scan(const int *in, int *out, int n, int *s_warp) {
 // One CTA.  Shared memory: three arrays over chunk counts 0..n_chunks and
 // three over the segments.
 __global__ void __launch_bounds__(PT) k_pack_plan(const int32_t *__restrict__ cu, int S, int n_chunks,
-                                                  int4 *__restrict__ plan) {
+                                                  bool reverse, int4 *__restrict__ plan) {
     extern __shared__ int sm[];
     __shared__ int s_warp[PT / 32];
     const int M = n_chunks + 1;
@@ -95,7 +97,8 @@ __global__ void __launch_bounds__(PT) k_pack_plan(const int32_t *__restrict__ cu
     __syncthreads();
     for (int s = tid; s < S; s += PT) {
         const int c = nc[s], r0 = __ldg(cu + s), r1 = __ldg(cu + s + 1), b = base[s], rk = rank[s];
-        for (int j = 0; j < c; ++j) plan[1 + first[j] + rk] = make_int4(r0 + j * NEWTON_L, r1, j, b + j);
+        for (int j = 0; j < c; ++j)   // level: j, or the chunks after j (reverse)
+            plan[1 + first[reverse ? c - 1 - j : j] + rk] = make_int4(r0 + j * NEWTON_L, r1, j, b + j);
     }
     if (tid == 0) plan[0] = make_int4(total, 0, 0, 0);
 }
@@ -117,7 +120,7 @@ size_t pack_plan_bytes(int64_t T, int64_t S) {
     return sizeof(int4) * static_cast<size_t>(1 + n_chunks + S);
 }
 
-cudaError_t launch_pack_plan(const int32_t *cu, int S, int n_chunks, int4 *plan,
+cudaError_t launch_pack_plan(const int32_t *cu, int S, int n_chunks, int4 *plan, bool reverse,
                              cudaStream_t stream) {
     static std::atomic<unsigned long long> configured{0};
     cudaError_t e = once_per_device(configured, [](int) {
@@ -125,7 +128,7 @@ cudaError_t launch_pack_plan(const int32_t *cu, int S, int n_chunks, int4 *plan,
                                     static_cast<int>(plan_smem(PACK_PLAN_MAX_S, PACK_PLAN_MAX_CHUNKS)));
     });
     if (e != cudaSuccess) return e;
-    k_pack_plan<<<1, PT, plan_smem(S, n_chunks), stream>>>(cu, S, n_chunks, plan);
+    k_pack_plan<<<1, PT, plan_smem(S, n_chunks), stream>>>(cu, S, n_chunks, reverse, plan);
     return cudaGetLastError();
 }
 

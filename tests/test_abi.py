@@ -180,6 +180,6 @@ def test_pack_workspace_and_plan_checks():
     assert lib.nrnn_newton_workspace_bytes_pack(4096, 64, 0, 99, 2, 8) == 0      # K
     assert nr.workspace_bytes(1, 4096, 64, torch.float32, 3, "fused", num_segments=8) == pack
     fake = ctypes.c_void_p(256)
-    assert lib.nrnn_debug_pack_plan(fake, 1, 4096, fake, None) == -1
-    assert lib.nrnn_debug_pack_plan(fake, 9, 4096, fake, None) == -1
-    assert lib.nrnn_debug_pack_plan(None, 8, 4096, fake, None) == -1
+    assert lib.nrnn_debug_pack_plan(fake, 1, 4096, 0, fake, None) == -1
+    assert lib.nrnn_debug_pack_plan(fake, 9, 4096, 1, fake, None) == -1
+    assert lib.nrnn_debug_pack_plan(None, 8, 4096, 0, fake, None) == -1

@@ -130,3 +130,55 @@ def test_ragged_workload_pack_on_sampled_units(nr):
     Href, _ = oracle.newton(Pc, oracle.pack_params(prm)[:, units], w.K, cu_seqlens=cu, threads=8)
     err = np.max(np.abs(H[:, :, torch.as_tensor(units, device="cuda")].double().cpu().numpy() - Href))
     assert err <= 1e-4, err
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_backward_on_segment_aligned_pack(nr, dtype):
+    """The adjoint scan on segment-aligned chunks (each chain from the segment's
+    end; a segment's short last chunk stores dL/dP row by row) against the
+    oracle's adjoint and against the same call on time-axis chunks."""
+    cu = syn.cu_from_lengths(EDGE_LENGTHS)
+    N, d_h = int(cu[-1]), 40
+    tdt = TDT[dtype]
+    w = syn.small_workload(B=1, T=N, d_h=d_h, dtype=dtype, seed=97)
+    P = syn.direct_preact(w)
+    prm = syn.make_params(w)
+    H = oracle.sequential(P, prm, cu_seqlens=cu).astype(np.float32)
+    gH = np.random.default_rng(98).normal(size=H.shape).astype(np.float32)
+    if dtype == "bf16":
+        H, gH = syn.round_bf16(H), syn.round_bf16(gH)
+    gP_ref, gprm_ref = oracle.backward(P, prm, H, gH, cu_seqlens=cu)
+    ws_pack = torch.empty(nr.workspace_bytes(1, N, d_h, tdt, 1, "fused", num_segments=len(cu) - 1),
+                          dtype=torch.uint8, device="cuda")
+    ws_plain = torch.empty(nr.workspace_bytes(1, N, d_h, tdt, 1, "fused"), dtype=torch.uint8,
+                           device="cuda")
+    assert ws_pack.numel() > ws_plain.numel()
+    args = (dev(P, tdt), prm, dev(H, tdt), dev(gH, tdt))
+    gP, gprm = nr.newton_backward(*args, cu_seqlens=cu, workspace=ws_pack)
+    gP2, _ = nr.newton_backward(*args, cu_seqlens=cu, workspace=ws_plain)
+    scale = max(1.0, float(np.max(np.abs(gP_ref))))
+    tol = 2e-5 if dtype == "f32" else 2e-2
+    assert np.max(np.abs(host(gP) - gP_ref)) <= tol * scale
+    assert np.max(np.abs(host(gP) - host(gP2))) <= tol * scale
+    rel = np.max(np.abs(gprm.cpu().numpy() - gprm_ref)) / max(1.0, float(np.max(np.abs(gprm_ref))))
+    assert rel <= (1e-4 if dtype == "f32" else 1e-2)
+
+
+@pytest.mark.parametrize("lengths", [EDGE_LENGTHS, list(syn.segment_lengths(7, 64, 262144, 256, 8192))])
+def test_reverse_plan_order(nr, lengths):
+    """The backward's plan: every chunk once, ordered by the number of chunks
+    of its segment after it, within that by the segment's chunk count, and
+    each chunk after the chunk that follows it in time."""
+    cu = syn.cu_from_lengths(lengths)
+    plan = nr.pack_plan(cu, int(cu[-1]), reverse=True).numpy()
+    want = expected_chunks(cu)
+    seg = np.searchsorted(cu, plan[:, 0], side="right") - 1
+    got = {(int(s), int(e[2])): tuple(int(v) for v in e) for s, e in zip(seg, plan)}
+    assert got == want
+    chunks = -(-np.diff(cu) // 64)
+    after = chunks[seg] - 1 - plan[:, 2]
+    assert np.all(np.diff(after) >= 0)
+    for r in np.unique(after):
+        assert np.all(np.diff(chunks[seg[after == r]]) <= 0)
+    pos = {(int(s), int(e[2])): i for i, (s, e) in enumerate(zip(seg, plan))}
+    assert all(pos[(s, j + 1)] < pos[(s, j)] for (s, j) in want if (s, j + 1) in want)
