@@ -9,6 +9,7 @@
 
 #include "../../include/nrnn.h"
 #include "nrnn_internal.h"
+#include "pack_plan.cuh"
 
 using namespace nrnn;
 
@@ -57,28 +58,63 @@ SyncLayout layout(int64_t B, int64_t T, int64_t d_h, int dtype, int K, bool fuse
     return s;
 }
 
+// A pack's chunk plan, built by the first block of the clear kernel while the
+// others clear.
+struct PlanJob {
+    const int32_t *cu;
+    int S, n_chunks;
+    bool reverse;
+    int4 *plan;   // null: no plan
+};
+
+constexpr int CLEAR_THREADS = 256;
+
 // The per-call clears of a forward or backward as one kernel instead of two
 // memset nodes: the workspace's synchronisation area (counters, error word,
 // look-back slots; bytes a multiple of 16) and a small output (the residual
-// word, or the parameter gradients; bytes a multiple of 4).
-__global__ void k_clear(uint4 *ws, size_t ws16, uint32_t *out, size_t out4) {
+// word, or the parameter gradients; bytes a multiple of 4); with a plan job
+// block 0 builds the pack's chunk plan instead (no clearing in it).
+__global__ void __launch_bounds__(CLEAR_THREADS)
+    k_clear(uint4 *ws, size_t ws16, uint32_t *out, size_t out4, PlanJob job) {
     // the Newton kernel that follows may be scheduled now; it waits for this
     // grid's completion (griddepcontrol.wait) before it touches memory
     asm volatile("griddepcontrol.launch_dependents;");
-    const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
-    const size_t i0 = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    const bool planner = job.plan != nullptr;
+    if (planner && blockIdx.x == 0) {
+        extern __shared__ int sm[];
+        build_pack_plan<CLEAR_THREADS>(job.cu, job.S, job.n_chunks, job.reverse, job.plan, sm);
+        return;
+    }
+    const unsigned first = planner ? 1u : 0u, blocks = gridDim.x - first;
+    const size_t stride = static_cast<size_t>(blocks) * blockDim.x;
+    const size_t i0 = static_cast<size_t>(blockIdx.x - first) * blockDim.x + threadIdx.x;
     for (size_t i = i0; i < ws16; i += stride) ws[i] = make_uint4(0u, 0u, 0u, 0u);
     for (size_t i = i0; i < out4; i += stride) out[i] = 0u;
 }
 
 cudaError_t clear_for_call(void *ws, size_t ws_bytes, void *out, size_t out_bytes,
-                           cudaStream_t stream) {
+                           cudaStream_t stream, const PlanJob &job = PlanJob{}) {
     const size_t ws16 = ws_bytes / 16, out4 = out_bytes / 4;
     const size_t n = ws16 > out4 ? ws16 : out4;
-    if (n == 0) return cudaSuccess;
-    const size_t blocks = (n + 255) / 256;
-    k_clear<<<static_cast<unsigned>(blocks < 1216 ? blocks : 1216), 256, 0, stream>>>(
-        static_cast<uint4 *>(ws), ws16, static_cast<uint32_t *>(out), out4);
+    const bool planner = job.plan != nullptr;
+    if (n == 0 && !planner) return cudaSuccess;
+    size_t blocks = (n + CLEAR_THREADS - 1) / CLEAR_THREADS;
+    blocks = blocks < 1216 ? blocks : 1216;
+    if (blocks == 0) blocks = 1;
+    size_t smem = 0;
+    if (planner) {
+        static std::atomic<unsigned long long> configured{0};
+        cudaError_t e = once_per_device(configured, [](int) {
+            return cudaFuncSetAttribute(k_clear, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        static_cast<int>(pack_plan_smem(PACK_PLAN_MAX_S,
+                                                                        PACK_PLAN_MAX_CHUNKS)));
+        });
+        if (e != cudaSuccess) return e;
+        smem = pack_plan_smem(job.S, job.n_chunks);
+        blocks += 1;   // block 0 plans
+    }
+    k_clear<<<static_cast<unsigned>(blocks), CLEAR_THREADS, smem, stream>>>(
+        static_cast<uint4 *>(ws), ws16, static_cast<uint32_t *>(out), out4, job);
     return cudaGetLastError();
 }
 
@@ -342,15 +378,14 @@ int nrnn_newton_forward_init(const void *preact, int dtype, const float *params,
     uint32_t *err = reinterpret_cast<uint32_t *>(ws + ly.error_off);
     const int S = static_cast<int>(cu_seqlens ? num_segments : 0);
 
-    // the chunk plan of a segment-aligned pack, before the clear kernel (whose
-    // dependents, the Newton launches, read it)
-    if (ly.plan && K > 0 && B * T > 0 &&
-        launch_pack_plan(cu_seqlens, S, static_cast<int>((T + NEWTON_L - 1) / NEWTON_L),
-                         reinterpret_cast<int4 *>(ws + ly.plan_off), false, stream) != cudaSuccess)
-        return NRNN_ERR_CUDA;
-    // one kernel clears counters, error word, slots and rho; rho accumulates by
-    // atomicMax into residual_dev
-    cudaError_t e = clear_for_call(ws, ly.zero_bytes, residual_dev, sizeof(float), stream);
+    // one kernel clears counters, error word, slots and rho (rho accumulates by
+    // atomicMax into residual_dev) and builds the chunk plan of a
+    // segment-aligned pack, which its dependents, the Newton launches, read
+    PlanJob job{};
+    if (ly.plan && K > 0 && B * T > 0)
+        job = PlanJob{cu_seqlens, S, static_cast<int>((T + NEWTON_L - 1) / NEWTON_L), false,
+                      reinterpret_cast<int4 *>(ws + ly.plan_off)};
+    cudaError_t e = clear_for_call(ws, ly.zero_bytes, residual_dev, sizeof(float), stream, job);
     if (e != cudaSuccess) return NRNN_ERR_CUDA;
 
     if (B * T > 0) {
@@ -499,12 +534,12 @@ int nrnn_newton_backward(const void *preact, int dtype, const float *params, int
     unsigned char *ws = static_cast<unsigned char *>(workspace);
     if (B * T == 0)
         return cuda_status(cudaMemsetAsync(gparams, 0, sizeof(float) * 6 * d_h, stream));
-    if (ly.plan && launch_pack_plan(cu_seqlens, static_cast<int>(num_segments),
-                                    static_cast<int>((T + NEWTON_L - 1) / NEWTON_L),
-                                    reinterpret_cast<int4 *>(ws + ly.plan_off), true,
-                                    stream) != cudaSuccess)
-        return NRNN_ERR_CUDA;
-    cudaError_t e = clear_for_call(ws, ly.zero_bytes, gparams, sizeof(float) * 6 * d_h, stream);
+    PlanJob job{};
+    if (ly.plan)
+        job = PlanJob{cu_seqlens, static_cast<int>(num_segments),
+                      static_cast<int>((T + NEWTON_L - 1) / NEWTON_L), true,
+                      reinterpret_cast<int4 *>(ws + ly.plan_off)};
+    cudaError_t e = clear_for_call(ws, ly.zero_bytes, gparams, sizeof(float) * 6 * d_h, stream, job);
     if (e != cudaSuccess) return NRNN_ERR_CUDA;
     CUtensorMap tmP, tmH, tmG, tmGP;
     if (!make_map(&tmP, preact, dtype, 3 * d_h, T, B) || !make_map(&tmH, H, dtype, d_h, T, B) ||
