@@ -180,3 +180,20 @@ def test_x_input_pageable_empty_and_errors(nr):
     assert call(Wd.data_ptr(), need - 256) == -7          # NRNN_ERR_WORKSPACE
     assert call(Wd.data_ptr(), need) == 0
     assert np.max(np.abs(as_f64(Hh) - oracle.newton(Pref, inp["params"], 3)[0])) <= TOL["f32"]
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_x_input_pack_blocks_on_segment_aligned_chunks(nr, dtype):
+    """Blocks of 16 whole segments of a 32-segment pack: each block is a pack
+    of its own with at most one segment per 8 chunks, so the forward inside
+    runs on segment-aligned chunks."""
+    lens = syn.segment_lengths(5, 32, 16384, 256, 768)
+    cu = syn.cu_from_lengths(lens)
+    N = int(cu[-1])
+    inp, Pref = _x_case(dtype, 1, N, 32, 40, seed=68)
+    H, rho = nr.newton_forward_x_host(host_tensor(inp["x"], TDT[dtype]),
+                                      torch.from_numpy(inp["W_x"]).to(TDT[dtype]).cuda(),
+                                      inp["params"], cu_seqlens=cu, K=3, tokens_per_block=N // 2)
+    Href, rho_ref = oracle.newton(Pref, inp["params"], 3, cu_seqlens=cu)
+    assert np.max(np.abs(as_f64(H) - Href)) <= TOL[dtype]
+    assert abs(rho - rho_ref) <= TOL[dtype]
