@@ -421,9 +421,11 @@ int nrnn_newton_forward_noalloc(const void *preact, int dtype, const float *para
 
 /*
  * Debug: from the next call on, the Newton tile with index `tile` (tile =
- * (b * ceil(d_h / 32) + unit_tile) * ceil(T / 64) + chunk) never publishes
- * its look-back slot, so that the later chunks of its column wait for it
- * until their bounded wait gives up.  The call then still terminates and,
+ * (b * ceil(d_h / 32) + unit_tile) * ceil(T / 64) + chunk; on the
+ * segment-aligned chunks of a pack unit_tile * (ceil(T / 64) + num_segments)
+ * + the chunk's index in segment order) never publishes its look-back slot,
+ * so that the later chunks of its column wait for it until their bounded
+ * wait gives up.  The call then still terminates and,
  * with residual_host non-NULL, returns NRNN_ERR_TIMEOUT (H_out is invalid).
  * tile < 0 switches it off (the default).  Process-wide; returns the
  * previous value.  For testing the failure path only.

@@ -182,3 +182,32 @@ def test_reverse_plan_order(nr, lengths):
         assert np.all(np.diff(chunks[seg[after == r]]) <= 0)
     pos = {(int(s), int(e[2])): i for i, (s, e) in enumerate(zip(seg, plan))}
     assert all(pos[(s, j + 1)] < pos[(s, j)] for (s, j) in want if (s, j + 1) in want)
+
+
+@pytest.mark.parametrize("algo", ["fused", "per_iter"])
+def test_lookback_timeout_on_segment_aligned_chunks(nr, algo):
+    """A withheld chunk of a segment-aligned pack (the first chunk of the
+    2000-row segment, index 23 in segment order) makes the later chunks of its
+    chain give up their bounded waits: the call reports NRNN_ERR_TIMEOUT, and
+    the next call is correct."""
+    cu = syn.cu_from_lengths(EDGE_LENGTHS)
+    N, d_h = int(cu[-1]), 16
+    w = syn.small_workload(B=1, T=N, d_h=d_h, seed=96)
+    P = syn.direct_preact(w)
+    prm = syn.make_params(w)
+    ws = torch.empty(nr.workspace_bytes(1, N, d_h, torch.float32, 2, algo, num_segments=len(cu) - 1),
+                     dtype=torch.uint8, device="cuda")
+    chunks = -(-np.diff(cu) // 64)
+    assert int(chunks[:7].sum()) == 23 and chunks[7] > 1
+    old_limit = nr.set_wait_limit_ns(2_000_000)               # 2 ms
+    try:
+        nr.debug_withhold_publish(23)
+        with pytest.raises(nr.NrnnError) as ei:
+            nr.newton_forward(dev(P), prm, cu_seqlens=cu, K=2, algo=algo, workspace=ws)
+        assert ei.value.status == -6
+    finally:
+        nr.debug_withhold_publish(-1)
+        nr.set_wait_limit_ns(old_limit)
+    Href, _ = oracle.newton(P, prm, 2, cu_seqlens=cu)
+    H, _ = nr.newton_forward(dev(P), prm, cu_seqlens=cu, K=2, algo=algo, workspace=ws)
+    assert np.max(np.abs(host(H) - Href)) <= 2e-5
