@@ -199,21 +199,22 @@ bool make_map_2d_sw128(CUtensorMap *m, const void *base, int64_t inner, int64_t 
                        CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
-// 3-D bf16 map over x (B, T, d_in) row-major: dims (d_in, T, B), box (64, rows, 1),
-// 128-byte swizzle.
-bool make_map_x_sw128(CUtensorMap *m, const void *x, int64_t d_in, int64_t T, int64_t B,
-                      uint32_t box_rows) {
+// 3-D bf16 map over x (B, T, d_in) row-major: dims (d_in, T, B), box
+// (box_inner, rows, 1), 128-byte (box_inner 64) or 64-byte (box_inner 32) swizzle.
+bool make_map_x_swizzled(CUtensorMap *m, const void *x, int64_t d_in, int64_t T, int64_t B,
+                         uint32_t box_rows, uint32_t box_inner) {
     auto fn = encode_fn();
     if (fn == nullptr) return false;
     cuuint64_t dims[3] = {static_cast<cuuint64_t>(d_in), static_cast<cuuint64_t>(T),
                           static_cast<cuuint64_t>(B)};
     cuuint64_t strides[2] = {static_cast<cuuint64_t>(d_in * 2),
                              static_cast<cuuint64_t>(d_in * 2 * T)};
-    cuuint32_t box[3] = {64, box_rows, 1};
+    cuuint32_t box[3] = {box_inner, box_rows, 1};
     cuuint32_t estr[3] = {1, 1, 1};
     const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(x), dims,
                           strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          box_inner == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
@@ -482,8 +483,9 @@ int nrnn_newton_forward_x(const void *x, const void *W_x, int dtype, const float
     if (e != cudaSuccess) return NRNN_ERR_CUDA;
     if (B * T > 0) {
         CUtensorMap tmX, tmW;
-        if (!make_map_x_sw128(&tmX, x, d_in, T, B, NEWTON_L) ||
-            !make_map_2d_sw128(&tmW, W_x, d_in, 3 * d_h, 64, TILE_U))
+        // 32-wide K slices with the 64-byte swizzle (the kernel's stages)
+        if (!make_map_x_swizzled(&tmX, x, d_in, T, B, NEWTON_L, 32) ||
+            !make_map_2d(&tmW, W_x, d_in, 3 * d_h, 32, TILE_U, NRNN_BF16, CU_TENSOR_MAP_SWIZZLE_64B))
             return NRNN_ERR_CUDA;
         NewtonArgs a{};
         a.params = params;

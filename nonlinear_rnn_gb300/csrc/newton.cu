@@ -43,12 +43,19 @@ constexpr int U = TILE_U;
 // early look-back reads when at most this many chunks per column are resident
 constexpr int EARLY_LOOKBACK_CHUNKS = 4;
 
-// fused-projection prologue (XPROJ): bf16 operands, 64-wide K slices
-constexpr int XP_BK = 64;
+// fused-projection prologue (XPROJ): bf16 operands, 32-wide K slices (64-byte
+// rows, 64-byte swizzle), two stages in a ring that the P' tile aliases
+constexpr int XP_BK = 32;
 constexpr int XP_W_BOX_BYTES = 32 * XP_BK * 2;               // 32 W_x rows of one gate
-constexpr int XP_A_BYTES = 128 * XP_BK * 2;                  // 128 M rows (96 used)
-constexpr int XP_X_BYTES = L * XP_BK * 2;                    // 128 x rows (time steps)
-constexpr int XP_STAGE_BYTES = XP_A_BYTES + XP_X_BYTES;      // 32 KiB
+// the A operand holds the 96 W_x rows of the tile's three gates; the MMA's
+// M = 128 reads 32 rows more, which run on into the x tile that follows (their
+// TMEM lanes 96..127 are never read), so a stage needs no room for them
+constexpr int XP_A_BYTES = 3 * XP_W_BOX_BYTES;               // 96 W_x rows
+constexpr int XP_X_BYTES = L * XP_BK * 2;                    // 64 x rows (time steps)
+constexpr int XP_STAGE_BYTES = XP_A_BYTES + XP_X_BYTES;      // 10 KiB
+// the ring: two stages, or the P' tile written over them, whichever is larger
+// (24 KiB: 8 CTAs per SM, as registers allow)
+constexpr int XP_RING_BYTES = 2 * XP_STAGE_BYTES > 3 * L * U * 4 ? 2 * XP_STAGE_BYTES : 3 * L * U * 4;
 constexpr uint32_t XP_TMEM_COLS = L;                         // one fp32 column per time step
 constexpr uint32_t XP_IDESC = idesc_kmajor<false>(128, L);
 // Each thread's SEG rows are split into two halves of HALF rows that run side
@@ -196,7 +203,7 @@ __global__ void __launch_bounds__(NW * 32, newton_min_blocks<TS, FUSED>())
              const __grid_constant__ CUtensorMap tmO, const __grid_constant__ CUtensorMap tmX,
              const __grid_constant__ CUtensorMap tmW, const NewtonArgs a) {
     extern __shared__ __align__(128) unsigned char dsmem_raw[];
-    // the 128-byte swizzle of the XPROJ stages needs a 1024-byte aligned base
+    // the swizzled XPROJ stages want an aligned base (1024 bytes covers every swizzle)
     unsigned char *dsmem = XPROJ ? reinterpret_cast<unsigned char *>(
                                        (reinterpret_cast<uintptr_t>(dsmem_raw) + 1023) &
                                        ~static_cast<uintptr_t>(1023))
@@ -372,8 +379,8 @@ __global__ void __launch_bounds__(NW * 32, newton_min_blocks<TS, FUSED>())
                 const uint32_t A = smem_u32(dsmem + st * XP_STAGE_BYTES);
 #pragma unroll
                 for (int kk = 0; kk < XP_BK / 16; ++kk)
-                    mma<false, XP_IDESC>(tmem, sw128_desc(A + kk * 32),
-                                         sw128_desc(A + XP_A_BYTES + kk * 32),
+                    mma<false, XP_IDESC>(tmem, sw64_desc(A + kk * 32),
+                                         sw64_desc(A + XP_A_BYTES + kk * 32),
                                          (kt > 0 || kk > 0) ? 1u : 0u);
                 mma_commit(&s_xempty[st]);
             }
@@ -697,8 +704,12 @@ cudaError_t launch_one(const CUtensorMap &tmP, const CUtensorMap &tmH, const CUt
 cudaError_t launch_x(const CUtensorMap &tmX, const CUtensorMap &tmW, const CUtensorMap &tmO,
                      const NewtonArgs &a, int64_t n_ctas, cudaStream_t stream) {
     static std::atomic<unsigned long long> configured{0};
-    constexpr size_t smem = 2 * XP_STAGE_BYTES + 1024;   // stages alias the P' tile; + alignment
-    static_assert(2 * XP_STAGE_BYTES >= 3 * L * U * 4, "P' tile must fit in the stage ring");
+    constexpr size_t smem = XP_RING_BYTES + 1024;   // stages alias the P' tile; + alignment
+    static_assert(XP_RING_BYTES >= 3 * L * U * 4 && XP_RING_BYTES >= 2 * XP_STAGE_BYTES,
+                  "the ring holds two stages and the P' tile");
+    static_assert(XP_BK * 2 == 64 && XP_A_BYTES % 512 == 0 && XP_STAGE_BYTES % 512 == 0,
+                  "64-byte swizzled tiles of 64-byte rows start on 512-byte boundaries");
+    static_assert(XP_STAGE_BYTES >= 128 * XP_BK * 2, "the MMA's 128 A rows stay inside the stage");
     cudaError_t e = once_per_device(configured, [](int) {
         return cudaFuncSetAttribute(k_newton<__nv_bfloat16, true, true>,
                                     cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));

@@ -18,6 +18,18 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t smem_addr) {
     return d;
 }
 
+// The same with the 64-byte swizzle: 8-row x 64-byte core blocks every 512
+// bytes (SBO), layout type 4 (SWIZZLE_64B).
+__device__ __forceinline__ uint64_t sw64_desc(uint32_t smem_addr) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((smem_addr & 0x3ffffu) >> 4);          // start address
+    d |= static_cast<uint64_t>(16u >> 4) << 16;                        // LBO (unused here)
+    d |= static_cast<uint64_t>(512u >> 4) << 32;                       // SBO
+    d |= static_cast<uint64_t>(1u) << 46;                              // version
+    d |= static_cast<uint64_t>(4u) << 61;                              // SWIZZLE_64B
+    return d;
+}
+
 __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, uint64_t *bar,
                                             int x, int y) {
     asm volatile(
