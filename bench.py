@@ -48,8 +48,8 @@ def peaks():
     if os.path.exists(p):
         with open(p) as fh:
             d = json.load(fh)
-        return {"hbm_gbs": d["hbm_gbs"], "src": "measured"}
-    return {"hbm_gbs": 6800.0, "src": "fallback"}
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d.get("bf16_tflops", 1900.0), "src": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "src": "fallback"}
 
 
 def max_over_ranks(ms, world, device):
@@ -508,6 +508,14 @@ def run_ours(args, w, rank, world, local):
             nxt[name] = {"slots": slots, "ms": dm, "bytes": nbytes,
                          "achieved_gbs": nbytes / (dm * 1e-3) / 1e9,
                          "frac": nbytes / (dm * 1e-3) / 1e9 / pk["hbm_gbs"]}
+            if with_x:
+                # the step's projection x W_x^T is a GEMM of 2 slots 3 d_h d_in
+                # flops: against the tensor roof of the storage type (bf16
+                # measured; fp32 runs three TF32 products at half that rate)
+                flops = 2.0 * slots * 3 * w.d_h * w.d_in * (3 if w.dtype == "f32" else 1)
+                tf = pk["bf16_tflops"] * (0.5 if w.dtype == "f32" else 1.0)
+                nxt[name]["tensor"] = {"flops": flops, "achieved_tflops": flops / (dm * 1e-3) / 1e12,
+                                       "peak_tflops": tf, "frac": flops / (dm * 1e-3) / 1e12 / tf}
 
         # a step for every token of the workload as a slot (P and h far larger
         # than L2: the kernel's bandwidth), then the batch sizes of serving;
