@@ -24,10 +24,11 @@
 //
 // Tiles of P (three gate blocks) and of H^(k-1) are staged in shared memory
 // by TMA (cp.async.bulk.tensor, completion on an mbarrier).  CTAs take tiles
-// from an atomic ticket in chunk-major order, so every CTA whose result a
-// CTA waits for has already started: the look-back cannot deadlock.  Every
-// wait is bounded by the caller's limit and reports a timeout in the error
-// word instead of hanging.
+// from an atomic ticket in chunk-major order (for a pack cut into
+// segment-aligned chunks: level by level from the chunk plan), so every CTA
+// whose result a CTA waits for has already started: the look-back cannot
+// deadlock.  Every wait is bounded by the caller's limit and reports a
+// timeout in the error word instead of hanging.
 #include "nrnn_device.cuh"
 #include "nrnn_internal.h"
 #include "tcgen05.cuh"
