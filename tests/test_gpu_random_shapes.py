@@ -85,3 +85,38 @@ def test_random_packs_with_room_for_segment_aligned_chunks(nr):
         Href, rho_ref = oracle.newton(P, prm, K, cu_seqlens=cu)
         assert float(np.max(np.abs(H.double().cpu().numpy() - Href))) <= 2e-5
         assert abs(rho.item() - rho_ref) <= 2e-5
+
+
+@pytest.mark.parametrize("i", range(6))
+def test_random_backward_matches_oracle(nr, i):
+    """The adjoint scan on random shapes (batch rows, packs with and without
+    room for segment-aligned chunks) against the oracle's adjoint."""
+    rng = np.random.default_rng(8000 + i)
+    dtype = ("f32", "bf16")[i % 2]
+    tdt = TDT[dtype]
+    d_h = int(8 * rng.integers(1, 16))
+    if i >= 2:
+        S = int(rng.integers(2, 5))
+        lens = rng.integers(1, 64 * (12 if i >= 4 else 3), size=S)
+        cu = syn.cu_from_lengths(lens)
+        B, T = 1, int(cu[-1])
+    else:
+        cu, B, T = None, int(rng.integers(1, 4)), int(rng.integers(1, 1500))
+    w = syn.small_workload(B=B, T=T, d_h=d_h, dtype=dtype, seed=8100 + i)
+    P = syn.direct_preact(w)
+    prm = syn.make_params(w)
+    Pd = torch.from_numpy(np.ascontiguousarray(P, dtype=np.float32)).cuda().to(tdt)
+    Pq = Pd.float().cpu().numpy().astype(np.float64)
+    H = oracle.sequential(Pq, prm, cu_seqlens=cu).astype(np.float32)
+    gH = rng.normal(size=H.shape).astype(np.float32)
+    Hd = torch.from_numpy(H).cuda().to(tdt)
+    gHd = torch.from_numpy(gH).cuda().to(tdt)
+    Hq = Hd.float().cpu().numpy().astype(np.float64)
+    gHq = gHd.float().cpu().numpy().astype(np.float64)
+    gP_ref, gprm_ref = oracle.backward(Pq, prm, Hq, gHq, cu_seqlens=cu)
+    gP, gprm = nr.newton_backward(Pd, prm, Hd, gHd, cu_seqlens=cu)
+    scale = max(1.0, float(np.max(np.abs(gP_ref))))
+    tol = 2e-5 if dtype == "f32" else 2e-2
+    assert float(np.max(np.abs(gP.float().cpu().numpy() - gP_ref))) <= tol * scale
+    rel = np.max(np.abs(gprm.cpu().numpy() - gprm_ref)) / max(1.0, float(np.max(np.abs(gprm_ref))))
+    assert rel <= (1e-4 if dtype == "f32" else 1e-2)
