@@ -134,7 +134,9 @@ size_t nrnn_newton_workspace_bytes_pack(int64_t N, int64_t d_h, int dtype, int K
  *                 there, and returns NRNN_ERR_TIMEOUT if a bounded device
  *                 wait gave up, else NRNN_ERR_DIVERGED if rho > residual_fail
  *                 or rho is not finite (H_out is written either way).
- *   workspace     device, ws_bytes >= nrnn_newton_workspace_bytes(...);
+ *   workspace     device, ws_bytes >= nrnn_newton_workspace_bytes(...)
+ *                 (a pack: nrnn_newton_workspace_bytes_pack(...) lets the
+ *                 kernels cut each segment into chunks of its own);
  *                 256-byte aligned; its contents need no initialisation and
  *                 are scratch after the call.  Calls that share a
  *                 workspace must not overlap on the GPU.
