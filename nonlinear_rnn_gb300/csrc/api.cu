@@ -92,8 +92,20 @@ __global__ void __launch_bounds__(CLEAR_THREADS)
     for (size_t i = i0; i < out4; i += stride) out[i] = 0u;
 }
 
+// Above this much shared memory for the plan, it is built by a kernel of its
+// own before the clear kernel: every block of a launch reserves the same
+// shared memory, and a large reservation would leave the clearing blocks one
+// per SM.
+constexpr size_t PLAN_IN_CLEAR_MAX_SMEM = 64 * 1024;
+
 cudaError_t clear_for_call(void *ws, size_t ws_bytes, void *out, size_t out_bytes,
-                           cudaStream_t stream, const PlanJob &job = PlanJob{}) {
+                           cudaStream_t stream, const PlanJob &job_in = PlanJob{}) {
+    PlanJob job = job_in;
+    if (job.plan != nullptr && pack_plan_smem(job.S, job.n_chunks) > PLAN_IN_CLEAR_MAX_SMEM) {
+        cudaError_t e = launch_pack_plan(job.cu, job.S, job.n_chunks, job.plan, job.reverse, stream);
+        if (e != cudaSuccess) return e;
+        job.plan = nullptr;
+    }
     const size_t ws16 = ws_bytes / 16, out4 = out_bytes / 4;
     const size_t n = ws16 > out4 ? ws16 : out4;
     const bool planner = job.plan != nullptr;

@@ -211,3 +211,26 @@ def test_lookback_timeout_on_segment_aligned_chunks(nr, algo):
     Href, _ = oracle.newton(P, prm, 2, cu_seqlens=cu)
     H, _ = nr.newton_forward(dev(P), prm, cu_seqlens=cu, K=2, algo=algo, workspace=ws)
     assert np.max(np.abs(host(H) - Href)) <= 2e-5
+
+
+@pytest.mark.parametrize("algo", ["fused", "per_iter"])
+def test_long_pack_whose_plan_takes_its_own_kernel(nr, algo):
+    """A pack of 400000 rows and 8 segments: 6250 chunks, so the plan needs
+    more shared memory than the clear kernel's blocks should reserve and is
+    built by a kernel of its own; the forward on it against the oracle."""
+    lens = syn.segment_lengths(11, 8, 400000, 20000, 80000)
+    cu = syn.cu_from_lengths(lens)
+    N = int(cu[-1])
+    assert N == 400000
+    w = syn.small_workload(B=1, T=N, d_h=16, seed=101)
+    P = syn.direct_preact(w)
+    prm = syn.make_params(w)
+    ws = torch.empty(nr.workspace_bytes(1, N, 16, torch.float32, 2, algo, num_segments=8),
+                     dtype=torch.uint8, device="cuda")
+    assert ws.numel() > nr.workspace_bytes(1, N, 16, torch.float32, 2, algo)
+    H, rho = nr.newton_forward(dev(P), prm, cu_seqlens=cu, K=2, algo=algo, check=False, workspace=ws)
+    Href, rho_ref = oracle.newton(P, prm, 2, cu_seqlens=cu)
+    assert np.max(np.abs(host(H) - Href)) <= 2e-5
+    assert abs(rho.item() - rho_ref) <= 2e-5
+    plan = nr.pack_plan(cu, N).numpy()
+    assert len(plan) == int(sum(-(-int(l) // 64) for l in lens))
