@@ -60,7 +60,7 @@ typedef enum {
     NRNN_OK = 0,
     NRNN_ERR_INVALID_ARG = -1,  /* null pointer, negative size, bad dtype, misaligned */
     NRNN_ERR_CU_SEQLENS = -2,   /* cu_seqlens violates the rules above */
-    NRNN_ERR_UNSUPPORTED = -3,  /* valid request this build does not handle (d_h % 8) */
+    NRNN_ERR_UNSUPPORTED = -3,  /* valid request the library does not handle (d_h % 8) */
     NRNN_ERR_CUDA = -4,         /* a CUDA runtime/driver call or a launch failed */
     NRNN_ERR_DIVERGED = -5,     /* rho > residual_fail, or rho is NaN/inf */
     NRNN_ERR_TIMEOUT = -6,      /* a bounded device wait gave up (result invalid) */
