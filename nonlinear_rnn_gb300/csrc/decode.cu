@@ -301,6 +301,157 @@ __global__ void __launch_bounds__(128)
     }
 }
 
+// k_decode_step_xtc_sk (bf16, one tile of at most 64 slots, 8-unit tiles):
+// the same projection split along d_in over the KS CTAs of a thread-block
+// cluster, for the small batches where one CTA per 8 units leaves most SMs
+// idle and each CTA's K loop of d_in / 64 slices is the latency.  Rank r of
+// the cluster accumulates the slices [r kt / KS, (r + 1) kt / KS) through a
+// 2-stage ring, writes its fp32 partial sums (3 gates x 64 slots x 8 units)
+// into its own shared memory, and after a cluster barrier sums the partials
+// of all KS ranks for its quarter of the slots (distributed shared memory
+// reads), rounds them to bf16 and applies the step.  No multicast: every CTA
+// loads its own operand tiles.
+constexpr int SK_UNITS = 8;
+constexpr int SK_KS = 4;
+constexpr int SK_STAGES = 2;
+constexpr int SK_PART_FLOATS = 3 * XT_SLOTS * SK_UNITS;
+static_assert(SK_STAGES * XT_STAGE_BYTES >= SK_PART_FLOATS * 4, "the partials fit in the ring");
+static_assert(XT_SLOTS % SK_KS == 0 && (XT_SLOTS / SK_KS) * SK_UNITS == 128,
+              "one (slot, unit) pair per thread in the epilogue");
+
+__device__ __forceinline__ uint32_t sk_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ float sk_ld_remote(const float *p, uint32_t rank) {
+    uint32_t a;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"(smem_u32(p)), "r"(rank));
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(a) : "memory");
+    return v;
+}
+__device__ __forceinline__ void sk_cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+__global__ void __launch_bounds__(128)
+    k_decode_step_xtc_sk(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
+                         const float *__restrict__ params, const __nv_bfloat16 *__restrict__ h_in,
+                         __nv_bfloat16 *__restrict__ h_out, int slots, int d_in, int d_h) {
+    constexpr int W_BOX_BYTES = SK_UNITS * XT_BK * 2;
+    extern __shared__ unsigned char sk_raw[];
+    unsigned char *smem = reinterpret_cast<unsigned char *>(
+        (reinterpret_cast<uintptr_t>(sk_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    __shared__ __align__(8) uint64_t full_bar[SK_STAGES], empty_bar[SK_STAGES], acc_bar;
+    __shared__ uint32_t s_tmem, s_err;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const uint32_t rank = sk_rank();
+    const int u0 = blockIdx.x * SK_UNITS;
+    const int kt_all = (d_in + XT_BK - 1) / XT_BK;
+    const int kt0 = static_cast<int>(rank) * kt_all / SK_KS;
+    const int kt_count = (static_cast<int>(rank) + 1) * kt_all / SK_KS - kt0;
+    if (tid == 0) {
+        for (int i = 0; i < SK_STAGES; ++i) {
+            mbar_init(&full_bar[i], 1);
+            mbar_init(&empty_bar[i], 1);
+        }
+        mbar_init(&acc_bar, 1);
+        s_err = 0u;
+        fence_mbar_init();
+        prefetch_tensormap(&tmX);
+        prefetch_tensormap(&tmW);
+    }
+    if (warp == 2) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_u32(&s_tmem)),
+                     "r"(XT_TMEM_COLS)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    __syncthreads();
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    const uint32_t tmem = s_tmem;
+    if (kt_count > 0) {
+        if (warp == 0 && lane == 0) {
+            for (int k = 0; k < kt_count; ++k) {
+                const int st = k % SK_STAGES, kt = kt0 + k;
+                if (k >= SK_STAGES)
+                    mbar_wait_bounded(&empty_bar[st], ((k / SK_STAGES) - 1) & 1, XT_WAIT_NS, &s_err);
+                unsigned char *A = smem + st * XT_STAGE_BYTES;
+                mbar_arrive_expect_tx(&full_bar[st], 3 * W_BOX_BYTES + XT_B_BYTES);
+#pragma unroll
+                for (int g = 0; g < 3; ++g)   // gate g at rows 32 g
+                    tma_load_2d(A + g * 32 * XT_BK * 2, &tmW, &full_bar[st], kt * XT_BK, g * d_h + u0);
+                tma_load_2d(A + XT_A_BYTES, &tmX, &full_bar[st], kt * XT_BK, 0);
+            }
+        } else if (warp == 1 && lane == 0) {
+            for (int k = 0; k < kt_count; ++k) {
+                const int st = k % SK_STAGES;
+                mbar_wait_bounded(&full_bar[st], (k / SK_STAGES) & 1, XT_WAIT_NS, &s_err);
+                asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+                const uint32_t A = smem_u32(smem + st * XT_STAGE_BYTES);
+#pragma unroll
+                for (int kk = 0; kk < XT_BK / 16; ++kk)
+                    mma<false, XT_IDESC>(tmem, sw128_desc(A + kk * 32), sw128_desc(A + XT_A_BYTES + kk * 32),
+                                         (k > 0 || kk > 0) ? 1u : 0u);
+                mma_commit(&empty_bar[st]);
+            }
+            mma_commit(&acc_bar);
+        }
+        __syncwarp();
+    }
+    const bool ok = kt_count == 0 || mbar_wait_bounded(&acc_bar, 0, XT_WAIT_NS, &s_err);
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    fence_proxy_async_smem();   // the partials overwrite the stages
+    float *part = reinterpret_cast<float *>(smem);   // [3 gates][64 slots][8 units]
+    if (warp < 3) {
+#pragma unroll 1
+        for (int cc = 0; cc < XT_SLOTS / 32; ++cc) {
+            uint32_t v[32];
+            if (kt_count > 0) tmem_ld_cols<32>(tmem + (static_cast<uint32_t>(warp * 32) << 16) + cc * 32, v);
+            if (lane < SK_UNITS) {
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                    part[(warp * XT_SLOTS + cc * 32 + i) * SK_UNITS + lane] =
+                        !ok ? __int_as_float(0x7fffffff) : (kt_count > 0 ? __uint_as_float(v[i]) : 0.f);
+            }
+        }
+    }
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    // every rank's partials are complete and visible to the cluster (this also
+    // makes sure every CTA of the cluster runs before any remote read)
+    sk_cluster_sync();
+    if (warp == 2) {
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                     "r"(XT_TMEM_COLS)
+                     : "memory");
+    }
+    // rank r finishes slots [16 r, 16 r + 16): thread t takes slot 16 r + t / 8, unit t % 8
+    const int ul = tid % SK_UNITS, s = static_cast<int>(rank) * (XT_SLOTS / SK_KS) + tid / SK_UNITS;
+    const int u = u0 + ul;
+    if (u < d_h && s < slots) {
+        float pg[3];
+#pragma unroll
+        for (int g = 0; g < 3; ++g) {
+            float acc = 0.f;
+#pragma unroll
+            for (int q = 0; q < SK_KS; ++q)
+                acc += sk_ld_remote(&part[(g * XT_SLOTS + s) * SK_UNITS + ul], static_cast<uint32_t>(q));
+            pg[g] = round_to<__nv_bfloat16>(acc);
+        }
+        const int64_t i = static_cast<int64_t>(s) * d_h + u;
+        const float h = (h_in != nullptr) ? to_f32(h_in[i]) : 0.f;
+        h_out[i] = from_f32<__nv_bfloat16>(
+            cell_f_storage<__nv_bfloat16>(h, pg[0], pg[1], pg[2], load_unit_params(params, d_h, u, true)));
+    }
+    // no CTA leaves while the others may still read its partials
+    sk_cluster_sync();
+}
+
 }  // namespace
 
 int decode_xtc_units(int slots, int d_h) {
@@ -329,10 +480,51 @@ cudaError_t launch_xtc(const CUtensorMap &tmX, const CUtensorMap &tmW, const flo
     return cudaGetLastError();
 }
 
+// The split-K cluster form for one slot tile of 8-unit CTAs that leave most
+// SMs idle and have at least SK_KS slices of d_in each.
+bool decode_split_k(int slots, int d_in, int d_h) {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return false;
+    const int64_t ctas = (d_h + SK_UNITS - 1) / SK_UNITS;   // 4 fit an SM (shared memory)
+    return slots <= XT_SLOTS && (d_in + XT_BK - 1) / XT_BK >= SK_KS &&
+           ctas * SK_KS <= 4 * static_cast<int64_t>(sms) && decode_xtc_units(slots, d_h) == SK_UNITS;
+}
+
+cudaError_t launch_xtc_sk(const CUtensorMap &tmX, const CUtensorMap &tmW, const float *params,
+                          const void *h_in, void *h_out, int slots, int d_in, int d_h,
+                          cudaStream_t stream) {
+    static std::atomic<unsigned long long> configured{0};
+    constexpr size_t smem = static_cast<size_t>(SK_STAGES) * XT_STAGE_BYTES + 1024;
+    cudaError_t e = once_per_device(configured, [](int) {
+        return cudaFuncSetAttribute(k_decode_step_xtc_sk, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    static_cast<int>(smem));
+    });
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((d_h + SK_UNITS - 1) / SK_UNITS, 1, SK_KS);
+    cfg.blockDim = dim3(128);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 1;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = SK_KS;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, k_decode_step_xtc_sk, tmX, tmW, params,
+                              static_cast<const __nv_bfloat16 *>(h_in),
+                              static_cast<__nv_bfloat16 *>(h_out), slots, d_in, d_h);
+}
+
 cudaError_t launch_decode_step_xtc(const CUtensorMap &tmX, const CUtensorMap &tmW,
                                    const float *params, const void *h_in, void *h_out, int slots,
                                    int d_in, int d_h, cudaStream_t stream) {
     if (slots == 0) return cudaSuccess;
+    if (decode_split_k(slots, d_in, d_h))
+        return launch_xtc_sk(tmX, tmW, params, h_in, h_out, slots, d_in, d_h, stream);
     if (decode_xtc_units(slots, d_h) == 32)
         return launch_xtc<32>(tmX, tmW, params, h_in, h_out, slots, d_in, d_h, stream);
     return launch_xtc<8>(tmX, tmW, params, h_in, h_out, slots, d_in, d_h, stream);

@@ -105,12 +105,17 @@ def test_decode_step_with_projection_at_other_sizes(dtype, slots, d_in, d_h):
 
 
 @pytest.mark.parametrize("slots,d_in,d_h,zero_h", [(200, 200, 96, False), (512, 136, 512, False),
-                                                   (70, 64, 40, True)])
+                                                   (70, 64, 40, True), (64, 1024, 1024, False),
+                                                   (33, 296, 72, False), (64, 256, 40, True)])
 def test_decode_step_x_bf16_tensor_core_path_through_the_c_abi(slots, d_in, d_h, zero_h):
     """nrnn_decode_step_x for bf16 runs the projection on the tensor cores for
     any slot count: 8-unit tiles (200 x 96; 70 x 40 from the zero state, with a
     ragged unit tile) and 32-unit tiles (512 x 512, 128 CTAs); ragged slot
-    tiles and a K tail (d_in not a multiple of 64) are zero-filled by TMA."""
+    tiles and a K tail (d_in not a multiple of 64) are zero-filled by TMA.  One
+    tile of at most 64 slots with at least four 64-wide slices of d_in takes
+    the split-K cluster form (64 x 1024 -> 1024; 33 slots with a 296-wide
+    d_in split 1 / 1 / 1 / 2 slices and a ragged unit tile; 64 x 256 -> 40
+    from the zero state)."""
     import ctypes
     import nonlinear_rnn_gb300 as nr
     lib = nr.load()
