@@ -112,6 +112,36 @@ def test_jacobian_matches_central_difference():
 
 
 # ------------------------------------------------------- the sequential unroll
+def test_sequential_matches_a_plain_python_unroll():
+    """A second float64 path written from the cell's definition with the math
+    module: z = sig(P_z + a_z h + b_z), r = sig(P_r + a_r h + b_r),
+    c = tanh(P_c + a_c (r h) + b_c), h <- (1 - z) h + z c, from h = 0; and the
+    Jacobian J = (1 - z) + z (1 - z) a_z (c - h) + z (1 - c^2) a_c (r + h r (1 - r) a_r)
+    the chain rule gives, evaluated by hand at every step."""
+    rng = np.random.default_rng(77)
+    B, T, d_h = 2, 5, 3
+    P = rng.normal(0, 1.5, size=(B, T, 3 * d_h))
+    prm = _params(d_h, rng, scale=1.5, bias=0.7)
+    H = oracle.sequential(P, prm)
+    sig = lambda v: 1.0 / (1.0 + math.exp(-v))   # noqa: E731
+    for b in range(B):
+        for j in range(d_h):
+            a_z, a_r, a_c = prm["a_z"][j], prm["a_r"][j], prm["a_c"][j]
+            b_z, b_r, b_c = prm["b_z"][j], prm["b_r"][j], prm["b_c"][j]
+            h = 0.0
+            for t in range(T):
+                pz, pr, pc = P[b, t, j], P[b, t, d_h + j], P[b, t, 2 * d_h + j]
+                z = sig(pz + a_z * h + b_z)
+                r = sig(pr + a_r * h + b_r)
+                c = math.tanh(pc + a_c * (r * h) + b_c)
+                J = (1 - z) + z * (1 - z) * a_z * (c - h) + z * (1 - c * c) * a_c * (r + h * r * (1 - r) * a_r)
+                f, J_or = oracle.cell(h, pz, pr, pc, [a_z, a_r, a_c, b_z, b_r, b_c])
+                h = (1 - z) * h + z * c
+                assert abs(f - h) <= 1e-14
+                assert abs(J_or - J) <= 1e-13
+                assert abs(H[b, t, j] - h) <= 1e-14
+
+
 def test_sequential_state_stays_in_unit_interval():
     w = syn.small_workload(B=3, T=500, d_h=12)
     P = syn.direct_preact(w) * 4.0
