@@ -14,7 +14,10 @@ pytestmark = pytest.mark.gpu
 
 CASES = [dict(B=2, T=300, d_in=136, d_h=40, lens=None),      # ragged T, d_h, d_in tails
          dict(B=1, T=None, d_in=64, d_h=32, lens=[130, 1, 0, 300, 77]),
-         dict(B=3, T=1000, d_in=512, d_h=96, lens=None)]
+         dict(B=3, T=1000, d_in=512, d_h=96, lens=None),
+         dict(B=1, T=64, d_in=8, d_h=8, lens=None),          # one 32-wide slice, mostly zero-filled
+         dict(B=2, T=129, d_in=40, d_h=72, lens=None),       # a 32-wide slice and a tail of 8
+         dict(B=1, T=200, d_in=1024, d_h=32, lens=None)]     # 32 slices through the 2-stage ring
 
 
 @pytest.mark.parametrize("case", range(len(CASES)))
