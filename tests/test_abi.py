@@ -183,3 +183,19 @@ def test_pack_workspace_and_plan_checks():
     assert lib.nrnn_debug_pack_plan(fake, 1, 4096, 0, fake, None) == -1
     assert lib.nrnn_debug_pack_plan(fake, 9, 4096, 1, fake, None) == -1
     assert lib.nrnn_debug_pack_plan(None, 8, 4096, 0, fake, None) == -1
+
+
+def test_host_pipeline_default_blocks():
+    """By default the host-buffer forward cuts the problem into about 16
+    blocks: the three staging slots then hold one block each, so the staging
+    area is about 3/16 of what one block of all rows takes (plus workspaces)."""
+    f32 = torch.float32
+    B, T, d_h = 16, 4096, 256
+    one = nr.host_staging_bytes(B, T, d_h, f32, 3, tokens_per_block=B * T)
+    default = nr.host_staging_bytes(B, T, d_h, f32, 3)
+    row = nr.host_staging_bytes(B, T, d_h, f32, 3, tokens_per_block=T)
+    assert default == row                     # 16 blocks of one row each
+    assert default < one / 4
+    # the x-input form adds the x rows of each slot and the projection's workspace
+    xs = nr.x_host_staging_bytes(B, T, 128, d_h, f32, 3)
+    assert xs >= default + 3 * T * 128 * 4 + 3 * d_h * 128 * 4
