@@ -165,7 +165,8 @@ __device__ __forceinline__ float residual_rows(const float *Pf, const TS *Pt, in
                         make_float2(to_f32(Pt[2 * L * U + lo]), to_f32(Pt[2 * L * U + hi])), prm,
                         sz, sr, sc);
         }
-        const float2 hq = make_float2(round_to<TS>(G[j].x), round_to<TS>(G[j].y));
+        // the per-iteration kernel keeps G rounded to the storage type already
+        const float2 hq = FUSED ? make_float2(round_to<TS>(G[j].x), round_to<TS>(G[j].y)) : G[j];
         float2 hs = prev;
         if (GENERAL) {
             if ((hm >> j) & 1u) hs.x = 0.f;
@@ -535,10 +536,11 @@ __global__ void __launch_bounds__(NW * 32, newton_min_blocks<TS, FUSED>())
     if (a.last) {
         // each warp read only its own prefix slot in the apply step: reuse the
         // slots for the last row of each warp
-        s_aggA[warp][lane] = round_to<TS>(G[HALF - 1].y);
+        // (the per-iteration kernel's G and hb are rounded to the storage type already)
+        s_aggA[warp][lane] = FUSED ? round_to<TS>(G[HALF - 1].y) : G[HALF - 1].y;
         __syncthreads();
-        const float2 prev = make_float2((warp == 0) ? round_to<TS>(hb) : s_aggA[warp - 1][lane],
-                                        round_to<TS>(G[HALF - 1].x));
+        const float2 prev = make_float2((warp == 0) ? (FUSED ? round_to<TS>(hb) : hb) : s_aggA[warp - 1][lane],
+                                        FUSED ? round_to<TS>(G[HALF - 1].x) : G[HALF - 1].x);
         float m = general ? residual_rows<TS, FUSED, true>(Pf, Pt, warp, lane, G, prev, hm, nvalid, prm2)
                           : residual_rows<TS, FUSED, false>(Pf, Pt, warp, lane, G, prev, hm, nvalid, prm2);
         if (!uok) m = 0.f;
