@@ -112,10 +112,16 @@ __device__ __forceinline__ Derivs2 derivs2(float2 hs, float2 pz, float2 pr, floa
     return d;
 }
 
+// A thread keeps only the Jacobians of its rows across the look-back and
+// evaluates the gates a second time for the gradients: one more cell
+// evaluation per element buys twice the resident CTAs (64 registers and 8 CTAs
+// per SM for bf16; 5 for fp32, whose 40 KB of tiles allow no more).
+template <typename TS> constexpr int bw_min_blocks() { return sizeof(TS) == 2 ? 8 : 5; }
+
 // PLAN: the chunks of a pack are segment-aligned, taken from a.plan (last
 // chunks of the segments first).
 template <typename TS, bool EARLY, bool PLAN>
-__global__ void __launch_bounds__(NW * 32, 4)
+__global__ void __launch_bounds__(NW * 32, bw_min_blocks<TS>())
     k_backward(const __grid_constant__ CUtensorMap tmP, const __grid_constant__ CUtensorMap tmH,
                const __grid_constant__ CUtensorMap tmG, const __grid_constant__ CUtensorMap tmGP,
                const BackwardArgs a) {
@@ -170,11 +176,6 @@ __global__ void __launch_bounds__(NW * 32, 4)
     const int u0 = ut * U;
     const int tile = (b * a.n_ut + ut) * a.n_chunks + (PLAN ? s_tile[5] : c);
     unsigned long long *slot = a.slots + static_cast<size_t>(tile) * 32 + lane;
-    unsigned long long pre1 = SLOT_EMPTY, pre2 = SLOT_EMPTY;
-    if (EARLY && warp == 0) {
-        if (c + 1 < n_chain) pre1 = ld_relaxed_u64(slot + 32);
-        if (c + 2 < n_chain) pre2 = ld_relaxed_u64(slot + 64);
-    }
 
     if (tid == 0) {
         mbar_init(&s_bar, 1);
@@ -212,22 +213,23 @@ __global__ void __launch_bounds__(NW * 32, 4)
         if ((hm >> i) & 1u) return 0.f;
         return i == 0 ? hb : to_f32(Hs[(r0 + i - 1) * U + lane]);
     };
-    // per-row derivatives at (h~ = H_{t-1}, P_t); J = 0 at a head and past the end
-    float2 Jr[HALF], dz[HALF], dr[HALF], dc[HALF], rh[HALF];
-#pragma unroll
-    for (int i = 0; i < HALF; ++i) {
+    // per-row derivatives at (h~ = H_{t-1}, P_t) of both rows of pair i (read
+    // from the P tile before the gradient loop overwrites them)
+    auto row_derivs = [&](int i) {
         const int rl = r0 + i, ru = rl + HALF;
         const float2 hs = make_float2(shifted(i), shifted(i + HALF));
         const float2 pz = make_float2(to_f32(Ps[(0 * L + rl) * U + lane]), to_f32(Ps[(0 * L + ru) * U + lane]));
         const float2 pr = make_float2(to_f32(Ps[(1 * L + rl) * U + lane]), to_f32(Ps[(1 * L + ru) * U + lane]));
         const float2 pc = make_float2(to_f32(Ps[(2 * L + rl) * U + lane]), to_f32(Ps[(2 * L + ru) * U + lane]));
-        const Derivs2 d = derivs2<TS>(hs, pz, pr, pc, q, a_z, a_r, a_c);
-        Jr[i] = make_float2(((hm >> i) & 1u) || i >= nvalid ? 0.f : d.J.x,
-                            ((hm >> (i + HALF)) & 1u) || i + HALF >= nvalid ? 0.f : d.J.y);
-        dz[i] = d.dz;
-        dr[i] = d.dr;
-        dc[i] = d.dc;
-        rh[i] = d.rh;
+        return derivs2<TS>(hs, pz, pr, pc, q, a_z, a_r, a_c);
+    };
+    // J = 0 at a head and past the end
+    float2 Jr[HALF];
+#pragma unroll
+    for (int i = 0; i < HALF; ++i) {
+        const float2 J = row_derivs(i).J;
+        Jr[i] = make_float2(((hm >> i) & 1u) || i >= nvalid ? 0.f : J.x,
+                            ((hm >> (i + HALF)) & 1u) || i + HALF >= nvalid ? 0.f : J.y);
     }
 
     // compose nu_{t+1} -> nu_t = J_t nu_{t+1} + J_t gH_t over each half, last
@@ -239,6 +241,12 @@ __global__ void __launch_bounds__(NW * 32, 4)
                                       i + HALF < nvalid ? to_f32(Gs[(r0 + i + HALF) * U + lane]) : 0.f);
         B2 = fma2(Jr[i], B2, mul2(Jr[i], gh));
         A2 = mul2(A2, Jr[i]);
+    }
+    // warp 0 reads the slots of chunks c + 1 and c + 2 before the barrier
+    unsigned long long pre1 = SLOT_EMPTY, pre2 = SLOT_EMPTY;
+    if (EARLY && warp == 0) {
+        if (c + 1 < n_chain) pre1 = ld_relaxed_u64(slot + 32);
+        if (c + 2 < n_chain) pre2 = ld_relaxed_u64(slot + 64);
     }
     s_aggA[warp][lane] = A2.x * A2.y;
     s_aggB[warp][lane] = fmaf(A2.x, B2.y, B2.x);
@@ -282,13 +290,14 @@ __global__ void __launch_bounds__(NW * 32, 4)
                                        vu ? to_f32(Gs[(r0 + i + HALF) * U + lane]) + nu.y : 0.f);
         nu = mul2(Jr[i], lam);
         const float2 hs = make_float2(shifted(i), shifted(i + HALF));
-        const float2 gz = mul2(lam, dz[i]), gr = mul2(lam, dr[i]), gc = mul2(lam, dc[i]);
+        const Derivs2 d = row_derivs(i);   // the gate factors again
+        const float2 gz = mul2(lam, d.dz), gr = mul2(lam, d.dr), gc = mul2(lam, d.dc);
         g_bz = add2(g_bz, gz);
         g_br = add2(g_br, gr);
         g_bc = add2(g_bc, gc);
         g_az = fma2(gz, hs, g_az);
         g_ar = fma2(gr, hs, g_ar);
-        g_ac = fma2(gc, rh[i], g_ac);
+        g_ac = fma2(gc, d.rh, g_ac);
         // dL/dP of both rows goes into the P tile, whose values are no longer
         // read (rows past T and units past d_h are clipped by the store)
         const int rl = r0 + i, ru = rl + HALF;
@@ -350,22 +359,21 @@ cudaError_t launch_bw(const CUtensorMap &tmP, const CUtensorMap &tmH, const CUte
     return cudaGetLastError();
 }
 
-// the early reads pay when at most 4 chunks per column are resident at once
-// (4 CTAs per SM); a segment-aligned pack has one column per segment and unit
-// tile
-bool bw_early(const BackwardArgs &a, bool plan) {
+// the early reads pay when at most 4 chunks per column are resident at once;
+// a segment-aligned pack has one column per segment and unit tile
+bool bw_early(const BackwardArgs &a, bool plan, int ctas_per_sm) {
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
         return false;
-    return static_cast<int64_t>(sms) * 4 <= 4 * static_cast<int64_t>(plan ? a.S : a.B) * a.n_ut;
+    return static_cast<int64_t>(sms) * ctas_per_sm <= 4 * static_cast<int64_t>(plan ? a.S : a.B) * a.n_ut;
 }
 
 template <typename TS>
 cudaError_t launch_bw(const CUtensorMap &tmP, const CUtensorMap &tmH, const CUtensorMap &tmG,
                       const CUtensorMap &tmGP, const BackwardArgs &a, int64_t n_ctas,
                       cudaStream_t stream, bool plan) {
-    const bool early = bw_early(a, plan);
+    const bool early = bw_early(a, plan, bw_min_blocks<TS>());
     if (plan)
         return early ? launch_bw<TS, true, true>(tmP, tmH, tmG, tmGP, a, n_ctas, stream)
                      : launch_bw<TS, false, true>(tmP, tmH, tmG, tmGP, a, n_ctas, stream);
