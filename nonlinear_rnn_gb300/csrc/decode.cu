@@ -11,6 +11,9 @@
 // k_decode_step_xtc: the same for bf16 on the tensor cores (see below).
 // Every decode kernel evaluates the cell in the storage type's formulation,
 // as the Newton kernels do: ex2/rcp for fp32, tanh.approx for bf16.
+#include <algorithm>
+#include <atomic>
+
 #include "nrnn_device.cuh"
 #include "nrnn_internal.h"
 #include "tcgen05.cuh"
@@ -47,32 +50,24 @@ __device__ __forceinline__ void unpack16(const uint4 &v, float (&o)[8]) {
     }
 }
 
-// The same step with 16 bytes per load: a thread takes the 16 / sizeof(TS)
-// adjacent units of one slot (4 fp32 or 8 bf16), so each thread has four
-// 16-byte loads in flight instead of four scalar ones.  Needs d_h a multiple
-// of that width and 16-byte aligned P, params, h_in and h_out.
+// The same step with 16 bytes per load: a thread takes the VEC = 16 /
+// sizeof(TS) adjacent units of one unit group (4 fp32 or 8 bf16), keeps their
+// parameters in registers and walks the slots with a stride of `lanes`, two
+// slots per pass, so that eight 16-byte loads are in flight and the
+// parameters are read once per thread, not once per slot (for bf16 they are
+// three times the bytes of the slot's data).  Needs d_h a multiple of VEC and
+// 16-byte aligned P, params, h_in and h_out.
 template <typename TS>
 __global__ void __launch_bounds__(256)
     k_decode_step_vec(const TS *__restrict__ P, const float *__restrict__ params,
-                      const TS *__restrict__ h_in, TS *__restrict__ h_out, int slots, int d_h) {
+                      const TS *__restrict__ h_in, TS *__restrict__ h_out, int slots, int d_h,
+                      int lanes) {
     constexpr int VEC = 16 / sizeof(TS);
     const int groups = d_h / VEC;
     const int64_t v = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-    if (v >= static_cast<int64_t>(slots) * groups) return;
-    const int s = static_cast<int>(v / groups);
-    const int j0 = static_cast<int>(v - static_cast<int64_t>(s) * groups) * VEC;
-    const TS *p = P + static_cast<int64_t>(s) * 3 * d_h + j0;
-    const int64_t i0 = static_cast<int64_t>(s) * d_h + j0;
-    float z[VEC], r[VEC], c[VEC], h[VEC];
-    unpack16(*reinterpret_cast<const uint4 *>(p), z);
-    unpack16(*reinterpret_cast<const uint4 *>(p + d_h), r);
-    unpack16(*reinterpret_cast<const uint4 *>(p + 2 * d_h), c);
-    if (h_in != nullptr) {
-        unpack16(*reinterpret_cast<const uint4 *>(h_in + i0), h);
-    } else {
-#pragma unroll
-        for (int e = 0; e < VEC; ++e) h[e] = 0.f;
-    }
+    if (v >= static_cast<int64_t>(lanes) * groups) return;
+    const int s_first = static_cast<int>(v / groups);
+    const int j0 = static_cast<int>(v - static_cast<int64_t>(s_first) * groups) * VEC;
     // parameters of the VEC units: 6 rows of params, VEC floats each
     float prm[6][VEC];
 #pragma unroll
@@ -85,13 +80,41 @@ __global__ void __launch_bounds__(256)
             prm[g][4 * q + 2] = w.z;
             prm[g][4 * q + 3] = w.w;
         }
-    __align__(16) TS o[VEC];
+    const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
+    for (int64_t s = s_first; s < slots; s += 2 * static_cast<int64_t>(lanes)) {
+        const bool two = s + lanes < slots;
+        uint4 in[2][4];
 #pragma unroll
-    for (int e = 0; e < VEC; ++e) {
-        const UnitParams up{prm[0][e], prm[1][e], prm[2][e], prm[3][e], prm[4][e], prm[5][e]};
-        o[e] = from_f32<TS>(cell_f_storage<TS>(h[e], z[e], r[e], c[e], up));
+        for (int k = 0; k < 2; ++k) {
+            const int64_t sk = s + k * lanes;
+            if (k == 0 || two) {
+                const TS *p = P + sk * 3 * d_h + j0;
+                in[k][0] = *reinterpret_cast<const uint4 *>(p);
+                in[k][1] = *reinterpret_cast<const uint4 *>(p + d_h);
+                in[k][2] = *reinterpret_cast<const uint4 *>(p + 2 * d_h);
+                in[k][3] = (h_in != nullptr)
+                               ? *reinterpret_cast<const uint4 *>(h_in + sk * d_h + j0)
+                               : zero;
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            if (k == 1 && !two) break;
+            float z[VEC], r[VEC], c[VEC], h[VEC];
+            unpack16(in[k][0], z);
+            unpack16(in[k][1], r);
+            unpack16(in[k][2], c);
+            unpack16(in[k][3], h);
+            __align__(16) TS o[VEC];
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) {
+                const UnitParams up{prm[0][e], prm[1][e], prm[2][e], prm[3][e], prm[4][e], prm[5][e]};
+                o[e] = from_f32<TS>(cell_f_storage<TS>(h[e], z[e], r[e], c[e], up));
+            }
+            *reinterpret_cast<uint4 *>(h_out + (s + k * lanes) * d_h + j0) =
+                *reinterpret_cast<const uint4 *>(o);
+        }
     }
-    *reinterpret_cast<uint4 *>(h_out + i0) = *reinterpret_cast<const uint4 *>(o);
 }
 
 // k_decode_step_x: a CTA takes DX_UNITS units (one warp each) and a group of
@@ -537,16 +560,35 @@ cudaError_t launch_decode_step(int dtype, const void *P, const float *params, co
     const int vec = dtype == 1 ? 8 : 4;
     const auto a16 = [](const void *q) { return (reinterpret_cast<uintptr_t>(q) & 15u) == 0; };
     if (d_h % vec == 0 && a16(P) && a16(params) && a16(h_out) && (h_in == nullptr || a16(h_in))) {
-        const unsigned vblocks = static_cast<unsigned>((n / vec + 255) / 256);
+        // one resident wave of threads, each taking an equal number of two-slot passes
+        static std::atomic<int> resident[2] = {0, 0};   // CTAs per SM, by dtype
+        int dev = 0, sms = 0, per_sm = resident[dtype == 1].load();
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return cudaErrorUnknown;
+        if (per_sm == 0) {
+            const cudaError_t oe =
+                dtype == 1
+                    ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_decode_step_vec<__nv_bfloat16>, 256, 0)
+                    : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_decode_step_vec<float>, 256, 0);
+            if (oe != cudaSuccess) return oe;
+            resident[dtype == 1].store(per_sm);
+        }
+        const int64_t groups = d_h / vec;
+        const int64_t target =
+            std::max<int64_t>(1, static_cast<int64_t>(sms) * std::max(per_sm, 1) * 256 / groups);
+        const int64_t passes = (slots + 2 * target - 1) / (2 * target);
+        const int lanes = static_cast<int>((slots + 2 * passes - 1) / (2 * passes));
+        const unsigned vblocks = static_cast<unsigned>((groups * lanes + 255) / 256);
         if (dtype == 1)
             k_decode_step_vec<__nv_bfloat16><<<vblocks, 256, 0, stream>>>(
                 static_cast<const __nv_bfloat16 *>(P), params,
                 static_cast<const __nv_bfloat16 *>(h_in), static_cast<__nv_bfloat16 *>(h_out),
-                slots, d_h);
+                slots, d_h, lanes);
         else
             k_decode_step_vec<float><<<vblocks, 256, 0, stream>>>(
                 static_cast<const float *>(P), params, static_cast<const float *>(h_in),
-                static_cast<float *>(h_out), slots, d_h);
+                static_cast<float *>(h_out), slots, d_h, lanes);
         return cudaGetLastError();
     }
     const unsigned blocks = static_cast<unsigned>((n + 255) / 256);
