@@ -4,8 +4,8 @@
 // size (slots, d_h), prefill then decode_wx + decode_step(..., out=) per token).
 //
 // k_decode_step: h_out = f(h_in, P) elementwise from given preactivations
-// (k_decode_step_vec: the same on 16-byte vectors when shapes and alignment
-// allow).
+// (k_decode_step_vec: the same on vectors of 4 units when shapes and
+// alignment allow).
 // k_decode_step_x: the same step with the input projection fused in, for
 // small slot counts (a batched matrix-vector product per step; see below).
 // k_decode_step_xtc: the same for bf16 on the tensor cores (see below).
@@ -13,6 +13,7 @@
 // as the Newton kernels do: ex2/rcp for fp32, tanh.approx for bf16.
 #include <algorithm>
 #include <atomic>
+#include <type_traits>
 
 #include "nrnn_device.cuh"
 #include "nrnn_internal.h"
@@ -50,69 +51,77 @@ __device__ __forceinline__ void unpack16(const uint4 &v, float (&o)[8]) {
     }
 }
 
-// The same step with 16 bytes per load: a thread takes the VEC = 16 /
-// sizeof(TS) adjacent units of one unit group (4 fp32 or 8 bf16), keeps their
-// parameters in registers and walks the slots with a stride of `lanes`, two
-// slots per pass, so that eight 16-byte loads are in flight and the
-// parameters are read once per thread, not once per slot (for bf16 they are
-// three times the bytes of the slot's data).  Needs d_h a multiple of VEC and
-// 16-byte aligned P, params, h_in and h_out.
+__device__ __forceinline__ void unpack8(const uint2 &v, float (&o)[4]) {
+    o[0] = __uint_as_float(v.x << 16);
+    o[1] = __uint_as_float(v.x & 0xffff0000u);
+    o[2] = __uint_as_float(v.y << 16);
+    o[3] = __uint_as_float(v.y & 0xffff0000u);
+}
+// The same step on vectors: a thread takes 4 adjacent units of one slot row
+// (16-byte fp32 or 8-byte bf16 loads), keeps their parameters in registers
+// and walks the slots with a stride of `lanes`, two slots per pass, so that
+// eight loads are in flight and the parameters are read once per thread, not
+// once per slot.  Four bf16 units rather than eight keep a thread at 64
+// registers, so that 4 CTAs of 256 threads fit on an SM.  Needs d_h a
+// multiple of 4 and 16-byte aligned P, params, h_in and h_out.
 template <typename TS>
 __global__ void __launch_bounds__(256)
     k_decode_step_vec(const TS *__restrict__ P, const float *__restrict__ params,
                       const TS *__restrict__ h_in, TS *__restrict__ h_out, int slots, int d_h,
                       int lanes) {
-    constexpr int VEC = 16 / sizeof(TS);
+    constexpr int VEC = 4;
+    using V = typename std::conditional<sizeof(TS) == 2, uint2, uint4>::type;
     const int groups = d_h / VEC;
     const int64_t v = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     if (v >= static_cast<int64_t>(lanes) * groups) return;
     const int s_first = static_cast<int>(v / groups);
     const int j0 = static_cast<int>(v - static_cast<int64_t>(s_first) * groups) * VEC;
-    // parameters of the VEC units: 6 rows of params, VEC floats each
     float prm[6][VEC];
 #pragma unroll
-    for (int g = 0; g < 6; ++g)
-#pragma unroll
-        for (int q = 0; q < VEC / 4; ++q) {
-            const float4 w = *reinterpret_cast<const float4 *>(params + g * d_h + j0 + 4 * q);
-            prm[g][4 * q] = w.x;
-            prm[g][4 * q + 1] = w.y;
-            prm[g][4 * q + 2] = w.z;
-            prm[g][4 * q + 3] = w.w;
-        }
-    const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
+    for (int g = 0; g < 6; ++g) {
+        const float4 w = *reinterpret_cast<const float4 *>(params + g * d_h + j0);
+        prm[g][0] = w.x;
+        prm[g][1] = w.y;
+        prm[g][2] = w.z;
+        prm[g][3] = w.w;
+    }
+    const V zero{};
     for (int64_t s = s_first; s < slots; s += 2 * static_cast<int64_t>(lanes)) {
         const bool two = s + lanes < slots;
-        uint4 in[2][4];
+        V in[2][4];
 #pragma unroll
         for (int k = 0; k < 2; ++k) {
             const int64_t sk = s + k * lanes;
             if (k == 0 || two) {
                 const TS *p = P + sk * 3 * d_h + j0;
-                in[k][0] = *reinterpret_cast<const uint4 *>(p);
-                in[k][1] = *reinterpret_cast<const uint4 *>(p + d_h);
-                in[k][2] = *reinterpret_cast<const uint4 *>(p + 2 * d_h);
-                in[k][3] = (h_in != nullptr)
-                               ? *reinterpret_cast<const uint4 *>(h_in + sk * d_h + j0)
-                               : zero;
+                in[k][0] = *reinterpret_cast<const V *>(p);
+                in[k][1] = *reinterpret_cast<const V *>(p + d_h);
+                in[k][2] = *reinterpret_cast<const V *>(p + 2 * d_h);
+                in[k][3] = (h_in != nullptr) ? *reinterpret_cast<const V *>(h_in + sk * d_h + j0) : zero;
             }
         }
 #pragma unroll
         for (int k = 0; k < 2; ++k) {
             if (k == 1 && !two) break;
             float z[VEC], r[VEC], c[VEC], h[VEC];
-            unpack16(in[k][0], z);
-            unpack16(in[k][1], r);
-            unpack16(in[k][2], c);
-            unpack16(in[k][3], h);
+            if constexpr (sizeof(TS) == 2) {
+                unpack8(in[k][0], z);
+                unpack8(in[k][1], r);
+                unpack8(in[k][2], c);
+                unpack8(in[k][3], h);
+            } else {
+                unpack16(in[k][0], z);
+                unpack16(in[k][1], r);
+                unpack16(in[k][2], c);
+                unpack16(in[k][3], h);
+            }
             __align__(16) TS o[VEC];
 #pragma unroll
             for (int e = 0; e < VEC; ++e) {
                 const UnitParams up{prm[0][e], prm[1][e], prm[2][e], prm[3][e], prm[4][e], prm[5][e]};
                 o[e] = from_f32<TS>(cell_f_storage<TS>(h[e], z[e], r[e], c[e], up));
             }
-            *reinterpret_cast<uint4 *>(h_out + (s + k * lanes) * d_h + j0) =
-                *reinterpret_cast<const uint4 *>(o);
+            *reinterpret_cast<V *>(h_out + (s + k * lanes) * d_h + j0) = *reinterpret_cast<const V *>(o);
         }
     }
 }
@@ -557,7 +566,7 @@ cudaError_t launch_decode_step(int dtype, const void *P, const float *params, co
                                void *h_out, int slots, int d_h, cudaStream_t stream) {
     const int64_t n = static_cast<int64_t>(slots) * d_h;
     if (n == 0) return cudaSuccess;
-    const int vec = dtype == 1 ? 8 : 4;
+    const int vec = 4;
     const auto a16 = [](const void *q) { return (reinterpret_cast<uintptr_t>(q) & 15u) == 0; };
     if (d_h % vec == 0 && a16(P) && a16(params) && a16(h_out) && (h_in == nullptr || a16(h_in))) {
         // one resident wave of threads, each taking an equal number of two-slot passes

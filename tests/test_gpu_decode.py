@@ -38,14 +38,16 @@ def test_decode_step_matches_oracle_and_carries_state(dtype):
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
-@pytest.mark.parametrize("d_h, offset", [(6, 0), (16, 0), (40, 0), (16, 1)])
-def test_decode_step_vector_and_scalar_paths(dtype, d_h, offset):
-    # d_h a multiple of the 16-byte width with aligned buffers takes the vector
-    # kernel; d_h = 6 (and 40 for bf16) or an output one element off alignment
-    # takes the scalar one; both against the oracle, h_in given
+@pytest.mark.parametrize("d_h, offset, slots", [(6, 0, 333), (16, 0, 333), (40, 0, 333), (16, 1, 333),
+                                                (256, 0, 5001)])
+def test_decode_step_vector_and_scalar_paths(dtype, d_h, offset, slots):
+    # d_h a multiple of 4 with aligned buffers takes the vector kernel (each
+    # thread walks the slots two per pass: 5001 slots of 256 units take
+    # several passes and end on a single slot); d_h = 6 or an output one
+    # element off alignment takes the scalar one; both against the oracle,
+    # h_in given
     import nonlinear_rnn_gb300 as nr
     tdt = torch.float32 if dtype == "f32" else torch.bfloat16
-    slots = 333
     w = syn.small_workload(B=slots, T=1, d_h=d_h, dtype=dtype, seed=64 + d_h)
     P = syn.direct_preact(w)[:, 0]
     prm = syn.make_params(w)
