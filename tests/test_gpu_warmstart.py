@@ -24,9 +24,12 @@ def host(t):
     return t.float().cpu().numpy().astype(np.float64)
 
 
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
 @pytest.mark.parametrize("sweeps", [0, 1, 2, 5])
 @pytest.mark.parametrize("ragged", [False, True])
-def test_picard_matches_oracle(nr, sweeps, ragged):
+def test_picard_matches_oracle(nr, dtype, sweeps, ragged):
+    # d_h = 24 and 40: a thread's units (2 fp32 or 4 bf16) end the tile part way
+    tdt = torch.float32 if dtype == "f32" else torch.bfloat16
     if ragged:
         cu = syn.cu_from_lengths([100, 1, 0, 200, 129])
         w = syn.small_workload(B=1, T=int(cu[-1]), d_h=24, seed=41)
@@ -35,9 +38,12 @@ def test_picard_matches_oracle(nr, sweeps, ragged):
         w = syn.small_workload(B=2, T=300, d_h=40, seed=42)
     P = syn.direct_preact(w)
     prm = syn.make_params(w)
-    G = nr.picard(dev(P), prm, sweeps, cu_seqlens=cu)
-    ref = oracle.picard(P, prm, sweeps, cu_seqlens=cu)
-    assert np.max(np.abs(host(G) - ref)) <= 1e-6
+    Pd = dev(P, tdt)
+    G = nr.picard(Pd, prm, sweeps, cu_seqlens=cu)
+    # the oracle on the stored preactivations; bf16 stores each sweep's G
+    # rounded (a few bf16 units in the last place after five sweeps)
+    ref = oracle.picard(host(Pd), prm, sweeps, cu_seqlens=cu)
+    assert np.max(np.abs(host(G) - ref)) <= (1e-6 if dtype == "f32" else 2e-2)
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
