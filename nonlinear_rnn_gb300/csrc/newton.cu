@@ -166,7 +166,7 @@ __device__ __forceinline__ float residual_rows(const float *Pf, const TS *Pt, in
                         sz, sr, sc);
         }
         // the per-iteration kernel keeps G rounded to the storage type already
-        const float2 hq = FUSED ? make_float2(round_to<TS>(G[j].x), round_to<TS>(G[j].y)) : G[j];
+        const float2 hq = FUSED ? round2_to<TS>(G[j]) : G[j];
         float2 hs = prev;
         if (GENERAL) {
             if ((hm >> j) & 1u) hs.x = 0.f;
@@ -528,7 +528,7 @@ __global__ void __launch_bounds__(NW * 32, newton_min_blocks<TS, FUSED>())
 #pragma unroll
         for (int j = 0; j < HALF; ++j) {
             h2 = fma2(J2[j], h2, G[j]);
-            G[j] = FUSED ? h2 : make_float2(round_to<TS>(h2.x), round_to<TS>(h2.y));
+            G[j] = FUSED ? h2 : round2_to<TS>(h2);
         }
     }
 

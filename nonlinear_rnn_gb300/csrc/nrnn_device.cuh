@@ -29,6 +29,13 @@ template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(flo
 template <typename TS> __device__ __forceinline__ float round_to(float v) {
     return to_f32(from_f32<TS>(v));
 }
+// both values of a pair rounded to the storage type and widened back (bf16:
+// one packed conversion instead of two)
+template <typename TS> __device__ __forceinline__ float2 round2_to(float2 v);
+template <> __device__ __forceinline__ float2 round2_to<float>(float2 v) { return v; }
+template <> __device__ __forceinline__ float2 round2_to<__nv_bfloat16>(float2 v) {
+    return __bfloat1622float2(__floats2bfloat162_rn(v.x, v.y));
+}
 
 // ------------------------------------------------------------- PTX primitives
 __device__ __forceinline__ float ex2_approx(float x) {
