@@ -265,12 +265,15 @@ int nrnn_decode_step(const void *preact, int dtype, const float *params, int64_t
  * Decode step with the input projection fused in (FAQs: "decode_wx +
  * decode_step"): P_s = W_x x_s (fp32 accumulation on the CUDA cores, rounded
  * to dtype as the stored preactivation would be), then h_out = f(h_in, P).
- * Meant for small slot counts.  bf16: the product on the tensor cores, 64
- * slots by 8 or 32 units per CTA with the step in the epilogue, so W_x streams
- * from HBM once per 64 slots.  fp32: a batched matrix-vector product on the
- * CUDA cores (each W_x row read once per group of 8 slots).  For hundreds of
- * slots and more, nrnn_input_projection into a (slots, 3 d_h) buffer followed
- * by nrnn_decode_step is faster (the Python binding switches above 64 slots).
+ * bf16: the product on the tensor cores with the step in the epilogue; up to
+ * 64 slots, 64 slots by 8 or 32 units per CTA, so W_x streams from HBM once
+ * per 64 slots; above that, when d_in >= 512, d_h is a multiple of 8 and
+ * params, h_in and h_out are 16-byte aligned, a GEMM of 128-slot by 64-unit
+ * tiles on one persistent CTA per SM.  fp32: a batched matrix-vector product
+ * on the CUDA cores (each W_x row read once per group of 8 slots).  For
+ * hundreds of slots with fp32 or a short d_in, nrnn_input_projection into a
+ * (slots, 3 d_h) buffer followed by nrnn_decode_step is faster (the Python
+ * binding switches there above 64 slots).
  *   x       device, (slots, d_in) of dtype, 16-byte aligned
  *   W_x     device, (3 d_h, d_in) of dtype, 16-byte aligned
  *   h_in    device (slots, d_h) or NULL;  h_out device (slots, d_h), may be h_in

@@ -480,6 +480,7 @@ def sequential_forward(preact: torch.Tensor, params, cu_seqlens=None,
 # above this many slots decode_step(x=, W_x=) projects on the tensor cores
 # (nrnn_input_projection) and then steps (nrnn_decode_step)
 DECODE_X_MAX_SLOTS = 64
+DECODE_XG_MIN_D_IN = 512   # bf16 from here on: the C-ABI call's GEMM form at any slot count
 
 
 def decode_step(params, h: torch.Tensor | None = None, preact: torch.Tensor | None = None,
@@ -508,8 +509,10 @@ def decode_step(params, h: torch.Tensor | None = None, preact: torch.Tensor | No
                                       _ptr(H), _stream(dev))
         else:
             W_x = _device_tensor(W_x, "W_x")
-            if slots > DECODE_X_MAX_SLOTS:
-                # large batches: the projection on the tensor cores, then the step
+            if slots > DECODE_X_MAX_SLOTS and not (src.dtype == torch.bfloat16 and
+                                                   src.shape[1] >= DECODE_XG_MIN_D_IN):
+                # large batches (fp32, or a short bf16 d_in): the projection on
+                # the tensor cores, then the step
                 P = input_projection(src, W_x)
                 st = lib.nrnn_decode_step(_ptr(P), _dtype_code(P), _ptr(prm), slots, d_h, _ptr(h),
                                           _ptr(H), _stream(dev))

@@ -653,6 +653,18 @@ int nrnn_decode_step_x(const void *x, const void *W_x, int dtype, const float *p
     if (dtype == NRNN_BF16) {
         // the projection on the tensor cores, the step in the epilogue
         CUtensorMap tmX, tmW;
+        if (slots >= DECODE_XG_MIN_SLOTS && d_in >= DECODE_XG_MIN_D_IN && d_h % 8 == 0 &&
+            aligned16(params) && aligned16(h_out) && (h_in == nullptr || aligned16(h_in))) {
+            // more than one slot tile: M = 128 slots by 64 units (z, r, c rows) per
+            // tile; a shorter K loop leaves the epilogue's cell work exposed
+            if (!make_map_2d_sw128(&tmX, x, d_in, slots, 64, 128) ||
+                !make_map_2d_sw128(&tmW, W_x, d_in, 3 * d_h, 64, 64))
+                return NRNN_ERR_CUDA;
+            return cuda_status(launch_decode_step_xg(tmX, tmW, params, h_in, h_out,
+                                                     static_cast<int>(slots), static_cast<int>(d_in),
+                                                     static_cast<int>(d_h),
+                                                     static_cast<cudaStream_t>(stream)));
+        }
         const int units = decode_xtc_units(static_cast<int>(slots), static_cast<int>(d_h));
         if (!make_map_2d_sw128(&tmX, x, d_in, slots, 64, 64) ||
             !make_map_2d_sw128(&tmW, W_x, d_in, 3 * d_h, 64, static_cast<uint32_t>(units)))

@@ -484,6 +484,183 @@ __global__ void __launch_bounds__(128)
     sk_cluster_sync();
 }
 
+// k_decode_step_xg (bf16, more slots than one 64-slot tile): the step's
+// projection as a GEMM in the usual orientation, M = 128 slots and N = 192 =
+// the z, r and c rows of W_x for 64 units (three TMA boxes of 64 rows, one per
+// gate, stacked into one B tile), K = d_in through a 4-stage ring.  One
+// persistent CTA per SM takes (slot tile, unit tile) pairs, unit tiles
+// fastest (CTAs working at once share x tiles in L2), and keeps two TMEM
+// accumulators: while the MMA thread fills one, four epilogue warps read the
+// other (warp q: slots 32 q .. 32 q + 31 of the tile, one per lane), round
+// the three gate preactivations to bf16 (the values the stored-P route reads)
+// and apply the cell to h_in in groups of 8 units (16-byte loads and stores).
+constexpr int XG_BM = 128;
+constexpr int XG_UNITS = 64;
+constexpr int XG_BN = 3 * XG_UNITS;
+constexpr int XG_BK = 64;
+constexpr int XG_STAGES = 4;
+constexpr int XG_A_BYTES = XG_BM * XG_BK * 2;                       // 16 KiB
+constexpr int XG_W_BOX_BYTES = XG_UNITS * XG_BK * 2;                // 8 KiB per gate
+constexpr int XG_STAGE_BYTES = XG_A_BYTES + 3 * XG_W_BOX_BYTES;     // 40 KiB
+constexpr uint32_t XG_ACC_STRIDE = 256;                             // TMEM columns per accumulator
+constexpr uint32_t XG_TMEM_COLS = 2 * XG_ACC_STRIDE;
+constexpr uint32_t XG_IDESC = idesc_kmajor<false>(XG_BM, XG_BN);
+constexpr int XG_EPI_THREADS = 128;
+constexpr size_t XG_SMEM = static_cast<size_t>(XG_STAGES) * XG_STAGE_BYTES + 1024;
+static_assert(XG_STAGE_BYTES % 1024 == 0, "stages keep the 128-byte swizzle's 1024-byte alignment");
+
+__global__ void __launch_bounds__(256, 1)
+    k_decode_step_xg(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
+                     const float *__restrict__ params, const __nv_bfloat16 *__restrict__ h_in,
+                     __nv_bfloat16 *__restrict__ h_out, int slots, int d_in, int d_h) {
+    extern __shared__ unsigned char xg_raw[];
+    unsigned char *smem = reinterpret_cast<unsigned char *>(
+        (reinterpret_cast<uintptr_t>(xg_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    __shared__ __align__(8) uint64_t full_bar[XG_STAGES], empty_bar[XG_STAGES], accf_bar[2],
+        acce_bar[2];
+    __shared__ uint32_t s_tmem, s_err;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int tiles_n = (d_h + XG_UNITS - 1) / XG_UNITS;
+    const int n_tiles = ((slots + XG_BM - 1) / XG_BM) * tiles_n;
+    const int kt_count = (d_in + XG_BK - 1) / XG_BK;
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < XG_STAGES; ++i) {
+            mbar_init(&full_bar[i], 1);
+            mbar_init(&empty_bar[i], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&accf_bar[b], 1);
+            mbar_init(&acce_bar[b], XG_EPI_THREADS);
+        }
+        s_err = 0u;
+        fence_mbar_init();
+        prefetch_tensormap(&tmX);
+        prefetch_tensormap(&tmW);
+    }
+    if (warp == 2) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_u32(&s_tmem)),
+                     "r"(XG_TMEM_COLS)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    __syncthreads();
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    const uint32_t tmem = s_tmem;
+
+    if (warp == 0 && lane == 0) {
+        // ---------------------------------------------------------- TMA producer
+        int it = 0;
+        for (int t = blockIdx.x; t < n_tiles; t += gridDim.x) {
+            const int m0 = (t / tiles_n) * XG_BM, n0 = (t % tiles_n) * XG_UNITS;
+            for (int kt = 0; kt < kt_count; ++kt, ++it) {
+                const int st = it % XG_STAGES;
+                if (it >= XG_STAGES)
+                    mbar_wait_bounded(&empty_bar[st], ((it / XG_STAGES) - 1) & 1, XT_WAIT_NS, &s_err);
+                unsigned char *A = smem + st * XG_STAGE_BYTES;
+                mbar_arrive_expect_tx(&full_bar[st], XG_STAGE_BYTES);
+                tma_load_2d(A, &tmX, &full_bar[st], kt * XG_BK, m0);
+#pragma unroll
+                for (int g = 0; g < 3; ++g)   // gate g at rows 64 g of the B tile
+                    tma_load_2d(A + XG_A_BYTES + g * XG_W_BOX_BYTES, &tmW, &full_bar[st], kt * XG_BK,
+                                g * d_h + n0);
+            }
+        }
+    } else if (warp == 1 && lane == 0) {
+        // ------------------------------------------------------------ MMA issuer
+        int it = 0, j = 0;
+        for (int t = blockIdx.x; t < n_tiles; t += gridDim.x, ++j) {
+            const int buf = j & 1;
+            if (j >= 2) mbar_wait_bounded(&acce_bar[buf], ((j >> 1) - 1) & 1, XT_WAIT_NS, &s_err);
+            asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+            const uint32_t d = tmem + buf * XG_ACC_STRIDE;
+            for (int kt = 0; kt < kt_count; ++kt, ++it) {
+                const int st = it % XG_STAGES;
+                mbar_wait_bounded(&full_bar[st], (it / XG_STAGES) & 1, XT_WAIT_NS, &s_err);
+                asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+                const uint32_t A = smem_u32(smem + st * XG_STAGE_BYTES);
+#pragma unroll
+                for (int kk = 0; kk < XG_BK / 16; ++kk)   // 32 bytes of K per MMA
+                    mma<false, XG_IDESC>(d, sw128_desc(A + kk * 32), sw128_desc(A + XG_A_BYTES + kk * 32),
+                                         (kt > 0 || kk > 0) ? 1u : 0u);
+                mma_commit(&empty_bar[st]);
+            }
+            mma_commit(&accf_bar[buf]);
+        }
+    } else if (warp >= 4) {
+        // --------------------------------------------------------------- epilogue
+        const int q = warp - 4;
+        int j = 0;
+        for (int t = blockIdx.x; t < n_tiles; t += gridDim.x, ++j) {
+            const int buf = j & 1;
+            const int m0 = (t / tiles_n) * XG_BM, n0 = (t % tiles_n) * XG_UNITS;
+            const bool ok = mbar_wait_bounded(&accf_bar[buf], (j >> 1) & 1, XT_WAIT_NS, &s_err);
+            asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+            const int slot = m0 + 32 * q + lane;
+            const uint32_t trow = tmem + (static_cast<uint32_t>(32 * q) << 16) + buf * XG_ACC_STRIDE;
+#pragma unroll 1
+            for (int half = 0; half < 2; ++half) {
+                uint32_t vz[32], vr[32], vc[32];
+                tmem_ld_cols<32>(trow + 32 * half, vz);
+                tmem_ld_cols<32>(trow + XG_UNITS + 32 * half, vr);
+                tmem_ld_cols<32>(trow + 2 * XG_UNITS + 32 * half, vc);
+                if (slot >= slots) continue;
+#pragma unroll
+                for (int g8 = 0; g8 < 4; ++g8) {
+                    const int u = n0 + 32 * half + 8 * g8;
+                    if (u >= d_h) break;   // d_h is a multiple of 8
+                    const int64_t i = static_cast<int64_t>(slot) * d_h + u;
+                    float h[8];
+                    if (h_in != nullptr) {
+                        unpack16(*reinterpret_cast<const uint4 *>(h_in + i), h);
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) h[e] = 0.f;
+                    }
+                    float prm[6][8];
+#pragma unroll
+                    for (int r = 0; r < 6; ++r) {
+                        const float4 a = *reinterpret_cast<const float4 *>(params + r * d_h + u);
+                        const float4 b = *reinterpret_cast<const float4 *>(params + r * d_h + u + 4);
+                        prm[r][0] = a.x;
+                        prm[r][1] = a.y;
+                        prm[r][2] = a.z;
+                        prm[r][3] = a.w;
+                        prm[r][4] = b.x;
+                        prm[r][5] = b.y;
+                        prm[r][6] = b.z;
+                        prm[r][7] = b.w;
+                    }
+                    __align__(16) __nv_bfloat16 o[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const int c = 8 * g8 + e;
+                        const float nan = __int_as_float(0x7fffffff);
+                        const float pz = ok ? round_to<__nv_bfloat16>(__uint_as_float(vz[c])) : nan;
+                        const float pr = ok ? round_to<__nv_bfloat16>(__uint_as_float(vr[c])) : nan;
+                        const float pc = ok ? round_to<__nv_bfloat16>(__uint_as_float(vc[c])) : nan;
+                        const UnitParams up{prm[0][e], prm[1][e], prm[2][e], prm[3][e], prm[4][e], prm[5][e]};
+                        o[e] = from_f32<__nv_bfloat16>(cell_f_storage<__nv_bfloat16>(h[e], pz, pr, pc, up));
+                    }
+                    *reinterpret_cast<uint4 *>(h_out + i) = *reinterpret_cast<const uint4 *>(o);
+                }
+            }
+            asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+            mbar_arrive(&acce_bar[buf]);
+        }
+    }
+    __syncwarp();
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    __syncthreads();
+    if (warp == 2) {
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                     "r"(XG_TMEM_COLS)
+                     : "memory");
+    }
+}
+
 }  // namespace
 
 int decode_xtc_units(int slots, int d_h) {
@@ -560,6 +737,29 @@ cudaError_t launch_decode_step_xtc(const CUtensorMap &tmX, const CUtensorMap &tm
     if (decode_xtc_units(slots, d_h) == 32)
         return launch_xtc<32>(tmX, tmW, params, h_in, h_out, slots, d_in, d_h, stream);
     return launch_xtc<8>(tmX, tmW, params, h_in, h_out, slots, d_in, d_h, stream);
+}
+
+cudaError_t launch_decode_step_xg(const CUtensorMap &tmX, const CUtensorMap &tmW,
+                                  const float *params, const void *h_in, void *h_out, int slots,
+                                  int d_in, int d_h, cudaStream_t stream) {
+    if (slots == 0) return cudaSuccess;
+    static std::atomic<unsigned long long> configured{0};
+    cudaError_t e = once_per_device(configured, [](int) {
+        return cudaFuncSetAttribute(k_decode_step_xg, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    static_cast<int>(XG_SMEM));
+    });
+    if (e != cudaSuccess) return e;
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return cudaErrorUnknown;
+    const int64_t tiles = static_cast<int64_t>((slots + XG_BM - 1) / XG_BM) * ((d_h + XG_UNITS - 1) / XG_UNITS);
+    const unsigned grid = static_cast<unsigned>(std::min<int64_t>(tiles, sms));
+    k_decode_step_xg<<<grid, 256, XG_SMEM, stream>>>(tmX, tmW, params,
+                                                     static_cast<const __nv_bfloat16 *>(h_in),
+                                                     static_cast<__nv_bfloat16 *>(h_out), slots,
+                                                     d_in, d_h);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_decode_step(int dtype, const void *P, const float *params, const void *h_in,

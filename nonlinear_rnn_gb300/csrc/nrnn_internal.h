@@ -184,6 +184,14 @@ int decode_xtc_units(int slots, int d_h);
 cudaError_t launch_decode_step_xtc(const CUtensorMap &tmX, const CUtensorMap &tmW,
                                    const float *params, const void *h_in, void *h_out, int slots,
                                    int d_in, int d_h, cudaStream_t stream);
+// the same in the GEMM orientation for more than one 64-slot tile: tmX over x
+// (d_in, slots) with a 64 x 128 box, tmW over W_x (d_in, 3 d_h) with a 64 x 64
+// box, both with the 128-byte swizzle; h_in (if given) and h_out 16-byte aligned
+constexpr int DECODE_XG_MIN_SLOTS = 65;
+constexpr int DECODE_XG_MIN_D_IN = 512;
+cudaError_t launch_decode_step_xg(const CUtensorMap &tmX, const CUtensorMap &tmW,
+                                  const float *params, const void *h_in, void *h_out, int slots,
+                                  int d_in, int d_h, cudaStream_t stream);
 
 cudaError_t launch_sequential(int dtype, const void *P, const float *params, int B, int T,
                               int d_h, const int32_t *cu, int S, void *H, cudaStream_t stream);

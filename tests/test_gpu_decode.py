@@ -84,11 +84,12 @@ def test_decode_step_with_fused_projection(dtype):
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
-@pytest.mark.parametrize("slots,d_in,d_h", [(64, 2048, 16), (300, 136, 40), (8, 8, 8)])
+@pytest.mark.parametrize("slots,d_in,d_h", [(64, 2048, 16), (300, 136, 40), (8, 8, 8), (300, 512, 48)])
 def test_decode_step_with_projection_at_other_sizes(dtype, slots, d_in, d_h):
     # 64 slots x d_in 2048: the fused kernel reading x from global memory (it
     # does not fit the staging buffer); 300 slots: the binding's
-    # projection-then-step path; 8 x 8: the smallest shape
+    # projection-then-step path (fp32, or bf16 with d_in 136), or for bf16
+    # with d_in 512 the C-ABI call's GEMM form; 8 x 8: the smallest shape
     import nonlinear_rnn_gb300 as nr
     tdt = torch.float32 if dtype == "f32" else torch.bfloat16
     rng = np.random.default_rng(slots + d_in)
@@ -108,16 +109,24 @@ def test_decode_step_with_projection_at_other_sizes(dtype, slots, d_in, d_h):
 
 @pytest.mark.parametrize("slots,d_in,d_h,zero_h", [(200, 200, 96, False), (512, 136, 512, False),
                                                    (70, 64, 40, True), (64, 1024, 1024, False),
-                                                   (33, 296, 72, False), (64, 256, 40, True)])
+                                                   (33, 296, 72, False), (64, 256, 40, True),
+                                                   (64, 72, 96, False), (200, 520, 96, False),
+                                                   (129, 512, 200, False), (1000, 1024, 1024, False),
+                                                   (300, 512, 8, False), (70, 640, 40, True)])
 def test_decode_step_x_bf16_tensor_core_path_through_the_c_abi(slots, d_in, d_h, zero_h):
     """nrnn_decode_step_x for bf16 runs the projection on the tensor cores for
-    any slot count: 8-unit tiles (200 x 96; 70 x 40 from the zero state, with a
-    ragged unit tile) and 32-unit tiles (512 x 512, 128 CTAs); ragged slot
-    tiles and a K tail (d_in not a multiple of 64) are zero-filled by TMA.  One
-    tile of at most 64 slots with at least four 64-wide slices of d_in takes
-    the split-K cluster form (64 x 1024 -> 1024; 33 slots with a 296-wide
-    d_in split 1 / 1 / 1 / 2 slices and a ragged unit tile; 64 x 256 -> 40
-    from the zero state)."""
+    any slot count.  Above one 64-slot tile with d_in >= 512 it is a GEMM of
+    128-slot by 64-unit tiles (z, r and c rows of W_x) on persistent CTAs with
+    the step in the epilogue: 200 x 520 -> 96 (a K tail of 8), 129 x 512 -> 200
+    (ragged slot and unit tiles), 1000 x 1024 -> 1024 (several tiles per CTA,
+    both TMEM accumulators in turn), 300 x 512 -> 8 (one 8-unit group of a
+    64-unit tile), 70 x 640 -> 40 from the zero state.  Otherwise 64 slots by 8
+    or 32 units per CTA: 200 x 200 -> 96 and 70 x 64 -> 40 (8-unit tiles),
+    512 x 136 -> 512 (32-unit tiles), 64 x 72 -> 96; ragged tiles and a K tail
+    are zero-filled by TMA.  One tile of at most 64 slots with at least four
+    64-wide slices of d_in takes the split-K cluster form (64 x 1024 -> 1024;
+    33 slots with a 296-wide d_in split 1 / 1 / 1 / 2 slices and a ragged unit
+    tile; 64 x 256 -> 40 from the zero state)."""
     import ctypes
     import nonlinear_rnn_gb300 as nr
     lib = nr.load()
