@@ -532,8 +532,12 @@ __global__ void __launch_bounds__(NW * 32, newton_min_blocks<TS, FUSED>())
         }
     }
 
-    // residual max|F(H^(K))| at the values as stored
-    if (a.last) {
+    // residual max|F(H^(K))| at the values as stored (every fused launch; the
+    // last per-iteration one).  The early fused forms take it as a constant
+    // condition: their register allocation comes out faster that way (B16
+    // T16384 bf16 1.016 -> 1.011 ms), the plain form's slower (B4 T131072
+    // 0.147 -> 0.149 ms)
+    if ((FUSED && EARLY) || a.last) {
         // each warp read only its own prefix slot in the apply step: reuse the
         // slots for the last row of each warp
         // (the per-iteration kernel's G and hb are rounded to the storage type already)
