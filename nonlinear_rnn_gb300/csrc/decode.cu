@@ -595,7 +595,10 @@ __global__ void __launch_bounds__(256, 1)
         for (int t = blockIdx.x; t < n_tiles; t += gridDim.x, ++j) {
             const int buf = j & 1;
             const int m0 = (t / tiles_n) * XG_BM, n0 = (t % tiles_n) * XG_UNITS;
-            const bool ok = mbar_wait_bounded(&accf_bar[buf], (j >> 1) & 1, XT_WAIT_NS, &s_err);
+            // a wait that ran out anywhere in the CTA (the producer's, the
+            // MMA thread's or this one) turns this tile's outputs into NaN
+            const bool ok = mbar_wait_bounded(&accf_bar[buf], (j >> 1) & 1, XT_WAIT_NS, &s_err) &&
+                            *reinterpret_cast<volatile uint32_t *>(&s_err) == 0u;
             asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
             const int slot = m0 + 32 * q + lane;
             const uint32_t trow = tmem + (static_cast<uint32_t>(32 * q) << 16) + buf * XG_ACC_STRIDE;
