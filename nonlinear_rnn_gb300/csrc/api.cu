@@ -653,8 +653,10 @@ int nrnn_decode_step_x(const void *x, const void *W_x, int dtype, const float *p
     if (dtype == NRNN_BF16) {
         // the projection on the tensor cores, the step in the epilogue
         CUtensorMap tmX, tmW;
+        const int64_t xg_tiles = (slots + 127) / 128 * ((d_h + 63) / 64);   // 32-bit tile indices
         if (slots >= DECODE_XG_MIN_SLOTS && d_in >= DECODE_XG_MIN_D_IN && d_h % 8 == 0 &&
-            aligned16(params) && aligned16(h_out) && (h_in == nullptr || aligned16(h_in))) {
+            xg_tiles <= INT32_MAX && aligned16(params) && aligned16(h_out) &&
+            (h_in == nullptr || aligned16(h_in))) {
             // more than one slot tile: M = 128 slots by 64 units (z, r, c rows) per
             // tile; a shorter K loop leaves the epilogue's cell work exposed
             if (!make_map_2d_sw128(&tmX, x, d_in, slots, 64, 128) ||
