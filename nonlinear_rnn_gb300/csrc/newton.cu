@@ -199,7 +199,11 @@ constexpr int newton_min_blocks() { return (!FUSED && sizeof(TS) == 2) ? 9 : 8; 
 // EARLY: warp 0 reads the nearest predecessors' look-back slots before the
 // CTA barrier (see with_lookback_mode)
 // PLAN: the chunks of a pack are segment-aligned, taken from a.plan.
-template <typename TS, bool FUSED, bool XPROJ = false, bool EARLY = false, bool PLAN = false>
+// WARM (fused only): the first iteration starts from a given iterate H^(0)
+// instead of 0 (a constant, so that the common start from 0 compiles without
+// the initial-iterate loads; the per-iteration kernel reads H^(k-1) always).
+template <typename TS, bool FUSED, bool XPROJ = false, bool EARLY = false, bool PLAN = false,
+          bool WARM = false>
 __global__ void __launch_bounds__(NW * 32, newton_min_blocks<TS, FUSED>())
     k_newton(const __grid_constant__ CUtensorMap tmP, const __grid_constant__ CUtensorMap tmH,
              const __grid_constant__ CUtensorMap tmO, const __grid_constant__ CUtensorMap tmX,
@@ -282,7 +286,7 @@ __global__ void __launch_bounds__(NW * 32, newton_min_blocks<TS, FUSED>())
     const int t0 = PLAN ? s_tile[3] : c * L, t_end = PLAN ? s_tile[4] : a.T;
     const int chain = PLAN ? s_tile[5] : c;
     const int u0 = ut * U;
-    const bool load_h = a.H_prev != nullptr;   // H^(k-1) (per-iteration) or H^(0) (fused)
+    const bool load_h = FUSED ? WARM : a.H_prev != nullptr;   // H^(0) (fused) or H^(k-1)
 
     if (tid == 0) {
         if constexpr (XPROJ) {
@@ -682,19 +686,28 @@ bool early_lookback(const NewtonArgs &a, int ctas_per_sm, bool plan) {
     return resident <= EARLY_LOOKBACK_CHUNKS * columns;
 }
 
-template <typename TS, bool FUSED, bool EARLY, bool PLAN>
+template <typename TS, bool FUSED, bool EARLY, bool PLAN, bool WARM>
 cudaError_t launch_one(const CUtensorMap &tmP, const CUtensorMap &tmH, const CUtensorMap &tmO,
                        const NewtonArgs &a, int64_t n_ctas, cudaStream_t stream) {
     static std::atomic<unsigned long long> configured{0};
     const size_t smem = smem_bytes_for<TS, FUSED>(a.H_prev != nullptr);
     cudaError_t e = once_per_device(configured, [](int) {
-        return cudaFuncSetAttribute(k_newton<TS, FUSED, false, EARLY, PLAN>,
+        return cudaFuncSetAttribute(k_newton<TS, FUSED, false, EARLY, PLAN, WARM>,
                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     static_cast<int>(smem_bytes_for<TS, FUSED>(true)));
     });
     if (e != cudaSuccess) return e;
-    return launch_dependent(k_newton<TS, FUSED, false, EARLY, PLAN>, static_cast<unsigned>(n_ctas),
-                            NW * 32, smem, stream, tmP, tmH, tmO, tmP, tmP, a);
+    return launch_dependent(k_newton<TS, FUSED, false, EARLY, PLAN, WARM>,
+                            static_cast<unsigned>(n_ctas), NW * 32, smem, stream, tmP, tmH, tmO, tmP,
+                            tmP, a);
+}
+
+template <typename TS, bool FUSED, bool EARLY, bool PLAN>
+cudaError_t launch_one(const CUtensorMap &tmP, const CUtensorMap &tmH, const CUtensorMap &tmO,
+                       const NewtonArgs &a, int64_t n_ctas, cudaStream_t stream) {
+    if (FUSED && a.H_prev != nullptr)   // a fused forward from a given iterate
+        return launch_one<TS, FUSED, EARLY, PLAN, FUSED>(tmP, tmH, tmO, a, n_ctas, stream);
+    return launch_one<TS, FUSED, EARLY, PLAN, false>(tmP, tmH, tmO, a, n_ctas, stream);
 }
 
 template <typename TS, bool FUSED>

@@ -83,6 +83,25 @@ def test_decode_step_with_fused_projection(dtype):
     assert np.max(np.abs(host(h) - ref)) <= (2e-6 if dtype == "f32" else 1.6e-2)
 
 
+@pytest.mark.parametrize("slots,d_in,d_h", [(40, 72, 24), (300, 512, 48)])
+def test_decode_step_with_projection_in_place(slots, d_in, d_h):
+    # bf16, out = h: the carried state is overwritten by the step (one tile of
+    # 8-unit CTAs; the GEMM form, whose epilogue reads and writes each 8-unit
+    # group of a slot in the same thread)
+    import nonlinear_rnn_gb300 as nr
+    rng = np.random.default_rng(slots + 3 * d_h)
+    x = syn.round_bf16(rng.normal(size=(slots, d_in)).astype(np.float32))
+    W = syn.round_bf16((rng.uniform(-1, 1, size=(3 * d_h, d_in)) / math.sqrt(d_in)).astype(np.float32))
+    h0 = syn.round_bf16(rng.uniform(-0.5, 0.5, size=(slots, d_h)).astype(np.float32))
+    prm = syn.make_params(syn.small_workload(d_h=d_h, seed=66))
+    P = syn.round_bf16(oracle.input_projection(x, W).astype(np.float32))
+    ref = oracle.decode_step(P, prm, h0)
+    hd = dev(h0, torch.bfloat16)
+    h = nr.decode_step(prm, h=hd, x=dev(x, torch.bfloat16), W_x=dev(W, torch.bfloat16), out=hd)
+    assert h.data_ptr() == hd.data_ptr()
+    assert np.max(np.abs(host(h) - ref)) <= 1.6e-2
+
+
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 @pytest.mark.parametrize("slots,d_in,d_h", [(64, 2048, 16), (300, 136, 40), (8, 8, 8), (300, 512, 48)])
 def test_decode_step_with_projection_at_other_sizes(dtype, slots, d_in, d_h):
