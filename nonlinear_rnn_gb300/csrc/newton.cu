@@ -199,9 +199,10 @@ constexpr int newton_min_blocks() { return (!FUSED && sizeof(TS) == 2) ? 9 : 8; 
 // EARLY: warp 0 reads the nearest predecessors' look-back slots before the
 // CTA barrier (see with_lookback_mode)
 // PLAN: the chunks of a pack are segment-aligned, taken from a.plan.
-// WARM (fused only): the first iteration starts from a given iterate H^(0)
-// instead of 0 (a constant, so that the common start from 0 compiles without
-// the initial-iterate loads; the per-iteration kernel reads H^(k-1) always).
+// WARM: an iterate is given (fused: H^(0) instead of 0; per-iteration:
+// H^(k-1), i.e. every launch but the first of a forward from 0).  A constant,
+// so that the start from 0 compiles without the iterate's loads and the other
+// launches without the zero-state cell.
 template <typename TS, bool FUSED, bool XPROJ = false, bool EARLY = false, bool PLAN = false,
           bool WARM = false>
 __global__ void __launch_bounds__(NW * 32, newton_min_blocks<TS, FUSED>())
@@ -286,7 +287,7 @@ __global__ void __launch_bounds__(NW * 32, newton_min_blocks<TS, FUSED>())
     const int t0 = PLAN ? s_tile[3] : c * L, t_end = PLAN ? s_tile[4] : a.T;
     const int chain = PLAN ? s_tile[5] : c;
     const int u0 = ut * U;
-    const bool load_h = FUSED ? WARM : a.H_prev != nullptr;   // H^(0) (fused) or H^(k-1)
+    const bool load_h = WARM;   // H^(0) (fused) or H^(k-1) (per-iteration) given
 
     if (tid == 0) {
         if constexpr (XPROJ) {
@@ -475,7 +476,7 @@ __global__ void __launch_bounds__(NW * 32, newton_min_blocks<TS, FUSED>())
     for (int k = a.k_first; k <= a.k_last; ++k) {
         float2 J2[HALF];
         float A_lo, B_lo, A, Bv;
-        if (k == 1 && !load_h) {   // from H^(0) = 0: every shifted state is 0
+        if ((!FUSED || k == 1) && !load_h) {   // from H^(0) = 0: every shifted state is 0
             if (general)
                 warp_pairs<TS, FUSED, true, true>(Pv, warp, lane, G, hb, hm, nvalid, prm2, J2, A_lo, B_lo, A, Bv);
             else
@@ -705,8 +706,8 @@ cudaError_t launch_one(const CUtensorMap &tmP, const CUtensorMap &tmH, const CUt
 template <typename TS, bool FUSED, bool EARLY, bool PLAN>
 cudaError_t launch_one(const CUtensorMap &tmP, const CUtensorMap &tmH, const CUtensorMap &tmO,
                        const NewtonArgs &a, int64_t n_ctas, cudaStream_t stream) {
-    if (FUSED && a.H_prev != nullptr)   // a fused forward from a given iterate
-        return launch_one<TS, FUSED, EARLY, PLAN, FUSED>(tmP, tmH, tmO, a, n_ctas, stream);
+    if (a.H_prev != nullptr)   // an iterate given: H^(0) (fused), H^(k-1) (per-iteration)
+        return launch_one<TS, FUSED, EARLY, PLAN, true>(tmP, tmH, tmO, a, n_ctas, stream);
     return launch_one<TS, FUSED, EARLY, PLAN, false>(tmP, tmH, tmO, a, n_ctas, stream);
 }
 
