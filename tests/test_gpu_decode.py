@@ -169,3 +169,37 @@ def test_decode_step_x_bf16_tensor_core_path_through_the_c_abi(slots, d_in, d_h,
     torch.cuda.synchronize()
     assert not torch.isnan(out).any()
     assert np.max(np.abs(host(out) - ref)) <= 1.6e-2
+
+
+@pytest.mark.parametrize("i", range(8))
+def test_decode_step_x_bf16_random_shapes(i):
+    """Seeded random slot counts, d_in and d_h through nrnn_decode_step_x
+    (bf16): both tensor-core forms, ragged slot and unit tiles, K tails, the
+    zero state and in-place updates, against the oracle on the float64
+    projection rounded to bf16."""
+    import ctypes
+    import nonlinear_rnn_gb300 as nr
+    rng = np.random.default_rng(9100 + i)
+    slots = int(rng.integers(1, 1500))
+    d_in = int(8 * rng.integers(1, 160))      # 8 .. 1272
+    d_h = int(8 * rng.integers(1, 40))        # 8 .. 312
+    zero_h, in_place = bool(i % 3 == 0), bool(i % 2 == 1)
+    lib = nr.load()
+    x = syn.round_bf16(rng.normal(size=(slots, d_in)).astype(np.float32))
+    W = syn.round_bf16((rng.uniform(-1, 1, size=(3 * d_h, d_in)) / math.sqrt(d_in)).astype(np.float32))
+    h0 = np.zeros((slots, d_h), np.float32) if zero_h else \
+        syn.round_bf16(rng.uniform(-0.5, 0.5, size=(slots, d_h)).astype(np.float32))
+    prm = syn.make_params(syn.small_workload(d_h=d_h, seed=9200 + i))
+    P = syn.round_bf16(oracle.input_projection(x, W).astype(np.float32))
+    ref = oracle.decode_step(P, prm, None if zero_h else h0)
+    xd, Wd, hd = dev(x, torch.bfloat16), dev(W, torch.bfloat16), dev(h0, torch.bfloat16)
+    out = hd if in_place else torch.full((slots, d_h), float("nan"), dtype=torch.bfloat16, device="cuda")
+    pd = nr.params_tensor(prm, d_h, "cuda")
+    p = lambda t: ctypes.c_void_p(t.data_ptr())   # noqa: E731
+    st = lib.nrnn_decode_step_x(p(xd), p(Wd), 1, p(pd), slots, d_in, d_h,
+                                None if zero_h else p(hd), p(out),
+                                ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert st == 0, (slots, d_in, d_h)
+    torch.cuda.synchronize()
+    assert not torch.isnan(out).any(), (slots, d_in, d_h)
+    assert np.max(np.abs(host(out) - ref)) <= 1.6e-2, (slots, d_in, d_h)
