@@ -79,6 +79,25 @@ def test_newton_matches_oracle_small(nr, dtype, algo, K):
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("algo", ["fused", "per_iter"])
+def test_one_column_of_16384_chunks(nr, dtype, algo):
+    # B = 1, T = 2^20, d_h = 8: a single look-back chain of 16384 chunks, so that
+    # every resident CTA belongs to the same column (the deepest chains the
+    # look-back meets), and 24 of each tile's 32 unit lanes idle
+    w = syn.small_workload(B=1, T=1 << 20, d_h=8, dtype=dtype, seed=31)
+    P = syn.direct_preact(w)
+    prm = syn.make_params(w)
+    Pd = dev(P, TDT[dtype])
+    Href, rho_ref = oracle.newton(host(Pd), prm, 2)
+    out = nan_out(w.B, w.T, w.d_h, TDT[dtype])
+    H, rho = nr.newton_forward(Pd, prm, K=2, algo=algo, check=False, out=out)
+    assert not torch.isnan(H).any()
+    err = float(np.max(np.abs(host(H) - Href)))
+    assert err <= (2e-5 if dtype == "f32" else 5e-2), err
+    assert abs(rho.item() - rho_ref) <= (2e-5 if dtype == "f32" else 5e-2)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
 def test_fused_and_per_iteration_agree(nr, dtype):
     w = syn.small_workload(B=2, T=1000, d_h=64, dtype=dtype, seed=5)
     P = dev(syn.direct_preact(w), TDT[dtype])
