@@ -45,3 +45,28 @@ def test_backward_matches_oracle(dtype, case):
     # parameter gradients: sums over B*T terms
     rel = np.max(np.abs(gprm.cpu().numpy() - gprm_ref)) / max(1.0, float(np.max(np.abs(gprm_ref))))
     assert rel <= (1e-4 if dtype == "f32" else 1e-2)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("B,T,d_h", [(1, 1 << 20, 8), (1, 128, 8192)])
+def test_backward_extreme_shapes(dtype, B, T, d_h):
+    """One reverse look-back chain of 16384 chunks (T = 2^20, 8 units: every
+    resident CTA in one column), and 256 unit tiles of two chunks each
+    (d_h = 8192), against the oracle's adjoint."""
+    import nonlinear_rnn_gb300 as nr
+    tdt = torch.float32 if dtype == "f32" else torch.bfloat16
+    w = syn.small_workload(B=B, T=T, d_h=d_h, dtype=dtype, seed=90 + d_h)
+    P = syn.direct_preact(w)
+    prm = syn.make_params(w)
+    Pd = dev(P, tdt)
+    Pq = host(Pd)
+    H = oracle.sequential(Pq, prm).astype(np.float32)
+    gH = np.random.default_rng(91 + d_h).normal(size=H.shape).astype(np.float32)
+    Hd, gHd = dev(H, tdt), dev(gH, tdt)
+    gP_ref, gprm_ref = oracle.backward(Pq, prm, host(Hd), host(gHd))
+    gP, gprm = nr.newton_backward(Pd, prm, Hd, gHd)
+    scale = max(1.0, float(np.max(np.abs(gP_ref))))
+    tol = 2e-5 if dtype == "f32" else 2e-2
+    assert np.max(np.abs(host(gP) - gP_ref)) <= tol * scale
+    rel = np.max(np.abs(gprm.cpu().numpy() - gprm_ref)) / max(1.0, float(np.max(np.abs(gprm_ref))))
+    assert rel <= (1e-4 if dtype == "f32" else 1e-2)

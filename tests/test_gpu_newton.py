@@ -98,6 +98,24 @@ def test_one_column_of_16384_chunks(nr, dtype, algo):
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("algo", ["fused", "per_iter"])
+def test_256_unit_tiles(nr, dtype, algo):
+    # d_h = 8192 (256 unit tiles) over T = 200 (four chunks, the last ragged):
+    # many short columns, and a preactivation row of 24576 values
+    w = syn.small_workload(B=1, T=200, d_h=8192, dtype=dtype, seed=34)
+    P = syn.direct_preact(w)
+    prm = syn.make_params(w)
+    Pd = dev(P, TDT[dtype])
+    Href, rho_ref = oracle.newton(host(Pd), prm, 3)
+    out = nan_out(w.B, w.T, w.d_h, TDT[dtype])
+    H, rho = nr.newton_forward(Pd, prm, K=3, algo=algo, check=False, out=out)
+    assert not torch.isnan(H).any()
+    err = float(np.max(np.abs(host(H) - Href)))
+    assert err <= (2e-5 if dtype == "f32" else 5e-2), err
+    assert abs(rho.item() - rho_ref) <= (2e-5 if dtype == "f32" else 5e-2)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
 def test_fused_and_per_iteration_agree(nr, dtype):
     w = syn.small_workload(B=2, T=1000, d_h=64, dtype=dtype, seed=5)
     P = dev(syn.direct_preact(w), TDT[dtype])
