@@ -115,6 +115,33 @@ def test_256_unit_tiles(nr, dtype, algo):
     assert abs(rho.item() - rho_ref) <= (2e-5 if dtype == "f32" else 5e-2)
 
 
+@pytest.mark.parametrize("algo", ["fused", "per_iter"])
+def test_forwards_on_two_streams_at_once(nr, algo):
+    # two forwards with their own workspaces in flight together on two
+    # streams (the look-back waits only on CTAs of its own grid that have
+    # started): each equals the same forward run alone, up to the order in
+    # which a chunk's carry was composed (an inclusive prefix, or aggregates
+    # and an earlier inclusive: the same value up to rounding)
+    shapes = [dict(B=4, T=5000, d_h=96, seed=51), dict(B=1, T=40000, d_h=40, seed=52)]
+    Ps, prms, refs = [], [], []
+    for sh in shapes:
+        w = syn.small_workload(B=sh["B"], T=sh["T"], d_h=sh["d_h"], seed=sh["seed"])
+        P, prm = dev(syn.direct_preact(w)), syn.make_params(w)
+        H, rho = nr.newton_forward(P, prm, K=3, algo=algo, check=False)
+        Ps.append(P), prms.append(prm), refs.append((H.clone(), rho.item()))
+    torch.cuda.synchronize()
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    for _ in range(3):
+        outs = []
+        for P, prm, st in zip(Ps, prms, streams):
+            with torch.cuda.stream(st):
+                outs.append(nr.newton_forward(P, prm, K=3, algo=algo, check=False))
+        torch.cuda.synchronize()
+        for (H, rho), (Hr, rr) in zip(outs, refs):
+            assert (H - Hr).abs().max().item() <= 1e-5
+            assert abs(rho.item() - rr) <= 1e-5
+
+
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 def test_fused_and_per_iteration_agree(nr, dtype):
     w = syn.small_workload(B=2, T=1000, d_h=64, dtype=dtype, seed=5)
